@@ -1,0 +1,425 @@
+"""Benchmark of the Muon step on GB300.
+
+Default: one GPU, the 28-layer Qwen2.5-7B-shaped set (196 matrices, 6.53e9
+matrix parameters, bf16 grads, fp32 weights and momentum), NS5, 3 warm-up and
+10 timed steps.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+
+With N > 1 (torchrun), every rank runs its own replica of the workload (the
+step has no cross-matrix exchange); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Muon step ms per param set; NS5 TFLOP/s as % of GB300 dense BF16 tensor peak"
+# tf32 / bf16 dense tensor ratio from the nominal GB300 figures (1.1 vs 2.25 PFLOP/s)
+TF32_OVER_BF16 = 1.1 / 2.25
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qwen7b_28l")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.lines = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ distributed plumbing
+def dist_init(n_gpus):
+    """(rank, world, local_rank); initialises torch.distributed when launched by torchrun."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Max of a host float over ranks (identity at world size 1)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ workload accounting
+def algorithmic_ns_flops(shapes, ns_steps=5):
+    """Tensor FLOPs of the Gram-form NS step, symmetric products counted at half:
+    SYRK r^2 c, final 2 r^2 c, (4J - 3) r x r symmetric products of r^3 each."""
+    rr = 0 if ns_steps == 0 else (1 if ns_steps == 1 else 4 * ns_steps - 3)
+    bf16 = tf32 = 0.0
+    for m, n in shapes:
+        r, c = min(m, n), max(m, n)
+        bf16 += 3.0 * r * r * c
+        tf32 += rr * float(r) ** 3
+    return bf16, tf32
+
+
+def elementwise_bytes(shapes, grad_bytes):
+    """HBM bytes of the NS step outside the GEMM operand traffic: momentum pass
+    (G read, M read+write, bf16 X0 write) and the fused apply (W read+write)."""
+    tot = 0
+    for m, n in shapes:
+        tot += m * n * (grad_bytes + 8 + 2 + 8)
+    return tot
+
+
+# ------------------------------------------------------------------ CPU oracle sample
+def oracle_sample(shapes, grad_dtype, reps_per_bucket=1, seed=2):
+    """Time the fp64 oracle (as it stands) on one matrix per distinct oriented shape
+    and scale to the whole list.  Returns (estimated seconds per param set, detail)."""
+    import numpy as np
+    from oracle import muon_ref as R
+    import workloads
+
+    buckets = {}
+    for i, (m, n) in enumerate(shapes):
+        buckets.setdefault((min(m, n), max(m, n)), []).append(i)
+    est, detail = 0.0, []
+    for key, idx in sorted(buckets.items()):
+        i = idx[0]
+        m, n = shapes[i]
+        w = workloads.gen_tensor((m, n), workloads.W_STD, workloads.seed_of(seed, 0, i, "W")).double().numpy()
+        g = workloads.gen_tensor((m, n), workloads.G_STD, workloads.seed_of(seed, 0, i, "G"),
+                                 dtype=grad_dtype).double().numpy()
+        mm = workloads.gen_tensor((m, n), workloads.M_STD, workloads.seed_of(seed, 0, i, "M")).double().numpy()
+        ts = []
+        for _ in range(reps_per_bucket):
+            t0 = time.perf_counter()
+            R.muon_step(w, g, mm, workloads.LR, workloads.WD, workloads.MU, 5, "ns")
+            ts.append(time.perf_counter() - t0)
+        t = min(ts)
+        est += t * len(idx)
+        detail.append({"shape": [m, n], "count": len(idx), "s": round(t, 3)})
+    return est, detail
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world, local):
+    import torch
+    import matrix_orthogonalising_optimizer_muon_gb300 as lib
+    import workloads
+
+    wl = workloads.WORKLOADS[args.workload]
+    shapes = list(wl.shapes)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+
+    # ---- inputs resident in HBM (seeded on the device); fresh grads per step
+    t0 = time.time()
+    W, G, M = [], [], []
+    for i, (m, n) in enumerate(shapes):
+        W.append(workloads.gen_tensor((m, n), workloads.W_STD, workloads.seed_of(wl.index, 0, i, "W"), dev))
+        M.append(workloads.gen_tensor((m, n), workloads.M_STD, workloads.seed_of(wl.index, 0, i, "M"), dev))
+        G.append(workloads.gen_tensor((m, n), workloads.G_STD, workloads.seed_of(wl.index, 0, i, "G"), dev,
+                                      wl.grad_dtype))
+    plan = lib.MuonPlan(shapes, wl.grad_dtype, timing=True)
+    torch.cuda.synchronize()
+    setup_s = time.time() - t0
+    lr, wd, mu = workloads.LR, workloads.WD, workloads.MU
+    stream = torch.cuda.current_stream()
+    plan.bind(W, G, M)
+
+    def one_step(t):
+        if wl.rownorm_k and t % wl.rownorm_k != 0:
+            plan.step_bound(lr, wd, mu, mode="rownorm", eps=wl.eps, stream=stream)
+        else:
+            plan.step_bound(lr, wd, mu, 5, "ns", stream=stream)
+
+    for t in range(args.warmup):
+        one_step(t)
+    plan.sync()
+    try:
+        plan.stage_times()               # drop the warm-up steps' event groups
+    except lib.MuonError:
+        pass
+
+    # ---- timed region: K steps, CUDA events on the launching stream
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches = 0
+    ev0.record(stream)
+    for t in range(args.steps):
+        one_step(args.warmup + t)
+        launches += plan.info()["launches_last_step"]
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    plan.sync()
+    stage_ms, stage_fl = plan.stage_times()   # per-stage event times summed over the K steps
+    elapsed_ms = ev0.elapsed_time(ev1)
+    ms_step = max_over_ranks(elapsed_ms / args.steps, world)
+    return dict(wl=wl, shapes=shapes, plan=plan, W=W, G=G, M=M, ms_step=ms_step, stage_ms=stage_ms,
+                stage_fl=stage_fl, launches=launches, clocks=clk, peaks=peaks, peak_src=peak_src,
+                setup_s=setup_s, one_step=one_step)
+
+
+def run_e2e(res, args):
+    """Same step through the public API with host buffers: every step copies the
+    gradients host->device from pinned memory and reads the updated weights back."""
+    import torch
+    W, G = res["W"], res["G"]
+    host_g = [torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in G]
+    host_w = [torch.empty(w.shape, dtype=w.dtype, pin_memory=True) for w in W]
+    for hg, g in zip(host_g, G):
+        hg.copy_(g)
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    steps = max(1, min(args.steps, 5))
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for t in range(steps):
+        for hg, g in zip(host_g, G):
+            g.copy_(hg, non_blocking=True)
+        res["one_step"](t)
+        for hw, w in zip(host_w, W):
+            hw.copy_(w, non_blocking=True)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    h2d = sum(g.numel() * g.element_size() for g in G)
+    d2h = sum(w.numel() * w.element_size() for w in W)
+    return ev0.elapsed_time(ev1) / steps, h2d, d2h, steps
+
+
+def report_ours(args, res, rank, world):
+    wl, shapes = res["wl"], res["shapes"]
+    peaks, src = res["peaks"], res["peak_src"]
+    K = args.steps
+    ms_step = res["ms_step"]
+    st_ms, st_fl = res["stage_ms"], res["stage_fl"]
+    gemm_ms = (st_ms[1] + st_ms[2] + st_ms[3]) / K
+    fl_bf16 = (st_fl[0] + st_fl[2]) / K
+    fl_tf32 = st_fl[1] / K
+    ns_steps_run = sum(1 for t in range(K) if not (wl.rownorm_k and (args.warmup + t) % wl.rownorm_k))
+    # roofline of the tensor-core products: algorithmic FLOPs over their event
+    # time, against the sustained measured peak blended by dtype (tf32 = bf16 x 1.1/2.25)
+    bf16_peak = peaks["bf16_tflops_sustained"] if "bf16_tflops_sustained" in peaks else peaks["bf16_tflops"]
+    tf32_peak = bf16_peak * TF32_OVER_BF16
+    roofline = None
+    ns5 = {}
+    if gemm_ms > 0 and ns_steps_run:
+        per_ns = ns_steps_run / K
+        fl = (fl_bf16 + fl_tf32) / per_ns
+        t_ms = gemm_ms / per_ns
+        achieved = fl / (t_ms * 1e-3) / 1e12
+        blended = fl / (fl_bf16 / per_ns / bf16_peak + fl_tf32 / per_ns / tf32_peak) if fl else bf16_peak
+        roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(blended, 1),
+                    "unit": "TFLOP/s", "frac": round(achieved / blended, 4), "traffic": None,
+                    "kernel": "gemm_kernel (SYRK + r x r tf32 products + final product), per NS step",
+                    "peak_note": "%s sustained bf16 %.1f, tf32 = bf16 x 1.1/2.25 = %.1f, blended by FLOPs"
+                                 % (src, bf16_peak, tf32_peak)}
+        ns5 = {"ns5_tflops": round(achieved, 1),
+               "ns5_frac_bf16_peak": round(achieved / peaks["bf16_tflops"], 4),
+               "ns5_gemm_ms": round(t_ms, 3)}
+    line = {
+        "metric": METRIC, "value": round(ms_step, 3), "unit": "ms", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16+tf32 tensor (fp32 accumulate), fp32 elementwise",
+        "data": "synthetic (seeded Gaussian, shapes of the workload)",
+        "config": {"workload": wl.name, "matrices": len(shapes),
+                   "params": int(sum(m * n for m, n in shapes)), "grad_dtype": wl.grad_dtype,
+                   "ns_steps": 5, "rownorm_k": wl.rownorm_k,
+                   "l2": "inputs larger than L2 (%.1f GB of W, G, M per step)" %
+                         (sum(m * n for m, n in shapes) * (10 if wl.grad_dtype == "bf16" else 12) / 1e9),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "stages_ms_per_step": {"momentum_norm": round(st_ms[0] / K, 3), "syrk": round(st_ms[1] / K, 3),
+                               "ns_rxr": round(st_ms[2] / K, 3), "final_apply": round(st_ms[3] / K, 3),
+                               "rownorm": round(st_ms[4] / K, 3)},
+        "roofline": roofline,
+        "gpu_launches": res["launches"],
+        "clocks": res["clocks"],
+    }
+    line.update(ns5)
+    if st_ms[0] > 0:
+        gb = elementwise_bytes(shapes, 2 if wl.grad_dtype == "bf16" else 4)
+        mom_bytes = sum(m * n * ((2 if wl.grad_dtype == "bf16" else 4) + 8 + 2) for m, n in shapes)
+        line["momentum_kernel_gbs"] = round(mom_bytes / (st_ms[0] / K * 1e-3) / 1e9, 1)
+        line["momentum_kernel_hbm_frac"] = round(line["momentum_kernel_gbs"] / peaks["hbm_gbs"], 4)
+    return line
+
+
+# ------------------------------------------------------------------ reference arm (the oracle)
+def run_reference(args, rank, world):
+    """The fp64 CPU oracle, as it stands, on the host cores.  Each step times the
+    oracle on one matrix of one oriented shape (round robin over the shapes);
+    the per-param-set time scales each shape's mean time by its count."""
+    import workloads
+    wl = workloads.WORKLOADS[args.workload]
+    shapes = list(wl.shapes)
+    if rank != 0:
+        return None
+    keys = sorted({(min(m, n), max(m, n)) for m, n in shapes})
+    counts = {k: sum(1 for m, n in shapes if (min(m, n), max(m, n)) == k) for k in keys}
+    first = {k: next(i for i, (m, n) in enumerate(shapes) if (min(m, n), max(m, n)) == k) for k in keys}
+    times = {k: [] for k in keys}
+
+    def sample(k):
+        i = first[k]
+        sub = [shapes[i]]
+        t, _ = oracle_sample(sub, wl.grad_dtype, seed=wl.index)
+        return t
+
+    t0 = time.time()
+    for s in range(args.warmup):
+        sample(keys[s % len(keys)])
+    for s in range(args.steps):
+        k = keys[s % len(keys)]
+        times[k].append(sample(k))
+    for k in keys:                      # every shape timed at least once
+        if not times[k]:
+            times[k].append(sample(k))
+    per_set = sum(counts[k] * statistics.mean(times[k]) for k in keys)
+    ms = per_set * 1e3
+    cores = os.cpu_count()
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(ms, 1), "unit": "ms", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 1), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "matrices": len(shapes),
+                   "params": int(sum(m * n for m, n in shapes))},
+        "cpu_baseline": {"value": round(ms, 1), "unit": "ms", "cores": cores, "kind": "oracle",
+                         "sample": "per step one matrix of one oriented shape (round robin over %d shapes), "
+                                   "fp64 numpy direct NS5; scaled by the shape counts" % len(keys)},
+        "e2e": {"value": round(ms, 1), "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": round(time.time() - t0, 1),
+    }
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_init(args.gpus)
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return
+    res = run_ours(args, rank, world, local)
+    line = report_ours(args, res, rank, world)
+    if not args.no_e2e:
+        e2e_ms, h2d, d2h, nsteps = run_e2e(res, args)
+        e2e_ms = max_over_ranks(e2e_ms, world)
+        line["e2e"] = {"value": round(e2e_ms, 3), "unit": "ms", "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h, "steps": nsteps,
+                       "what": "grads host->device (pinned) + muon_step + updated weights device->host"}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        t, detail = oracle_sample(res["shapes"], res["wl"].grad_dtype, seed=res["wl"].index)
+        line["cpu_baseline"] = {"value": round(t * 1e3, 1), "unit": "ms", "cores": os.cpu_count(),
+                                "kind": "oracle",
+                                "sample": "one matrix per oriented shape, fp64 numpy direct NS5, scaled by "
+                                          "shape counts: %s" % json.dumps(detail)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    barrier(world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,171 @@
+/*
+ * muon.h - C ABI of a single-GPU Muon optimizer step for GB300 (sm_103a).
+ *
+ * What one step computes, per weight matrix W (m x n, row-major fp32):
+ *   M   <- mu*M + G                         ("Muon is Scalable for LLM Training" blog, eq. (1))
+ *   U    = mu*M + G                         (same page, Nesterov-style input)
+ *   X0   = O(U) / ||U||_F                   (same page, Background; orientation O: transpose
+ *                                            when m > n, "Scaling Muon for Diffusion
+ *                                            Transformers" sec. 3.1)
+ *   X_J  = J quintic Newton-Schulz steps    (blog eq. (2), (a,b,c) = (3.4445,-4.7750,2.0315)),
+ *          carried in the r x r Gram space  (DMuon, "Gram Newton-Schulz"; r = min(m,n))
+ *   W   <- W - lr*(0.2*sqrt(max(m,n))*O^{-1}(X_J) + wd*W)          (blog eq. (4))
+ * RowNorm mode replaces X_J by R_eps(O(U)), each oriented row divided by
+ * max(||row||_2, eps) (DiT paper sec. 3.1), with the same update scale.
+ *
+ * Conventions for every entry point:
+ *  - Matrices are dense, row-major, contiguous, in device memory of the current
+ *    CUDA device; params and momentum are fp32 and updated in place; grads are
+ *    the plan's grad dtype and only read.  The caller owns all of them.
+ *  - Pointer arrays (params, grads, momentum) are HOST arrays of n device
+ *    pointers, in the order of the shapes given to muon_plan_create.  They may
+ *    change from call to call; the array itself is read before the call returns.
+ *  - stream is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    All device work is enqueued on it; no call synchronises the host except
+ *    muon_sync and muon_debug_copy_update.
+ *  - Errors: every argument is validated on the host before anything is
+ *    launched, and an invalid call returns MUON_ERR_INVALID_ARG (or
+ *    MUON_ERR_UNSUPPORTED) with no buffer touched.  A failed launch returns
+ *    MUON_ERR_CUDA.  A device-side bounded wait that expires (a tensor-core
+ *    pipeline stall) is recorded in the plan's device status word and returned
+ *    by the next muon_sync as MUON_ERR_TIMEOUT.  No C++ exception crosses this
+ *    boundary.
+ */
+#ifndef MUON_GB300_H
+#define MUON_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MUON_OK = 0,
+    MUON_ERR_INVALID_ARG = 1,   /* bad shape, null pointer, overlap, hyperparameter out of range */
+    MUON_ERR_UNSUPPORTED = 2,   /* dtype / size this build does not handle */
+    MUON_ERR_OOM = 3,           /* workspace allocation failed */
+    MUON_ERR_CUDA = 4,          /* a CUDA runtime or launch error */
+    MUON_ERR_TIMEOUT = 5,       /* a device-side bounded wait expired */
+    MUON_ERR_NONFINITE = 6      /* reserved */
+} muon_status;
+
+typedef enum { MUON_F32 = 0, MUON_BF16 = 1 } muon_dtype;
+typedef enum { MUON_MODE_NS = 0, MUON_MODE_ROWNORM = 1 } muon_mode;
+
+/* Shape of one matrix as stored: rows x cols, row-major. */
+typedef struct { int64_t rows, cols; } muon_shape;
+
+typedef struct {
+    /* nonzero: NS steps also write the orthogonalised update O (fp32, stored
+       layout m x n) into the workspace so muon_debug_copy_update can return it */
+    int32_t keep_update;
+    /* nonzero: each step records CUDA events around its stages (read with muon_stage_times) */
+    int32_t timing;
+    int32_t reserved[6];
+} muon_plan_opts;
+
+typedef struct muon_plan_s* muon_plan;
+
+/*
+ * muon_plan_create - plan a step for a fixed list of matrix shapes ("muon_plan(shapes)").
+ *   shapes     host array of n shapes (rows, cols >= 1).
+ *   grad_dtype dtype of every gradient: MUON_F32 or MUON_BF16.
+ *   opts       may be NULL (all zero).
+ *   out        receives the plan.
+ * Orients every shape to r x c (r = min, c = max; DiT paper sec. 3.1),
+ * buckets equal (r, c) so each Gram Newton-Schulz product runs as one grouped
+ * launch over all matrices of all buckets (DMuon, batching same-shape matrices),
+ * and allocates the workspace once (bf16 X0, fp32 r x r Gram buffers, pointer
+ * tables, status word) on the current device.  The plan owns the workspace;
+ * muon_plan_destroy frees it.  Returns MUON_ERR_OOM if cudaMalloc fails.
+ */
+muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype grad_dtype,
+                             const muon_plan_opts* opts, muon_plan* out);
+
+void muon_plan_destroy(muon_plan p);
+
+/*
+ * muon_step - one Muon step over every matrix of the plan.
+ *   params, grads, momentum  host arrays of n device pointers (see conventions).
+ *   lr >= 0, wd >= 0, 0 <= mu < 1, all finite.
+ *   ns_steps in [0, 16]: Newton-Schulz iterations (5 in the pages; 0 gives O = X0).
+ *   mode MUON_MODE_NS, or MUON_MODE_ROWNORM (then equal to muon_rownorm_step with eps = 1e-8).
+ * A matrix whose Nesterov input U is all zero gets O = 0 (only weight decay acts).
+ * params and momentum must not overlap each other, the grads, or any other matrix.
+ */
+muon_status muon_step(muon_plan p, float* const* params, const void* const* grads,
+                      float* const* momentum, float lr, float wd, float mu,
+                      int32_t ns_steps, muon_mode mode, void* stream);
+
+/*
+ * muon_rownorm_step - one RowNorm step (DiT paper sec. 3, "periodic RowNorm Muon"):
+ *   M <- mu*M + G;  U = mu*M + G;  R = R_eps(O(U)) over the rows of the oriented
+ *   matrix (stored columns when m > n);  W <- W - lr*(0.2*sqrt(max(m,n))*R + wd*W).
+ *   eps > 0 and finite.  Other arguments as muon_step.
+ */
+muon_status muon_rownorm_step(muon_plan p, float* const* params, const void* const* grads,
+                              float* const* momentum, float lr, float wd, float mu,
+                              float eps, void* stream);
+
+/*
+ * muon_sync - wait for the plan's work on stream, then read and clear the
+ * device status word.  Returns MUON_ERR_TIMEOUT if a bounded device wait
+ * expired since the last muon_sync, MUON_ERR_CUDA on a CUDA error.
+ */
+muon_status muon_sync(muon_plan p, void* stream);
+
+/*
+ * muon_debug_copy_update - copy the orthogonalised update O of matrix i from
+ * the last NS step (stored layout, m x n fp32) into dst (device memory, m*n
+ * floats).  Needs opts.keep_update; synchronises stream.
+ */
+muon_status muon_debug_copy_update(muon_plan p, int32_t i, float* dst, void* stream);
+
+/*
+ * muon_debug_copy_workspace - copy one workspace buffer of matrix i, as it is
+ * after the last step, into dst (host or device memory), for step-by-step
+ * parity checks.  Synchronises stream.  which:
+ *   0 X0 workspace: bf16 U in the oriented layout, r rows of ld elements (unnormalised)
+ *   1 G buffer 0, 2 G buffer 1, 3 P, 4 T, 5 Q buffer 0, 6 Q buffer 1: fp32, r rows of ld
+ *   7 bf16 Q of the final product: r rows of ld
+ *   8 1/||U||_F: one fp32
+ * *ld receives the leading dimension (elements) of the copied rows; the copy
+ * is r*ld elements (one for which = 8) of 2 (bf16) or 4 (fp32) bytes.
+ * After a step with ns_steps = J, buffer 1 holds G_0 = X0 X0^T when J <= 1,
+ * buffer 3 holds P_J, and buffer 7 holds Q_J.
+ */
+muon_status muon_debug_copy_workspace(muon_plan p, int32_t i, int32_t which, void* dst, int32_t* ld,
+                                      void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* muon_status_string(muon_status s);
+
+/* Plan introspection. */
+typedef struct {
+    int32_t n_matrices;
+    int32_t n_buckets;
+    int64_t workspace_bytes;
+    int32_t launches_last_step;   /* kernels the last step enqueued */
+    int32_t sm_count;
+} muon_plan_info_t;
+
+muon_status muon_plan_info(muon_plan p, muon_plan_info_t* info);
+
+/*
+ * muon_stage_times - device time (ms) per stage, summed over the steps run
+ * since the previous call, measured with CUDA events recorded on each step's
+ * stream (needs opts.timing; waits for those steps, then resets the sums).
+ * Stages: [0] momentum + Nesterov + norm, [1] Gram SYRK, [2] r x r
+ * Newton-Schulz products, [3] final product + fused apply, [4] RowNorm steps.
+ * n_stages <= 5.  flops (nullable) receives the algorithmic tensor FLOPs of
+ * stages 1-3 over the same steps (symmetric products counted at half).
+ * Returns MUON_ERR_INVALID_ARG when no timed step was run.
+ */
+muon_status muon_stage_times(muon_plan p, float* ms, double* flops, int32_t n_stages);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MUON_GB300_H */

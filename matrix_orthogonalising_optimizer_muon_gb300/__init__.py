@@ -1,0 +1,282 @@
+"""Python binding of libmuon_gb300.so, a single-GPU Muon optimizer step for GB300.
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  PyTorch provides the device memory and the stream.  There is no
+fallback: if the library cannot be loaded, every entry point raises.
+
+The C entry points keep their names (``muon_plan_create``, ``muon_step``,
+``muon_rownorm_step``, ``muon_sync``, ``muon_debug_copy_update``,
+``muon_debug_copy_workspace``, ``muon_plan_info``, ``muon_stage_times``,
+``muon_status_string``, ``muon_plan_destroy``); ``MuonPlan`` wraps them for
+torch tensors and ``PeriodicRowNormMuon`` adds the step schedule of periodic
+RowNorm Muon (full NS5 every K steps, RowNorm otherwise; "Scaling Muon for
+Diffusion Transformers", sec. 3).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB, build, up_to_date
+
+__all__ = [
+    "MuonError", "MuonPlan", "PeriodicRowNormMuon", "load", "build",
+    "MUON_OK", "MUON_ERR_INVALID_ARG", "MUON_ERR_UNSUPPORTED", "MUON_ERR_OOM",
+    "MUON_ERR_CUDA", "MUON_ERR_TIMEOUT", "MUON_F32", "MUON_BF16",
+    "MUON_MODE_NS", "MUON_MODE_ROWNORM", "EXPORTED",
+]
+
+MUON_OK, MUON_ERR_INVALID_ARG, MUON_ERR_UNSUPPORTED, MUON_ERR_OOM = 0, 1, 2, 3
+MUON_ERR_CUDA, MUON_ERR_TIMEOUT, MUON_ERR_NONFINITE = 4, 5, 6
+MUON_F32, MUON_BF16 = 0, 1
+MUON_MODE_NS, MUON_MODE_ROWNORM = 0, 1
+
+# Newton-Schulz steps and momentum the pages use ("Muon is Scalable" blog).
+DEFAULT_NS_STEPS = 5
+DEFAULT_MU = 0.95
+
+
+class MuonShape(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_int64), ("cols", ctypes.c_int64)]
+
+
+class MuonPlanOpts(ctypes.Structure):
+    _fields_ = [("keep_update", ctypes.c_int32), ("timing", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 6)]
+
+
+class MuonPlanInfo(ctypes.Structure):
+    _fields_ = [("n_matrices", ctypes.c_int32), ("n_buckets", ctypes.c_int32),
+                ("workspace_bytes", ctypes.c_int64), ("launches_last_step", ctypes.c_int32),
+                ("sm_count", ctypes.c_int32)]
+
+
+_P = ctypes.c_void_p
+_PP = ctypes.POINTER(ctypes.c_void_p)
+# name -> (restype, argtypes); every function declared in include/muon.h
+EXPORTED = {
+    "muon_plan_create": (ctypes.c_int, [ctypes.POINTER(MuonShape), ctypes.c_int32, ctypes.c_int,
+                                        ctypes.POINTER(MuonPlanOpts), ctypes.POINTER(_P)]),
+    "muon_plan_destroy": (None, [_P]),
+    "muon_step": (ctypes.c_int, [_P, _PP, _PP, _PP, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                 ctypes.c_int32, ctypes.c_int, _P]),
+    "muon_rownorm_step": (ctypes.c_int, [_P, _PP, _PP, _PP, ctypes.c_float, ctypes.c_float,
+                                         ctypes.c_float, ctypes.c_float, _P]),
+    "muon_sync": (ctypes.c_int, [_P, _P]),
+    "muon_debug_copy_update": (ctypes.c_int, [_P, ctypes.c_int32, _P, _P]),
+    "muon_debug_copy_workspace": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int32, _P,
+                                                 ctypes.POINTER(ctypes.c_int32), _P]),
+    "muon_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "muon_plan_info": (ctypes.c_int, [_P, ctypes.POINTER(MuonPlanInfo)]),
+    "muon_stage_times": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_float),
+                                        ctypes.POINTER(ctypes.c_double), ctypes.c_int32]),
+}
+
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load (building first if missing) the CUDA library and declare its signatures."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    if path is None:
+        path = LIB
+        if not up_to_date():
+            build()
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in EXPORTED.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path == LIB:
+        _lib = lib
+    return lib
+
+
+class MuonError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = load().muon_status_string(code)
+        super().__init__("%s: %s" % (where, msg.decode() if msg else code))
+
+
+def _check(code: int, where: str):
+    if code != MUON_OK:
+        raise MuonError(code, where)
+
+
+def muon_status_string(code: int) -> str:
+    return load().muon_status_string(code).decode()
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr_array(ptrs):
+    return (ctypes.c_void_p * len(ptrs))(*ptrs)
+
+
+class MuonPlan:
+    """A planned Muon step over a fixed list of matrix shapes (``muon_plan_create``).
+
+    ``step`` takes lists of torch tensors: params (fp32), grads (``grad_dtype``)
+    and momentum (fp32), all contiguous CUDA tensors of the planned shapes, and
+    updates params and momentum in place on the current stream."""
+
+    def __init__(self, shapes, grad_dtype: str = "bf16", keep_update: bool = False,
+                 timing: bool = False):
+        self.lib = load()
+        self.shapes = [(int(m), int(n)) for m, n in shapes]
+        self.grad_dtype = grad_dtype
+        arr = (MuonShape * len(self.shapes))(*[MuonShape(m, n) for m, n in self.shapes])
+        opts = MuonPlanOpts(1 if keep_update else 0, 1 if timing else 0)
+        h = ctypes.c_void_p()
+        gd = {"bf16": MUON_BF16, "f32": MUON_F32}[grad_dtype]
+        _check(self.lib.muon_plan_create(arr, len(self.shapes), gd, ctypes.byref(opts),
+                                         ctypes.byref(h)), "muon_plan_create")
+        self.handle = h
+
+    def close(self):
+        if getattr(self, "handle", None):
+            self.lib.muon_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    # ---------------------------------------------------------------- marshalling
+    def _pointers(self, params, grads, momentum):
+        import torch
+        n = len(self.shapes)
+        if not (len(params) == len(grads) == len(momentum) == n):
+            raise ValueError("expected %d params, grads and momentum tensors" % n)
+        gdt = torch.bfloat16 if self.grad_dtype == "bf16" else torch.float32
+        for i, (w, g, m) in enumerate(zip(params, grads, momentum)):
+            shp = self.shapes[i]
+            for t, dt, name in ((w, torch.float32, "param"), (g, gdt, "grad"),
+                                (m, torch.float32, "momentum")):
+                if tuple(t.shape) != shp or t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+                    raise ValueError("%s %d: need a contiguous CUDA %s tensor of shape %s, got %s %s"
+                                     % (name, i, dt, shp, t.dtype, tuple(t.shape)))
+        return (_ptr_array([t.data_ptr() for t in params]),
+                _ptr_array([t.data_ptr() for t in grads]),
+                _ptr_array([t.data_ptr() for t in momentum]))
+
+    def step(self, params, grads, momentum, lr: float, wd: float, mu: float = DEFAULT_MU,
+             ns_steps: int = DEFAULT_NS_STEPS, mode: str = "ns", stream=None):
+        """One Muon step (``muon_step``)."""
+        w, g, m = self._pointers(params, grads, momentum)
+        md = {"ns": MUON_MODE_NS, "rownorm": MUON_MODE_ROWNORM}[mode]
+        _check(self.lib.muon_step(self.handle, w, g, m, lr, wd, mu, ns_steps, md,
+                                  _stream_handle(stream)), "muon_step")
+
+    def rownorm_step(self, params, grads, momentum, lr: float, wd: float, mu: float = DEFAULT_MU,
+                     eps: float = 1e-8, stream=None):
+        """One RowNorm step (``muon_rownorm_step``)."""
+        w, g, m = self._pointers(params, grads, momentum)
+        _check(self.lib.muon_rownorm_step(self.handle, w, g, m, lr, wd, mu, eps,
+                                          _stream_handle(stream)), "muon_rownorm_step")
+
+    def bind(self, params, grads, momentum):
+        """Validate the tensors once and keep their pointer arrays for ``step_bound``.
+        The tensors must stay alive and in place while bound."""
+        self._bound = self._pointers(params, grads, momentum)
+        self._bound_refs = (list(params), list(grads), list(momentum))
+
+    def step_bound(self, lr: float, wd: float, mu: float = DEFAULT_MU, ns_steps: int = DEFAULT_NS_STEPS,
+                   mode: str = "ns", eps: float = 1e-8, stream=None):
+        """``muon_step`` / ``muon_rownorm_step`` on the tensors given to ``bind``."""
+        w, g, m = self._bound
+        if mode == "ns":
+            _check(self.lib.muon_step(self.handle, w, g, m, lr, wd, mu, ns_steps, MUON_MODE_NS,
+                                      _stream_handle(stream)), "muon_step")
+        else:
+            _check(self.lib.muon_rownorm_step(self.handle, w, g, m, lr, wd, mu, eps,
+                                              _stream_handle(stream)), "muon_rownorm_step")
+
+    def sync(self, stream=None):
+        _check(self.lib.muon_sync(self.handle, _stream_handle(stream)), "muon_sync")
+
+    def debug_update(self, i: int, stream=None):
+        """O of matrix i from the last NS step (needs keep_update), as a CUDA fp32 tensor."""
+        import torch
+        m, n = self.shapes[i]
+        out = torch.empty((m, n), dtype=torch.float32, device="cuda")
+        _check(self.lib.muon_debug_copy_update(self.handle, i, ctypes.c_void_p(out.data_ptr()),
+                                               _stream_handle(stream)), "muon_debug_copy_update")
+        return out
+
+    def debug_workspace(self, i: int, which: int, stream=None):
+        """A workspace buffer of matrix i (``muon_debug_copy_workspace``) as a CPU tensor
+        of r rows (fp32; the bf16 buffers 0 and 7 are widened exactly)."""
+        import torch
+        m, n = self.shapes[i]
+        r, c = min(m, n), max(m, n)
+        ld = ctypes.c_int32()
+        if which == 8:
+            out = torch.empty(1, dtype=torch.float32)
+            _check(self.lib.muon_debug_copy_workspace(self.handle, i, which,
+                                                      ctypes.c_void_p(out.data_ptr()),
+                                                      ctypes.byref(ld), _stream_handle(stream)),
+                   "muon_debug_copy_workspace")
+            return out
+        bf = which in (0, 7)
+        width = ((c if which == 0 else r) + 7) // 8 * 8
+        out = torch.empty((r, width), dtype=torch.bfloat16 if bf else torch.float32)
+        _check(self.lib.muon_debug_copy_workspace(self.handle, i, which,
+                                                  ctypes.c_void_p(out.data_ptr()),
+                                                  ctypes.byref(ld), _stream_handle(stream)),
+               "muon_debug_copy_workspace")
+        assert ld.value == width
+        cols = c if which == 0 else r
+        return out[:, :cols].float()
+
+    def info(self) -> dict:
+        inf = MuonPlanInfo()
+        _check(self.lib.muon_plan_info(self.handle, ctypes.byref(inf)), "muon_plan_info")
+        return {k: getattr(inf, k) for k, _ in MuonPlanInfo._fields_}
+
+    def stage_times(self):
+        """Summed over the timed steps since the previous call: (ms per stage [momentum,
+        syrk, rxr NS, final+apply, rownorm], algorithmic flops [syrk, rxr, final])."""
+        ms = (ctypes.c_float * 5)()
+        fl = (ctypes.c_double * 3)()
+        _check(self.lib.muon_stage_times(self.handle, ms, fl, 5), "muon_stage_times")
+        return list(ms), list(fl)
+
+
+class PeriodicRowNormMuon:
+    """Periodic RowNorm Muon over one plan: step t runs NS (``ns_steps``) iff t % K == 0,
+    RowNorm otherwise ("Scaling Muon for Diffusion Transformers", sec. 3; steps from 0)."""
+
+    def __init__(self, plan: MuonPlan, k: int, eps: float = 1e-8, ns_steps: int = DEFAULT_NS_STEPS):
+        if k <= 0:
+            raise ValueError("K must be positive")
+        self.plan, self.k, self.eps, self.ns_steps = plan, k, eps, ns_steps
+        self.t = 0
+
+    def mode_at(self, t: int) -> str:
+        return "ns" if t % self.k == 0 else "rownorm"
+
+    def step(self, params, grads, momentum, lr, wd, mu=DEFAULT_MU, stream=None) -> str:
+        mode = self.mode_at(self.t)
+        if mode == "ns":
+            self.plan.step(params, grads, momentum, lr, wd, mu, self.ns_steps, "ns", stream)
+        else:
+            self.plan.rownorm_step(params, grads, momentum, lr, wd, mu, self.eps, stream)
+        self.t += 1
+        return mode

@@ -1,0 +1,851 @@
+// C ABI of the Muon step (include/muon.h): planner, argument validation and the
+// stream-ordered launch sequence.  Host code only; kernels live in gemm.cu and
+// elementwise.cu.
+//
+// Step (mode NS), per plan, every kernel grouped over all matrices:
+//   momentum (m <= n)  |  momentum + transpose (m > n)  |  1/||U||_F
+//   G0 = a^2 X X^T                                         (one launch, all buckets)
+//   k = 1..J:  P = aI + bG + cG^2;  {Q' = P Q, T = P P};  G' = G T
+//   O = a Q X fused with W -= lr (0.2 sqrt(c) O + wd W)    (one launch, all buckets)
+// (Gram Newton-Schulz from DMuon's technical summary; coefficients, Nesterov
+// input, normalisation and eq. (4) from the "Muon is Scalable" blog summary;
+// orientation and RowNorm from the DiT paper sec. 3.1.)
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "../../include/muon.h"
+#include "kernels.h"
+
+using namespace muon;
+
+namespace {
+
+// Quintic coefficients of the Newton-Schulz step ("Muon is Scalable" blog, eq. (2)).
+constexpr float kNsA = 3.4445f;
+constexpr float kNsB = -4.7750f;
+constexpr float kNsC = 2.0315f;
+constexpr int kMaxNsSteps = 16;
+constexpr int kMaxDim = 1 << 20;        // per-dimension limit of this build
+constexpr int kMaxR = 32768;            // r x r workspace limit of this build
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 3-D tensor map over `batch` row-major matrices (rows x inner, leading dim ld,
+// item stride rows * ld), 128-byte swizzle, zero fill outside the extents.
+bool make_map(CUtensorMap* map, void* base, bool bf16, uint64_t inner, uint64_t rows, uint64_t batch, uint64_t ld,
+              uint32_t box_inner, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const uint64_t esz = bf16 ? 2 : 4;
+    cuuint64_t dims[3] = {inner, rows, batch};
+    cuuint64_t strides[2] = {ld * esz, ld * rows * esz};
+    cuuint32_t box[3] = {box_inner, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+inline long long round_up(long long a, long long b) { return ceil_div(a, b) * b; }
+
+struct Bucket {
+    int r = 0, c = 0, batch = 0;
+    int ldr = 0;   // leading dim of r x r buffers (multiple of 8)
+    int ldu = 0;   // leading dim of X0 rows (multiple of 8)
+    std::vector<int> mats;
+    int slot_base = 0;
+    long long ut_off = 0;   // element offset of item 0 in the X0 workspace
+    float* G[2] = {nullptr, nullptr};
+    float* P = nullptr;
+    float* T = nullptr;
+    float* Q[2] = {nullptr, nullptr};
+    __nv_bfloat16* Qb = nullptr;
+    int* d_item_mat = nullptr;
+    float* Odbg = nullptr;
+    CUtensorMap ut_a, ut_b, ut_mn, qb_a;
+    CUtensorMap ga[2], gb[2], pa, pb, tb, qb[2];
+};
+
+struct ListDev {
+    int* list = nullptr;
+    long long* blk = nullptr;
+    int n = 0;
+    long long blocks = 0;
+};
+
+}  // namespace
+
+struct muon_plan_s {
+    int device = 0;
+    int sm_count = 0;
+    muon_dtype gdt = MUON_F32;
+    muon_plan_opts opts{};
+    std::vector<muon_shape> shapes;
+    std::vector<MatDev> mats;
+    std::vector<int> mat_bucket, mat_item;
+    std::vector<Bucket> buckets;
+
+    void* ws = nullptr;
+    size_t ws_bytes = 0;
+    __nv_bfloat16* ut = nullptr;
+    MatDev* d_mats = nullptr;
+    float* partials = nullptr;
+    float* cpartials = nullptr;
+    float* rowinv = nullptr;
+    float* alpha = nullptr;
+    int* status = nullptr;
+    unsigned char* d_transposed = nullptr;
+    void** d_ptrs = nullptr;   // [G(n) | M(n) | W(n)]
+
+    ListDev mom_rows, mom_tiles, all, rn_rows, rn_stats, rn_final, rn_apply;
+
+    void** h_pinned = nullptr;
+    std::vector<void*> h_cache;
+    cudaEvent_t upload_ev = nullptr;
+    bool uploaded = false;
+
+    // opts.timing: one event group per step since the last muon_stage_times call
+    struct StepEvents {
+        cudaEvent_t e[6];
+        bool ns;
+    };
+    std::vector<StepEvents> evs;
+    size_t n_timed = 0;
+    double flops[3] = {0, 0, 0};   // summed over the timed steps
+    int last_launches = 0;
+};
+
+namespace {
+
+muon_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA; }
+
+#define MUON_TRY(expr)                                    \
+    do {                                                  \
+        cudaError_t e__ = (expr);                         \
+        if (e__ != cudaSuccess) return MUON_ERR_CUDA;     \
+    } while (0)
+
+bool finite_nonneg(float x) { return std::isfinite(x) && x >= 0.f; }
+
+// Every params / momentum / grads range must be disjoint from every other.
+muon_status check_pointers(const muon_plan_s* p, float* const* params, const void* const* grads,
+                           float* const* momentum) {
+    if (!params || !grads || !momentum) return MUON_ERR_INVALID_ARG;
+    const size_t n = p->shapes.size();
+    const size_t gsz = p->gdt == MUON_BF16 ? 2 : 4;
+    std::vector<std::pair<uintptr_t, uintptr_t>> ranges;
+    ranges.reserve(3 * n);
+    for (size_t i = 0; i < n; ++i) {
+        if (!params[i] || !grads[i] || !momentum[i]) return MUON_ERR_INVALID_ARG;
+        const size_t numel = (size_t)p->shapes[i].rows * (size_t)p->shapes[i].cols;
+        const uintptr_t w = reinterpret_cast<uintptr_t>(params[i]);
+        const uintptr_t g = reinterpret_cast<uintptr_t>(grads[i]);
+        const uintptr_t m = reinterpret_cast<uintptr_t>(momentum[i]);
+        ranges.push_back({w, w + numel * 4});
+        ranges.push_back({m, m + numel * 4});
+        ranges.push_back({g, g + numel * gsz});
+    }
+    std::sort(ranges.begin(), ranges.end());
+    for (size_t k = 1; k < ranges.size(); ++k)
+        if (ranges[k].first < ranges[k - 1].second) return MUON_ERR_INVALID_ARG;
+    return MUON_OK;
+}
+
+muon_status check_device(const muon_plan_s* p) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MUON_ERR_CUDA;
+    return dev == p->device ? MUON_OK : MUON_ERR_INVALID_ARG;
+}
+
+// Copies the per-call pointer tables to the device when they changed.
+muon_status upload_pointers(muon_plan_s* p, float* const* params, const void* const* grads, float* const* momentum,
+                            cudaStream_t s) {
+    const size_t n = p->shapes.size();
+    bool same = p->uploaded;
+    for (size_t i = 0; same && i < n; ++i)
+        same = p->h_cache[i] == grads[i] && p->h_cache[n + i] == momentum[i] && p->h_cache[2 * n + i] == params[i];
+    if (same) return MUON_OK;
+    if (p->uploaded) MUON_TRY(cudaEventSynchronize(p->upload_ev));   // pinned buffer free again
+    for (size_t i = 0; i < n; ++i) {
+        p->h_cache[i] = const_cast<void*>(grads[i]);
+        p->h_cache[n + i] = momentum[i];
+        p->h_cache[2 * n + i] = params[i];
+    }
+    std::memcpy(p->h_pinned, p->h_cache.data(), 3 * n * sizeof(void*));
+    MUON_TRY(cudaMemcpyAsync(p->d_ptrs, p->h_pinned, 3 * n * sizeof(void*), cudaMemcpyHostToDevice, s));
+    MUON_TRY(cudaEventRecord(p->upload_ev, s));
+    p->uploaded = true;
+    return MUON_OK;
+}
+
+ElemArgs elem_args(const muon_plan_s* p, const ListDev& l, float mu, float lr, float wd, float eps) {
+    ElemArgs a{};
+    const size_t n = p->shapes.size();
+    a.mats = p->d_mats;
+    a.list = l.list;
+    a.nlist = l.n;
+    a.list_blk = l.blk;
+    a.G = const_cast<const void* const*>(p->d_ptrs);
+    a.M = reinterpret_cast<float* const*>(p->d_ptrs + n);
+    a.W = reinterpret_cast<float* const*>(p->d_ptrs + 2 * n);
+    a.ut = p->ut;
+    a.partials = p->partials;
+    a.alpha = p->alpha;
+    a.rowinv = p->rowinv;
+    a.mu = mu;
+    a.lr = lr;
+    a.wd = wd;
+    a.eps = eps;
+    a.grad_bf16 = p->gdt == MUON_BF16;
+    return a;
+}
+
+int sym_tiles(int r) {
+    const int tm = (int)ceil_div(r, kBM);
+    int t = 0;
+    for (int i = 0; i < tm; ++i) t += i / 2 + 1;
+    return t;
+}
+
+GemmProblem problem(int M, int N, int K, int batch, bool sym, int epi) {
+    GemmProblem q{};
+    q.M = M;
+    q.N = N;
+    q.K = K;
+    q.batch = batch;
+    q.tiles_m = (int)ceil_div(M, kBM);
+    q.tiles_n = (int)ceil_div(N, kBN);
+    q.tiles_per_item = sym ? sym_tiles(M) : q.tiles_m * q.tiles_n;
+    q.sym = sym ? 1 : 0;
+    q.epi = epi;
+    return q;
+}
+
+// Collects problems into grouped launches of up to kMaxProblems.
+struct Grouper {
+    muon_plan_s* p;
+    cudaStream_t s;
+    bool tf32;
+    GemmLaunch L;
+    muon_status st = MUON_OK;
+    int launches = 0;
+    Grouper(muon_plan_s* plan, cudaStream_t stream, bool is_tf32) : p(plan), s(stream), tf32(is_tf32) { reset(); }
+    void reset() {
+        std::memset(&L, 0, sizeof(L));
+        L.status = p->status;
+    }
+    void add(const CUtensorMap& a, const CUtensorMap& b, GemmProblem q) {
+        if (L.nprob == kMaxProblems) flush();
+        q.tile_begin = L.total_tiles;
+        L.mapA[L.nprob] = a;
+        L.mapB[L.nprob] = b;
+        L.prob[L.nprob] = q;
+        L.nprob++;
+        L.total_tiles += q.tiles_per_item * q.batch;
+    }
+    void flush() {
+        if (L.nprob == 0) return;
+        if (st == MUON_OK) {
+            st = cuda_status(gemm_launch(L, tf32, p->sm_count, s));
+            ++launches;
+        }
+        reset();
+    }
+};
+
+constexpr size_t kMaxTimedSteps = 4096;
+
+// Event group for the next timed step (the last group is reused past the cap).
+muon_plan_s::StepEvents* next_events(muon_plan_s* p) {
+    if (p->n_timed < p->evs.size()) return &p->evs[p->n_timed++];
+    if (p->evs.size() >= kMaxTimedSteps) return &p->evs.back();
+    muon_plan_s::StepEvents g{};
+    for (auto& e : g.e)
+        if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    p->evs.push_back(g);
+    p->n_timed = p->evs.size();
+    return &p->evs.back();
+}
+
+void free_plan(muon_plan_s* p) {
+    if (!p) return;
+    if (p->ws) cudaFree(p->ws);
+    if (p->h_pinned) cudaFreeHost(p->h_pinned);
+    if (p->upload_ev) cudaEventDestroy(p->upload_ev);
+    for (auto& g : p->evs)
+        for (auto& e : g.e)
+            if (e) cudaEventDestroy(e);
+    delete p;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* muon_status_string(muon_status s) {
+    switch (s) {
+        case MUON_OK: return "MUON_OK";
+        case MUON_ERR_INVALID_ARG: return "MUON_ERR_INVALID_ARG: invalid argument";
+        case MUON_ERR_UNSUPPORTED: return "MUON_ERR_UNSUPPORTED: unsupported dtype or size";
+        case MUON_ERR_OOM: return "MUON_ERR_OOM: workspace allocation failed";
+        case MUON_ERR_CUDA: return "MUON_ERR_CUDA: CUDA runtime or launch error";
+        case MUON_ERR_TIMEOUT: return "MUON_ERR_TIMEOUT: a bounded device wait expired";
+        case MUON_ERR_NONFINITE: return "MUON_ERR_NONFINITE";
+    }
+    return "MUON_ERR_UNKNOWN";
+}
+
+muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype grad_dtype, const muon_plan_opts* opts,
+                             muon_plan* out) {
+    if (!out) return MUON_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!shapes || n <= 0) return MUON_ERR_INVALID_ARG;
+    if (grad_dtype != MUON_F32 && grad_dtype != MUON_BF16) return MUON_ERR_UNSUPPORTED;
+    for (int i = 0; i < n; ++i) {
+        if (shapes[i].rows <= 0 || shapes[i].cols <= 0) return MUON_ERR_INVALID_ARG;
+        if (shapes[i].rows > kMaxDim || shapes[i].cols > kMaxDim) return MUON_ERR_UNSUPPORTED;
+        if (std::min(shapes[i].rows, shapes[i].cols) > kMaxR) return MUON_ERR_UNSUPPORTED;
+    }
+    muon_plan_s* p = new (std::nothrow) muon_plan_s();
+    if (!p) return MUON_ERR_OOM;
+    if (cudaGetDevice(&p->device) != cudaSuccess) {
+        delete p;
+        return MUON_ERR_CUDA;
+    }
+    if (cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess) {
+        delete p;
+        return MUON_ERR_CUDA;
+    }
+    if (!encode_fn()) {
+        delete p;
+        return MUON_ERR_CUDA;
+    }
+    p->gdt = grad_dtype;
+    if (opts) p->opts = *opts;
+    p->shapes.assign(shapes, shapes + n);
+
+    // ---- orient + bucket by (r, c) (DiT paper sec. 3.1; DMuon batching)
+    p->mats.resize(n);
+    p->mat_bucket.resize(n);
+    p->mat_item.resize(n);
+    for (int i = 0; i < n; ++i) {
+        MatDev& md = p->mats[i];
+        std::memset(&md, 0, sizeof(md));
+        md.m = shapes[i].rows;
+        md.n = shapes[i].cols;
+        md.r = (int)std::min(md.m, md.n);
+        md.c = (int)std::max(md.m, md.n);
+        md.transposed = md.m > md.n;
+        md.scale = 0.2f * std::sqrt((float)md.c);   // blog eq. (4)
+        int b = -1;
+        for (size_t k = 0; k < p->buckets.size(); ++k)
+            if (p->buckets[k].r == md.r && p->buckets[k].c == md.c) b = (int)k;
+        if (b < 0) {
+            Bucket nb;
+            nb.r = md.r;
+            nb.c = md.c;
+            nb.ldr = (int)round_up(md.r, 8);
+            nb.ldu = (int)round_up(md.c, 8);
+            p->buckets.push_back(nb);
+            b = (int)p->buckets.size() - 1;
+        }
+        p->mat_bucket[i] = b;
+        p->mat_item[i] = (int)p->buckets[b].mats.size();
+        p->buckets[b].mats.push_back(i);
+    }
+
+    // ---- workspace layout (256-byte aligned slices of one allocation)
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = (size_t)round_up((long long)(off + bytes), 256);
+        return o;
+    };
+    long long ut_elems = 0, slots = 0;
+    for (auto& b : p->buckets) {
+        b.batch = (int)b.mats.size();
+        b.slot_base = (int)slots;
+        slots += b.batch;
+        b.ut_off = ut_elems;
+        ut_elems += (long long)b.batch * b.r * b.ldu;
+    }
+    long long mom_part = 0, col_part = 0, inv_elems = 0;
+    std::vector<int> rows_list, tiles_list, all_list, rnr_list, rnc_list;
+    for (int i = 0; i < n; ++i) {
+        MatDev& md = p->mats[i];
+        const Bucket& b = p->buckets[p->mat_bucket[i]];
+        md.slot = b.slot_base + p->mat_item[i];
+        md.ldu = b.ldu;
+        md.ut_off = b.ut_off + (long long)p->mat_item[i] * b.r * b.ldu;
+        md.nblk = (int)(md.transposed ? ceil_div(md.m, kTile) * ceil_div(md.n, kTile)
+                                      : ceil_div(md.m * md.n, kMomElemsPerBlock));
+        md.part_off = mom_part;
+        mom_part += md.nblk;
+        if (md.transposed) {
+            md.cpart_off = col_part;
+            col_part += ceil_div(md.m, kColSlab) * md.n;
+            md.inv_off = inv_elems;
+            inv_elems += round_up(md.n, 4);
+            tiles_list.push_back(i);
+            rnc_list.push_back(i);
+        } else {
+            rows_list.push_back(i);
+            rnr_list.push_back(i);
+        }
+        all_list.push_back(i);
+    }
+    const size_t o_ut = take((size_t)ut_elems * 2);
+    const size_t o_mats = take(sizeof(MatDev) * n);
+    const size_t o_part = take(sizeof(float) * std::max<long long>(mom_part, 1));
+    const size_t o_cpart = take(sizeof(float) * std::max<long long>(col_part, 1));
+    const size_t o_inv = take(sizeof(float) * std::max<long long>(inv_elems, 1));
+    const size_t o_alpha = take(sizeof(float) * std::max<long long>(slots, 1));
+    const size_t o_status = take(sizeof(int));
+    const size_t o_tr = take((size_t)n);
+    const size_t o_ptrs = take(sizeof(void*) * 3 * n);
+    std::vector<size_t> o_item(p->buckets.size()), o_rr(p->buckets.size()), o_qb(p->buckets.size()),
+        o_odbg(p->buckets.size());
+    for (size_t k = 0; k < p->buckets.size(); ++k) {
+        Bucket& b = p->buckets[k];
+        o_item[k] = take(sizeof(int) * b.batch);
+        const size_t rr = (size_t)b.batch * b.r * b.ldr;
+        o_rr[k] = take(rr * 4);   // G0
+        take(rr * 4);             // G1
+        take(rr * 4);             // P
+        take(rr * 4);             // T
+        take(rr * 4);             // Q0
+        take(rr * 4);             // Q1
+        o_qb[k] = take(rr * 2);   // bf16 Q for the final product
+        o_odbg[k] = p->opts.keep_update ? take((size_t)b.batch * b.r * b.c * 4) : 0;
+    }
+    // launch lists: int lists, then long long prefixes
+    struct HostList {
+        std::vector<int>* v;
+        ListDev* d;
+        int kind;
+    };
+    HostList hl[] = {{&rows_list, &p->mom_rows, 0}, {&tiles_list, &p->mom_tiles, 1}, {&all_list, &p->all, 2},
+                     {&rnr_list, &p->rn_rows, 3},   {&rnc_list, &p->rn_stats, 4},   {&rnc_list, &p->rn_final, 5},
+                     {&rnc_list, &p->rn_apply, 6}};
+    std::vector<size_t> o_list(7), o_blk(7);
+    for (int k = 0; k < 7; ++k) {
+        o_list[k] = take(sizeof(int) * std::max<size_t>(hl[k].v->size(), 1));
+        o_blk[k] = take(sizeof(long long) * (hl[k].v->size() + 1));
+    }
+    p->ws_bytes = off;
+    if (cudaMalloc(&p->ws, p->ws_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        free_plan(p);
+        return MUON_ERR_OOM;
+    }
+    char* base = static_cast<char*>(p->ws);
+    p->ut = reinterpret_cast<__nv_bfloat16*>(base + o_ut);
+    p->d_mats = reinterpret_cast<MatDev*>(base + o_mats);
+    p->partials = reinterpret_cast<float*>(base + o_part);
+    p->cpartials = reinterpret_cast<float*>(base + o_cpart);
+    p->rowinv = reinterpret_cast<float*>(base + o_inv);
+    p->alpha = reinterpret_cast<float*>(base + o_alpha);
+    p->status = reinterpret_cast<int*>(base + o_status);
+    p->d_transposed = reinterpret_cast<unsigned char*>(base + o_tr);
+    p->d_ptrs = reinterpret_cast<void**>(base + o_ptrs);
+
+    std::vector<unsigned char> tr(n);
+    for (int i = 0; i < n; ++i) tr[i] = (unsigned char)p->mats[i].transposed;
+    bool ok = cudaMemcpy(p->d_mats, p->mats.data(), sizeof(MatDev) * n, cudaMemcpyHostToDevice) == cudaSuccess;
+    ok = ok && cudaMemcpy(p->d_transposed, tr.data(), n, cudaMemcpyHostToDevice) == cudaSuccess;
+    ok = ok && cudaMemset(p->status, 0, sizeof(int)) == cudaSuccess;
+    ok = ok && cudaMemset(p->d_ptrs, 0, sizeof(void*) * 3 * n) == cudaSuccess;
+
+    for (int k = 0; ok && k < 7; ++k) {
+        std::vector<int>& v = *hl[k].v;
+        ListDev& d = *hl[k].d;
+        d.list = reinterpret_cast<int*>(base + o_list[k]);
+        d.blk = reinterpret_cast<long long*>(base + o_blk[k]);
+        d.n = (int)v.size();
+        std::vector<long long> pre(v.size() + 1, 0);
+        for (size_t j = 0; j < v.size(); ++j) {
+            const MatDev& md = p->mats[v[j]];
+            long long nb = 0;
+            switch (hl[k].kind) {
+                case 0: case 1: nb = md.nblk; break;
+                case 2: nb = 1; break;
+                case 3: nb = md.m; break;
+                case 4: nb = ceil_div(md.m, kColSlab) * ceil_div(md.n, kColWidth); break;
+                case 5: nb = ceil_div(md.n, kElemThreads); break;
+                case 6: nb = ceil_div(md.m * md.n, kApplyElemsPerBlock); break;
+            }
+            pre[j + 1] = pre[j] + nb;
+        }
+        d.blocks = pre.back();
+        if (!v.empty()) ok = cudaMemcpy(d.list, v.data(), sizeof(int) * v.size(), cudaMemcpyHostToDevice) == cudaSuccess;
+        ok = ok && cudaMemcpy(d.blk, pre.data(), sizeof(long long) * pre.size(), cudaMemcpyHostToDevice) == cudaSuccess;
+    }
+
+    for (size_t k = 0; ok && k < p->buckets.size(); ++k) {
+        Bucket& b = p->buckets[k];
+        b.d_item_mat = reinterpret_cast<int*>(base + o_item[k]);
+        ok = cudaMemcpy(b.d_item_mat, b.mats.data(), sizeof(int) * b.batch, cudaMemcpyHostToDevice) == cudaSuccess;
+        const size_t rr = (size_t)b.batch * b.r * b.ldr;
+        float* f = reinterpret_cast<float*>(base + o_rr[k]);
+        b.G[0] = f;
+        b.G[1] = reinterpret_cast<float*>(base + o_rr[k] + (size_t)round_up(rr * 4, 256));
+        b.P = reinterpret_cast<float*>(base + o_rr[k] + 2 * (size_t)round_up(rr * 4, 256));
+        b.T = reinterpret_cast<float*>(base + o_rr[k] + 3 * (size_t)round_up(rr * 4, 256));
+        b.Q[0] = reinterpret_cast<float*>(base + o_rr[k] + 4 * (size_t)round_up(rr * 4, 256));
+        b.Q[1] = reinterpret_cast<float*>(base + o_rr[k] + 5 * (size_t)round_up(rr * 4, 256));
+        b.Qb = reinterpret_cast<__nv_bfloat16*>(base + o_qb[k]);
+        b.Odbg = p->opts.keep_update ? reinterpret_cast<float*>(base + o_odbg[k]) : nullptr;
+        __nv_bfloat16* ut = p->ut + b.ut_off;
+        ok = ok && make_map(&b.ut_a, ut, true, b.c, b.r, b.batch, b.ldu, 64, kBM);
+        ok = ok && make_map(&b.ut_b, ut, true, b.c, b.r, b.batch, b.ldu, 64, kBN);
+        ok = ok && make_map(&b.ut_mn, ut, true, b.c, b.r, b.batch, b.ldu, 64, 64);
+        ok = ok && make_map(&b.qb_a, b.Qb, true, b.r, b.r, b.batch, b.ldr, 64, kBM);
+        for (int g = 0; g < 2; ++g) {
+            ok = ok && make_map(&b.ga[g], b.G[g], false, b.r, b.r, b.batch, b.ldr, 32, kBM);
+            ok = ok && make_map(&b.gb[g], b.G[g], false, b.r, b.r, b.batch, b.ldr, 32, kBN);
+            ok = ok && make_map(&b.qb[g], b.Q[g], false, b.r, b.r, b.batch, b.ldr, 32, kBN);
+        }
+        ok = ok && make_map(&b.pa, b.P, false, b.r, b.r, b.batch, b.ldr, 32, kBM);
+        ok = ok && make_map(&b.pb, b.P, false, b.r, b.r, b.batch, b.ldr, 32, kBN);
+        ok = ok && make_map(&b.tb, b.T, false, b.r, b.r, b.batch, b.ldr, 32, kBN);
+    }
+    ok = ok && cudaMallocHost(&p->h_pinned, sizeof(void*) * 3 * n) == cudaSuccess;
+    ok = ok && cudaEventCreateWithFlags(&p->upload_ev, cudaEventDisableTiming) == cudaSuccess;
+    ok = ok && gemm_prepare(p->device) == cudaSuccess;
+    ok = ok && cudaDeviceSynchronize() == cudaSuccess;
+    if (!ok) {
+        cudaGetLastError();
+        free_plan(p);
+        return MUON_ERR_CUDA;
+    }
+    p->h_cache.assign(3 * n, nullptr);
+    *out = p;
+    return MUON_OK;
+}
+
+void muon_plan_destroy(muon_plan p) {
+    if (!p) return;
+    cudaDeviceSynchronize();
+    free_plan(p);
+}
+
+muon_status muon_rownorm_step(muon_plan p, float* const* params, const void* const* grads, float* const* momentum,
+                              float lr, float wd, float mu, float eps, void* stream) {
+    if (!p) return MUON_ERR_INVALID_ARG;
+    if (!finite_nonneg(lr) || !finite_nonneg(wd) || !std::isfinite(mu) || mu < 0.f || mu >= 1.f ||
+        !std::isfinite(eps) || eps <= 0.f)
+        return MUON_ERR_INVALID_ARG;
+    muon_status st = check_pointers(p, params, grads, momentum);
+    if (st != MUON_OK) return st;
+    if ((st = check_device(p)) != MUON_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((st = upload_pointers(p, params, grads, momentum, s)) != MUON_OK) return st;
+    muon_plan_s::StepEvents* se = nullptr;
+    if (p->opts.timing && !(se = next_events(p))) return MUON_ERR_CUDA;
+    if (se) {
+        se->ns = false;
+        MUON_TRY(cudaEventRecord(se->e[0], s));
+    }
+    int launches = 0;
+    ElemArgs a = elem_args(p, p->rn_rows, mu, lr, wd, eps);
+    MUON_TRY(launch_rownorm_rows(a, p->rn_rows.blocks, s));
+    launches += p->rn_rows.blocks > 0;
+    a = elem_args(p, p->rn_stats, mu, lr, wd, eps);
+    a.partials = p->cpartials;
+    MUON_TRY(launch_rownorm_colstats(a, p->rn_stats.blocks, s));
+    a = elem_args(p, p->rn_final, mu, lr, wd, eps);
+    a.partials = p->cpartials;
+    MUON_TRY(launch_rownorm_colfinal(a, p->rn_final.blocks, s));
+    a = elem_args(p, p->rn_apply, mu, lr, wd, eps);
+    MUON_TRY(launch_rownorm_colapply(a, p->rn_apply.blocks, s));
+    launches += p->rn_stats.blocks > 0 ? 3 : 0;
+    if (se) MUON_TRY(cudaEventRecord(se->e[5], s));
+    p->last_launches = launches;
+    return MUON_OK;
+}
+
+muon_status muon_step(muon_plan p, float* const* params, const void* const* grads, float* const* momentum, float lr,
+                      float wd, float mu, int32_t ns_steps, muon_mode mode, void* stream) {
+    if (!p) return MUON_ERR_INVALID_ARG;
+    if (mode == MUON_MODE_ROWNORM) return muon_rownorm_step(p, params, grads, momentum, lr, wd, mu, 1e-8f, stream);
+    if (mode != MUON_MODE_NS) return MUON_ERR_INVALID_ARG;
+    if (!finite_nonneg(lr) || !finite_nonneg(wd) || !std::isfinite(mu) || mu < 0.f || mu >= 1.f ||
+        ns_steps < 0 || ns_steps > kMaxNsSteps)
+        return MUON_ERR_INVALID_ARG;
+    muon_status st = check_pointers(p, params, grads, momentum);
+    if (st != MUON_OK) return st;
+    if ((st = check_device(p)) != MUON_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((st = upload_pointers(p, params, grads, momentum, s)) != MUON_OK) return st;
+    muon_plan_s::StepEvents* se = nullptr;
+    if (p->opts.timing && !(se = next_events(p))) return MUON_ERR_CUDA;
+    const int n = (int)p->shapes.size();
+    int launches = 0;
+
+    // ---- momentum, Nesterov, sum of squares, bf16 X0 (oriented)
+    if (se) {
+        se->ns = true;
+        MUON_TRY(cudaEventRecord(se->e[0], s));
+    }
+    ElemArgs a = elem_args(p, p->mom_rows, mu, lr, wd, 0.f);
+    MUON_TRY(launch_momentum_rows(a, p->mom_rows.blocks, s));
+    launches += p->mom_rows.blocks > 0;
+    a = elem_args(p, p->mom_tiles, mu, lr, wd, 0.f);
+    MUON_TRY(launch_momentum_tiles(a, p->mom_tiles.blocks, s));
+    launches += p->mom_tiles.blocks > 0;
+    a = elem_args(p, p->all, mu, lr, wd, 0.f);
+    MUON_TRY(launch_norm_finalize(a, s));
+    ++launches;
+    if (se) MUON_TRY(cudaEventRecord(se->e[1], s));
+
+    double fl_syrk = 0, fl_rr = 0, fl_final = 0;
+    for (auto& b : p->buckets) {
+        const double r = b.r, c = b.c;
+        fl_syrk += b.batch * r * r * c;
+        fl_final += b.batch * 2.0 * r * r * c;
+        const int J = ns_steps;
+        const int nrr = J == 0 ? 0 : (J == 1 ? 1 : 4 * J - 3);
+        fl_rr += b.batch * (double)nrr * r * r * r;
+    }
+    if (se) {
+        p->flops[0] += fl_syrk;
+        p->flops[1] += fl_rr;
+        p->flops[2] += fl_final;
+    }
+
+    // ---- G0 = alpha^2 X0 X0^T (lower triangle, mirrored), all buckets in one launch
+    {
+        Grouper g(p, s, false);
+        for (auto& b : p->buckets) {
+            GemmProblem q = problem(b.r, b.r, b.c, b.batch, true, kEpiSyrk);
+            q.C = b.G[0];
+            q.strideC = (long long)b.r * b.ldr;
+            q.ldc = b.ldr;
+            q.alpha = p->alpha + b.slot_base;
+            g.add(b.ut_a, b.ut_b, q);
+        }
+        g.flush();
+        if (g.st != MUON_OK) return g.st;
+        launches += g.launches;
+    }
+    if (se) MUON_TRY(cudaEventRecord(se->e[2], s));
+
+    // ---- Newton-Schulz in the Gram space
+    const int J = ns_steps;
+    int gc = 0;   // current G buffer
+    int qc = 0;   // current Q buffer
+    for (int k = 1; k <= J; ++k) {
+        {   // P = aI + bG + cG^2 (at k = 1 this is also Q_1)
+            Grouper g(p, s, true);
+            for (auto& b : p->buckets) {
+                GemmProblem q = problem(b.r, b.r, b.r, b.batch, true, kEpiPoly);
+                q.strideC = (long long)b.r * b.ldr;
+                q.ldc = b.ldr;
+                q.C = b.P;
+                if (k == 1 && J > 1) q.C2 = b.Q[0];
+                if (k == 1 && J == 1) {
+                    q.Cb = b.Qb;
+                    q.ldcb = b.ldr;
+                    q.strideCb = (long long)b.r * b.ldr;
+                }
+                q.Gin = b.G[gc];
+                q.strideG = (long long)b.r * b.ldr;
+                q.ldg = b.ldr;
+                q.coef_a = kNsA;
+                q.coef_b = kNsB;
+                q.coef_c = kNsC;
+                g.add(b.ga[gc], b.gb[gc], q);
+            }
+            g.flush();
+            if (g.st != MUON_OK) return g.st;
+            launches += g.launches;
+        }
+        {   // Q' = P Q (k >= 2) and T = P P (k < J)
+            Grouper g(p, s, true);
+            for (auto& b : p->buckets) {
+                if (k >= 2) {
+                    GemmProblem q = problem(b.r, b.r, b.r, b.batch, true, kEpiPlain);
+                    q.strideC = (long long)b.r * b.ldr;
+                    q.ldc = b.ldr;
+                    if (k < J) {
+                        q.C = b.Q[qc ^ 1];
+                    } else {
+                        q.Cb = b.Qb;
+                        q.ldcb = b.ldr;
+                        q.strideCb = (long long)b.r * b.ldr;
+                    }
+                    g.add(b.pa, b.qb[qc], q);
+                }
+                if (k < J) {
+                    GemmProblem q = problem(b.r, b.r, b.r, b.batch, true, kEpiPlain);
+                    q.strideC = (long long)b.r * b.ldr;
+                    q.ldc = b.ldr;
+                    q.C = b.T;
+                    g.add(b.pa, b.pb, q);
+                }
+            }
+            g.flush();
+            if (g.st != MUON_OK) return g.st;
+            launches += g.launches;
+            if (k >= 2) qc ^= 1;
+        }
+        if (k < J) {   // G' = G T
+            Grouper g(p, s, true);
+            for (auto& b : p->buckets) {
+                GemmProblem q = problem(b.r, b.r, b.r, b.batch, true, kEpiPlain);
+                q.strideC = (long long)b.r * b.ldr;
+                q.ldc = b.ldr;
+                q.C = b.G[gc ^ 1];
+                g.add(b.ga[gc], b.tb, q);
+            }
+            g.flush();
+            if (g.st != MUON_OK) return g.st;
+            launches += g.launches;
+            gc ^= 1;
+        }
+    }
+    if (J == 0) {
+        for (auto& b : p->buckets) {
+            MUON_TRY(launch_identity_bf16(b.Qb, b.r, b.ldr, b.batch, s));
+            ++launches;
+        }
+    }
+    if (se) MUON_TRY(cudaEventRecord(se->e[3], s));
+
+    // ---- O = alpha Q X0, fused W <- W - lr (s O + wd W) in the stored layout
+    {
+        Grouper g(p, s, false);
+        float* const* W = reinterpret_cast<float* const*>(p->d_ptrs + 2 * n);
+        for (auto& b : p->buckets) {
+            GemmProblem q = problem(b.r, b.c, b.r, b.batch, false, kEpiApply);
+            q.b_mn = 1;
+            q.alpha = p->alpha + b.slot_base;
+            q.item_mat = b.d_item_mat;
+            q.W = W;
+            q.transposed = p->d_transposed;
+            q.Odbg = b.Odbg;
+            q.lr = lr;
+            q.wd = wd;
+            q.scale = 0.2f * std::sqrt((float)b.c);
+            g.add(b.qb_a, b.ut_mn, q);
+        }
+        g.flush();
+        if (g.st != MUON_OK) return g.st;
+        launches += g.launches;
+    }
+    if (se) MUON_TRY(cudaEventRecord(se->e[4], s));
+    p->last_launches = launches;
+    return MUON_OK;
+}
+
+muon_status muon_sync(muon_plan p, void* stream) {
+    if (!p) return MUON_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MUON_ERR_CUDA;
+    int st = 0;
+    if (cudaMemcpy(&st, p->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MUON_ERR_CUDA;
+    if (st != 0) {
+        if (cudaMemset(p->status, 0, sizeof(int)) != cudaSuccess) return MUON_ERR_CUDA;
+        return MUON_ERR_TIMEOUT;
+    }
+    return MUON_OK;
+}
+
+muon_status muon_debug_copy_update(muon_plan p, int32_t i, float* dst, void* stream) {
+    if (!p || !dst || i < 0 || i >= (int)p->shapes.size()) return MUON_ERR_INVALID_ARG;
+    if (!p->opts.keep_update) return MUON_ERR_INVALID_ARG;
+    const Bucket& b = p->buckets[p->mat_bucket[i]];
+    const size_t numel = (size_t)b.r * b.c;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(dst, b.Odbg + (size_t)p->mat_item[i] * numel, numel * sizeof(float), cudaMemcpyDefault, s) !=
+        cudaSuccess)
+        return MUON_ERR_CUDA;
+    return cudaStreamSynchronize(s) == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
+}
+
+muon_status muon_debug_copy_workspace(muon_plan p, int32_t i, int32_t which, void* dst, int32_t* ld,
+                                      void* stream) {
+    if (!p || !dst || !ld || i < 0 || i >= (int)p->shapes.size() || which < 0 || which > 8)
+        return MUON_ERR_INVALID_ARG;
+    const Bucket& b = p->buckets[p->mat_bucket[i]];
+    const int item = p->mat_item[i];
+    const size_t rr = (size_t)b.r * b.ldr;
+    const void* src = nullptr;
+    size_t bytes = 0;
+    *ld = b.ldr;
+    switch (which) {
+        case 0:
+            src = p->ut + b.ut_off + (size_t)item * b.r * b.ldu;
+            bytes = (size_t)b.r * b.ldu * 2;
+            *ld = b.ldu;
+            break;
+        case 1: case 2: src = b.G[which - 1] + item * rr; bytes = rr * 4; break;
+        case 3: src = b.P + item * rr; bytes = rr * 4; break;
+        case 4: src = b.T + item * rr; bytes = rr * 4; break;
+        case 5: case 6: src = b.Q[which - 5] + item * rr; bytes = rr * 4; break;
+        case 7: src = b.Qb + item * rr; bytes = rr * 2; break;
+        case 8: src = p->alpha + p->mats[i].slot; bytes = 4; *ld = 1; break;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDefault, s) != cudaSuccess) return MUON_ERR_CUDA;
+    return cudaStreamSynchronize(s) == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
+}
+
+muon_status muon_plan_info(muon_plan p, muon_plan_info_t* info) {
+    if (!p || !info) return MUON_ERR_INVALID_ARG;
+    info->n_matrices = (int32_t)p->shapes.size();
+    info->n_buckets = (int32_t)p->buckets.size();
+    info->workspace_bytes = (int64_t)p->ws_bytes;
+    info->launches_last_step = p->last_launches;
+    info->sm_count = p->sm_count;
+    return MUON_OK;
+}
+
+muon_status muon_stage_times(muon_plan p, float* ms, double* flops, int32_t n_stages) {
+    if (!p || !ms || n_stages < 0 || n_stages > 5) return MUON_ERR_INVALID_ARG;
+    if (p->n_timed == 0) return MUON_ERR_INVALID_ARG;
+    double acc[5] = {0, 0, 0, 0, 0};
+    for (size_t g = 0; g < p->n_timed; ++g) {
+        const auto& se = p->evs[g];
+        float t = 0.f;
+        if (se.ns) {
+            if (cudaEventSynchronize(se.e[4]) != cudaSuccess) return MUON_ERR_CUDA;
+            for (int k = 0; k < 4; ++k) {
+                if (cudaEventElapsedTime(&t, se.e[k], se.e[k + 1]) != cudaSuccess) return MUON_ERR_CUDA;
+                acc[k] += t;
+            }
+        } else {
+            if (cudaEventSynchronize(se.e[5]) != cudaSuccess) return MUON_ERR_CUDA;
+            if (cudaEventElapsedTime(&t, se.e[0], se.e[5]) != cudaSuccess) return MUON_ERR_CUDA;
+            acc[4] += t;
+        }
+    }
+    for (int k = 0; k < n_stages; ++k) ms[k] = (float)acc[k];
+    if (flops)
+        for (int k = 0; k < 3; ++k) flops[k] = p->flops[k];
+    p->n_timed = 0;
+    p->flops[0] = p->flops[1] = p->flops[2] = 0;
+    return MUON_OK;
+}
+
+}  // extern "C"

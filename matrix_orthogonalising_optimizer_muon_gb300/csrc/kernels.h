@@ -1,0 +1,129 @@
+// Kernel parameter blocks and launch entry points shared by the host planner
+// (capi.cu) and the kernel translation units (gemm.cu, elementwise.cu).
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace muon {
+
+// ------------------------------------------------------------------ GEMM
+// Tile of one tensor-core product: BM x BN output, one tcgen05.mma M=128 N=256.
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kStages = 4;
+constexpr int kMaxProblems = 8;
+constexpr int kGemmThreads = 192;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
+
+enum Epilogue : int {
+    kEpiSyrk = 0,    // C = alpha^2 * acc                        (G0 = X0 X0^T)
+    kEpiPoly = 1,    // C = a I + b Gin + c * acc                 (P = aI + bG + cG^2)
+    kEpiPlain = 2,   // C = acc                                   (P Q, P P, G T)
+    kEpiApply = 3,   // W -= lr (s * alpha * acc + wd W) in the stored layout (final O = Q X0)
+};
+
+// One batched product C_item = A_item * B_item^T (A: M x K, B: N x K as loaded by
+// TMA; B may be MN-major, i.e. stored K x N).  With sym = 1 the output is
+// symmetric (M = N): only tiles touching the lower triangle are computed and
+// each lower element is also written to its mirror position.
+struct GemmProblem {
+    int M, N, K, batch;
+    int tiles_m, tiles_n, tiles_per_item, tile_begin;
+    int sym, b_mn, epi, pad0;
+    // fp32 outputs (row-major, leading dim ldc, batch stride strideC); C2 optional second copy
+    float* C;
+    float* C2;
+    long long strideC;
+    int ldc, ldcb;
+    // optional bf16 copy of the output (row-major, leading dim ldcb)
+    __nv_bfloat16* Cb;
+    long long strideCb;
+    // kEpiPoly: G input of the polynomial
+    const float* Gin;
+    long long strideG;
+    int ldg, pad1;
+    // per-item 1/||U||_F (kEpiSyrk uses its square, kEpiApply the value)
+    const float* alpha;
+    float coef_a, coef_b, coef_c, pad2;
+    // kEpiApply
+    const int* item_mat;               // item -> plan matrix index
+    float* const* W;                   // plan matrix index -> params pointer
+    const unsigned char* transposed;   // plan matrix index -> stored as c x r
+    float* Odbg;                       // optional O (fp32, stored layout), item stride M*N
+    float lr, wd, scale, pad3;
+};
+
+struct GemmLaunch {
+    CUtensorMap mapA[kMaxProblems];
+    CUtensorMap mapB[kMaxProblems];
+    GemmProblem prob[kMaxProblems];
+    int nprob;
+    int total_tiles;
+    int* status;
+    int pad;
+};
+
+size_t gemm_smem_bytes(bool tf32);
+cudaError_t gemm_prepare(int device);   // sets the dynamic shared-memory limit once
+cudaError_t gemm_launch(const GemmLaunch& L, bool tf32, int grid, cudaStream_t s);
+
+// ------------------------------------------------------------------ elementwise
+// Per plan matrix, resident on the device.
+struct MatDev {
+    long long m, n;          // stored shape
+    int r, c;                // oriented: r = min, c = max
+    int transposed;          // m > n
+    int slot;                // bucket-item slot (alpha table)
+    long long ut_off;        // element offset of X0 (bf16, r x ldu) in the X0 workspace
+    int ldu;                 // leading dim of X0 rows (multiple of 8)
+    int nblk;                // momentum blocks of this matrix (= its partial sums)
+    long long part_off;      // offset of its momentum partial sums
+    long long cpart_off;     // offset of its RowNorm column partial sums (m > n)
+    long long inv_off;       // offset of its RowNorm per-column inverse norms (m > n)
+    float scale;             // 0.2 * sqrt(c)
+    int pad;
+};
+
+struct ElemArgs {
+    const MatDev* mats;
+    const int* list;           // plan matrix indices covered by this launch
+    int nlist;
+    int pad;
+    const long long* list_blk; // prefix block offsets, nlist + 1 entries
+    const void* const* G;      // per plan matrix
+    float* const* M;
+    float* const* W;
+    __nv_bfloat16* ut;         // X0 workspace
+    float* partials;           // block partial sums
+    float* alpha;              // per slot
+    float* rowinv;             // per-row inverse norms (RowNorm, transposed matrices)
+    float mu, lr, wd, eps;
+    int grad_bf16;
+    int pad2;
+};
+
+// Momentum + Nesterov + partial sum of squares + bf16 X0 in the oriented layout.
+cudaError_t launch_momentum_rows(const ElemArgs& a, long long blocks, cudaStream_t s);   // m <= n
+cudaError_t launch_momentum_tiles(const ElemArgs& a, long long blocks, cudaStream_t s);  // m > n (transpose)
+// alpha[slot] = 1 / sqrt(sum of partials) (0 for a zero input); one warp per matrix.
+cudaError_t launch_norm_finalize(const ElemArgs& a, cudaStream_t s);
+// Fill a batch of r x r bf16 identities (ns_steps = 0).
+cudaError_t launch_identity_bf16(__nv_bfloat16* q, int r, int ld, int batch, cudaStream_t s);
+// RowNorm: rows of the stored matrix (m <= n), one block per row, fused apply.
+cudaError_t launch_rownorm_rows(const ElemArgs& a, long long blocks, cudaStream_t s);
+// RowNorm, m > n: column statistics, finalize, apply.
+cudaError_t launch_rownorm_colstats(const ElemArgs& a, long long blocks, cudaStream_t s);
+cudaError_t launch_rownorm_colfinal(const ElemArgs& a, long long blocks, cudaStream_t s);
+cudaError_t launch_rownorm_colapply(const ElemArgs& a, long long blocks, cudaStream_t s);
+
+// Block geometry the planner needs to size grids and partial-sum buffers.
+constexpr int kElemThreads = 256;
+constexpr int kMomVecPerThread = 4;                                  // 8-element vectors per thread
+constexpr long long kMomElemsPerBlock = 8LL * kElemThreads * kMomVecPerThread;   // rows kernel
+constexpr int kTile = 64;                                            // transpose tile (64 x 64)
+constexpr int kColSlab = 64;                                         // RowNorm column-stat rows per block
+constexpr int kColWidth = 4 * kElemThreads;                          // columns per column-stat block
+constexpr long long kApplyElemsPerBlock = 4LL * kElemThreads * 4;    // RowNorm col apply
+
+}  // namespace muon

@@ -1,0 +1,72 @@
+"""Host-side checks that need no GPU: the library builds, loads and exports every
+entry point declared in include/muon.h; argument validation that happens before
+any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import matrix_orthogonalising_optimizer_muon_gb300 as mu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "muon.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(muon_[a-z_]+)\s*\(", src)))
+
+
+def test_header_and_binding_agree():
+    names = declared_functions()
+    assert "muon_step" in names and "muon_plan_create" in names and "muon_rownorm_step" in names
+    assert sorted(mu.EXPORTED) == names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = mu.load()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings():
+    lib = mu.load()
+    for code in range(7):
+        s = lib.muon_status_string(code).decode()
+        assert s.startswith("MUON_")
+    assert b"UNKNOWN" in lib.muon_status_string(99)
+
+
+def test_plan_create_rejects_bad_arguments_before_cuda():
+    lib = mu.load()
+    h = ctypes.c_void_p()
+    shapes = (mu.MuonShape * 2)(mu.MuonShape(4, 8), mu.MuonShape(0, 3))
+    assert lib.muon_plan_create(shapes, 2, mu.MUON_BF16, None, ctypes.byref(h)) == mu.MUON_ERR_INVALID_ARG
+    assert lib.muon_plan_create(shapes, 0, mu.MUON_BF16, None, ctypes.byref(h)) == mu.MUON_ERR_INVALID_ARG
+    assert lib.muon_plan_create(shapes, 1, 7, None, ctypes.byref(h)) == mu.MUON_ERR_UNSUPPORTED
+    assert lib.muon_plan_create(None, 1, mu.MUON_BF16, None, ctypes.byref(h)) == mu.MUON_ERR_INVALID_ARG
+    assert lib.muon_step(None, None, None, None, 0.1, 0.1, 0.9, 5, 0, None) == mu.MUON_ERR_INVALID_ARG
+    assert lib.muon_sync(None, None) == mu.MUON_ERR_INVALID_ARG
+    big = (mu.MuonShape * 1)(mu.MuonShape(1 << 21, 4))
+    assert lib.muon_plan_create(big, 1, mu.MUON_F32, None, ctypes.byref(h)) == mu.MUON_ERR_UNSUPPORTED
+
+
+def test_schedule_helper():
+    class FakePlan:
+        def __init__(self):
+            self.calls = []
+
+        def step(self, *a, **k):
+            self.calls.append("ns")
+
+        def rownorm_step(self, *a, **k):
+            self.calls.append("rownorm")
+
+    p = FakePlan()
+    sched = mu.PeriodicRowNormMuon(p, k=4)
+    modes = [sched.step([], [], [], 0.02, 0.1) for _ in range(8)]
+    assert modes == ["ns", "rownorm", "rownorm", "rownorm"] * 2
+    assert p.calls == modes
+    with pytest.raises(ValueError):
+        mu.PeriodicRowNormMuon(p, k=0)

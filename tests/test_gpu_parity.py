@@ -1,0 +1,233 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on seeded
+inputs.  Bars: relative Frobenius error <= 2e-2 on the orthogonalised update O
+(bf16/tf32 tensor-core path) and <= 1e-5 on momentum, on weights given the
+GPU's own O, and on RowNorm outputs."""
+import numpy as np
+import pytest
+
+from oracle import muon_ref as R
+from tests.gpu_util import (LR, WD, MU, check_ns_matrix, check_rownorm_matrix, host_inputs,
+                            nesterov_u, rel, run_step)
+
+pytestmark = pytest.mark.gpu
+
+TOL_O = 2e-2
+TOL_FP32 = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import matrix_orthogonalising_optimizer_muon_gb300 as lib
+    lib.load()
+
+
+def assert_ns(res, i, tol_o=TOL_O, ns_steps=5):
+    e = check_ns_matrix(res, i, ns_steps, tol_o)
+    assert e["m"] <= TOL_FP32, (i, e)
+    assert e["o"] <= tol_o, (i, e)
+    assert e["w_given_o"] <= TOL_FP32, (i, e)
+    assert e["w_e2e"] <= e["w_bound"], (i, e)
+    return e
+
+
+# --------------------------------------------------------------- stage by stage
+def test_stages_ns0_x0_alpha_gram_and_final_product():
+    """ns_steps = 0: X0 workspace (momentum kernels), 1/||U||, G0 (SYRK, bf16 K-major
+    operands) and O = X0 through the final product (MN-major bf16 operand)."""
+    shapes = [(300, 700), (700, 300), (128, 256)]
+    res = run_step(shapes, "bf16", base_seed=11, ns_steps=0)
+    plan = res["plan"]
+    for i, (m, n) in enumerate(shapes):
+        u = nesterov_u(res["inputs"][i])
+        ut, _ = R.orient(u)
+        x_ws = plan.debug_workspace(i, 0).double().numpy()
+        # bf16 round-to-nearest of the fp32 U: within one bf16 half-ulp (+fp32 noise)
+        assert np.all(np.abs(x_ws - ut) <= np.abs(ut) * (2.0 ** -8) + 1e-30), i
+        alpha = float(plan.debug_workspace(i, 8)[0])
+        assert abs(alpha * np.linalg.norm(u) - 1) < 1e-5, i
+        g0 = plan.debug_workspace(i, 1).double().numpy()
+        g_ref = (x_ws @ x_ws.T) * alpha ** 2           # from the GPU's own bf16 operand
+        assert rel(g0, g_ref) < 2e-3, i
+        assert np.array_equal(g0, g0.T), i             # mirrored lower triangle
+        qb = plan.debug_workspace(i, 7).double().numpy()
+        assert np.array_equal(qb, np.eye(min(m, n))), i
+        e = assert_ns(res, i, tol_o=1e-2, ns_steps=0)
+        assert e["o"] < 1e-2
+
+
+def test_stages_ns1_polynomial_epilogue():
+    """ns_steps = 1: P1 = aI + bG0 + cG0^2 (tf32 product + polynomial epilogue)."""
+    shapes = [(384, 1000), (1000, 384)]
+    res = run_step(shapes, "bf16", base_seed=12, ns_steps=1)
+    plan = res["plan"]
+    a, b, c = R.NS_COEFFS
+    for i in range(len(shapes)):
+        g0 = plan.debug_workspace(i, 1).double().numpy()
+        p1 = plan.debug_workspace(i, 3).double().numpy()
+        r = g0.shape[0]
+        p_ref = a * np.eye(r) + b * g0 + c * (g0 @ g0)
+        assert rel(p1, p_ref) < 2e-3, i
+        qb = plan.debug_workspace(i, 7).double().numpy()
+        assert rel(qb, p_ref) < 1e-2, i
+        assert_ns(res, i, ns_steps=1)
+
+
+def test_stages_ns2_products():
+    """ns_steps = 2: T = P1 P1, G1 = G0 T, Q2 = P2 P1 (all tf32 symmetric products)."""
+    shapes = [(256, 640)]
+    res = run_step(shapes, "f32", base_seed=13, ns_steps=2)
+    plan = res["plan"]
+    a, b, c = R.NS_COEFFS
+    g0 = plan.debug_workspace(0, 1).double().numpy()
+    r = g0.shape[0]
+    p1 = a * np.eye(r) + b * g0 + c * g0 @ g0
+    t = plan.debug_workspace(0, 4).double().numpy()
+    assert rel(t, p1 @ p1) < 3e-3
+    g1 = plan.debug_workspace(0, 2).double().numpy()
+    assert rel(g1, g0 @ p1 @ p1) < 5e-3
+    p2 = plan.debug_workspace(0, 3).double().numpy()
+    assert rel(p2, a * np.eye(r) + b * g1 + c * g1 @ g1) < 3e-3
+    qb = plan.debug_workspace(0, 7).double().numpy()
+    assert rel(qb, p2 @ p1) < 1e-2
+    assert_ns(res, 0, ns_steps=2)
+
+
+# --------------------------------------------------------------- full steps
+def test_single_256x1024_fp32_grads():
+    """The 256 x 1024 single-matrix workload (fp32 W, G, M; seed 0)."""
+    import workloads
+    wl = workloads.WORKLOADS["single"]
+    inputs = [workloads.matrix_inputs(wl, 0, 0)]
+    res = run_step(list(wl.shapes), "f32", inputs=inputs)
+    e = assert_ns(res, 0)
+    assert e["o"] < 1e-2
+
+
+RAGGED = [(7, 13), (13, 7), (130, 300), (300, 130), (384, 384), (129, 1000), (1000, 129),
+          (1, 64), (64, 1), (256, 1024), (520, 2100)]
+
+
+@pytest.mark.parametrize("grad_dtype", ["bf16", "f32"])
+def test_mixed_ragged_plan_ns5(grad_dtype):
+    """Many buckets in one plan, ragged tails in every dimension, both orientations."""
+    res = run_step(RAGGED, grad_dtype, base_seed=21)
+    for i in range(len(RAGGED)):
+        assert_ns(res, i)
+
+
+def test_batched_bucket_ns5():
+    """Several same-shape matrices batched in one bucket (grouped launch items)."""
+    shapes = [(200, 520)] * 5 + [(520, 200)] * 3
+    res = run_step(shapes, "bf16", base_seed=22)
+    for i in range(len(shapes)):
+        assert_ns(res, i)
+
+
+@pytest.mark.parametrize("ns_steps", [3, 10])
+def test_other_ns_step_counts(ns_steps):
+    res = run_step([(192, 576), (576, 192)], "bf16", base_seed=23, ns_steps=ns_steps)
+    for i in range(2):
+        assert_ns(res, i, ns_steps=ns_steps)
+
+
+def test_zero_input_gives_weight_decay_only():
+    import torch
+    shapes = [(64, 160), (160, 64)]
+    inputs = [(w, torch.zeros_like(g), torch.zeros_like(m)) for w, g, m in host_inputs(shapes, "bf16", 24)]
+    res = run_step(shapes, "bf16", inputs=inputs)
+    for i in range(2):
+        assert float(res["O"][i].abs().max()) == 0.0
+        w0 = inputs[i][0].double().numpy()
+        assert rel(res["W"][i].numpy(), (1 - LR * WD) * w0) < 1e-6
+
+
+def test_deterministic():
+    shapes = [(300, 700), (700, 300)]
+    a = run_step(shapes, "bf16", base_seed=25, keep_update=False)
+    b = run_step(shapes, "bf16", base_seed=25, keep_update=False)
+    for i in range(2):
+        assert np.array_equal(a["W"][i].numpy(), b["W"][i].numpy())
+        assert np.array_equal(a["M"][i].numpy(), b["M"][i].numpy())
+
+
+# --------------------------------------------------------------- RowNorm
+ROWNORM_SHAPES = [(7, 13), (13, 7), (256, 1024), (1024, 256), (130, 20000), (20000, 130), (96, 96),
+                  (33, 4097)]
+
+
+@pytest.mark.parametrize("grad_dtype", ["bf16", "f32"])
+def test_rownorm_step(grad_dtype):
+    res = run_step(ROWNORM_SHAPES, grad_dtype, base_seed=31, mode="rownorm", keep_update=False)
+    for i in range(len(ROWNORM_SHAPES)):
+        e = check_rownorm_matrix(res, i)
+        assert e["m"] <= TOL_FP32 and e["w"] <= TOL_FP32, (ROWNORM_SHAPES[i], e)
+
+
+def test_rownorm_eps_floor():
+    """Rows whose norm is below eps are divided by eps, not normalised."""
+    import torch
+    shapes = [(8, 32), (32, 8)]
+    inputs = [(w, g * 1e-9, m * 0) for w, g, m in host_inputs(shapes, "f32", 32)]
+    eps = 1e-3
+    res = run_step(shapes, "f32", inputs=inputs, mode="rownorm", eps=eps, keep_update=False)
+    for i in range(2):
+        e = check_rownorm_matrix(res, i, eps=eps)
+        assert e["m"] <= TOL_FP32 and e["w"] <= TOL_FP32, e
+
+
+def test_periodic_rownorm_schedule_matches_oracle():
+    """K = 4 over 8 steps (NS at t = 0 and 4), fresh gradients each step."""
+    import torch
+    import matrix_orthogonalising_optimizer_muon_gb300 as lib
+    from workloads import gen_tensor, seed_of, G_STD
+    shapes = [(96, 320), (320, 96)]
+    inputs = host_inputs(shapes, "bf16", 33)
+    plan = lib.MuonPlan(shapes, "bf16")
+    sched = lib.PeriodicRowNormMuon(plan, k=4)
+    W = [x[0].cuda() for x in inputs]
+    M = [x[2].cuda() for x in inputs]
+    w_ref = [x[0].double().numpy() for x in inputs]
+    m_ref = [x[2].double().numpy() for x in inputs]
+    for t in range(8):
+        grads = [gen_tensor(s, G_STD, seed_of(33, t, i, "G"), dtype="bf16") for i, s in enumerate(shapes)]
+        mode = sched.step(W, [g.cuda() for g in grads], M, LR, WD)
+        assert mode == R.schedule_mode(t, 4)
+        for i in range(2):
+            w_ref[i], m_ref[i], _ = R.muon_step(w_ref[i], grads[i].double().numpy(), m_ref[i], LR, WD, MU,
+                                                5, mode, 1e-8)
+    plan.sync()
+    for i in range(2):
+        assert rel(M[i].cpu().numpy(), m_ref[i]) <= TOL_FP32
+        # two NS steps with O at <= 2e-2 each: W within lr * s * 2e-2 * ||O|| per NS step
+        bound = 2 * LR * R.update_scale(*shapes[i]) * TOL_O * np.sqrt(min(shapes[i])) / np.linalg.norm(w_ref[i])
+        assert rel(W[i].cpu().numpy(), w_ref[i]) <= bound + 1e-5
+
+
+# --------------------------------------------------------------- host validation through the ABI
+def test_invalid_arguments_are_rejected_without_touching_buffers():
+    import torch
+    import matrix_orthogonalising_optimizer_muon_gb300 as lib
+    shapes = [(32, 64)]
+    inp = host_inputs(shapes, "bf16", 41)
+    plan = lib.MuonPlan(shapes, "bf16")
+    W, G, M = inp[0][0].cuda(), inp[0][1].cuda(), inp[0][2].cuda()
+    W0, M0 = W.clone(), M.clone()
+    with pytest.raises(lib.MuonError) as ei:
+        plan.step([W], [G], [M], LR, WD, 1.0)
+    assert ei.value.code == lib.MUON_ERR_INVALID_ARG
+    with pytest.raises(lib.MuonError):
+        plan.step([W], [G], [M], LR, WD, MU, ns_steps=17)
+    with pytest.raises(lib.MuonError):
+        plan.step([W], [G], [M], float("nan"), WD, MU)
+    with pytest.raises(lib.MuonError):
+        plan.rownorm_step([W], [G], [M], LR, WD, MU, eps=0.0)
+    with pytest.raises(lib.MuonError):      # params aliasing momentum
+        plan.step([W], [G], [W], LR, WD, MU)
+    with pytest.raises(ValueError):
+        plan.step([W], [G.float()], [M], LR, WD, MU)
+    torch.cuda.synchronize()
+    assert torch.equal(W, W0) and torch.equal(M, M0)
+    plan.sync()
