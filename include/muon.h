@@ -127,13 +127,14 @@ muon_status muon_debug_copy_update(muon_plan p, int32_t i, float* dst, void* str
  * after the last step, into dst (host or device memory), for step-by-step
  * parity checks.  Synchronises stream.  which:
  *   0 X0 workspace: bf16 U in the oriented layout, r rows of ld elements (unnormalised)
- *   1 G buffer 0, 2 G buffer 1, 3 P, 4 T, 5 Q buffer 0, 6 Q buffer 1: fp32, r rows of ld
+ *   1 G buffer 0, 2 G buffer 1: fp16 s*G with s = 2^round(log2 r), r rows of ld
+ *   3 P, 4 T, 5 Q buffer 0, 6 Q buffer 1: fp16, r rows of ld
  *   7 bf16 Q of the final product: r rows of ld
  *   8 1/||U||_F: one fp32
  * *ld receives the leading dimension (elements) of the copied rows; the copy
- * is r*ld elements (one for which = 8) of 2 (bf16) or 4 (fp32) bytes.
- * After a step with ns_steps = J, buffer 1 holds G_0 = X0 X0^T when J <= 1,
- * buffer 3 holds P_J, and buffer 7 holds Q_J.
+ * is r*ld elements of 2 bytes (one 4-byte float for which = 8).
+ * After a step with ns_steps = J, G buffer 0 holds s*G_0 when J <= 2, G
+ * buffer 1 holds s*G_1 when J >= 2, buffer 3 holds P_J and buffer 7 holds Q_J.
  */
 muon_status muon_debug_copy_workspace(muon_plan p, int32_t i, int32_t which, void* dst, int32_t* ld,
                                       void* stream);

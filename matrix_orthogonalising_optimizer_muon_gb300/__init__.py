@@ -221,29 +221,31 @@ class MuonPlan:
         return out
 
     def debug_workspace(self, i: int, which: int, stream=None):
-        """A workspace buffer of matrix i (``muon_debug_copy_workspace``) as a CPU tensor
-        of r rows (fp32; the bf16 buffers 0 and 7 are widened exactly)."""
+        """A workspace buffer of matrix i (``muon_debug_copy_workspace``) as a CPU fp32
+        tensor of r rows (widened exactly from bf16 / fp16).  G buffers hold s*G."""
         import torch
         m, n = self.shapes[i]
         r, c = min(m, n), max(m, n)
         ld = ctypes.c_int32()
         if which == 8:
             out = torch.empty(1, dtype=torch.float32)
-            _check(self.lib.muon_debug_copy_workspace(self.handle, i, which,
-                                                      ctypes.c_void_p(out.data_ptr()),
-                                                      ctypes.byref(ld), _stream_handle(stream)),
-                   "muon_debug_copy_workspace")
-            return out
-        bf = which in (0, 7)
-        width = ((c if which == 0 else r) + 7) // 8 * 8
-        out = torch.empty((r, width), dtype=torch.bfloat16 if bf else torch.float32)
-        _check(self.lib.muon_debug_copy_workspace(self.handle, i, which,
-                                                  ctypes.c_void_p(out.data_ptr()),
+        else:
+            width = ((c if which == 0 else r) + 7) // 8 * 8
+            dt = torch.bfloat16 if which in (0, 7) else torch.float16
+            out = torch.empty((r, width), dtype=dt)
+        _check(self.lib.muon_debug_copy_workspace(self.handle, i, which, ctypes.c_void_p(out.data_ptr()),
                                                   ctypes.byref(ld), _stream_handle(stream)),
                "muon_debug_copy_workspace")
-        assert ld.value == width
-        cols = c if which == 0 else r
-        return out[:, :cols].float()
+        if which == 8:
+            return out
+        assert ld.value == out.shape[1]
+        return out[:, :(c if which == 0 else r)].float()
+
+    @staticmethod
+    def gram_scale(r: int) -> float:
+        """The power of two s the library carries G as (s*G) in its fp16 r x r buffers."""
+        import math
+        return 2.0 ** round(math.log2(r))
 
     def info(self) -> dict:
         inf = MuonPlanInfo()

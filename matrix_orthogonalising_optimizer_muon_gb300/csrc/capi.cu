@@ -56,12 +56,12 @@ bool make_map(CUtensorMap* map, void* base, bool bf16, uint64_t inner, uint64_t 
               uint32_t box_inner, uint32_t box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    const uint64_t esz = bf16 ? 2 : 4;
+    const uint64_t esz = 2;   // bf16 or fp16
     cuuint64_t dims[3] = {inner, rows, batch};
     cuuint64_t strides[2] = {ld * esz, ld * rows * esz};
     cuuint32_t box[3] = {box_inner, box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides,
+    return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides,
               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -76,10 +76,11 @@ struct Bucket {
     std::vector<int> mats;
     int slot_base = 0;
     long long ut_off = 0;   // element offset of item 0 in the X0 workspace
-    float* G[2] = {nullptr, nullptr};
-    float* P = nullptr;
-    float* T = nullptr;
-    float* Q[2] = {nullptr, nullptr};
+    float gscale = 1.f;     // G is carried as s G, s = 2^round(log2 r)
+    __half* G[2] = {nullptr, nullptr};
+    __half* P = nullptr;
+    __half* T = nullptr;
+    __half* Q[2] = {nullptr, nullptr};
     __nv_bfloat16* Qb = nullptr;
     int* d_item_mat = nullptr;
     float* Odbg = nullptr;
@@ -246,11 +247,11 @@ GemmProblem problem(int M, int N, int K, int batch, bool sym, int epi) {
 struct Grouper {
     muon_plan_s* p;
     cudaStream_t s;
-    bool tf32;
+    bool bf16;
     GemmLaunch L;
     muon_status st = MUON_OK;
     int launches = 0;
-    Grouper(muon_plan_s* plan, cudaStream_t stream, bool is_tf32) : p(plan), s(stream), tf32(is_tf32) { reset(); }
+    Grouper(muon_plan_s* plan, cudaStream_t stream, bool is_bf16) : p(plan), s(stream), bf16(is_bf16) { reset(); }
     void reset() {
         std::memset(&L, 0, sizeof(L));
         L.status = p->status;
@@ -267,7 +268,7 @@ struct Grouper {
     void flush() {
         if (L.nprob == 0) return;
         if (st == MUON_OK) {
-            st = cuda_status(gemm_launch(L, tf32, p->sm_count, s));
+            st = cuda_status(gemm_launch(L, bf16, p->sm_count, s));
             ++launches;
         }
         reset();
@@ -430,12 +431,12 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
         Bucket& b = p->buckets[k];
         o_item[k] = take(sizeof(int) * b.batch);
         const size_t rr = (size_t)b.batch * b.r * b.ldr;
-        o_rr[k] = take(rr * 4);   // G0
-        take(rr * 4);             // G1
-        take(rr * 4);             // P
-        take(rr * 4);             // T
-        take(rr * 4);             // Q0
-        take(rr * 4);             // Q1
+        o_rr[k] = take(rr * 2);   // G0 (fp16, scaled)
+        take(rr * 2);             // G1
+        take(rr * 2);             // P
+        take(rr * 2);             // T
+        take(rr * 2);             // Q0
+        take(rr * 2);             // Q1
         o_qb[k] = take(rr * 2);   // bf16 Q for the final product
         o_odbg[k] = p->opts.keep_update ? take((size_t)b.batch * b.r * b.c * 4) : 0;
     }
@@ -507,13 +508,14 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
         b.d_item_mat = reinterpret_cast<int*>(base + o_item[k]);
         ok = cudaMemcpy(b.d_item_mat, b.mats.data(), sizeof(int) * b.batch, cudaMemcpyHostToDevice) == cudaSuccess;
         const size_t rr = (size_t)b.batch * b.r * b.ldr;
-        float* f = reinterpret_cast<float*>(base + o_rr[k]);
-        b.G[0] = f;
-        b.G[1] = reinterpret_cast<float*>(base + o_rr[k] + (size_t)round_up(rr * 4, 256));
-        b.P = reinterpret_cast<float*>(base + o_rr[k] + 2 * (size_t)round_up(rr * 4, 256));
-        b.T = reinterpret_cast<float*>(base + o_rr[k] + 3 * (size_t)round_up(rr * 4, 256));
-        b.Q[0] = reinterpret_cast<float*>(base + o_rr[k] + 4 * (size_t)round_up(rr * 4, 256));
-        b.Q[1] = reinterpret_cast<float*>(base + o_rr[k] + 5 * (size_t)round_up(rr * 4, 256));
+        const size_t step = (size_t)round_up((long long)rr * 2, 256);
+        b.G[0] = reinterpret_cast<__half*>(base + o_rr[k]);
+        b.G[1] = reinterpret_cast<__half*>(base + o_rr[k] + step);
+        b.P = reinterpret_cast<__half*>(base + o_rr[k] + 2 * step);
+        b.T = reinterpret_cast<__half*>(base + o_rr[k] + 3 * step);
+        b.Q[0] = reinterpret_cast<__half*>(base + o_rr[k] + 4 * step);
+        b.Q[1] = reinterpret_cast<__half*>(base + o_rr[k] + 5 * step);
+        b.gscale = std::ldexp(1.f, (int)std::lround(std::log2((double)b.r)));
         b.Qb = reinterpret_cast<__nv_bfloat16*>(base + o_qb[k]);
         b.Odbg = p->opts.keep_update ? reinterpret_cast<float*>(base + o_odbg[k]) : nullptr;
         __nv_bfloat16* ut = p->ut + b.ut_off;
@@ -522,13 +524,13 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
         ok = ok && make_map(&b.ut_mn, ut, true, b.c, b.r, b.batch, b.ldu, 64, 64);
         ok = ok && make_map(&b.qb_a, b.Qb, true, b.r, b.r, b.batch, b.ldr, 64, kBM);
         for (int g = 0; g < 2; ++g) {
-            ok = ok && make_map(&b.ga[g], b.G[g], false, b.r, b.r, b.batch, b.ldr, 32, kBM);
-            ok = ok && make_map(&b.gb[g], b.G[g], false, b.r, b.r, b.batch, b.ldr, 32, kBN);
-            ok = ok && make_map(&b.qb[g], b.Q[g], false, b.r, b.r, b.batch, b.ldr, 32, kBN);
+            ok = ok && make_map(&b.ga[g], b.G[g], false, b.r, b.r, b.batch, b.ldr, 64, kBM);
+            ok = ok && make_map(&b.gb[g], b.G[g], false, b.r, b.r, b.batch, b.ldr, 64, kBN);
+            ok = ok && make_map(&b.qb[g], b.Q[g], false, b.r, b.r, b.batch, b.ldr, 64, kBN);
         }
-        ok = ok && make_map(&b.pa, b.P, false, b.r, b.r, b.batch, b.ldr, 32, kBM);
-        ok = ok && make_map(&b.pb, b.P, false, b.r, b.r, b.batch, b.ldr, 32, kBN);
-        ok = ok && make_map(&b.tb, b.T, false, b.r, b.r, b.batch, b.ldr, 32, kBN);
+        ok = ok && make_map(&b.pa, b.P, false, b.r, b.r, b.batch, b.ldr, 64, kBM);
+        ok = ok && make_map(&b.pb, b.P, false, b.r, b.r, b.batch, b.ldr, 64, kBN);
+        ok = ok && make_map(&b.tb, b.T, false, b.r, b.r, b.batch, b.ldr, 64, kBN);
     }
     ok = ok && cudaMallocHost(&p->h_pinned, sizeof(void*) * 3 * n) == cudaSuccess;
     ok = ok && cudaEventCreateWithFlags(&p->upload_ev, cudaEventDisableTiming) == cudaSuccess;
@@ -634,15 +636,16 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
         p->flops[2] += fl_final;
     }
 
-    // ---- G0 = alpha^2 X0 X0^T (lower triangle, mirrored), all buckets in one launch
+    // ---- G0' = s alpha^2 X0 X0^T (lower triangle, mirrored), all buckets in one launch
     {
-        Grouper g(p, s, false);
+        Grouper g(p, s, true);
         for (auto& b : p->buckets) {
             GemmProblem q = problem(b.r, b.r, b.c, b.batch, true, kEpiSyrk);
             q.C = b.G[0];
             q.strideC = (long long)b.r * b.ldr;
             q.ldc = b.ldr;
             q.alpha = p->alpha + b.slot_base;
+            q.out_scale = b.gscale;
             g.add(b.ut_a, b.ut_b, q);
         }
         g.flush();
@@ -651,56 +654,47 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
     }
     if (se) MUON_TRY(cudaEventRecord(se->e[2], s));
 
-    // ---- Newton-Schulz in the Gram space
+    // ---- Newton-Schulz in the Gram space (fp16 operands, G carried as s G)
     const int J = ns_steps;
     int gc = 0;   // current G buffer
     int qc = 0;   // current Q buffer
+    auto rr_problem = [](const Bucket& b, int epi) {
+        GemmProblem q = problem(b.r, b.r, b.r, b.batch, true, epi);
+        q.strideC = (long long)b.r * b.ldr;
+        q.ldc = b.ldr;
+        return q;
+    };
     for (int k = 1; k <= J; ++k) {
-        {   // P = aI + bG + cG^2 (at k = 1 this is also Q_1)
-            Grouper g(p, s, true);
+        {   // P = aI + (b/s) G' + (c/s^2) G'^2 (at k = 1 this is also Q_1)
+            Grouper g(p, s, false);
             for (auto& b : p->buckets) {
-                GemmProblem q = problem(b.r, b.r, b.r, b.batch, true, kEpiPoly);
-                q.strideC = (long long)b.r * b.ldr;
-                q.ldc = b.ldr;
+                GemmProblem q = rr_problem(b, kEpiPoly);
                 q.C = b.P;
                 if (k == 1 && J > 1) q.C2 = b.Q[0];
-                if (k == 1 && J == 1) {
-                    q.Cb = b.Qb;
-                    q.ldcb = b.ldr;
-                    q.strideCb = (long long)b.r * b.ldr;
-                }
+                if (k == 1 && J == 1) q.Cb = b.Qb;
                 q.Gin = b.G[gc];
-                q.strideG = (long long)b.r * b.ldr;
-                q.ldg = b.ldr;
                 q.coef_a = kNsA;
-                q.coef_b = kNsB;
-                q.coef_c = kNsC;
+                q.coef_b = kNsB / b.gscale;
+                q.coef_c = kNsC / (b.gscale * b.gscale);
                 g.add(b.ga[gc], b.gb[gc], q);
             }
             g.flush();
             if (g.st != MUON_OK) return g.st;
             launches += g.launches;
         }
-        {   // Q' = P Q (k >= 2) and T = P P (k < J)
-            Grouper g(p, s, true);
+        {   // Q' = P Q (k >= 2) and T = P P (k < J), independent: one launch
+            Grouper g(p, s, false);
             for (auto& b : p->buckets) {
                 if (k >= 2) {
-                    GemmProblem q = problem(b.r, b.r, b.r, b.batch, true, kEpiPlain);
-                    q.strideC = (long long)b.r * b.ldr;
-                    q.ldc = b.ldr;
-                    if (k < J) {
+                    GemmProblem q = rr_problem(b, kEpiPlain);
+                    if (k < J)
                         q.C = b.Q[qc ^ 1];
-                    } else {
+                    else
                         q.Cb = b.Qb;
-                        q.ldcb = b.ldr;
-                        q.strideCb = (long long)b.r * b.ldr;
-                    }
                     g.add(b.pa, b.qb[qc], q);
                 }
                 if (k < J) {
-                    GemmProblem q = problem(b.r, b.r, b.r, b.batch, true, kEpiPlain);
-                    q.strideC = (long long)b.r * b.ldr;
-                    q.ldc = b.ldr;
+                    GemmProblem q = rr_problem(b, kEpiPlain);
                     q.C = b.T;
                     g.add(b.pa, b.pb, q);
                 }
@@ -710,12 +704,10 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
             launches += g.launches;
             if (k >= 2) qc ^= 1;
         }
-        if (k < J) {   // G' = G T
-            Grouper g(p, s, true);
+        if (k < J) {   // G'' = G' T
+            Grouper g(p, s, false);
             for (auto& b : p->buckets) {
-                GemmProblem q = problem(b.r, b.r, b.r, b.batch, true, kEpiPlain);
-                q.strideC = (long long)b.r * b.ldr;
-                q.ldc = b.ldr;
+                GemmProblem q = rr_problem(b, kEpiPlain);
                 q.C = b.G[gc ^ 1];
                 g.add(b.ga[gc], b.tb, q);
             }
@@ -735,7 +727,7 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
 
     // ---- O = alpha Q X0, fused W <- W - lr (s O + wd W) in the stored layout
     {
-        Grouper g(p, s, false);
+        Grouper g(p, s, true);
         float* const* W = reinterpret_cast<float* const*>(p->d_ptrs + 2 * n);
         for (auto& b : p->buckets) {
             GemmProblem q = problem(b.r, b.c, b.r, b.batch, false, kEpiApply);
@@ -799,10 +791,10 @@ muon_status muon_debug_copy_workspace(muon_plan p, int32_t i, int32_t which, voi
             bytes = (size_t)b.r * b.ldu * 2;
             *ld = b.ldu;
             break;
-        case 1: case 2: src = b.G[which - 1] + item * rr; bytes = rr * 4; break;
-        case 3: src = b.P + item * rr; bytes = rr * 4; break;
-        case 4: src = b.T + item * rr; bytes = rr * 4; break;
-        case 5: case 6: src = b.Q[which - 5] + item * rr; bytes = rr * 4; break;
+        case 1: case 2: src = b.G[which - 1] + item * rr; bytes = rr * 2; break;
+        case 3: src = b.P + item * rr; bytes = rr * 2; break;
+        case 4: src = b.T + item * rr; bytes = rr * 2; break;
+        case 5: case 6: src = b.Q[which - 5] + item * rr; bytes = rr * 2; break;
         case 7: src = b.Qb + item * rr; bytes = rr * 2; break;
         case 8: src = p->alpha + p->mats[i].slot; bytes = 4; *ld = 1; break;
     }

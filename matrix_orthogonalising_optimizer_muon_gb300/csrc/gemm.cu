@@ -1,27 +1,28 @@
 // Batched, grouped tensor-core products of the Gram Newton-Schulz iteration on
-// sm_103a: TMA-fed shared-memory pipeline, tcgen05.mma with the accumulator in
-// TMEM, warp-specialised persistent CTAs.
+// sm_103a: TMA-fed shared-memory pipeline, tcgen05.mma (kind::f16) with the
+// accumulator in TMEM, warp-specialised persistent CTAs.
 //
 // Products (DMuon, "Gram Newton-Schulz": the recursion runs on r x r matrices;
 // SYRK-style symmetric products compute only the lower triangle):
-//   G0 = alpha^2 * X X^T            bf16 x bf16 -> fp32, K = c     (kEpiSyrk, symmetric)
-//   P  = aI + bG + c * (G G)        tf32 x tf32 -> fp32, K = r     (kEpiPoly, symmetric)
-//   Q' = P Q,  T = P P,  G' = G T   tf32 x tf32 -> fp32, K = r     (kEpiPlain, symmetric)
-//   O  = alpha * Q X                bf16 x bf16 -> fp32, K = r     (kEpiApply, fused update
-//                                   W -= lr (0.2 sqrt(c) O + wd W), blog eq. (4))
-// Every r x r product of commuting polynomials in G0 is symmetric, so all of
-// them are lower-triangle products.  r x r outputs are stored already rounded
-// to tf32 (nearest even) because the next product reads them as tf32 operands.
+//   G0' = s alpha^2 X X^T            bf16 x bf16 -> fp32, K = c   (kEpiSyrk, symmetric)
+//   P   = aI + (b/s) G' + (c/s^2) G'G'  fp16 x fp16 -> fp32, K = r (kEpiPoly, symmetric)
+//   Q'  = P Q,  T = P P,  G'' = G' T    fp16 x fp16 -> fp32, K = r (kEpiPlain, symmetric)
+//   O   = alpha Q X                  bf16 x bf16 -> fp32, K = r   (kEpiApply: fused
+//                                    W -= lr (0.2 sqrt(c) O + wd W), blog eq. (4))
+// G is carried scaled, G' = s G with s = 2^round(log2 r), so every r x r value
+// sits in fp16's normal range: sigma_max(X0) <= ||X0||_F = 1 bounds |G'| by
+// 1.44 s, |P| by 3.45 and |Q| by 3.45^J.  fp16 keeps 11 significant bits (as
+// tf32) at the bf16 tensor rate.  Every r x r product of commuting polynomials
+// in G0 is symmetric, so all of them are lower-triangle products.
 #include "kernels.h"
 #include "ptx.cuh"
 
 namespace muon {
 
-template <bool TF32>
 struct GemmCfg {
-    static constexpr int BK = TF32 ? 32 : 64;            // one 128-byte swizzle row of K
-    static constexpr int ESZ = TF32 ? 4 : 2;
-    static constexpr int UK = TF32 ? 8 : 16;             // K of one tcgen05.mma
+    static constexpr int BK = 64;                        // one 128-byte swizzle row of K
+    static constexpr int ESZ = 2;
+    static constexpr int UK = 16;                        // K of one tcgen05.mma kind::f16
     static constexpr int A_BYTES = kBM * BK * ESZ;       // 16 KB
     static constexpr int B_BYTES = kBN * BK * ESZ;       // 32 KB
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -30,9 +31,7 @@ struct GemmCfg {
     static constexpr int SMEM_BYTES = BAR_OFFSET + 256 + 1024;   // + barriers + alignment slack
 };
 
-size_t gemm_smem_bytes(bool tf32) {
-    return tf32 ? GemmCfg<true>::SMEM_BYTES : GemmCfg<false>::SMEM_BYTES;
-}
+size_t gemm_smem_bytes() { return GemmCfg::SMEM_BYTES; }
 
 struct TileCoord {
     int p, item, m0, n0;
@@ -75,153 +74,170 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
     }
 }
 
+__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack_bf162(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
 // ------------------------------------------------------------------ epilogues
+// v[j] is element (row, col0 + j) of a symmetric result.  The lower part goes to
+// (row, col), its mirror to (col, row).  Rows beyond M are masked (their lanes
+// still took part in the collective TMEM load).
 __device__ __forceinline__ void store_sym(const GemmProblem& P, int item, int row, int col0, const float (&v)[32]) {
-    // v[j] is element (row, col0 + j).  Lower part goes to (row, col), its
-    // mirror to (col, row).  Rows beyond M are masked (their lanes still ran
-    // the collective TMEM load).
     if (row >= P.M) return;
-    float* C = P.C ? P.C + item * P.strideC : nullptr;
-    float* C2 = P.C2 ? P.C2 + item * P.strideC : nullptr;
-    __nv_bfloat16* Cb = P.Cb ? P.Cb + item * P.strideCb : nullptr;
+    const long long ib = item * P.strideC;
+    __half* C = P.C ? P.C + ib : nullptr;
+    __half* C2 = P.C2 ? P.C2 + ib : nullptr;
+    __nv_bfloat16* Cb = P.Cb ? P.Cb + ib : nullptr;
+    const long long rbase = (long long)row * P.ldc + col0;
     const bool full = (col0 + 31 <= row) && (col0 + 31 < P.N);
     if (full) {
-        if (C) {
-            float4* dst = reinterpret_cast<float4*>(C + (long long)row * P.ldc + col0);
+        uint4 h[4], b[4];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        for (int q = 0; q < 4; ++q) {
+            h[q] = make_uint4(pack_half2(v[8 * q], v[8 * q + 1]), pack_half2(v[8 * q + 2], v[8 * q + 3]),
+                              pack_half2(v[8 * q + 4], v[8 * q + 5]), pack_half2(v[8 * q + 6], v[8 * q + 7]));
+            b[q] = make_uint4(pack_bf162(v[8 * q], v[8 * q + 1]), pack_bf162(v[8 * q + 2], v[8 * q + 3]),
+                              pack_bf162(v[8 * q + 4], v[8 * q + 5]), pack_bf162(v[8 * q + 6], v[8 * q + 7]));
+        }
+        if (C) {
+            uint4* d = reinterpret_cast<uint4*>(C + rbase);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) d[q] = h[q];
         }
         if (C2) {
-            float4* dst = reinterpret_cast<float4*>(C2 + (long long)row * P.ldc + col0);
+            uint4* d = reinterpret_cast<uint4*>(C2 + rbase);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            for (int q = 0; q < 4; ++q) d[q] = h[q];
         }
         if (Cb) {
-            uint4* dst = reinterpret_cast<uint4*>(Cb + (long long)row * P.ldcb + col0);
+            uint4* d = reinterpret_cast<uint4*>(Cb + rbase);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                __nv_bfloat162 h0 = __floats2bfloat162_rn(v[8 * q + 0], v[8 * q + 1]);
-                __nv_bfloat162 h1 = __floats2bfloat162_rn(v[8 * q + 2], v[8 * q + 3]);
-                __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * q + 4], v[8 * q + 5]);
-                __nv_bfloat162 h3 = __floats2bfloat162_rn(v[8 * q + 6], v[8 * q + 7]);
-                uint4 pk;
-                pk.x = *reinterpret_cast<uint32_t*>(&h0);
-                pk.y = *reinterpret_cast<uint32_t*>(&h1);
-                pk.z = *reinterpret_cast<uint32_t*>(&h2);
-                pk.w = *reinterpret_cast<uint32_t*>(&h3);
-                dst[q] = pk;
-            }
+            for (int q = 0; q < 4; ++q) d[q] = b[q];
         }
     } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
             const int col = col0 + j;
             if (col <= row && col < P.N) {
-                if (C) C[(long long)row * P.ldc + col] = v[j];
-                if (C2) C2[(long long)row * P.ldc + col] = v[j];
-                if (Cb) Cb[(long long)row * P.ldcb + col] = __float2bfloat16_rn(v[j]);
+                if (C) C[rbase + j] = __float2half_rn(v[j]);
+                if (C2) C2[rbase + j] = __float2half_rn(v[j]);
+                if (Cb) Cb[rbase + j] = __float2bfloat16_rn(v[j]);
             }
         }
     }
-    // mirror: for fixed j the warp's lanes write consecutive rows of row `col`
+    // mirror: for fixed j the warp's lanes write consecutive entries of row `col`
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
         const int col = col0 + j;
         if (col < row && col < P.N) {
-            if (C) C[(long long)col * P.ldc + row] = v[j];
-            if (C2) C2[(long long)col * P.ldc + row] = v[j];
-            if (Cb) Cb[(long long)col * P.ldcb + row] = __float2bfloat16_rn(v[j]);
+            const long long idx = (long long)col * P.ldc + row;
+            if (C) C[idx] = __float2half_rn(v[j]);
+            if (C2) C2[idx] = __float2half_rn(v[j]);
+            if (Cb) Cb[idx] = __float2bfloat16_rn(v[j]);
+        }
+    }
+}
+
+__device__ __forceinline__ void epilogue_apply(const GemmProblem& P, int item, int row, int col0,
+                                               const uint32_t (&raw)[32]) {
+    if (row >= P.M) return;
+    const float al = P.alpha[item];
+    const int mat = P.item_mat[item];
+    float* W = P.W[mat];
+    const bool tr = P.transposed[mat] != 0;
+    float* O = P.Odbg ? P.Odbg + (long long)item * P.M * P.N : nullptr;
+    const float lr = P.lr, wd = P.wd, s = P.scale;
+    if (!tr) {
+        // stored layout = oriented layout: element (row, col) at row * N + col
+        const long long base = (long long)row * P.N + col0;
+        const bool vec = (col0 + 31 < P.N) && ((P.N & 3) == 0) && ((reinterpret_cast<uintptr_t>(W) & 15) == 0);
+        if (vec) {
+            float4* w4 = reinterpret_cast<float4*>(W + base);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                float4 w = w4[q];
+                const float o0 = al * __uint_as_float(raw[4 * q + 0]);
+                const float o1 = al * __uint_as_float(raw[4 * q + 1]);
+                const float o2 = al * __uint_as_float(raw[4 * q + 2]);
+                const float o3 = al * __uint_as_float(raw[4 * q + 3]);
+                w.x = w.x - lr * (s * o0 + wd * w.x);
+                w.y = w.y - lr * (s * o1 + wd * w.y);
+                w.z = w.z - lr * (s * o2 + wd * w.z);
+                w.w = w.w - lr * (s * o3 + wd * w.w);
+                w4[q] = w;
+                if (O) {
+                    O[base + 4 * q + 0] = o0;
+                    O[base + 4 * q + 1] = o1;
+                    O[base + 4 * q + 2] = o2;
+                    O[base + 4 * q + 3] = o3;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                if (col0 + j < P.N) {
+                    const float o = al * __uint_as_float(raw[j]);
+                    const float w = W[base + j];
+                    W[base + j] = w - lr * (s * o + wd * w);
+                    if (O) O[base + j] = o;
+                }
+            }
+        }
+    } else {
+        // stored as c x r: oriented (row, col) lives at col * M + row; lanes
+        // (consecutive rows) write consecutive addresses
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int col = col0 + j;
+            if (col < P.N) {
+                const long long idx = (long long)col * P.M + row;
+                const float o = al * __uint_as_float(raw[j]);
+                const float w = W[idx];
+                W[idx] = w - lr * (s * o + wd * w);
+                if (O) O[idx] = o;
+            }
         }
     }
 }
 
 __device__ __forceinline__ void epilogue_chunk(const GemmProblem& P, int item, int row, int col0,
                                                const uint32_t (&raw)[32]) {
-    float v[32];
     if (P.epi == kEpiApply) {
-        if (row >= P.M) return;
-        const float al = P.alpha[item];
-        const int mat = P.item_mat[item];
-        float* W = P.W[mat];
-        const bool tr = P.transposed[mat] != 0;
-        float* O = P.Odbg ? P.Odbg + (long long)item * P.M * P.N : nullptr;
-        const float lr = P.lr, wd = P.wd, s = P.scale;
-        if (!tr) {
-            // stored layout = oriented layout: element (row, col) at row * N + col
-            const long long base = (long long)row * P.N + col0;
-            const bool vec = (col0 + 31 < P.N) && ((P.N & 3) == 0) && ((reinterpret_cast<uintptr_t>(W) & 15) == 0);
-            if (vec) {
-                float4* w4 = reinterpret_cast<float4*>(W + base);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    float4 w = w4[q];
-                    const float o0 = al * __uint_as_float(raw[4 * q + 0]);
-                    const float o1 = al * __uint_as_float(raw[4 * q + 1]);
-                    const float o2 = al * __uint_as_float(raw[4 * q + 2]);
-                    const float o3 = al * __uint_as_float(raw[4 * q + 3]);
-                    w.x = w.x - lr * (s * o0 + wd * w.x);
-                    w.y = w.y - lr * (s * o1 + wd * w.y);
-                    w.z = w.z - lr * (s * o2 + wd * w.z);
-                    w.w = w.w - lr * (s * o3 + wd * w.w);
-                    w4[q] = w;
-                    if (O) {
-                        O[base + 4 * q + 0] = o0;
-                        O[base + 4 * q + 1] = o1;
-                        O[base + 4 * q + 2] = o2;
-                        O[base + 4 * q + 3] = o3;
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    if (col0 + j < P.N) {
-                        const float o = al * __uint_as_float(raw[j]);
-                        const float w = W[base + j];
-                        W[base + j] = w - lr * (s * o + wd * w);
-                        if (O) O[base + j] = o;
-                    }
-                }
-            }
-        } else {
-            // stored as c x r: oriented (row, col) lives at col * M + row; lanes
-            // (consecutive rows) write consecutive addresses
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int col = col0 + j;
-                if (col < P.N) {
-                    const long long idx = (long long)col * P.M + row;
-                    const float o = al * __uint_as_float(raw[j]);
-                    const float w = W[idx];
-                    W[idx] = w - lr * (s * o + wd * w);
-                    if (O) O[idx] = o;
-                }
-            }
-        }
+        epilogue_apply(P, item, row, col0, raw);
         return;
     }
+    float v[32];
     if (P.epi == kEpiSyrk) {
         const float al = P.alpha[item];
-        const float a2 = al * al;
+        const float k = P.out_scale * al * al;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = round_tf32(a2 * __uint_as_float(raw[j]));
+        for (int j = 0; j < 32; ++j) v[j] = k * __uint_as_float(raw[j]);
     } else if (P.epi == kEpiPoly) {
-        // P = a I + b G + c G^2; G read from the (tf32-valued) input
+        // P = a I + b' G' + c' G'^2, with G' read from the fp16 input the MMA used
         float g[32];
         if (row < P.M) {
-            const float* Grow = P.Gin + item * P.strideG + (long long)row * P.ldg + col0;
+            const __half* Grow = P.Gin + item * P.strideC + (long long)row * P.ldc + col0;
             if (col0 + 31 < P.N) {
-                const float4* g4 = reinterpret_cast<const float4*>(Grow);
+                const uint4* g4 = reinterpret_cast<const uint4*>(Grow);
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float4 t = g4[q];
-                    g[4 * q] = t.x;
-                    g[4 * q + 1] = t.y;
-                    g[4 * q + 2] = t.z;
-                    g[4 * q + 3] = t.w;
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 t = g4[q];
+                    const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+                        g[8 * q + 2 * e] = f.x;
+                        g[8 * q + 2 * e + 1] = f.y;
+                    }
                 }
             } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) g[j] = (col0 + j < P.N) ? Grow[j] : 0.f;
+                for (int j = 0; j < 32; ++j) g[j] = (col0 + j < P.N) ? __half2float(Grow[j]) : 0.f;
             }
         } else {
 #pragma unroll
@@ -231,19 +247,19 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem& P, int item, i
         for (int j = 0; j < 32; ++j) {
             float x = P.coef_c * __uint_as_float(raw[j]) + P.coef_b * g[j];
             if (col0 + j == row) x += P.coef_a;
-            v[j] = round_tf32(x);
+            v[j] = x;
         }
     } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = round_tf32(__uint_as_float(raw[j]));
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw[j]);
     }
     store_sym(P, item, row, col0, v);
 }
 
 // ------------------------------------------------------------------ kernel
-template <bool TF32>
+template <bool BF16>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmLaunch L) {
-    using Cfg = GemmCfg<TF32>;
+    using Cfg = GemmCfg;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::BAR_OFFSET);
@@ -336,7 +352,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 if (!mbar_wait(tempty + acc, aph ^ 1u, abort_flag, L.status, kStatusTimeoutMma)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * kBN;
-                const uint32_t idesc = idesc_make(TF32, kBM, kBN, false, P.b_mn != 0);
+                const uint32_t idesc = idesc_make(BF16, kBM, kBN, false, P.b_mn != 0);
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const uint32_t s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1u;
@@ -353,10 +369,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                         const uint64_t bd =
                             P.b_mn ? sdesc_sw128(b_addr + kk * Cfg::UK * 128, Cfg::MN_CHUNK_BYTES, 1024)
                                    : sdesc_sw128(b_addr + kk * Cfg::UK * Cfg::ESZ, 0, 1024);
-                        if (TF32)
-                            mma_tf32(d_tmem, ad, bd, idesc, (kb | kk) != 0);
-                        else
-                            mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+                        mma_f16kind(d_tmem, ad, bd, idesc, (kb | kk) != 0);
                     }
                     mma_commit(empty + s);   // frees the stage when these MMAs finish
                 }
@@ -406,20 +419,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 
 cudaError_t gemm_prepare(int device) {
     (void)device;
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         GemmCfg<false>::SMEM_BYTES);
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, GemmCfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                GemmCfg<true>::SMEM_BYTES);
+    return cudaFuncSetAttribute(gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                GemmCfg::SMEM_BYTES);
 }
 
-cudaError_t gemm_launch(const GemmLaunch& L, bool tf32, int grid, cudaStream_t s) {
+cudaError_t gemm_launch(const GemmLaunch& L, bool bf16, int grid, cudaStream_t s) {
     if (L.total_tiles <= 0) return cudaSuccess;
     if (grid > L.total_tiles) grid = L.total_tiles;
-    if (tf32)
-        gemm_kernel<true><<<grid, kGemmThreads, GemmCfg<true>::SMEM_BYTES, s>>>(L);
+    if (bf16)
+        gemm_kernel<true><<<grid, kGemmThreads, GemmCfg::SMEM_BYTES, s>>>(L);
     else
-        gemm_kernel<false><<<grid, kGemmThreads, GemmCfg<false>::SMEM_BYTES, s>>>(L);
+        gemm_kernel<false><<<grid, kGemmThreads, GemmCfg::SMEM_BYTES, s>>>(L);
     return cudaGetLastError();
 }
 

@@ -3,6 +3,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -17,35 +18,33 @@ constexpr int kMaxProblems = 8;
 constexpr int kGemmThreads = 192;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
 
 enum Epilogue : int {
-    kEpiSyrk = 0,    // C = alpha^2 * acc                        (G0 = X0 X0^T)
-    kEpiPoly = 1,    // C = a I + b Gin + c * acc                 (P = aI + bG + cG^2)
-    kEpiPlain = 2,   // C = acc                                   (P Q, P P, G T)
-    kEpiApply = 3,   // W -= lr (s * alpha * acc + wd W) in the stored layout (final O = Q X0)
+    kEpiSyrk = 0,    // C = s alpha^2 acc                          (G0' = s X0 X0^T)
+    kEpiPoly = 1,    // C = a I + b' Gin + c' acc                  (P = aI + bG + cG^2 in scaled G')
+    kEpiPlain = 2,   // C = acc                                    (P Q, P P, G' T)
+    kEpiApply = 3,   // W -= lr (s_w alpha acc + wd W), stored layout (final O = Q X0)
 };
 
-// One batched product C_item = A_item * B_item^T (A: M x K, B: N x K as loaded by
-// TMA; B may be MN-major, i.e. stored K x N).  With sym = 1 the output is
-// symmetric (M = N): only tiles touching the lower triangle are computed and
-// each lower element is also written to its mirror position.
+// One batched product C_item = A_item * B_item^T (A: M x K, B: N x K as loaded
+// by TMA; B may be MN-major, i.e. stored K x N).  Operands are 2-byte: bf16 for
+// the SYRK and the final product, fp16 for the r x r recursion.  With sym = 1
+// the output is symmetric (M = N): only tiles touching the lower triangle are
+// computed and each lower element is also written to its mirror position.
 struct GemmProblem {
     int M, N, K, batch;
     int tiles_m, tiles_n, tiles_per_item, tile_begin;
     int sym, b_mn, epi, pad0;
-    // fp32 outputs (row-major, leading dim ldc, batch stride strideC); C2 optional second copy
-    float* C;
-    float* C2;
+    // fp16 outputs (row-major, leading dim ldc, batch stride strideC); C2 an optional copy
+    __half* C;
+    __half* C2;
     long long strideC;
-    int ldc, ldcb;
-    // optional bf16 copy of the output (row-major, leading dim ldcb)
+    int ldc, pad1;
+    // optional bf16 copy of the output (same leading dim and stride)
     __nv_bfloat16* Cb;
-    long long strideCb;
-    // kEpiPoly: G input of the polynomial
-    const float* Gin;
-    long long strideG;
-    int ldg, pad1;
+    // kEpiPoly: G' input of the polynomial (same leading dim and stride)
+    const __half* Gin;
     // per-item 1/||U||_F (kEpiSyrk uses its square, kEpiApply the value)
     const float* alpha;
-    float coef_a, coef_b, coef_c, pad2;
+    float coef_a, coef_b, coef_c, out_scale;
     // kEpiApply
     const int* item_mat;               // item -> plan matrix index
     float* const* W;                   // plan matrix index -> params pointer
@@ -64,9 +63,10 @@ struct GemmLaunch {
     int pad;
 };
 
-size_t gemm_smem_bytes(bool tf32);
+size_t gemm_smem_bytes();
 cudaError_t gemm_prepare(int device);   // sets the dynamic shared-memory limit once
-cudaError_t gemm_launch(const GemmLaunch& L, bool tf32, int grid, cudaStream_t s);
+// bf16 = true: bf16 operands (SYRK, final product); false: fp16 operands (r x r products)
+cudaError_t gemm_launch(const GemmLaunch& L, bool bf16, int grid, cudaStream_t s);
 
 // ------------------------------------------------------------------ elementwise
 // Per plan matrix, resident on the device.

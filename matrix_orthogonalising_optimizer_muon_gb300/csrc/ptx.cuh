@@ -109,22 +109,14 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, one instruction, issued by one thread.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
+// D[tmem] (+)= A[smem] * B[smem]^T, one instruction, issued by one thread;
+// A and B are both bf16 or both fp16 (the type is in idesc).
+__device__ __forceinline__ void mma_f16kind(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
@@ -171,23 +163,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
     return d;
 }
 
-// Instruction descriptor for kind::f16 (bf16 inputs) / kind::tf32, fp32 accumulate.
-//  bits 4-5 D format (1 = f32); 7-9 A format, 10-12 B format (bf16 = 1, tf32 = 2);
+// Instruction descriptor for kind::f16 with fp32 accumulation.
+//  bits 4-5 D format (1 = f32); 7-9 A format, 10-12 B format (f16 = 0, bf16 = 1);
 //  bit 15 A MN-major, bit 16 B MN-major; 17-22 N >> 3; 24-28 M >> 4.
-__host__ __device__ constexpr uint32_t idesc_make(bool tf32, int M, int N, bool a_mn, bool b_mn) {
-    return (1u << 4) | ((tf32 ? 2u : 1u) << 7) | ((tf32 ? 2u : 1u) << 10) | ((a_mn ? 1u : 0u) << 15) |
+__host__ __device__ constexpr uint32_t idesc_make(bool bf16, int M, int N, bool a_mn, bool b_mn) {
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((a_mn ? 1u : 0u) << 15) |
            ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
            (static_cast<uint32_t>(M >> 4) << 24);
-}
-
-// fp32 -> tf32-representable fp32, round to nearest even on the 13 dropped bits.
-__device__ __forceinline__ float round_tf32(float x) {
-    uint32_t u = __float_as_uint(x);
-    if ((u & 0x7F800000u) != 0x7F800000u) {
-        u += 0xFFFu + ((u >> 13) & 1u);
-        u &= 0xFFFFE000u;
-    }
-    return __uint_as_float(u);
 }
 
 }  // namespace muon

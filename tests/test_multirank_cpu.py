@@ -43,9 +43,9 @@ def test_two_gloo_ranks_max_over_ranks():
 
 def test_flop_accounting_matches_gram_form():
     import bench
-    # one 3584 x 18944 matrix, J = 5: 3 r^2 c (bf16) + 17 r^3 (tf32)
-    bf16, tf32 = bench.algorithmic_ns_flops([(18944, 3584)], 5)
+    # one 3584 x 18944 matrix, J = 5: 3 r^2 c (r x c products) + 17 r^3 (r x r products)
+    rc, rrr = bench.algorithmic_ns_flops([(18944, 3584)], 5)
     r, c = 3584, 18944
-    assert bf16 == 3.0 * r * r * c and tf32 == 17.0 * r ** 3
+    assert rc == 3.0 * r * r * c and rrr == 17.0 * r ** 3
     assert bench.algorithmic_ns_flops([(8, 16)], 1) == (3.0 * 64 * 16, 512.0)
     assert bench.algorithmic_ns_flops([(8, 16)], 0)[1] == 0.0
