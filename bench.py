@@ -41,6 +41,28 @@ def parse_args():
     return ap.parse_args()
 
 
+def gemm_traffic(workload: str):
+    """DRAM bytes per NS step of all tensor-core products, from the committed ncu
+    summary; None unless it was taken on the current gemm kernel source."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "gemm_kernel_qwen7b_layer.md")
+    src = os.path.join(ROOT, "matrix_orthogonalising_optimizer_muon_gb300", "csrc", "gemm.cu")
+    if workload != "qwen7b_28l":
+        return None
+    try:
+        vals = {}
+        for line in open(path):
+            if ":" in line and line.split(":")[0] in ("traffic_bytes_per_ns_step_qwen7b_28l", "gemm_source_sha256_16"):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if vals.get("gemm_source_sha256_16") != sha:
+            return None
+        return float(vals["traffic_bytes_per_ns_step_qwen7b_28l"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -306,7 +328,7 @@ def report_ours(args, res, rank, world):
         t_ms = gemm_ms / per_ns
         achieved = fl / (t_ms * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                    "frac": round(achieved / peak, 4), "traffic": None,
+                    "frac": round(achieved / peak, 4), "traffic": gemm_traffic(wl.name),
                     "kernel": "gemm_kernel: all tensor-core products of one NS5 step (SYRK, 17 r x r, final)",
                     "peak_note": "%s sustained dense bf16 (fp16 runs at the same rate)" % src}
         ns5 = {"ns5_tflops": round(achieved, 1),

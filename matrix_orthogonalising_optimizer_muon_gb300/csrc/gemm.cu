@@ -143,74 +143,89 @@ __device__ __forceinline__ void store_sym(const GemmProblem& P, int item, int ro
     }
 }
 
-__device__ __forceinline__ void epilogue_apply(const GemmProblem& P, int item, int row, int col0,
-                                               const uint32_t (&raw)[32]) {
-    if (row >= P.M) return;
-    const float al = P.alpha[item];
+// Final product epilogue, in two phases so the 32 W loads of a chunk are all in
+// flight at once (and overlap the TMEM load): apply_load, then apply_store.
+struct ApplyCtx {
+    float* W;
+    float* O;
+    long long base;     // index of element (row, col0) in the stored layout
+    long long stride;   // index step per column: 1 (m <= n) or M (stored transposed)
+    bool vec;           // 8 float4 per chunk (m <= n, aligned, no tail)
+};
+
+__device__ __forceinline__ ApplyCtx apply_ctx(const GemmProblem& P, int item, int row, int col0) {
+    ApplyCtx c;
     const int mat = P.item_mat[item];
-    float* W = P.W[mat];
-    const bool tr = P.transposed[mat] != 0;
-    float* O = P.Odbg ? P.Odbg + (long long)item * P.M * P.N : nullptr;
-    const float lr = P.lr, wd = P.wd, s = P.scale;
-    if (!tr) {
+    c.W = P.W[mat];
+    c.O = P.Odbg ? P.Odbg + (long long)item * P.M * P.N : nullptr;
+    if (P.transposed[mat] == 0) {
         // stored layout = oriented layout: element (row, col) at row * N + col
-        const long long base = (long long)row * P.N + col0;
-        const bool vec = (col0 + 31 < P.N) && ((P.N & 3) == 0) && ((reinterpret_cast<uintptr_t>(W) & 15) == 0);
-        if (vec) {
-            float4* w4 = reinterpret_cast<float4*>(W + base);
+        c.base = (long long)row * P.N + col0;
+        c.stride = 1;
+        c.vec = (col0 + 31 < P.N) && ((P.N & 3) == 0) && ((reinterpret_cast<uintptr_t>(c.W) & 15) == 0);
+    } else {
+        // stored as c x r: oriented (row, col) lives at col * M + row, so the
+        // warp's lanes (consecutive rows) touch consecutive addresses
+        c.base = (long long)col0 * P.M + row;
+        c.stride = P.M;
+        c.vec = false;
+    }
+    return c;
+}
+
+__device__ __forceinline__ void apply_load(const GemmProblem& P, const ApplyCtx& c, int row, int col0,
+                                           float (&w)[32]) {
+    if (row >= P.M) return;
+    if (c.vec) {
+        const float4* w4 = reinterpret_cast<const float4*>(c.W + c.base);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                float4 w = w4[q];
-                const float o0 = al * __uint_as_float(raw[4 * q + 0]);
-                const float o1 = al * __uint_as_float(raw[4 * q + 1]);
-                const float o2 = al * __uint_as_float(raw[4 * q + 2]);
-                const float o3 = al * __uint_as_float(raw[4 * q + 3]);
-                w.x = w.x - lr * (s * o0 + wd * w.x);
-                w.y = w.y - lr * (s * o1 + wd * w.y);
-                w.z = w.z - lr * (s * o2 + wd * w.z);
-                w.w = w.w - lr * (s * o3 + wd * w.w);
-                w4[q] = w;
-                if (O) {
-                    O[base + 4 * q + 0] = o0;
-                    O[base + 4 * q + 1] = o1;
-                    O[base + 4 * q + 2] = o2;
-                    O[base + 4 * q + 3] = o3;
-                }
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                if (col0 + j < P.N) {
-                    const float o = al * __uint_as_float(raw[j]);
-                    const float w = W[base + j];
-                    W[base + j] = w - lr * (s * o + wd * w);
-                    if (O) O[base + j] = o;
-                }
-            }
+        for (int q = 0; q < 8; ++q) {
+            const float4 t = w4[q];
+            w[4 * q] = t.x;
+            w[4 * q + 1] = t.y;
+            w[4 * q + 2] = t.z;
+            w[4 * q + 3] = t.w;
         }
     } else {
-        // stored as c x r: oriented (row, col) lives at col * M + row; lanes
-        // (consecutive rows) write consecutive addresses
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const int col = col0 + j;
-            if (col < P.N) {
-                const long long idx = (long long)col * P.M + row;
-                const float o = al * __uint_as_float(raw[j]);
-                const float w = W[idx];
-                W[idx] = w - lr * (s * o + wd * w);
-                if (O) O[idx] = o;
-            }
+        for (int j = 0; j < 32; ++j) w[j] = (col0 + j < P.N) ? c.W[c.base + j * c.stride] : 0.f;
+    }
+}
+
+__device__ __forceinline__ void apply_store(const GemmProblem& P, const ApplyCtx& c, int item, int row, int col0,
+                                            const uint32_t (&raw)[32], float (&w)[32]) {
+    if (row >= P.M) return;
+    const float al = P.alpha[item];
+    const float lr = P.lr, wd = P.wd, s = P.scale;
+    float o[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        o[j] = al * __uint_as_float(raw[j]);
+        w[j] = w[j] - lr * (s * o[j] + wd * w[j]);
+    }
+    if (c.vec) {
+        float4* w4 = reinterpret_cast<float4*>(c.W + c.base);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) w4[q] = make_float4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        if (c.O) {
+            float4* o4 = reinterpret_cast<float4*>(c.O + c.base);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) o4[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (col0 + j < P.N) c.W[c.base + j * c.stride] = w[j];
+        if (c.O) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (col0 + j < P.N) c.O[c.base + j * c.stride] = o[j];
         }
     }
 }
 
 __device__ __forceinline__ void epilogue_chunk(const GemmProblem& P, int item, int row, int col0,
                                                const uint32_t (&raw)[32]) {
-    if (P.epi == kEpiApply) {
-        epilogue_apply(P, item, row, col0, raw);
-        return;
-    }
     float v[32];
     if (P.epi == kEpiSyrk) {
         const float al = P.alpha[item];
@@ -400,8 +415,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
                 if (P.sym && col0 > warp_row_max) break;             // whole chunk above the diagonal
                 uint32_t raw[32];
                 tmem_ld32(tbase + cc, raw);
-                tmem_ld_wait();
-                epilogue_chunk(P, tc.item, row, col0, raw);
+                if (P.epi == kEpiApply) {
+                    const ApplyCtx ac = apply_ctx(P, tc.item, row < P.M ? row : 0, col0);
+                    float w[32];
+                    apply_load(P, ac, row, col0, w);   // in flight with the TMEM load
+                    tmem_ld_wait();
+                    apply_store(P, ac, tc.item, row, col0, raw, w);
+                } else {
+                    tmem_ld_wait();
+                    epilogue_chunk(P, tc.item, row, col0, raw);
+                }
             }
             tc_fence_before();
             __syncwarp();
