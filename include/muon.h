@@ -139,6 +139,28 @@ muon_status muon_debug_copy_update(muon_plan p, int32_t i, float* dst, void* str
 muon_status muon_debug_copy_workspace(muon_plan p, int32_t i, int32_t which, void* dst, int32_t* ld,
                                       void* stream);
 
+/*
+ * muon_rownorm_matrix_noalloc - the RowNorm step of muon_rownorm_step for ONE
+ * matrix, without allocating any device memory.  The pages have no
+ * counterpart: this exists for callers that may not call cudaMalloc or have a
+ * library call it - frameworks whose own pooling allocator owns all device
+ * memory, processes under a hard memory budget, and latency-critical loops
+ * that cannot afford cudaMalloc/cudaFree's implicit device synchronisation.
+ *   param, momentum  fp32 rows x cols, updated in place; grad (grad_dtype) read.
+ *   lr, wd, mu, eps  as muon_rownorm_step.
+ * Scratch: when rows > cols the column statistics live in a 4 MiB array that is
+ * part of the library image (every GPU that loads the library holds it until
+ * the process exits); ceil(rows/64)*cols + cols floats must fit in 2^20, else
+ * MUON_ERR_UNSUPPORTED is returned and nothing is launched.  The first call on
+ * a device looks the array's device address up once (make that first call
+ * before any stream capture).  Calls share the array, so calls that overlap
+ * on the GPU (other streams, other host threads) race.  Nothing in the array
+ * needs clearing: each call writes every word it reads.
+ */
+muon_status muon_rownorm_matrix_noalloc(float* param, const void* grad, float* momentum, int64_t rows,
+                                        int64_t cols, muon_dtype grad_dtype, float lr, float wd, float mu,
+                                        float eps, void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* muon_status_string(muon_status s);
 

@@ -70,6 +70,9 @@ EXPORTED = {
     "muon_plan_info": (ctypes.c_int, [_P, ctypes.POINTER(MuonPlanInfo)]),
     "muon_stage_times": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_float),
                                         ctypes.POINTER(ctypes.c_double), ctypes.c_int32]),
+    "muon_rownorm_matrix_noalloc": (ctypes.c_int, [_P, _P, _P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                                   ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                                   ctypes.c_float, _P]),
 }
 
 _lib = None
