@@ -62,7 +62,10 @@ typedef struct {
     int32_t keep_update;
     /* nonzero: each step records CUDA events around its stages (read with muon_stage_times) */
     int32_t timing;
-    int32_t reserved[6];
+    /* nonzero: run every tensor-core product on the one-SM kernel (128 x 256 tiles)
+       instead of the CTA-pair kernel (256 x 256 tiles, tcgen05 cta_group::2) */
+    int32_t single_sm_gemm;
+    int32_t reserved[5];
 } muon_plan_opts;
 
 typedef struct muon_plan_s* muon_plan;

@@ -86,6 +86,7 @@ struct Bucket {
     float* Odbg = nullptr;
     CUtensorMap ut_a, ut_b, ut_mn, qb_a;
     CUtensorMap ga[2], gb[2], pa, pb, tb, qb[2];
+    CUtensorMap qa[2], ta;   // 128-row boxes of Q and T (B halves of the CTA-pair kernel)
 };
 
 struct ListDev {
@@ -100,6 +101,7 @@ struct ListDev {
 struct muon_plan_s {
     int device = 0;
     int sm_count = 0;
+    int pair_clusters = 0;   // co-resident CTA pairs for the 2-SM kernel (0: 1-SM kernel only)
     muon_dtype gdt = MUON_F32;
     muon_plan_opts opts{};
     std::vector<muon_shape> shapes;
@@ -248,16 +250,19 @@ struct Grouper {
     muon_plan_s* p;
     cudaStream_t s;
     bool bf16;
-    GemmLaunch L;
+    GemmLaunch L1;   // 1-SM kernel, 128 x 256 tiles
+    GemmLaunch L2;   // CTA-pair kernel, 256 x 256 tiles
     muon_status st = MUON_OK;
     int launches = 0;
-    Grouper(muon_plan_s* plan, cudaStream_t stream, bool is_bf16) : p(plan), s(stream), bf16(is_bf16) { reset(); }
-    void reset() {
+    Grouper(muon_plan_s* plan, cudaStream_t stream, bool is_bf16) : p(plan), s(stream), bf16(is_bf16) {
+        reset(L1);
+        reset(L2);
+    }
+    void reset(GemmLaunch& L) {
         std::memset(&L, 0, sizeof(L));
         L.status = p->status;
     }
-    void add(const CUtensorMap& a, const CUtensorMap& b, GemmProblem q) {
-        if (L.nprob == kMaxProblems) flush();
+    static void push(GemmLaunch& L, const CUtensorMap& a, const CUtensorMap& b, GemmProblem q) {
         q.tile_begin = L.total_tiles;
         L.mapA[L.nprob] = a;
         L.mapB[L.nprob] = b;
@@ -265,13 +270,40 @@ struct Grouper {
         L.nprob++;
         L.total_tiles += q.tiles_per_item * q.batch;
     }
-    void flush() {
-        if (L.nprob == 0) return;
+    // a128: A with 128-row boxes; b256 / b128: B with 256- / 128-row boxes (the
+    // same map for an MN-major B).  Problems with more than 128 rows go to the
+    // CTA-pair kernel (each CTA loads 128 rows of A and 128 of B).
+    void add(const CUtensorMap& a128, const CUtensorMap& b256, const CUtensorMap& b128, GemmProblem q) {
+        if (q.M > kBM && p->pair_clusters > 0) {
+            if (L2.nprob == kMaxProblems) flush2();
+            q.tiles_m = (int)ceil_div(q.M, 256);
+            q.tiles_n = (int)ceil_div(q.N, 256);
+            q.tiles_per_item = q.sym ? q.tiles_m * (q.tiles_m + 1) / 2 : q.tiles_m * q.tiles_n;
+            push(L2, a128, b128, q);
+        } else {
+            if (L1.nprob == kMaxProblems) flush1();
+            push(L1, a128, b256, q);
+        }
+    }
+    void flush1() {
+        if (L1.nprob == 0) return;
         if (st == MUON_OK) {
-            st = cuda_status(gemm_launch(L, bf16, p->sm_count, s));
+            st = cuda_status(gemm_launch(L1, bf16, p->sm_count, s));
             ++launches;
         }
-        reset();
+        reset(L1);
+    }
+    void flush2() {
+        if (L2.nprob == 0) return;
+        if (st == MUON_OK) {
+            st = cuda_status(gemm2_launch(L2, bf16, p->pair_clusters, s));
+            ++launches;
+        }
+        reset(L2);
+    }
+    void flush() {
+        flush2();
+        flush1();
     }
 };
 
@@ -527,14 +559,21 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
             ok = ok && make_map(&b.ga[g], b.G[g], false, b.r, b.r, b.batch, b.ldr, 64, kBM);
             ok = ok && make_map(&b.gb[g], b.G[g], false, b.r, b.r, b.batch, b.ldr, 64, kBN);
             ok = ok && make_map(&b.qb[g], b.Q[g], false, b.r, b.r, b.batch, b.ldr, 64, kBN);
+            ok = ok && make_map(&b.qa[g], b.Q[g], false, b.r, b.r, b.batch, b.ldr, 64, kBM);
         }
         ok = ok && make_map(&b.pa, b.P, false, b.r, b.r, b.batch, b.ldr, 64, kBM);
         ok = ok && make_map(&b.pb, b.P, false, b.r, b.r, b.batch, b.ldr, 64, kBN);
         ok = ok && make_map(&b.tb, b.T, false, b.r, b.r, b.batch, b.ldr, 64, kBN);
+        ok = ok && make_map(&b.ta, b.T, false, b.r, b.r, b.batch, b.ldr, 64, kBM);
     }
     ok = ok && cudaMallocHost(&p->h_pinned, sizeof(void*) * 3 * n) == cudaSuccess;
     ok = ok && cudaEventCreateWithFlags(&p->upload_ev, cudaEventDisableTiming) == cudaSuccess;
     ok = ok && gemm_prepare(p->device) == cudaSuccess;
+    if (ok && !p->opts.single_sm_gemm) {
+        int clusters = 0;
+        ok = gemm2_max_clusters(&clusters) == cudaSuccess;
+        p->pair_clusters = clusters;
+    }
     ok = ok && cudaDeviceSynchronize() == cudaSuccess;
     if (!ok) {
         cudaGetLastError();
@@ -646,7 +685,7 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
             q.ldc = b.ldr;
             q.alpha = p->alpha + b.slot_base;
             q.out_scale = b.gscale;
-            g.add(b.ut_a, b.ut_b, q);
+            g.add(b.ut_a, b.ut_b, b.ut_a, q);
         }
         g.flush();
         if (g.st != MUON_OK) return g.st;
@@ -676,7 +715,7 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
                 q.coef_a = kNsA;
                 q.coef_b = kNsB / b.gscale;
                 q.coef_c = kNsC / (b.gscale * b.gscale);
-                g.add(b.ga[gc], b.gb[gc], q);
+                g.add(b.ga[gc], b.gb[gc], b.ga[gc], q);
             }
             g.flush();
             if (g.st != MUON_OK) return g.st;
@@ -691,12 +730,12 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
                         q.C = b.Q[qc ^ 1];
                     else
                         q.Cb = b.Qb;
-                    g.add(b.pa, b.qb[qc], q);
+                    g.add(b.pa, b.qb[qc], b.qa[qc], q);
                 }
                 if (k < J) {
                     GemmProblem q = rr_problem(b, kEpiPlain);
                     q.C = b.T;
-                    g.add(b.pa, b.pb, q);
+                    g.add(b.pa, b.pb, b.pa, q);
                 }
             }
             g.flush();
@@ -709,7 +748,7 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
             for (auto& b : p->buckets) {
                 GemmProblem q = rr_problem(b, kEpiPlain);
                 q.C = b.G[gc ^ 1];
-                g.add(b.ga[gc], b.tb, q);
+                g.add(b.ga[gc], b.tb, b.ta, q);
             }
             g.flush();
             if (g.st != MUON_OK) return g.st;
@@ -740,7 +779,7 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
             q.lr = lr;
             q.wd = wd;
             q.scale = 0.2f * std::sqrt((float)b.c);
-            g.add(b.qb_a, b.ut_mn, q);
+            g.add(b.qb_a, b.ut_mn, b.ut_mn, q);
         }
         g.flush();
         if (g.st != MUON_OK) return g.st;

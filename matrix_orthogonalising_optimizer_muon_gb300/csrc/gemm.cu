@@ -440,13 +440,273 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     }
 }
 
+// ------------------------------------------------------------------ 2-SM kernel
+// A cluster of two CTAs on two SMs computes one 256 x 256 tile with
+// tcgen05.mma.cta_group::2 (M = 256): each CTA stages its own 128 rows of A
+// and one half (128 rows) of B, so each SM moves 32 KB through shared memory
+// per k-block of 4.2 MFLOP instead of 48 KB per 4.2 MFLOP on one SM alone.
+// The even CTA (leader) issues the MMAs; both CTAs' TMA loads signal the
+// leader's `full` barrier; MMA completion is multicast to both CTAs.
+struct Gemm2Cfg {
+    static constexpr int BK = 64;
+    static constexpr int ESZ = 2;
+    static constexpr int UK = 16;
+    static constexpr int A_BYTES = 128 * BK * ESZ;       // this CTA's 128 rows of A
+    static constexpr int B_BYTES = 128 * BK * ESZ;       // this CTA's half of B
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int MN_CHUNK_BYTES = 64 * BK * ESZ;
+    static constexpr int BAR_OFFSET = kStages2 * STAGE_BYTES;
+    static constexpr int SMEM_BYTES = BAR_OFFSET + 256 + 1024;
+};
+
+// Pair tiles: (tm2, tn) of 256 x 256; the CTA of rank `rank` owns rows
+// 256 tm2 + 128 rank .. + 127.  Symmetric outputs keep tn <= tm2.
+__device__ __forceinline__ TileCoord decode_pair_tile(const GemmLaunch& L, int t, uint32_t rank) {
+    int p = 0;
+    while (p + 1 < L.nprob && t >= L.prob[p + 1].tile_begin) ++p;
+    const GemmProblem& P = L.prob[p];
+    const int local = t - P.tile_begin;
+    const int item = local / P.tiles_per_item;
+    const int tl = local - item * P.tiles_per_item;
+    int tm, tn;
+    if (P.sym) {
+        tm = 0;
+        int acc = 0;
+        for (;;) {
+            if (tl < acc + tm + 1) {
+                tn = tl - acc;
+                break;
+            }
+            acc += tm + 1;
+            ++tm;
+        }
+    } else {
+        tm = tl % P.tiles_m;
+        tn = tl / P.tiles_m;
+    }
+    return {p, item, tm * 256 + 128 * (int)rank, tn * 256};
+}
+
+template <bool BF16>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+    gemm2_kernel(const __grid_constant__ GemmLaunch L) {
+    using Cfg = Gemm2Cfg;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::BAR_OFFSET);
+    uint64_t* empty = full + kStages2;
+    uint64_t* tfull = empty + kStages2;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int cluster_id = blockIdx.x >> 1;
+    const int nclusters = gridDim.x >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages2; ++s) {
+            mbar_init(full + s, 1);    // leader: its expect_tx arrival + both CTAs' bytes
+            mbar_init(empty + s, 1);   // both: the leader's multicast commit
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull + a, 1);   // both: the leader's multicast commit
+            mbar_init(tempty + a, 8);  // leader: 4 epilogue warps of each CTA
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        for (int p = 0; p < L.nprob; ++p) {
+            tma_prefetch_desc(&L.mapA[p]);
+            tma_prefetch_desc(&L.mapB[p]);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, 2 * kBN);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();   // barriers of both CTAs initialised before any remote signal
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer (both CTAs)
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = cluster_id; ok && t < L.total_tiles; t += nclusters) {
+                const TileCoord tc = decode_pair_tile(L, t, rank);
+                const GemmProblem& P = L.prob[tc.p];
+                const int kblocks = (P.K + Cfg::BK - 1) / Cfg::BK;
+                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                    const uint32_t s = it % kStages2;
+                    const uint32_t ph = (it / kStages2) & 1u;
+                    if (!mbar_wait_cluster(empty + s, ph ^ 1u, abort_flag, L.status, kStatusTimeoutProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sa = smem + s * Cfg::STAGE_BYTES;
+                    uint8_t* sb = sa + Cfg::A_BYTES;
+                    const uint32_t fb = mapa_shared(smem_u32(full + s), 0);
+                    if (leader) mbar_arrive_expect_tx(full + s, 2 * Cfg::STAGE_BYTES);
+                    tma_load_3d_pair(sa, &L.mapA[tc.p], fb, kb * Cfg::BK, tc.m0, tc.item);
+                    const int nb = tc.n0 + 128 * (int)rank;
+                    if (!P.b_mn) {
+                        tma_load_3d_pair(sb, &L.mapB[tc.p], fb, kb * Cfg::BK, nb, tc.item);
+                    } else {
+                        tma_load_3d_pair(sb, &L.mapB[tc.p], fb, nb, kb * Cfg::BK, tc.item);
+                        tma_load_3d_pair(sb + Cfg::MN_CHUNK_BYTES, &L.mapB[tc.p], fb, nb + 64, kb * Cfg::BK,
+                                         tc.item);
+                    }
+                }
+            }
+            if (!ok) {
+                // copies already issued signal the leader; give them time to land
+                const unsigned long long t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 2000000ull) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            // ---------------- MMA issuer (one thread of the even CTA)
+            uint32_t it = 0;
+            int local = 0;
+            bool ok = true;
+            for (int t = cluster_id; ok && t < L.total_tiles; t += nclusters, ++local) {
+                const TileCoord tc = decode_pair_tile(L, t, rank);
+                const GemmProblem& P = L.prob[tc.p];
+                const int kblocks = (P.K + Cfg::BK - 1) / Cfg::BK;
+                const uint32_t acc = local & 1;
+                const uint32_t aph = (local >> 1) & 1u;
+                if (!mbar_wait_cluster(tempty + acc, aph ^ 1u, abort_flag, L.status, kStatusTimeoutMma)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * kBN;
+                const uint32_t idesc = idesc_make(BF16, 256, kBN, false, P.b_mn != 0);
+                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                    const uint32_t s = it % kStages2;
+                    const uint32_t ph = (it / kStages2) & 1u;
+                    if (!mbar_wait_cluster(full + s, ph, abort_flag, L.status, kStatusTimeoutMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(smem + s * Cfg::STAGE_BYTES);
+                    const uint32_t b_addr = a_addr + Cfg::A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < Cfg::BK / Cfg::UK; ++kk) {
+                        const uint64_t ad = sdesc_sw128(a_addr + kk * Cfg::UK * Cfg::ESZ, 0, 1024);
+                        const uint64_t bd =
+                            P.b_mn ? sdesc_sw128(b_addr + kk * Cfg::UK * 128, Cfg::MN_CHUNK_BYTES, 1024)
+                                   : sdesc_sw128(b_addr + kk * Cfg::UK * Cfg::ESZ, 0, 1024);
+                        mma_f16kind_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+                    }
+                    mma_commit_pair(empty + s, 3);   // frees the stage in both CTAs
+                }
+                if (!ok) break;
+                mma_commit_pair(tfull + acc, 3);     // both CTAs' accumulators ready
+            }
+            mma_commit_pair(drain, 1);
+            mbar_drain(drain, 0);
+        }
+    } else {
+        // ---------------- epilogue: warps 2..5 of both CTAs, each on its own TMEM
+        const int wq = warp & 3;
+        const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), 0);
+        int local = 0;
+        for (int t = cluster_id; t < L.total_tiles; t += nclusters, ++local) {
+            const TileCoord tc = decode_pair_tile(L, t, rank);
+            const GemmProblem& P = L.prob[tc.p];
+            const uint32_t acc = local & 1;
+            const uint32_t aph = (local >> 1) & 1u;
+            if (!mbar_wait_cluster(tfull + acc, aph, abort_flag, L.status, kStatusTimeoutEpilogue)) break;
+            tc_fence_after();
+            const int row = tc.m0 + wq * 32 + lane;
+            const int warp_row_max = tc.m0 + wq * 32 + 31;
+            const uint32_t tbase = tmem_base + acc * kBN + (static_cast<uint32_t>(wq * 32) << 16);
+            for (int cc = 0; cc < kBN; cc += 32) {
+                const int col0 = tc.n0 + cc;
+                if (col0 >= P.N) break;
+                if (P.sym && col0 > warp_row_max) break;
+                uint32_t raw[32];
+                tmem_ld32(tbase + cc, raw);
+                if (P.epi == kEpiApply) {
+                    const ApplyCtx ac = apply_ctx(P, tc.item, row < P.M ? row : 0, col0);
+                    float w[32];
+                    apply_load(P, ac, row, col0, w);
+                    tmem_ld_wait();
+                    apply_store(P, ac, tc.item, row, col0, raw, w);
+                } else {
+                    tmem_ld_wait();
+                    epilogue_chunk(P, tc.item, row, col0, raw);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader)
+                    mbar_arrive(tempty + acc);
+                else
+                    mbar_arrive_remote(tempty_leader + acc * 8);
+            }
+        }
+    }
+
+    tc_fence_before();
+    cluster_sync();   // all pair MMAs done and both TMEMs drained
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, 2 * kBN);
+    }
+}
+
 cudaError_t gemm_prepare(int device) {
     (void)device;
     cudaError_t e =
         cudaFuncSetAttribute(gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, GemmCfg::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                GemmCfg::SMEM_BYTES);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 GemmCfg::SMEM_BYTES);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemm2_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Gemm2Cfg::SMEM_BYTES);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemm2_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Gemm2Cfg::SMEM_BYTES);
+    return e;
+}
+
+cudaError_t gemm2_max_clusters(int* out) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.dynamicSmemBytes = Gemm2Cfg::SMEM_BYTES;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(out, gemm2_kernel<true>, &cfg);
+}
+
+cudaError_t gemm2_launch(const GemmLaunch& L, bool bf16, int clusters, cudaStream_t s) {
+    if (L.total_tiles <= 0) return cudaSuccess;
+    if (clusters > L.total_tiles) clusters = L.total_tiles;
+    if (clusters < 1) clusters = 1;
+    if (bf16)
+        gemm2_kernel<true><<<2 * clusters, kGemmThreads, Gemm2Cfg::SMEM_BYTES, s>>>(L);
+    else
+        gemm2_kernel<false><<<2 * clusters, kGemmThreads, Gemm2Cfg::SMEM_BYTES, s>>>(L);
+    return cudaGetLastError();
 }
 
 cudaError_t gemm_launch(const GemmLaunch& L, bool bf16, int grid, cudaStream_t s) {

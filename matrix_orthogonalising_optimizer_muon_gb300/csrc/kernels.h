@@ -13,7 +13,8 @@ namespace muon {
 // Tile of one tensor-core product: BM x BN output, one tcgen05.mma M=128 N=256.
 constexpr int kBM = 128;
 constexpr int kBN = 256;
-constexpr int kStages = 4;
+constexpr int kStages = 4;      // 1-SM kernel: 48 KB per stage
+constexpr int kStages2 = 6;     // 2-SM kernel: 32 KB per stage per CTA
 constexpr int kMaxProblems = 8;
 constexpr int kGemmThreads = 192;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
 
@@ -67,6 +68,10 @@ size_t gemm_smem_bytes();
 cudaError_t gemm_prepare(int device);   // sets the dynamic shared-memory limit once
 // bf16 = true: bf16 operands (SYRK, final product); false: fp16 operands (r x r products)
 cudaError_t gemm_launch(const GemmLaunch& L, bool bf16, int grid, cudaStream_t s);
+// CTA-pair kernel (cluster of 2, tcgen05 cta_group::2, 256 x 256 tiles); problems
+// use pair tiling: tiles_m = ceil(M / 256), tiles_n = ceil(N / 256).
+cudaError_t gemm2_max_clusters(int* out);
+cudaError_t gemm2_launch(const GemmLaunch& L, bool bf16, int clusters, cudaStream_t s);
 
 // ------------------------------------------------------------------ elementwise
 // Per plan matrix, resident on the device.

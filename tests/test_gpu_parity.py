@@ -125,6 +125,16 @@ def test_mixed_ragged_plan_ns5(grad_dtype):
         assert_ns(res, i)
 
 
+def test_single_sm_kernel_ns5():
+    """The same mixed plan on the one-SM kernel only (128 x 256 tiles, cta_group::1):
+    both tensor-core kernels stay at the oracle's bar, and agree with each other."""
+    pair = run_step(RAGGED, "bf16", base_seed=26)
+    single = run_step(RAGGED, "bf16", base_seed=26, single_sm_gemm=True)
+    for i in range(len(RAGGED)):
+        assert_ns(single, i)
+        assert rel(single["O"][i].numpy(), pair["O"][i].double().numpy()) < 2e-3, RAGGED[i]
+
+
 def test_batched_bucket_ns5():
     """Several same-shape matrices batched in one bucket (grouped launch items)."""
     shapes = [(200, 520)] * 5 + [(520, 200)] * 3
