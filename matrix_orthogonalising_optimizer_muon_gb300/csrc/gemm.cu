@@ -96,28 +96,22 @@ __device__ __forceinline__ void store_sym(const GemmProblem& P, int item, int ro
     const long long rbase = (long long)row * P.ldc + col0;
     const bool full = (col0 + 31 <= row) && (col0 + 31 < P.N);
     if (full) {
-        uint4 h[4], b[4];
+        if (C || C2) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            h[q] = make_uint4(pack_half2(v[8 * q], v[8 * q + 1]), pack_half2(v[8 * q + 2], v[8 * q + 3]),
-                              pack_half2(v[8 * q + 4], v[8 * q + 5]), pack_half2(v[8 * q + 6], v[8 * q + 7]));
-            b[q] = make_uint4(pack_bf162(v[8 * q], v[8 * q + 1]), pack_bf162(v[8 * q + 2], v[8 * q + 3]),
-                              pack_bf162(v[8 * q + 4], v[8 * q + 5]), pack_bf162(v[8 * q + 6], v[8 * q + 7]));
-        }
-        if (C) {
-            uint4* d = reinterpret_cast<uint4*>(C + rbase);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) d[q] = h[q];
-        }
-        if (C2) {
-            uint4* d = reinterpret_cast<uint4*>(C2 + rbase);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) d[q] = h[q];
+            for (int q = 0; q < 4; ++q) {
+                const uint4 h = make_uint4(pack_half2(v[8 * q], v[8 * q + 1]), pack_half2(v[8 * q + 2], v[8 * q + 3]),
+                                           pack_half2(v[8 * q + 4], v[8 * q + 5]),
+                                           pack_half2(v[8 * q + 6], v[8 * q + 7]));
+                if (C) reinterpret_cast<uint4*>(C + rbase)[q] = h;
+                if (C2) reinterpret_cast<uint4*>(C2 + rbase)[q] = h;
+            }
         }
         if (Cb) {
-            uint4* d = reinterpret_cast<uint4*>(Cb + rbase);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) d[q] = b[q];
+            for (int q = 0; q < 4; ++q)
+                reinterpret_cast<uint4*>(Cb + rbase)[q] =
+                    make_uint4(pack_bf162(v[8 * q], v[8 * q + 1]), pack_bf162(v[8 * q + 2], v[8 * q + 3]),
+                               pack_bf162(v[8 * q + 4], v[8 * q + 5]), pack_bf162(v[8 * q + 6], v[8 * q + 7]));
         }
     } else {
 #pragma unroll
@@ -187,8 +181,28 @@ __device__ __forceinline__ void apply_load(const GemmProblem& P, const ApplyCtx&
             w[4 * q + 3] = t.w;
         }
     } else {
+        const float* base = c.W + c.base;
+        const int st = (int)c.stride;   // 1 or M (< 2^20): 32-bit offsets keep few registers live
+        const int nj = min(32, P.N - col0);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) w[j] = (col0 + j < P.N) ? c.W[c.base + j * c.stride] : 0.f;
+        for (int j = 0; j < 32; ++j) w[j] = (j < nj) ? base[j * st] : 0.f;
+    }
+}
+
+// Debug copy of O = alpha * acc (plans with keep_update only).  Kept out of line
+// so its registers do not weigh on the fused update of every other plan.
+__device__ __noinline__ void store_debug_update(const GemmProblem& P, const ApplyCtx& c, int row, int col0, float al,
+                                                const uint32_t (&raw)[32]) {
+    if (c.vec) {
+        float4* o4 = reinterpret_cast<float4*>(c.O + c.base);
+        for (int q = 0; q < 8; ++q)
+            o4[q] = make_float4(al * __uint_as_float(raw[4 * q]), al * __uint_as_float(raw[4 * q + 1]),
+                                al * __uint_as_float(raw[4 * q + 2]), al * __uint_as_float(raw[4 * q + 3]));
+    } else {
+        float* base = c.O + c.base;
+        const int st = (int)c.stride;
+        const int nj = min(32, P.N - col0);
+        for (int j = 0; j < nj; ++j) base[j * st] = al * __uint_as_float(raw[j]);
     }
 }
 
@@ -197,83 +211,68 @@ __device__ __forceinline__ void apply_store(const GemmProblem& P, const ApplyCtx
     if (row >= P.M) return;
     const float al = P.alpha[item];
     const float lr = P.lr, wd = P.wd, s = P.scale;
-    float o[32];
+    const int st = (int)c.stride;   // 1 or M (< 2^20): 32-bit offsets keep few registers live
+    const int nj = min(32, P.N - col0);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        o[j] = al * __uint_as_float(raw[j]);
-        w[j] = w[j] - lr * (s * o[j] + wd * w[j]);
-    }
+    for (int j = 0; j < 32; ++j) w[j] = w[j] - lr * (s * (al * __uint_as_float(raw[j])) + wd * w[j]);
     if (c.vec) {
         float4* w4 = reinterpret_cast<float4*>(c.W + c.base);
 #pragma unroll
         for (int q = 0; q < 8; ++q) w4[q] = make_float4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-        if (c.O) {
-            float4* o4 = reinterpret_cast<float4*>(c.O + c.base);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) o4[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-        }
     } else {
+        float* base = c.W + c.base;
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-            if (col0 + j < P.N) c.W[c.base + j * c.stride] = w[j];
-        if (c.O) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (col0 + j < P.N) c.O[c.base + j * c.stride] = o[j];
-        }
+            if (j < nj) base[j * st] = w[j];
     }
+    if (c.O) store_debug_update(P, c, row, col0, al, raw);
 }
 
 __device__ __forceinline__ void epilogue_chunk(const GemmProblem& P, int item, int row, int col0,
                                                const uint32_t (&raw)[32]) {
     float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw[j]);
     if (P.epi == kEpiSyrk) {
         const float al = P.alpha[item];
         const float k = P.out_scale * al * al;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = k * __uint_as_float(raw[j]);
+        for (int j = 0; j < 32; ++j) v[j] *= k;
     } else if (P.epi == kEpiPoly) {
-        // P = a I + b' G' + c' G'^2, with G' read from the fp16 input the MMA used
-        float g[32];
-        if (row < P.M) {
-            const __half* Grow = P.Gin + item * P.strideC + (long long)row * P.ldc + col0;
-            if (col0 + 31 < P.N) {
-                const uint4* g4 = reinterpret_cast<const uint4*>(Grow);
+        // P = a I + b' G' + c' G'^2, with G' read (8 values at a time) from the fp16
+        // input the MMA used
+        const __half* Grow = P.Gin + item * P.strideC + (long long)(row < P.M ? row : 0) * P.ldc + col0;
+        const bool vec = (row < P.M) && (col0 + 31 < P.N);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint4 t = g4[q];
-                    const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+        for (int q = 0; q < 4; ++q) {
+            float g[8];
+            if (vec) {
+                const uint4 t = reinterpret_cast<const uint4*>(Grow)[q];
+                const uint32_t w4[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-                        g[8 * q + 2 * e] = f.x;
-                        g[8 * q + 2 * e + 1] = f.y;
-                    }
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
+                    g[2 * e] = f.x;
+                    g[2 * e + 1] = f.y;
                 }
             } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) g[j] = (col0 + j < P.N) ? __half2float(Grow[j]) : 0.f;
+                for (int e = 0; e < 8; ++e)
+                    g[e] = (row < P.M && col0 + 8 * q + e < P.N) ? __half2float(Grow[8 * q + e]) : 0.f;
             }
-        } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) g[j] = 0.f;
+            for (int e = 0; e < 8; ++e) {
+                const int j = 8 * q + e;
+                v[j] = P.coef_c * v[j] + P.coef_b * g[e] + ((col0 + j == row) ? P.coef_a : 0.f);
+            }
         }
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            float x = P.coef_c * __uint_as_float(raw[j]) + P.coef_b * g[j];
-            if (col0 + j == row) x += P.coef_a;
-            v[j] = x;
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw[j]);
     }
     store_sym(P, item, row, col0, v);
 }
 
 // ------------------------------------------------------------------ kernel
 template <bool BF16>
-__global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmLaunch L) {
+__global__ void __maxnreg__(200) gemm_kernel(const __grid_constant__ GemmLaunch L) {
     using Cfg = GemmCfg;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -295,7 +294,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull + a, 1);
-            mbar_init(tempty + a, 4);
+            mbar_init(tempty + a, kEpiWarps);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -396,8 +395,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             mbar_drain(drain, 0);
         }
     } else {
-        // ---------------- epilogue: warps 2..5, TMEM lane quarter = warp % 4
+        // ---------------- epilogue: TMEM lane quarter = warp % 4; warps 2-5 take
+        // columns 0-127 of the tile, warps 6-9 columns 128-255
         const int wq = warp & 3;
+        const int c_begin = ((warp - 2) >> 2) * (kBN * 4 / kEpiWarps);
         int local = 0;
         for (int t = blockIdx.x; t < L.total_tiles; t += gridDim.x, ++local) {
             const TileCoord tc = decode_tile(L, t);
@@ -409,7 +410,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             const int row = tc.m0 + wq * 32 + lane;
             const int warp_row_max = tc.m0 + wq * 32 + 31;
             const uint32_t tbase = tmem_base + acc * kBN + (static_cast<uint32_t>(wq * 32) << 16);
-            for (int cc = 0; cc < kBN; cc += 32) {
+            for (int cc = c_begin; cc < c_begin + kBN * 4 / kEpiWarps; cc += 32) {
                 const int col0 = tc.n0 + cc;
                 if (col0 >= P.N) break;                              // warp-uniform
                 if (P.sym && col0 > warp_row_max) break;             // whole chunk above the diagonal
@@ -488,7 +489,7 @@ __device__ __forceinline__ TileCoord decode_pair_tile(const GemmLaunch& L, int t
 }
 
 template <bool BF16>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(200)
     gemm2_kernel(const __grid_constant__ GemmLaunch L) {
     using Cfg = Gemm2Cfg;
     extern __shared__ uint8_t smem_raw[];
@@ -515,7 +516,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull + a, 1);   // both: the leader's multicast commit
-            mbar_init(tempty + a, 8);  // leader: 4 epilogue warps of each CTA
+            mbar_init(tempty + a, 2 * kEpiWarps);   // leader: every epilogue warp of both CTAs
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -617,8 +618,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             mbar_drain(drain, 0);
         }
     } else {
-        // ---------------- epilogue: warps 2..5 of both CTAs, each on its own TMEM
+        // ---------------- epilogue of both CTAs, each on its own TMEM: lane quarter =
+        // warp % 4; warps 2-5 take columns 0-127 of the tile, warps 6-9 columns 128-255
         const int wq = warp & 3;
+        const int c_begin = ((warp - 2) >> 2) * (kBN * 4 / kEpiWarps);
         const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), 0);
         int local = 0;
         for (int t = cluster_id; t < L.total_tiles; t += nclusters, ++local) {
@@ -631,7 +634,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             const int row = tc.m0 + wq * 32 + lane;
             const int warp_row_max = tc.m0 + wq * 32 + 31;
             const uint32_t tbase = tmem_base + acc * kBN + (static_cast<uint32_t>(wq * 32) << 16);
-            for (int cc = 0; cc < kBN; cc += 32) {
+            for (int cc = c_begin; cc < c_begin + kBN * 4 / kEpiWarps; cc += 32) {
                 const int col0 = tc.n0 + cc;
                 if (col0 >= P.N) break;
                 if (P.sym && col0 > warp_row_max) break;

@@ -14,9 +14,17 @@ namespace muon {
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kStages = 4;      // 1-SM kernel: 48 KB per stage
-constexpr int kStages2 = 6;     // 2-SM kernel: 32 KB per stage per CTA
+#ifndef MUON_PAIR_STAGES
+#define MUON_PAIR_STAGES 6
+#endif
+constexpr int kStages2 = MUON_PAIR_STAGES;   // 2-SM kernel: 32 KB per stage per CTA
 constexpr int kMaxProblems = 8;
-constexpr int kGemmThreads = 192;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
+#ifndef MUON_EPI_WARPS
+#define MUON_EPI_WARPS 8
+#endif
+// 4: one warp per TMEM lane quarter; 8: two, each on half of the 256 columns
+constexpr int kEpiWarps = MUON_EPI_WARPS;
+constexpr int kGemmThreads = 32 * (2 + kEpiWarps);   // warp 0 TMA, warp 1 MMA + TMEM, warps 2.. epilogue
 
 enum Epilogue : int {
     kEpiSyrk = 0,    // C = s alpha^2 acc                          (G0' = s X0 X0^T)

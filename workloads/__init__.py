@@ -13,6 +13,8 @@ Workloads (shapes as stored, row-major m x n):
   matrices plus 28 transposed-aspect 3584 x 512 matrices.
 * ``dit1p3b``: 28 DiT blocks at hidden 2048: qkv 6144x2048, attn-out 2048x2048,
   mlp-in 8192x2048, mlp-out 2048x8192, adaLN 12288x2048 (periodic RowNorm, K=4).
+* ``dit_block``: one of those blocks (0.75 GB of W, G, M: still above L2), the
+  small case used to profile the RowNorm kernels.
 
 Values: W ~ N(0, 0.02^2), G ~ N(0, 1e-3^2), M ~ N(0, 1e-3^2); G is bf16 except
 in ``single``.  Each tensor gets its own seed from (workload, step, matrix, kind).
@@ -60,6 +62,7 @@ WORKLOADS = {
     "qwen7b_28l": Workload("qwen7b_28l", _qwen_layer() * 28, "bf16", 2, steps=10),
     "qwen7b_heads": Workload("qwen7b_heads", _qwen_heads(), "bf16", 3),
     "dit1p3b": Workload("dit1p3b", _dit_block() * 28, "bf16", 4, steps=8, rownorm_k=4),
+    "dit_block": Workload("dit_block", _dit_block(), "bf16", 5, steps=8, rownorm_k=4),
 }
 
 
