@@ -244,7 +244,7 @@ __global__ void k_identity_bf16(__nv_bfloat16* q, int r, int ld, long long total
 }
 
 // ------------------------------------------------------------------ RowNorm, m <= n (stored rows)
-constexpr int kRowMaxVec = 16;   // float4 groups per thread kept in registers (rows <= 16384)
+constexpr int kRowMaxVec = 8;    // float4 groups per thread kept in registers (rows <= 8192)
 
 template <bool BF16>
 __global__ void __launch_bounds__(kElemThreads) k_rownorm_rows(const ElemArgs a) {
@@ -265,7 +265,14 @@ __global__ void __launch_bounds__(kElemThreads) k_rownorm_rows(const ElemArgs a)
                      aligned16(M) && aligned16(W);
     float ss = 0.f;
     if (reg) {
-        float4 u[kRowMaxVec];
+        // W is loaded with G and M, so all three streams are in flight across the
+        // row reduction
+        float4 u[kRowMaxVec], wv[kRowMaxVec];
+#pragma unroll
+        for (int v = 0; v < kRowMaxVec; ++v) {
+            const long long j = 4LL * (v * kElemThreads + t);
+            if (j < n) wv[v] = *reinterpret_cast<const float4*>(W + j);
+        }
 #pragma unroll
         for (int v = 0; v < kRowMaxVec; ++v) {
             const long long j = 4LL * (v * kElemThreads + t);
@@ -285,7 +292,7 @@ __global__ void __launch_bounds__(kElemThreads) k_rownorm_rows(const ElemArgs a)
         for (int v = 0; v < kRowMaxVec; ++v) {
             const long long j = 4LL * (v * kElemThreads + t);
             if (j < n) {
-                float4 w = *reinterpret_cast<float4*>(W + j);
+                float4 w = wv[v];
                 w.x = w.x - lr * (k * u[v].x + wd * w.x);
                 w.y = w.y - lr * (k * u[v].y + wd * w.y);
                 w.z = w.z - lr * (k * u[v].z + wd * w.z);
@@ -337,6 +344,7 @@ __global__ void __launch_bounds__(kElemThreads) k_rownorm_colstats(const ElemArg
     if (j >= n) return;
     const bool vec = (n % 4 == 0) && g_vec_ok<BF16>(G) && aligned16(M);
     if (vec) {
+#pragma unroll 4
         for (long long i = i0; i < i1; ++i) {
             const long long e = i * n + j;
             const float4 g = load_g4<BF16>(G, e);
