@@ -65,7 +65,10 @@ typedef struct {
     /* nonzero: run every tensor-core product on the one-SM kernel (128 x 256 tiles)
        instead of the CTA-pair kernel (256 x 256 tiles, tcgen05 cta_group::2) */
     int32_t single_sm_gemm;
-    int32_t reserved[5];
+    /* nonzero: matrices with min(m, n) <= 128 also take the batched products instead of
+       the fused kernel that runs the whole step of such a matrix on one SM */
+    int32_t generic_small;
+    int32_t reserved[4];
 } muon_plan_opts;
 
 typedef struct muon_plan_s* muon_plan;
@@ -92,7 +95,10 @@ void muon_plan_destroy(muon_plan p);
  * muon_step - one Muon step over every matrix of the plan.
  *   params, grads, momentum  host arrays of n device pointers (see conventions).
  *   lr >= 0, wd >= 0, 0 <= mu < 1, all finite.
- *   ns_steps in [0, 16]: Newton-Schulz iterations (5 in the pages; 0 gives O = X0).
+ *   ns_steps in [0, 5]: Newton-Schulz iterations (5 in the pages; 0 gives O = X0).  The
+ *     Gram-space recursion carries G in fp16; a rounding-level negative eigenvalue of G
+ *     grows about 12x per step, so beyond five steps it can diverge on rank-deficient or
+ *     large square inputs.  Larger values return MUON_ERR_INVALID_ARG.
  *   mode MUON_MODE_NS, or MUON_MODE_ROWNORM (then equal to muon_rownorm_step with eps = 1e-8).
  * A matrix whose Nesterov input U is all zero gets O = 0 (only weight decay acts).
  * params and momentum must not overlap each other, the grads, or any other matrix.
@@ -167,6 +173,9 @@ muon_status muon_rownorm_matrix_noalloc(float* param, const void* grad, float* m
 /* Human-readable name of a status code (static string). */
 const char* muon_status_string(muon_status s);
 
+/* Text of the last CUDA error this thread's calls turned into MUON_ERR_CUDA (static string). */
+const char* muon_last_error_detail(void);
+
 /* Plan introspection. */
 typedef struct {
     int32_t n_matrices;
@@ -183,7 +192,8 @@ muon_status muon_plan_info(muon_plan p, muon_plan_info_t* info);
  * since the previous call, measured with CUDA events recorded on each step's
  * stream (needs opts.timing; waits for those steps, then resets the sums).
  * Stages: [0] momentum + Nesterov + norm, [1] Gram SYRK, [2] r x r
- * Newton-Schulz products, [3] final product + fused apply, [4] RowNorm steps.
+ * Newton-Schulz products (and the whole fused step of matrices with
+ * min(m, n) <= 128), [3] final product + fused apply, [4] RowNorm steps.
  * n_stages <= 5.  flops (nullable) receives the algorithmic tensor FLOPs of
  * stages 1-3 over the same steps (symmetric products counted at half).
  * Returns MUON_ERR_INVALID_ARG when no timed step was run.

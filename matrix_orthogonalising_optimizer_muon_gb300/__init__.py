@@ -42,7 +42,8 @@ class MuonShape(ctypes.Structure):
 
 class MuonPlanOpts(ctypes.Structure):
     _fields_ = [("keep_update", ctypes.c_int32), ("timing", ctypes.c_int32),
-                ("single_sm_gemm", ctypes.c_int32), ("reserved", ctypes.c_int32 * 5)]
+                ("single_sm_gemm", ctypes.c_int32), ("generic_small", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 4)]
 
 
 class MuonPlanInfo(ctypes.Structure):
@@ -67,6 +68,7 @@ EXPORTED = {
     "muon_debug_copy_workspace": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int32, _P,
                                                  ctypes.POINTER(ctypes.c_int32), _P]),
     "muon_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "muon_last_error_detail": (ctypes.c_char_p, []),
     "muon_plan_info": (ctypes.c_int, [_P, ctypes.POINTER(MuonPlanInfo)]),
     "muon_stage_times": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_float),
                                         ctypes.POINTER(ctypes.c_double), ctypes.c_int32]),
@@ -100,8 +102,11 @@ def load(path: str | None = None):
 class MuonError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
-        msg = load().muon_status_string(code)
-        super().__init__("%s: %s" % (where, msg.decode() if msg else code))
+        lib = load()
+        msg = lib.muon_status_string(code).decode()
+        if code == MUON_ERR_CUDA:
+            msg += " (%s)" % lib.muon_last_error_detail().decode()
+        super().__init__("%s: %s" % (where, msg))
 
 
 def _check(code: int, where: str):
@@ -132,12 +137,13 @@ class MuonPlan:
     updates params and momentum in place on the current stream."""
 
     def __init__(self, shapes, grad_dtype: str = "bf16", keep_update: bool = False,
-                 timing: bool = False, single_sm_gemm: bool = False):
+                 timing: bool = False, single_sm_gemm: bool = False, generic_small: bool = False):
         self.lib = load()
         self.shapes = [(int(m), int(n)) for m, n in shapes]
         self.grad_dtype = grad_dtype
         arr = (MuonShape * len(self.shapes))(*[MuonShape(m, n) for m, n in self.shapes])
-        opts = MuonPlanOpts(1 if keep_update else 0, 1 if timing else 0, 1 if single_sm_gemm else 0)
+        opts = MuonPlanOpts(1 if keep_update else 0, 1 if timing else 0, 1 if single_sm_gemm else 0,
+                            1 if generic_small else 0)
         h = ctypes.c_void_p()
         gd = {"bf16": MUON_BF16, "f32": MUON_F32}[grad_dtype]
         _check(self.lib.muon_plan_create(arr, len(self.shapes), gd, ctypes.byref(opts),

@@ -28,7 +28,12 @@ namespace {
 constexpr float kNsA = 3.4445f;
 constexpr float kNsB = -4.7750f;
 constexpr float kNsC = 2.0315f;
-constexpr int kMaxNsSteps = 16;
+// Limit on Newton-Schulz steps of the Gram-form recursion.  It carries G in 11
+// significant bits (fp16); rounding can leave a null-space eigenvalue of G slightly
+// negative, and each step multiplies such an eigenvalue by about p(0)^2 = a^2 ~ 11.9,
+// so on rank-deficient or large square inputs it grows to O(1) and diverges after
+// about six steps.  Five steps (the pages' choice) keep it below 1e-2.
+constexpr int kMaxNsSteps = 5;
 constexpr int kMaxDim = 1 << 20;        // per-dimension limit of this build
 constexpr int kMaxR = 32768;            // r x r workspace limit of this build
 
@@ -71,6 +76,7 @@ inline long long round_up(long long a, long long b) { return ceil_div(a, b) * b;
 
 struct Bucket {
     int r = 0, c = 0, batch = 0;
+    bool fused = false;     // r <= 128: whole step in the fused one-matrix-per-CTA kernel
     int ldr = 0;   // leading dim of r x r buffers (multiple of 8)
     int ldu = 0;   // leading dim of X0 rows (multiple of 8)
     std::vector<int> mats;
@@ -141,12 +147,21 @@ struct muon_plan_s {
 
 namespace {
 
-muon_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA; }
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+muon_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return MUON_OK;
+    g_last_cuda_error = e;
+    return MUON_ERR_CUDA;
+}
 
 #define MUON_TRY(expr)                                    \
     do {                                                  \
         cudaError_t e__ = (expr);                         \
-        if (e__ != cudaSuccess) return MUON_ERR_CUDA;     \
+        if (e__ != cudaSuccess) {                         \
+            g_last_cuda_error = e__;                      \
+            return MUON_ERR_CUDA;                         \
+        }                                                 \
     } while (0)
 
 bool finite_nonneg(float x) { return std::isfinite(x) && x >= 0.f; }
@@ -335,6 +350,10 @@ void free_plan(muon_plan_s* p) {
 }  // namespace
 
 extern "C" {
+
+const char* muon_last_error_detail(void) {
+    return g_last_cuda_error == cudaSuccess ? "no CUDA error recorded" : cudaGetErrorString(g_last_cuda_error);
+}
 
 const char* muon_status_string(muon_status s) {
     switch (s) {
@@ -548,6 +567,7 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
         b.Q[0] = reinterpret_cast<__half*>(base + o_rr[k] + 4 * step);
         b.Q[1] = reinterpret_cast<__half*>(base + o_rr[k] + 5 * step);
         b.gscale = std::ldexp(1.f, (int)std::lround(std::log2((double)b.r)));
+        b.fused = b.r <= kSmallMaxR && !p->opts.generic_small;
         b.Qb = reinterpret_cast<__nv_bfloat16*>(base + o_qb[k]);
         b.Odbg = p->opts.keep_update ? reinterpret_cast<float*>(base + o_odbg[k]) : nullptr;
         __nv_bfloat16* ut = p->ut + b.ut_off;
@@ -679,6 +699,7 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
     {
         Grouper g(p, s, true);
         for (auto& b : p->buckets) {
+            if (b.fused) continue;
             GemmProblem q = problem(b.r, b.r, b.c, b.batch, true, kEpiSyrk);
             q.C = b.G[0];
             q.strideC = (long long)b.r * b.ldr;
@@ -692,6 +713,49 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
         launches += g.launches;
     }
     if (se) MUON_TRY(cudaEventRecord(se->e[2], s));
+
+    // ---- r <= 128: the whole step of each matrix (SYRK, recursion, final product +
+    // update) in one fused launch; its time is counted in the r x r stage
+    {
+        GemmLaunch Ls;
+        std::memset(&Ls, 0, sizeof(Ls));
+        Ls.status = p->status;
+        float* const* W = reinterpret_cast<float* const*>(p->d_ptrs + 2 * n);
+        auto flush_small = [&]() -> muon_status {
+            if (Ls.nprob == 0) return MUON_OK;
+            const muon_status st2 = cuda_status(ns_small_launch(Ls, p->sm_count, s));
+            ++launches;
+            std::memset(&Ls, 0, sizeof(Ls));
+            Ls.status = p->status;
+            return st2;
+        };
+        for (auto& b : p->buckets) {
+            if (!b.fused) continue;
+            if (Ls.nprob == kMaxProblems && (st = flush_small()) != MUON_OK) return st;
+            GemmProblem q = problem(b.r, b.c, b.r, b.batch, false, kEpiApply);
+            q.tiles_per_item = 1;
+            q.tile_begin = Ls.total_tiles;
+            q.alpha = p->alpha + b.slot_base;
+            q.item_mat = b.d_item_mat;
+            q.W = W;
+            q.transposed = p->d_transposed;
+            q.Odbg = b.Odbg;
+            q.lr = lr;
+            q.wd = wd;
+            q.scale = 0.2f * std::sqrt((float)b.c);
+            q.out_scale = b.gscale;
+            q.coef_a = kNsA;
+            q.coef_b = kNsB / b.gscale;
+            q.coef_c = kNsC / (b.gscale * b.gscale);
+            q.ns_steps = ns_steps;
+            Ls.mapA[Ls.nprob] = b.ut_a;
+            Ls.mapB[Ls.nprob] = b.ut_mn;
+            Ls.prob[Ls.nprob] = q;
+            Ls.nprob++;
+            Ls.total_tiles += b.batch;
+        }
+        if ((st = flush_small()) != MUON_OK) return st;
+    }
 
     // ---- Newton-Schulz in the Gram space (fp16 operands, G carried as s G)
     const int J = ns_steps;
@@ -707,6 +771,7 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
         {   // P = aI + (b/s) G' + (c/s^2) G'^2 (at k = 1 this is also Q_1)
             Grouper g(p, s, false);
             for (auto& b : p->buckets) {
+            if (b.fused) continue;
                 GemmProblem q = rr_problem(b, kEpiPoly);
                 q.C = b.P;
                 if (k == 1 && J > 1) q.C2 = b.Q[0];
@@ -724,6 +789,7 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
         {   // Q' = P Q (k >= 2) and T = P P (k < J), independent: one launch
             Grouper g(p, s, false);
             for (auto& b : p->buckets) {
+            if (b.fused) continue;
                 if (k >= 2) {
                     GemmProblem q = rr_problem(b, kEpiPlain);
                     if (k < J)
@@ -746,6 +812,7 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
         if (k < J) {   // G'' = G' T
             Grouper g(p, s, false);
             for (auto& b : p->buckets) {
+            if (b.fused) continue;
                 GemmProblem q = rr_problem(b, kEpiPlain);
                 q.C = b.G[gc ^ 1];
                 g.add(b.ga[gc], b.tb, b.ta, q);
@@ -758,6 +825,7 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
     }
     if (J == 0) {
         for (auto& b : p->buckets) {
+            if (b.fused) continue;
             MUON_TRY(launch_identity_bf16(b.Qb, b.r, b.ldr, b.batch, s));
             ++launches;
         }
@@ -769,6 +837,7 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
         Grouper g(p, s, true);
         float* const* W = reinterpret_cast<float* const*>(p->d_ptrs + 2 * n);
         for (auto& b : p->buckets) {
+            if (b.fused) continue;
             GemmProblem q = problem(b.r, b.c, b.r, b.batch, false, kEpiApply);
             q.b_mn = 1;
             q.alpha = p->alpha + b.slot_base;

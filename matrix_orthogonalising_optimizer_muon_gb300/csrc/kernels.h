@@ -41,7 +41,7 @@ enum Epilogue : int {
 struct GemmProblem {
     int M, N, K, batch;
     int tiles_m, tiles_n, tiles_per_item, tile_begin;
-    int sym, b_mn, epi, pad0;
+    int sym, b_mn, epi, ns_steps;   // ns_steps: Newton-Schulz iterations (fused r <= 128 kernel)
     // fp16 outputs (row-major, leading dim ldc, batch stride strideC); C2 an optional copy
     __half* C;
     __half* C2;
@@ -80,6 +80,13 @@ cudaError_t gemm_launch(const GemmLaunch& L, bool bf16, int grid, cudaStream_t s
 // use pair tiling: tiles_m = ceil(M / 256), tiles_n = ceil(N / 256).
 cudaError_t gemm2_max_clusters(int* out);
 cudaError_t gemm2_launch(const GemmLaunch& L, bool bf16, int clusters, cudaStream_t s);
+// Whole NS step (SYRK, r x r recursion, final product + fused update) of matrices
+// with r <= 128, one matrix per CTA at a time.  One problem per bucket: M = r,
+// N = c, batch = matrices, tile_begin = prefix over matrices; mapA = X with
+// 64 x 128 boxes, mapB = X with 64 x 64 boxes (MN-major); epilogue fields as
+// kEpiApply plus out_scale = s, coef_a/b/c = a, b/s, c/s^2 and ns_steps.
+constexpr int kSmallMaxR = 128;
+cudaError_t ns_small_launch(const GemmLaunch& L, int grid, cudaStream_t s);
 
 // ------------------------------------------------------------------ elementwise
 // Per plan matrix, resident on the device.
