@@ -824,6 +824,23 @@ __device__ __forceinline__ void small_step_epilogue(int step, int k, int J, cons
     }
 }
 
+// L2 prefetch of the W entries the fused update of oriented rows [0, M) x columns
+// [n0, n0 + 128) reads, issued by the producer with the X chunk (two or three chunks
+// ahead of the epilogue).  Only whole 16-byte-aligned in-bounds row segments.
+__device__ __forceinline__ void prefetch_w_chunk(const GemmProblem& P, int item, int n0) {
+    const int mat = P.item_mat[item];
+    const float* W = P.W[mat];
+    if ((reinterpret_cast<uintptr_t>(W) & 15) || (P.M & 3) || (P.N & 3)) return;
+    const int c_end = min(n0 + 128, P.N);
+    if (P.transposed[mat] == 0) {
+        const uint32_t bytes = (uint32_t)(c_end - n0) * 4u;
+        for (int r = 0; r < P.M; ++r) prefetch_l2_bulk(W + (long long)r * P.N + n0, bytes);
+    } else {
+        const uint32_t bytes = (uint32_t)P.M * 4u;
+        for (int c = n0; c < c_end; ++c) prefetch_l2_bulk(W + (long long)c * P.M, bytes);
+    }
+}
+
 __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid_constant__ GemmLaunch L) {
     using Cfg = SmallCfg;
     extern __shared__ uint8_t smem_raw[];
@@ -895,6 +912,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
                         tma_load_3d(slot, &L.mapA[p], full + s, q * 64, 0, item);
                     } else {
                         const int n0 = (q - kbs) * 128;
+                        prefetch_w_chunk(P, item, n0);
                         mbar_arrive_expect_tx(full + s, 32768);
 #pragma unroll
                         for (int j = 0; j < 2; ++j)
