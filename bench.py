@@ -41,12 +41,22 @@ def parse_args():
     return ap.parse_args()
 
 
+def gemm_source_sha(csrc: str) -> str:
+    """First 16 hex digits of the SHA-256 of the tensor-core GEMM kernels' source
+    (gemm.cu followed by gemm_common.cuh)."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("gemm.cu", "gemm_common.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def gemm_traffic(workload: str):
     """DRAM bytes per NS step of all tensor-core products, from the committed ncu
     summary; None unless it was taken on the current gemm kernel source."""
-    import hashlib
     path = os.path.join(ROOT, "profiles", "gemm_kernel_qwen7b_layer.md")
-    src = os.path.join(ROOT, "matrix_orthogonalising_optimizer_muon_gb300", "csrc", "gemm.cu")
+    csrc = os.path.join(ROOT, "matrix_orthogonalising_optimizer_muon_gb300", "csrc")
     if workload != "qwen7b_28l":
         return None
     try:
@@ -55,7 +65,7 @@ def gemm_traffic(workload: str):
             if ":" in line and line.split(":")[0] in ("traffic_bytes_per_ns_step_qwen7b_28l", "gemm_source_sha256_16"):
                 k, v = line.split(":", 1)
                 vals[k.strip()] = v.strip()
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        sha = gemm_source_sha(csrc)
         if vals.get("gemm_source_sha256_16") != sha:
             return None
         return float(vals["traffic_bytes_per_ns_step_qwen7b_28l"])

@@ -86,6 +86,7 @@ cudaError_t gemm2_launch(const GemmLaunch& L, bool bf16, int clusters, cudaStrea
 // 64 x 128 boxes, mapB = X with 64 x 64 boxes (MN-major); epilogue fields as
 // kEpiApply plus out_scale = s, coef_a/b/c = a, b/s, c/s^2 and ns_steps.
 constexpr int kSmallMaxR = 128;
+cudaError_t ns_small_prepare();   // sets the fused kernel's dynamic shared-memory limit
 cudaError_t ns_small_launch(const GemmLaunch& L, int grid, cudaStream_t s);
 
 // ------------------------------------------------------------------ elementwise
