@@ -69,7 +69,7 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmLaunch& L, int t) {
 
 // ------------------------------------------------------------------ kernel
 template <bool BF16>
-__global__ void __maxnreg__(200) gemm_kernel(const __grid_constant__ GemmLaunch L) {
+__global__ void __maxnreg__(168) gemm_kernel(const __grid_constant__ GemmLaunch L) {
     using Cfg = GemmCfg;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -202,6 +202,8 @@ __global__ void __maxnreg__(200) gemm_kernel(const __grid_constant__ GemmLaunch 
             const GemmProblem& P = L.prob[tc.p];
             const uint32_t acc = local & 1;
             const uint32_t aph = (local >> 1) & 1u;
+            if (P.epi == kEpiApply || P.epi == kEpiPoly)
+                prefetch_epilogue_inputs(P, tc.item, tc.m0 + wq * 32, tc.n0 + c_begin, kBN * 4 / kEpiWarps, lane);
             if (!mbar_wait(tfull + acc, aph, abort_flag, L.status, kStatusTimeoutEpilogue)) break;
             tc_fence_after();
             const int row = tc.m0 + wq * 32 + lane;
@@ -286,7 +288,7 @@ __device__ __forceinline__ TileCoord decode_pair_tile(const GemmLaunch& L, int t
 }
 
 template <bool BF16>
-__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(200)
+__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
     gemm2_kernel(const __grid_constant__ GemmLaunch L) {
     using Cfg = Gemm2Cfg;
     extern __shared__ uint8_t smem_raw[];
@@ -426,6 +428,8 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(200)
             const GemmProblem& P = L.prob[tc.p];
             const uint32_t acc = local & 1;
             const uint32_t aph = (local >> 1) & 1u;
+            if (P.epi == kEpiApply || P.epi == kEpiPoly)
+                prefetch_epilogue_inputs(P, tc.item, tc.m0 + wq * 32, tc.n0 + c_begin, kBN * 4 / kEpiWarps, lane);
             if (!mbar_wait_cluster(tfull + acc, aph, abort_flag, L.status, kStatusTimeoutEpilogue)) break;
             tc_fence_after();
             const int row = tc.m0 + wq * 32 + lane;

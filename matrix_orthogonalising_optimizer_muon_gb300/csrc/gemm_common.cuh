@@ -138,23 +138,6 @@ __device__ __forceinline__ void apply_load(const GemmProblem& P, const ApplyCtx&
     }
 }
 
-// Debug copy of O = alpha * acc (plans with keep_update only).  Kept out of line
-// so its registers do not weigh on the fused update of every other plan.
-static __device__ __noinline__ void store_debug_update(const GemmProblem& P, const ApplyCtx& c, int row, int col0, float al,
-                                                const uint32_t (&raw)[32]) {
-    if (c.vec) {
-        float4* o4 = reinterpret_cast<float4*>(c.O + c.base);
-        for (int q = 0; q < 8; ++q)
-            o4[q] = make_float4(al * __uint_as_float(raw[4 * q]), al * __uint_as_float(raw[4 * q + 1]),
-                                al * __uint_as_float(raw[4 * q + 2]), al * __uint_as_float(raw[4 * q + 3]));
-    } else {
-        float* base = c.O + c.base;
-        const int st = (int)c.stride;
-        const int nj = min(32, P.N - col0);
-        for (int j = 0; j < nj; ++j) base[j * st] = al * __uint_as_float(raw[j]);
-    }
-}
-
 __device__ __forceinline__ void apply_store(const GemmProblem& P, const ApplyCtx& c, int item, int row, int col0,
                                             const uint32_t (&raw)[32], float (&w)[32]) {
     if (row >= P.M) return;
@@ -174,7 +157,54 @@ __device__ __forceinline__ void apply_store(const GemmProblem& P, const ApplyCtx
         for (int j = 0; j < 32; ++j)
             if (j < nj) base[j * st] = w[j];
     }
-    if (c.O) store_debug_update(P, c, row, col0, al, raw);
+    if (c.O) {   // debug copy of O = alpha acc (plans that keep the update)
+        float* o = c.O + c.base;
+        if (c.vec) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                reinterpret_cast<float4*>(o)[q] =
+                    make_float4(al * __uint_as_float(raw[4 * q]), al * __uint_as_float(raw[4 * q + 1]),
+                                al * __uint_as_float(raw[4 * q + 2]), al * __uint_as_float(raw[4 * q + 3]));
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (j < nj) o[j * st] = al * __uint_as_float(raw[j]);
+        }
+    }
+}
+
+// L2 prefetch of what the epilogue of this warp will read for its part of a tile:
+// rows [row0, row0 + 32) x columns [col0, col0 + ncols) of W (kEpiApply, stored
+// layout) or of G' (kEpiPoly).  Issued while the tile's main loop runs, so the
+// epilogue's loads hit L2.  Only whole, 16-byte-aligned in-bounds segments.
+__device__ __forceinline__ void prefetch_epilogue_inputs(const GemmProblem& P, int item, int row0, int col0,
+                                                         int ncols, int lane) {
+    if (col0 >= P.N || row0 >= P.M) return;
+    const int nc = min(ncols, P.N - col0);
+    if (P.epi == kEpiApply) {
+        const int mat = P.item_mat[item];
+        const float* W = P.W[mat];
+        if (reinterpret_cast<uintptr_t>(W) & 15) return;
+        if (P.transposed[mat] == 0) {
+            // one oriented row per lane: nc contiguous floats
+            const int row = row0 + lane;
+            if ((P.N & 3) || row >= P.M) return;
+            const uint32_t bytes = (uint32_t)(nc & ~3) * 4u;
+            if (bytes) prefetch_l2_bulk(W + (long long)row * P.N + col0, bytes);
+        } else {
+            // stored c x r: each oriented column is a contiguous run of rows
+            const int nr = min(32, P.M - row0);
+            if ((P.M & 3) || (row0 & 3)) return;
+            const uint32_t bytes = (uint32_t)(nr & ~3) * 4u;
+            if (bytes == 0) return;
+            for (int c = lane; c < nc; c += 32) prefetch_l2_bulk(W + (long long)(col0 + c) * P.M + row0, bytes);
+        }
+    } else if (P.epi == kEpiPoly) {
+        const int row = row0 + lane;
+        if (row >= P.M || (P.ldc & 7)) return;
+        const uint32_t bytes = (uint32_t)(nc & ~7) * 2u;
+        if (bytes) prefetch_l2_bulk(P.Gin + item * P.strideC + (long long)row * P.ldc + col0, bytes);
+    }
 }
 
 __device__ __forceinline__ void epilogue_chunk(const GemmProblem& P, int item, int row, int col0,

@@ -100,6 +100,12 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst_smem, const void* src) 
 __device__ __forceinline__ void cp_async_4(uint32_t dst_smem, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst_smem), "l"(src) : "memory");
 }
+// Bulk prefetch of [addr, addr + bytes) into L2; addr 16-byte aligned, bytes a
+// multiple of 16.  Callers only pass ranges inside their own buffers.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* addr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(addr)), "r"(bytes)
+                 : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
