@@ -71,6 +71,21 @@ bool make_map(CUtensorMap* map, void* base, bool bf16, uint64_t inner, uint64_t 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Store map over `batch` r x r row-major matrices (leading dim ld): 32 x 32 boxes
+// in the 64-byte-swizzled shared layout the pair kernel's epilogue stages.
+bool make_out_map(CUtensorMap* map, void* base, bool bf16, uint64_t r, uint64_t batch, uint64_t ld) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const uint64_t esz = 2;
+    cuuint64_t dims[3] = {r, r, batch};
+    cuuint64_t strides[2] = {ld * esz, ld * r * esz};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 inline long long round_up(long long a, long long b) { return ceil_div(a, b) * b; }
 
@@ -93,6 +108,7 @@ struct Bucket {
     CUtensorMap ut_a, ut_b, ut_mn, qb_a;
     CUtensorMap ga[2], gb[2], pa, pb, tb, qb[2];
     CUtensorMap qa[2], ta;   // 128-row boxes of Q and T (B halves of the CTA-pair kernel)
+    CUtensorMap og[2], op, ot, oq[2], oqb;   // store maps of G, P, T, Q (fp16) and Qb (bf16)
 };
 
 struct ListDev {
@@ -288,15 +304,24 @@ struct Grouper {
     // a128: A with 128-row boxes; b256 / b128: B with 256- / 128-row boxes (the
     // same map for an MN-major B).  Problems with more than 128 rows go to the
     // CTA-pair kernel (each CTA loads 128 rows of A and 128 of B).
-    void add(const CUtensorMap& a128, const CUtensorMap& b256, const CUtensorMap& b128, GemmProblem q) {
+    // oc / oc2: store maps of a symmetric problem's outputs (tma_out set by the
+    // caller); the pair kernel then writes them with TMA stores.
+    void add(const CUtensorMap& a128, const CUtensorMap& b256, const CUtensorMap& b128, GemmProblem q,
+             const CUtensorMap* oc = nullptr, const CUtensorMap* oc2 = nullptr) {
         if (q.M > kBM && p->pair_clusters > 0) {
             if (L2.nprob == kMaxProblems) flush2();
             q.tiles_m = (int)ceil_div(q.M, 256);
             q.tiles_n = (int)ceil_div(q.N, 256);
             q.tiles_per_item = q.sym ? q.tiles_m * (q.tiles_m + 1) / 2 : q.tiles_m * q.tiles_n;
+            if (!q.sym || !oc || ((q.tma_out & kTmaOutC2) && !oc2)) q.tma_out = 0;
+            if (q.tma_out) {
+                L2.mapC[L2.nprob] = *oc;
+                if (oc2) L2.mapC2[L2.nprob] = *oc2;
+            }
             push(L2, a128, b128, q);
         } else {
             if (L1.nprob == kMaxProblems) flush1();
+            q.tma_out = 0;
             push(L1, a128, b256, q);
         }
     }
@@ -585,6 +610,13 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
         ok = ok && make_map(&b.pb, b.P, false, b.r, b.r, b.batch, b.ldr, 64, kBN);
         ok = ok && make_map(&b.tb, b.T, false, b.r, b.r, b.batch, b.ldr, 64, kBN);
         ok = ok && make_map(&b.ta, b.T, false, b.r, b.r, b.batch, b.ldr, 64, kBM);
+        for (int g = 0; g < 2; ++g) {
+            ok = ok && make_out_map(&b.og[g], b.G[g], false, b.r, b.batch, b.ldr);
+            ok = ok && make_out_map(&b.oq[g], b.Q[g], false, b.r, b.batch, b.ldr);
+        }
+        ok = ok && make_out_map(&b.op, b.P, false, b.r, b.batch, b.ldr);
+        ok = ok && make_out_map(&b.ot, b.T, false, b.r, b.batch, b.ldr);
+        ok = ok && make_out_map(&b.oqb, b.Qb, true, b.r, b.batch, b.ldr);
     }
     ok = ok && cudaMallocHost(&p->h_pinned, sizeof(void*) * 3 * n) == cudaSuccess;
     ok = ok && cudaEventCreateWithFlags(&p->upload_ev, cudaEventDisableTiming) == cudaSuccess;
@@ -706,7 +738,8 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
             q.ldc = b.ldr;
             q.alpha = p->alpha + b.slot_base;
             q.out_scale = b.gscale;
-            g.add(b.ut_a, b.ut_b, b.ut_a, q);
+            q.tma_out = kTmaOutC;
+            g.add(b.ut_a, b.ut_b, b.ut_a, q, &b.og[0]);
         }
         g.flush();
         if (g.st != MUON_OK) return g.st;
@@ -780,7 +813,9 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
                 q.coef_a = kNsA;
                 q.coef_b = kNsB / b.gscale;
                 q.coef_c = kNsC / (b.gscale * b.gscale);
-                g.add(b.ga[gc], b.gb[gc], b.ga[gc], q);
+                // fp16 P (and the fp16 copy Q_1): TMA stores; P with a bf16 Q_1 (J = 1): per thread
+                q.tma_out = q.Cb ? 0 : (kTmaOutC | (q.C2 ? kTmaOutC2 : 0));
+                g.add(b.ga[gc], b.gb[gc], b.ga[gc], q, &b.op, q.C2 ? &b.oq[0] : nullptr);
             }
             g.flush();
             if (g.st != MUON_OK) return g.st;
@@ -792,16 +827,21 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
             if (b.fused) continue;
                 if (k >= 2) {
                     GemmProblem q = rr_problem(b, kEpiPlain);
-                    if (k < J)
+                    if (k < J) {
                         q.C = b.Q[qc ^ 1];
-                    else
+                        q.tma_out = kTmaOutC;
+                        g.add(b.pa, b.qb[qc], b.qa[qc], q, &b.oq[qc ^ 1]);
+                    } else {
                         q.Cb = b.Qb;
-                    g.add(b.pa, b.qb[qc], b.qa[qc], q);
+                        q.tma_out = kTmaOutC | kTmaOutBf16;
+                        g.add(b.pa, b.qb[qc], b.qa[qc], q, &b.oqb);
+                    }
                 }
                 if (k < J) {
                     GemmProblem q = rr_problem(b, kEpiPlain);
                     q.C = b.T;
-                    g.add(b.pa, b.pb, b.pa, q);
+                    q.tma_out = kTmaOutC;
+                    g.add(b.pa, b.pb, b.pa, q, &b.ot);
                 }
             }
             g.flush();
@@ -815,7 +855,8 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
             if (b.fused) continue;
                 GemmProblem q = rr_problem(b, kEpiPlain);
                 q.C = b.G[gc ^ 1];
-                g.add(b.ga[gc], b.tb, b.ta, q);
+                q.tma_out = kTmaOutC;
+                g.add(b.ga[gc], b.tb, b.ta, q, &b.og[gc ^ 1]);
             }
             g.flush();
             if (g.st != MUON_OK) return g.st;

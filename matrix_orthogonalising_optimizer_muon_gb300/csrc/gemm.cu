@@ -255,9 +255,12 @@ struct Gemm2Cfg {
     static constexpr int B_BYTES = 128 * BK * ESZ;       // this CTA's half of B
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int MN_CHUNK_BYTES = 64 * BK * ESZ;
-    static constexpr int BAR_OFFSET = kStages2 * STAGE_BYTES;
+    static constexpr int OUT_OFFSET = kStages2 * STAGE_BYTES;    // per epilogue warp: 2 x 2 KB store staging
+    static constexpr int OUT_BYTES = kEpiWarps * 4096;
+    static constexpr int BAR_OFFSET = OUT_OFFSET + OUT_BYTES;
     static constexpr int SMEM_BYTES = BAR_OFFSET + 256 + 1024;
 };
+static_assert(Gemm2Cfg::SMEM_BYTES <= 232448, "CTA-pair kernel exceeds the shared memory of one CTA");
 
 // Pair tiles: (tm2, tn) of 256 x 256; the CTA of rank `rank` owns rows
 // 256 tm2 + 128 rank .. + 127.  Symmetric outputs keep tn <= tm2.
@@ -422,6 +425,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
         const int wq = warp & 3;
         const int c_begin = ((warp - 2) >> 2) * (kBN * 4 / kEpiWarps);
         const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), 0);
+        uint8_t* stage_l = smem + Cfg::OUT_OFFSET + (warp - 2) * 4096;
         int local = 0;
         for (int t = cluster_id; t < L.total_tiles; t += nclusters, ++local) {
             const TileCoord tc = decode_pair_tile(L, t, rank);
@@ -435,18 +439,32 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
             const int row = tc.m0 + wq * 32 + lane;
             const int warp_row_max = tc.m0 + wq * 32 + 31;
             const uint32_t tbase = tmem_base + acc * kBN + (static_cast<uint32_t>(wq * 32) << 16);
+            const WPiece wc = w_piece_ctx(P, P.epi == kEpiApply ? tc.item : -1);
             for (int cc = c_begin; cc < c_begin + kBN * 4 / kEpiWarps; cc += 32) {
                 const int col0 = tc.n0 + cc;
                 if (col0 >= P.N) break;
                 if (P.sym && col0 > warp_row_max) break;
                 uint32_t raw[32];
-                tmem_ld32(tbase + cc, raw);
                 if (P.epi == kEpiApply) {
-                    const ApplyCtx ac = apply_ctx(P, tc.item, row < P.M ? row : 0, col0);
-                    float w[32];
-                    apply_load(P, ac, row, col0, w);
+                    // W piece (rows R0.., columns col0..) in with coalesced cp.async, updated
+                    // in shared memory, out with coalesced 16-byte stores
+                    const int R0 = tc.m0 + wq * 32;
+                    w_piece_load(wc, R0, col0, smem_u32(stage_l), lane);
+                    tmem_ld32(tbase + cc, raw);
                     tmem_ld_wait();
-                    apply_store(P, ac, tc.item, row, col0, raw, w);
+                    cp_async_wait<0>();
+                    __syncwarp();
+                    if (R0 < P.M) w_piece_update(P, wc, tc.item, R0, col0, stage_l, lane, raw);
+                    __syncwarp();
+                    w_piece_store(wc, R0, col0, stage_l, lane);
+                    __syncwarp();
+                    continue;
+                }
+                tmem_ld32(tbase + cc, raw);
+                if (P.tma_out) {
+                    tmem_ld_wait();
+                    epilogue_chunk_tma(P, &L.mapC[tc.p], &L.mapC2[tc.p], tc.item, tc.m0 + wq * 32, col0, lane, raw,
+                                       stage_l, stage_l + 2048);
                 } else {
                     tmem_ld_wait();
                     epilogue_chunk(P, tc.item, row, col0, raw);
@@ -461,6 +479,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
                     mbar_arrive_remote(tempty_leader + acc * 8);
             }
         }
+        if (lane == 0) bulk_wait<0>();   // TMA stores of the staging complete before the CTA exits
     }
 
     tc_fence_before();

@@ -207,9 +207,10 @@ __device__ __forceinline__ void prefetch_epilogue_inputs(const GemmProblem& P, i
     }
 }
 
-__device__ __forceinline__ void epilogue_chunk(const GemmProblem& P, int item, int row, int col0,
-                                               const uint32_t (&raw)[32]) {
-    float v[32];
+// Values of one 32-column chunk of a symmetric result for this thread's row:
+// kEpiSyrk scales, kEpiPoly adds a I + b' G', kEpiPlain passes the accumulator.
+__device__ __forceinline__ void epilogue_values(const GemmProblem& P, int item, int row, int col0,
+                                                const uint32_t (&raw)[32], float (&v)[32]) {
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw[j]);
     if (P.epi == kEpiSyrk) {
@@ -246,7 +247,212 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem& P, int item, i
             }
         }
     }
+}
+
+__device__ __forceinline__ void epilogue_chunk(const GemmProblem& P, int item, int row, int col0,
+                                               const uint32_t (&raw)[32]) {
+    float v[32];
+    epilogue_values(P, item, row, col0, raw, v);
     store_sym(P, item, row, col0, v);
+}
+
+// The same chunk written through shared memory with TMA stores: the warp's 32 x 32
+// block (rows R0 .. R0 + 31, columns col0 .. col0 + 31) is staged in `stl` as 64-byte
+// rows in the 64-byte-swizzled layout of the store box, and, for blocks below the
+// diagonal, its transpose in `stm`; lane 0 stores them at (col0, R0) and (R0, col0).
+// A block on the diagonal (col0 == R0) is staged as its lower triangle plus the
+// mirror of it and stored once, so the output is exactly symmetric (the products
+// read B transposed) and every element is written exactly once.  Rows and columns
+// beyond the matrix fall outside the store box's extents and are not written.
+__device__ __forceinline__ uint32_t stage64_off(int y, int x) {   // 2-byte element (y, x), x < 32
+    return (uint32_t)(y * 64 + ((((x >> 3) ^ ((y >> 1) & 3))) << 4) + ((x & 7) << 1));
+}
+
+__device__ __forceinline__ void epilogue_chunk_tma(const GemmProblem& P, const CUtensorMap* mc,
+                                                   const CUtensorMap* mc2, int item, int R0, int col0, int lane,
+                                                   const uint32_t (&raw)[32], uint8_t* stl, uint8_t* stm) {
+    float v[32];
+    epilogue_values(P, item, R0 + lane, col0, raw, v);
+    const bool diag = col0 == R0;
+    const bool bf = (P.tma_out & kTmaOutBf16) != 0;
+    if (lane == 0) bulk_wait_read<0>();   // the previous chunk's stores have read the staging
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float* x = v + 8 * q;
+        const uint4 pk = bf ? make_uint4(pack_bf162(x[0], x[1]), pack_bf162(x[2], x[3]), pack_bf162(x[4], x[5]),
+                                         pack_bf162(x[6], x[7]))
+                            : make_uint4(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]), pack_half2(x[4], x[5]),
+                                         pack_half2(x[6], x[7]));
+        *reinterpret_cast<uint4*>(stl + stage64_off(lane, 8 * q)) = pk;
+    }
+    if (diag) {
+        __syncwarp();   // rows staged; the upper triangle becomes the mirror of the lower
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (j < lane) {
+                const unsigned short h = bf ? __bfloat16_as_ushort(__float2bfloat16_rn(v[j]))
+                                            : __half_as_ushort(to_half(v[j]));
+                *reinterpret_cast<unsigned short*>(stl + stage64_off(j, lane)) = h;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const unsigned short h = bf ? __bfloat16_as_ushort(__float2bfloat16_rn(v[j]))
+                                        : __half_as_ushort(to_half(v[j]));
+            *reinterpret_cast<unsigned short*>(stm + stage64_off(j, lane)) = h;
+        }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // staging visible to the TMA unit
+    __syncwarp();
+    if (lane == 0) {
+        if (P.tma_out & kTmaOutC) tma_store_3d(mc, stl, col0, R0, item);
+        if (P.tma_out & kTmaOutC2) tma_store_3d(mc2, stl, col0, R0, item);
+        if (!diag) {
+            if (P.tma_out & kTmaOutC) tma_store_3d(mc, stm, R0, col0, item);
+            if (P.tma_out & kTmaOutC2) tma_store_3d(mc2, stm, R0, col0, item);
+        }
+        bulk_commit();
+    }
+}
+
+// ------------------------------------------------------------------ W staging (fused update)
+// A piece is oriented rows [rw, rw + 32) x columns [col0, col0 + 32) of one
+// matrix, staged in its stored orientation: 32 lines of 128 B (a line is an
+// oriented row when W is stored r x c, an oriented column when stored c x r),
+// 16-byte chunks XOR-swizzled by line so that both the coalesced copies and the
+// one-row-per-thread update are free of bank conflicts.
+constexpr int kWPiece = 32 * 32 * 4;   // one 32 x 32 fp32 piece of W
+
+struct WPiece {
+    float* W;        // the matrix, stored layout
+    long long ld;    // stored leading dimension: N (r x c) or M (c x r)
+    int M, N;        // oriented extent
+    bool tr;         // stored c x r
+    bool vec;        // 16-byte copies possible
+};
+
+// item < 0: an empty context (problems without the fused update)
+__device__ __forceinline__ WPiece w_piece_ctx(const GemmProblem& P, int item) {
+    WPiece c;
+    c.M = P.M;
+    c.N = P.N;
+    if (item < 0) {
+        c.W = nullptr;
+        c.ld = 0;
+        c.tr = false;
+        c.vec = false;
+        return c;
+    }
+    const int mat = P.item_mat[item];
+    c.W = P.W[mat];
+    c.tr = P.transposed[mat] != 0;
+    c.ld = c.tr ? P.M : P.N;
+    c.vec = ((c.ld & 3) == 0) && ((reinterpret_cast<uintptr_t>(c.W) & 15) == 0);
+    return c;
+}
+
+__device__ __forceinline__ uint32_t stage_off(int line, int e) {   // element e (0..31) of a line
+    return (uint32_t)(line * 128 + ((((e >> 2) ^ (line & 7))) << 4) + ((e & 3) << 2));
+}
+
+// Global address and validity of staged element (line, e) of the piece at (rw, col0).
+__device__ __forceinline__ float* w_elem(const WPiece& c, int rw, int col0, int line, int e, bool& ok) {
+    int row, col;
+    if (c.tr) {
+        col = col0 + line;
+        row = rw + e;
+    } else {
+        row = rw + line;
+        col = col0 + e;
+    }
+    ok = row < c.M && col < c.N;
+    return c.tr ? c.W + (long long)col * c.ld + row : c.W + (long long)row * c.ld + col;
+}
+
+// Issue the copies of one piece into `buf` (one commit group per call).
+__device__ __forceinline__ void w_piece_load(const WPiece& c, int rw, int col0, uint32_t buf, int lane) {
+    if (col0 < c.N && rw < c.M) {
+        if (c.vec) {
+            // lanes 8i..8i+7 take the eight 16-byte chunks of line 4s + i
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const int line = 4 * s + (lane >> 3), e = 4 * (lane & 7);
+                bool ok;
+                const float* g = w_elem(c, rw, col0, line, e, ok);
+                if (ok) cp_async_16(buf + stage_off(line, e), g);
+            }
+        } else {
+#pragma unroll 4
+            for (int line = 0; line < 32; ++line) {
+                bool ok;
+                const float* g = w_elem(c, rw, col0, line, lane, ok);
+                if (ok) cp_async_4(buf + stage_off(line, lane), g);
+            }
+        }
+    }
+    cp_async_commit();
+}
+
+// Write a staged piece back to global memory with the same coalesced mapping.
+__device__ __forceinline__ void w_piece_store(const WPiece& c, int rw, int col0, const uint8_t* buf, int lane) {
+    if (col0 >= c.N || rw >= c.M) return;
+    if (c.vec) {
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const int line = 4 * s + (lane >> 3), e = 4 * (lane & 7);
+            bool ok;
+            float* g = w_elem(c, rw, col0, line, e, ok);
+            if (ok) *reinterpret_cast<float4*>(g) = *reinterpret_cast<const float4*>(buf + stage_off(line, e));
+        }
+    } else {
+#pragma unroll 4
+        for (int line = 0; line < 32; ++line) {
+            bool ok;
+            float* g = w_elem(c, rw, col0, line, lane, ok);
+            if (ok) *g = *reinterpret_cast<const float*>(buf + stage_off(line, lane));
+        }
+    }
+}
+
+// The fused update of this thread's row of a staged piece:
+// w -= lr (scale alpha acc + wd w), acc the 32 accumulator columns of the row.
+// Plans that keep the update also write O = alpha acc (fp32, stored layout).
+__device__ __forceinline__ void w_piece_update(const GemmProblem& P, const WPiece& c, int item, int rw, int col0,
+                                               uint8_t* buf, int lane, const uint32_t (&acc)[32]) {
+    const float al = P.alpha[item];
+    const float lr = P.lr, wd = P.wd, s = P.scale;
+    if (!c.tr) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            float4* p = reinterpret_cast<float4*>(buf + stage_off(lane, 4 * q));
+            float4 w = *p;
+            w.x -= lr * (s * (al * __uint_as_float(acc[4 * q])) + wd * w.x);
+            w.y -= lr * (s * (al * __uint_as_float(acc[4 * q + 1])) + wd * w.y);
+            w.z -= lr * (s * (al * __uint_as_float(acc[4 * q + 2])) + wd * w.z);
+            w.w -= lr * (s * (al * __uint_as_float(acc[4 * q + 3])) + wd * w.w);
+            *p = w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            float* p = reinterpret_cast<float*>(buf + stage_off(j, lane));
+            const float w = *p;
+            *p = w - lr * (s * (al * __uint_as_float(acc[j])) + wd * w);
+        }
+    }
+    if (P.Odbg != nullptr) {
+        float* O = P.Odbg + (long long)item * P.M * P.N;
+        const int row = rw + lane;
+        if (row < c.M) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const long long idx = c.tr ? (long long)(col0 + j) * c.ld + row : (long long)row * c.ld + col0 + j;
+                if (col0 + j < c.N) O[idx] = al * __uint_as_float(acc[j]);
+            }
+        }
+    }
 }
 
 }  // namespace muon

@@ -60,11 +60,18 @@ struct GemmProblem {
     const unsigned char* transposed;   // plan matrix index -> stored as c x r
     float* Odbg;                       // optional O (fp32, stored layout), item stride M*N
     float lr, wd, scale, pad3;
+    // symmetric outputs of the CTA-pair kernel written with TMA stores from shared
+    // memory: kTmaOutC (staged values via mapC), kTmaOutC2 (also via mapC2),
+    // kTmaOutBf16 (staged as bf16, else fp16); 0: per-thread stores
+    int tma_out, pad4;
 };
+constexpr int kTmaOutC = 1, kTmaOutC2 = 2, kTmaOutBf16 = 4;
 
 struct GemmLaunch {
     CUtensorMap mapA[kMaxProblems];
     CUtensorMap mapB[kMaxProblems];
+    CUtensorMap mapC[kMaxProblems];    // 32 x 32 store boxes (64-byte swizzle) of the outputs
+    CUtensorMap mapC2[kMaxProblems];
     GemmProblem prob[kMaxProblems];
     int nprob;
     int total_tiles;

@@ -32,7 +32,6 @@ namespace muon {
 constexpr int kSmallRing = 3;                       // X stream ring (SYRK k-blocks, final chunks)
 constexpr int kSmallThreads = 320;                  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-9 epilogue
 constexpr int kSmallEpiWarps = 8;
-constexpr int kWPiece = 32 * 32 * 4;                // one 32 x 32 fp32 piece of W
 constexpr int kWBufs = 3;                           // pieces in flight per epilogue warp
 struct SmallCfg {
     static constexpr int SLOT = 32768;              // one 128-column k-block or chunk of X (bf16)
@@ -150,134 +149,6 @@ __device__ __forceinline__ void small_step_epilogue(int step, int k, int J, cons
             }
         } else {   // kSmGT: G'' = G' T
             op_store_row<false>(smem + SmallCfg::GS, row, cc, r, v);
-        }
-    }
-}
-
-// ---------------------------------------------------------------- W staging
-// A piece is oriented rows [rw, rw + 32) x columns [col0, col0 + 32) of one
-// matrix, staged in its stored orientation: 32 lines of 128 B (a line is an
-// oriented row when W is stored r x c, an oriented column when stored c x r),
-// 16-byte chunks XOR-swizzled by line so that both the coalesced copies and the
-// one-row-per-thread update are free of bank conflicts.
-struct WPiece {
-    float* W;        // the matrix, stored layout
-    long long ld;    // stored leading dimension: N (r x c) or M (c x r)
-    int M, N;        // oriented extent
-    bool tr;         // stored c x r
-    bool vec;        // 16-byte copies possible
-};
-
-__device__ __forceinline__ WPiece w_piece_ctx(const GemmProblem& P, int item) {
-    WPiece c;
-    const int mat = P.item_mat[item];
-    c.W = P.W[mat];
-    c.M = P.M;
-    c.N = P.N;
-    c.tr = P.transposed[mat] != 0;
-    c.ld = c.tr ? P.M : P.N;
-    c.vec = ((c.ld & 3) == 0) && ((reinterpret_cast<uintptr_t>(c.W) & 15) == 0);
-    return c;
-}
-
-__device__ __forceinline__ uint32_t stage_off(int line, int e) {   // element e (0..31) of a line
-    return (uint32_t)(line * 128 + ((((e >> 2) ^ (line & 7))) << 4) + ((e & 3) << 2));
-}
-
-// Global address and validity of staged element (line, e) of the piece at (rw, col0).
-__device__ __forceinline__ float* w_elem(const WPiece& c, int rw, int col0, int line, int e, bool& ok) {
-    int row, col;
-    if (c.tr) {
-        col = col0 + line;
-        row = rw + e;
-    } else {
-        row = rw + line;
-        col = col0 + e;
-    }
-    ok = row < c.M && col < c.N;
-    return c.tr ? c.W + (long long)col * c.ld + row : c.W + (long long)row * c.ld + col;
-}
-
-// Issue the copies of one piece into `buf` (one commit group per call).
-__device__ __forceinline__ void w_piece_load(const WPiece& c, int rw, int col0, uint32_t buf, int lane) {
-    if (col0 < c.N && rw < c.M) {
-        if (c.vec) {
-            // lanes 8i..8i+7 take the eight 16-byte chunks of line 4s + i
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const int line = 4 * s + (lane >> 3), e = 4 * (lane & 7);
-                bool ok;
-                const float* g = w_elem(c, rw, col0, line, e, ok);
-                if (ok) cp_async_16(buf + stage_off(line, e), g);
-            }
-        } else {
-#pragma unroll 4
-            for (int line = 0; line < 32; ++line) {
-                bool ok;
-                const float* g = w_elem(c, rw, col0, line, lane, ok);
-                if (ok) cp_async_4(buf + stage_off(line, lane), g);
-            }
-        }
-    }
-    cp_async_commit();
-}
-
-// Write a staged piece back to global memory with the same coalesced mapping.
-__device__ __forceinline__ void w_piece_store(const WPiece& c, int rw, int col0, const uint8_t* buf, int lane) {
-    if (col0 >= c.N || rw >= c.M) return;
-    if (c.vec) {
-#pragma unroll
-        for (int s = 0; s < 8; ++s) {
-            const int line = 4 * s + (lane >> 3), e = 4 * (lane & 7);
-            bool ok;
-            float* g = w_elem(c, rw, col0, line, e, ok);
-            if (ok) *reinterpret_cast<float4*>(g) = *reinterpret_cast<const float4*>(buf + stage_off(line, e));
-        }
-    } else {
-#pragma unroll 4
-        for (int line = 0; line < 32; ++line) {
-            bool ok;
-            float* g = w_elem(c, rw, col0, line, lane, ok);
-            if (ok) *g = *reinterpret_cast<const float*>(buf + stage_off(line, lane));
-        }
-    }
-}
-
-// The fused update of this thread's row of a staged piece:
-// w -= lr (scale alpha acc + wd w), acc the 32 accumulator columns of the row.
-// Plans that keep the update also write O = alpha acc (fp32, stored layout).
-__device__ __forceinline__ void w_piece_update(const GemmProblem& P, const WPiece& c, int item, int rw, int col0,
-                                               uint8_t* buf, int lane, const uint32_t (&acc)[32]) {
-    const float al = P.alpha[item];
-    const float lr = P.lr, wd = P.wd, s = P.scale;
-    if (!c.tr) {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            float4* p = reinterpret_cast<float4*>(buf + stage_off(lane, 4 * q));
-            float4 w = *p;
-            w.x -= lr * (s * (al * __uint_as_float(acc[4 * q])) + wd * w.x);
-            w.y -= lr * (s * (al * __uint_as_float(acc[4 * q + 1])) + wd * w.y);
-            w.z -= lr * (s * (al * __uint_as_float(acc[4 * q + 2])) + wd * w.z);
-            w.w -= lr * (s * (al * __uint_as_float(acc[4 * q + 3])) + wd * w.w);
-            *p = w;
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            float* p = reinterpret_cast<float*>(buf + stage_off(j, lane));
-            const float w = *p;
-            *p = w - lr * (s * (al * __uint_as_float(acc[j])) + wd * w);
-        }
-    }
-    if (P.Odbg != nullptr) {
-        float* O = P.Odbg + (long long)item * P.M * P.N;
-        const int row = rw + lane;
-        if (row < c.M) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const long long idx = c.tr ? (long long)(col0 + j) * c.ld + row : (long long)row * c.ld + col0 + j;
-                if (col0 + j < c.N) O[idx] = al * __uint_as_float(acc[j]);
-            }
         }
     }
 }

@@ -15,6 +15,9 @@ Workloads (shapes as stored, row-major m x n):
   mlp-in 8192x2048, mlp-out 2048x8192, adaLN 12288x2048 (periodic RowNorm, K=4).
 * ``dit_block``: one of those blocks (0.75 GB of W, G, M: still above L2), the
   small case used to profile the RowNorm kernels.
+* ``qwen7b_heads_layer``: one layer of the per-head split (36 matrices 128 x 3584
+  and one 3584 x 512; 183 MB of W, G, M: above L2), the small case used to
+  profile the fused r <= 128 kernel.
 
 Values: W ~ N(0, 0.02^2), G ~ N(0, 1e-3^2), M ~ N(0, 1e-3^2); G is bf16 except
 in ``single``.  Each tensor gets its own seed from (workload, step, matrix, kind).
@@ -51,6 +54,10 @@ def _qwen_heads():
     return one * 28 + ((HIDDEN_7B, 512),) * 28
 
 
+def _qwen_heads_layer():
+    return ((128, HIDDEN_7B),) * (28 + 4 + 4) + ((HIDDEN_7B, 512),)
+
+
 def _dit_block():
     h = HIDDEN_DIT
     return ((3 * h, h), (h, h), (4 * h, h), (h, 4 * h), (6 * h, h))
@@ -63,6 +70,7 @@ WORKLOADS = {
     "qwen7b_heads": Workload("qwen7b_heads", _qwen_heads(), "bf16", 3),
     "dit1p3b": Workload("dit1p3b", _dit_block() * 28, "bf16", 4, steps=8, rownorm_k=4),
     "dit_block": Workload("dit_block", _dit_block(), "bf16", 5, steps=8, rownorm_k=4),
+    "qwen7b_heads_layer": Workload("qwen7b_heads_layer", _qwen_heads_layer(), "bf16", 6),
 }
 
 
