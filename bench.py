@@ -52,6 +52,38 @@ def gemm_source_sha(csrc: str) -> str:
     return h.hexdigest()[:16]
 
 
+def small_source_sha(csrc: str) -> str:
+    """First 16 hex digits of the SHA-256 of the fused r <= 128 kernel's source
+    (ns_small.cu followed by gemm_common.cuh)."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("ns_small.cu", "gemm_common.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def small_traffic(workload: str):
+    """DRAM bytes per launch of the fused r <= 128 kernel on the per-head workload,
+    from the committed ncu summary (a smaller capture scaled by matrices); None
+    unless it was taken on the current source."""
+    path = os.path.join(ROOT, "profiles", "ns_small_kernel_qwen7b_heads_5l.md")
+    csrc = os.path.join(ROOT, "matrix_orthogonalising_optimizer_muon_gb300", "csrc")
+    if workload != "qwen7b_heads":
+        return None
+    try:
+        vals = {}
+        for line in open(path):
+            if ":" in line and line.split(":")[0] in ("traffic_bytes_per_launch_qwen7b_heads", "small_source_sha256_16"):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+        if vals.get("small_source_sha256_16") != small_source_sha(csrc):
+            return None
+        return float(vals["traffic_bytes_per_launch_qwen7b_heads"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def gemm_traffic(workload: str):
     """DRAM bytes per NS step of all tensor-core products, from the committed ncu
     summary; None unless it was taken on the current gemm kernel source."""
@@ -185,15 +217,6 @@ def algorithmic_ns_flops(shapes, ns_steps=5):
     return rc, rrr
 
 
-def elementwise_bytes(shapes, grad_bytes):
-    """HBM bytes of the NS step outside the GEMM operand traffic: momentum pass
-    (G read, M read+write, bf16 X0 write) and the fused apply (W read+write)."""
-    tot = 0
-    for m, n in shapes:
-        tot += m * n * (grad_bytes + 8 + 2 + 8)
-    return tot
-
-
 # ------------------------------------------------------------------ CPU oracle sample
 def oracle_sample(shapes, grad_dtype, reps_per_bucket=1, seed=2):
     """Time the fp64 oracle (as it stands) on one matrix per distinct oriented shape
@@ -323,27 +346,40 @@ def report_ours(args, res, rank, world):
     K = args.steps
     ms_step = res["ms_step"]
     st_ms, st_fl = res["stage_ms"], res["stage_fl"]
-    gemm_ms = (st_ms[1] + st_ms[2] + st_ms[3]) / K
-    gemm_fl = (st_fl[0] + st_fl[1] + st_fl[2]) / K
-    ns_steps_run = sum(1 for t in range(K) if not (wl.rownorm_k and (args.warmup + t) % wl.rownorm_k))
-    # roofline of the tensor-core products (bf16 and fp16 operands, both at the
-    # dense 16-bit rate): algorithmic FLOPs over their event time, against the
-    # measured sustained bf16 peak (the products run inside a multi-second loop)
+    n_ns = sum(1 for t in range(K) if not (wl.rownorm_k and (args.warmup + t) % wl.rownorm_k))
+    n_rn = K - n_ns
+    per_ns = [x / n_ns if n_ns else 0.0 for x in st_ms]
+    gemm_ms = per_ns[1] + per_ns[2] + per_ns[3]
+    gemm_fl = (st_fl[0] + st_fl[1] + st_fl[2]) / n_ns if n_ns else 0.0
+    gbytes = 2 if wl.grad_dtype == "bf16" else 4
+    small = [(m, n) for m, n in shapes if min(m, n) <= 128]
+    small_bytes = sum(m * n * 12 for m, n in small)   # X read twice (bf16), W read + written (fp32)
+    # The roofline object describes the step's dominant kernel: the tensor-core
+    # products (algorithmic FLOPs over their event time, against the measured
+    # sustained bf16 peak: they run inside a multi-second loop), or, when the fused
+    # r <= 128 kernel dominates, its HBM traffic against the measured copy bandwidth.
     peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     roofline = None
     ns5 = {}
-    if gemm_ms > 0 and ns_steps_run:
-        per_ns = ns_steps_run / K
-        fl = gemm_fl / per_ns
-        t_ms = gemm_ms / per_ns
-        achieved = fl / (t_ms * 1e-3) / 1e12
+    if gemm_ms > 0 and gemm_fl > 0:
+        achieved = gemm_fl / (gemm_ms * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                     "frac": round(achieved / peak, 4), "traffic": gemm_traffic(wl.name),
-                    "kernel": "gemm_kernel: all tensor-core products of one NS5 step (SYRK, 17 r x r, final)",
+                    "kernel": "gemm2_kernel: all tensor-core products of one NS5 step (SYRK, 17 r x r, final)",
                     "peak_note": "%s sustained dense bf16 (fp16 runs at the same rate)" % src}
         ns5 = {"ns5_tflops": round(achieved, 1),
                "ns5_frac_bf16_peak": round(achieved / peaks["bf16_tflops"], 4),
-               "ns5_gemm_ms": round(t_ms, 3), "ns5_gemm_flops": fl}
+               "ns5_gemm_ms": round(gemm_ms, 3), "ns5_gemm_flops": gemm_fl}
+    if per_ns[5] > 0 and small_bytes:
+        gbs = small_bytes / (per_ns[5] * 1e-3) / 1e9
+        ns5["fused_small_ms"] = round(per_ns[5], 3)
+        ns5["fused_small_gbs"] = round(gbs, 1)
+        if per_ns[5] > gemm_ms:
+            roofline = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": small_traffic(wl.name),
+                        "kernel": "ns_small_kernel: the whole NS5 step of the %d matrices with r <= 128 "
+                                  "(12 B/elem: X read twice, W read and written)" % len(small),
+                        "peak_note": "%s copy bandwidth" % src}
     line = {
         "metric": METRIC, "value": round(ms_step, 3), "unit": "ms", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": False,
@@ -355,18 +391,23 @@ def report_ours(args, res, rank, world):
                    "l2": "inputs larger than L2 (%.1f GB of W, G, M per step)" %
                          (sum(m * n for m, n in shapes) * (10 if wl.grad_dtype == "bf16" else 12) / 1e9),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "stages_ms_per_step": {"momentum_norm": round(st_ms[0] / K, 3), "syrk": round(st_ms[1] / K, 3),
-                               "ns_rxr": round(st_ms[2] / K, 3), "final_apply": round(st_ms[3] / K, 3),
-                               "rownorm": round(st_ms[4] / K, 3)},
+        "stages_ms_per_ns_step": {"momentum_norm": round(per_ns[0], 3), "syrk": round(per_ns[1], 3),
+                                  "ns_rxr": round(per_ns[2], 3), "final_apply": round(per_ns[3], 3),
+                                  "fused_small": round(per_ns[5], 3)},
+        "ns_steps_timed": n_ns,
         "roofline": roofline,
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
     }
+    if n_rn:
+        line["rownorm_ms_per_rownorm_step"] = round(st_ms[4] / n_rn, 3)
+        line["rownorm_steps_timed"] = n_rn
+        rn_bytes = sum(m * n * (gbytes + 8 + 8) for m, n in shapes)   # G, M read + write, W read + write
+        line["rownorm_step_gbs"] = round(rn_bytes / (st_ms[4] / n_rn * 1e-3) / 1e9, 1)
     line.update(ns5)
-    if st_ms[0] > 0:
-        gb = elementwise_bytes(shapes, 2 if wl.grad_dtype == "bf16" else 4)
-        mom_bytes = sum(m * n * ((2 if wl.grad_dtype == "bf16" else 4) + 8 + 2) for m, n in shapes)
-        line["momentum_kernel_gbs"] = round(mom_bytes / (st_ms[0] / K * 1e-3) / 1e9, 1)
+    if per_ns[0] > 0:
+        mom_bytes = sum(m * n * (gbytes + 8 + 2) for m, n in shapes)
+        line["momentum_kernel_gbs"] = round(mom_bytes / (per_ns[0] * 1e-3) / 1e9, 1)
         line["momentum_kernel_hbm_frac"] = round(line["momentum_kernel_gbs"] / peaks["hbm_gbs"], 4)
     return line
 

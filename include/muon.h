@@ -192,10 +192,11 @@ muon_status muon_plan_info(muon_plan p, muon_plan_info_t* info);
  * since the previous call, measured with CUDA events recorded on each step's
  * stream (needs opts.timing; waits for those steps, then resets the sums).
  * Stages: [0] momentum + Nesterov + norm, [1] Gram SYRK, [2] r x r
- * Newton-Schulz products (and the whole fused step of matrices with
- * min(m, n) <= 128), [3] final product + fused apply, [4] RowNorm steps.
- * n_stages <= 5.  flops (nullable) receives the algorithmic tensor FLOPs of
- * stages 1-3 over the same steps (symmetric products counted at half).
+ * Newton-Schulz products, [3] final product + fused apply, [4] RowNorm steps,
+ * [5] the whole fused step of the matrices with min(m, n) <= 128 (one kernel).
+ * n_stages <= 6.  flops (nullable, 3 entries) receives the algorithmic tensor
+ * FLOPs of stages 1-3 over the same steps (symmetric products counted at half;
+ * the fused matrices of stage 5 are not included).
  * Returns MUON_ERR_INVALID_ARG when no timed step was run.
  */
 muon_status muon_stage_times(muon_plan p, float* ms, double* flops, int32_t n_stages);

@@ -263,10 +263,11 @@ class MuonPlan:
 
     def stage_times(self):
         """Summed over the timed steps since the previous call: (ms per stage [momentum,
-        syrk, rxr NS, final+apply, rownorm], algorithmic flops [syrk, rxr, final])."""
-        ms = (ctypes.c_float * 5)()
+        syrk, rxr NS, final+apply, rownorm, fused r <= 128 step], algorithmic tensor
+        flops [syrk, rxr, final] of the non-fused matrices)."""
+        ms = (ctypes.c_float * 6)()
         fl = (ctypes.c_double * 3)()
-        _check(self.lib.muon_stage_times(self.handle, ms, fl, 5), "muon_stage_times")
+        _check(self.lib.muon_stage_times(self.handle, ms, fl, 6), "muon_stage_times")
         return list(ms), list(fl)
 
 

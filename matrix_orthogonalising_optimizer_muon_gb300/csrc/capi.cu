@@ -151,8 +151,10 @@ struct muon_plan_s {
     bool uploaded = false;
 
     // opts.timing: one event group per step since the last muon_stage_times call
+    // NS: e[0] momentum | e[1] SYRK | e[2] fused r <= 128 | e[6] r x r | e[3] final | e[4];
+    // RowNorm: e[0] .. e[5]
     struct StepEvents {
-        cudaEvent_t e[6];
+        cudaEvent_t e[7];
         bool ns;
     };
     std::vector<StepEvents> evs;
@@ -712,8 +714,11 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
     ++launches;
     if (se) MUON_TRY(cudaEventRecord(se->e[1], s));
 
+    // algorithmic tensor FLOPs of the GEMM stages (the fused r <= 128 step is
+    // HBM-bound and timed as a stage of its own)
     double fl_syrk = 0, fl_rr = 0, fl_final = 0;
     for (auto& b : p->buckets) {
+        if (b.fused) continue;
         const double r = b.r, c = b.c;
         fl_syrk += b.batch * r * r * c;
         fl_final += b.batch * 2.0 * r * r * c;
@@ -789,6 +794,7 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
         }
         if ((st = flush_small()) != MUON_OK) return st;
     }
+    if (se) MUON_TRY(cudaEventRecord(se->e[6], s));
 
     // ---- Newton-Schulz in the Gram space (fp16 operands, G carried as s G)
     const int J = ns_steps;
@@ -963,18 +969,22 @@ muon_status muon_plan_info(muon_plan p, muon_plan_info_t* info) {
 }
 
 muon_status muon_stage_times(muon_plan p, float* ms, double* flops, int32_t n_stages) {
-    if (!p || !ms || n_stages < 0 || n_stages > 5) return MUON_ERR_INVALID_ARG;
+    if (!p || !ms || n_stages < 0 || n_stages > 6) return MUON_ERR_INVALID_ARG;
     if (p->n_timed == 0) return MUON_ERR_INVALID_ARG;
-    double acc[5] = {0, 0, 0, 0, 0};
+    double acc[6] = {0, 0, 0, 0, 0, 0};
+    // stage k runs from event from[k] to event to[k] (NS steps)
+    const int from[4] = {0, 1, 6, 3}, to[4] = {1, 2, 3, 4};
     for (size_t g = 0; g < p->n_timed; ++g) {
         const auto& se = p->evs[g];
         float t = 0.f;
         if (se.ns) {
             if (cudaEventSynchronize(se.e[4]) != cudaSuccess) return MUON_ERR_CUDA;
             for (int k = 0; k < 4; ++k) {
-                if (cudaEventElapsedTime(&t, se.e[k], se.e[k + 1]) != cudaSuccess) return MUON_ERR_CUDA;
+                if (cudaEventElapsedTime(&t, se.e[from[k]], se.e[to[k]]) != cudaSuccess) return MUON_ERR_CUDA;
                 acc[k] += t;
             }
+            if (cudaEventElapsedTime(&t, se.e[2], se.e[6]) != cudaSuccess) return MUON_ERR_CUDA;
+            acc[5] += t;
         } else {
             if (cudaEventSynchronize(se.e[5]) != cudaSuccess) return MUON_ERR_CUDA;
             if (cudaEventElapsedTime(&t, se.e[0], se.e[5]) != cudaSuccess) return MUON_ERR_CUDA;

@@ -314,3 +314,38 @@ def test_invalid_arguments_are_rejected_without_touching_buffers():
     torch.cuda.synchronize()
     assert torch.equal(W, W0) and torch.equal(M, M0)
     plan.sync()
+
+
+def test_stage_times_split_fused_and_gemm_stages():
+    """muon_stage_times: six stages; the fused r <= 128 step has its own stage and
+    its matrices are left out of the GEMM stages' algorithmic FLOPs; the stages
+    of NS steps add up to the step time."""
+    import torch
+    import matrix_orthogonalising_optimizer_muon_gb300 as lib
+    from workloads import gen_tensor
+    shapes = [(128, 1000), (300, 700), (700, 300), (64, 64)]
+    W = [gen_tensor(s, 0.02, 7 + i, "cuda") for i, s in enumerate(shapes)]
+    G = [gen_tensor(s, 1e-3, 17 + i, "cuda") for i, s in enumerate(shapes)]
+    M = [gen_tensor(s, 1e-3, 27 + i, "cuda") for i, s in enumerate(shapes)]
+    plan = lib.MuonPlan(shapes, "f32", timing=True)
+    plan.step(W, G, M, LR, WD, MU, 5, "ns")
+    plan.sync()
+    plan.stage_times()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for _ in range(3):
+        plan.step(W, G, M, LR, WD, MU, 5, "ns")
+    ev1.record()
+    plan.sync()
+    torch.cuda.synchronize()
+    ms, fl = plan.stage_times()
+    assert len(ms) == 6 and all(x >= 0 for x in ms)
+    assert ms[4] == 0.0                      # no RowNorm step ran
+    assert all(ms[k] > 0 for k in (0, 1, 2, 3, 5))
+    total = ev0.elapsed_time(ev1)
+    assert 0.7 * total <= sum(ms) <= 1.05 * total, (ms, total)
+    r, c = 300, 700                          # the two non-fused matrices (one per orientation)
+    assert fl[0] == pytest.approx(3 * 2 * r * r * c)
+    assert fl[1] == pytest.approx(3 * 2 * 17 * r ** 3)
+    assert fl[2] == pytest.approx(3 * 2 * 2 * r * r * c)
+    plan.close()

@@ -15,9 +15,9 @@ Workloads (shapes as stored, row-major m x n):
   mlp-in 8192x2048, mlp-out 2048x8192, adaLN 12288x2048 (periodic RowNorm, K=4).
 * ``dit_block``: one of those blocks (0.75 GB of W, G, M: still above L2), the
   small case used to profile the RowNorm kernels.
-* ``qwen7b_heads_layer``: one layer of the per-head split (36 matrices 128 x 3584
-  and one 3584 x 512; 183 MB of W, G, M: above L2), the small case used to
-  profile the fused r <= 128 kernel.
+* ``qwen7b_heads_5l``: five layers of the per-head split (180 matrices 128 x 3584
+  and five 3584 x 512; 0.9 GB of W, G, M: above L2, and enough matrices to fill
+  every SM), the small case used to profile the fused r <= 128 kernel.
 
 Values: W ~ N(0, 0.02^2), G ~ N(0, 1e-3^2), M ~ N(0, 1e-3^2); G is bf16 except
 in ``single``.  Each tensor gets its own seed from (workload, step, matrix, kind).
@@ -54,8 +54,8 @@ def _qwen_heads():
     return one * 28 + ((HIDDEN_7B, 512),) * 28
 
 
-def _qwen_heads_layer():
-    return ((128, HIDDEN_7B),) * (28 + 4 + 4) + ((HIDDEN_7B, 512),)
+def _qwen_heads_layers(n):
+    return (((128, HIDDEN_7B),) * (28 + 4 + 4) + ((HIDDEN_7B, 512),)) * n
 
 
 def _dit_block():
@@ -70,7 +70,7 @@ WORKLOADS = {
     "qwen7b_heads": Workload("qwen7b_heads", _qwen_heads(), "bf16", 3),
     "dit1p3b": Workload("dit1p3b", _dit_block() * 28, "bf16", 4, steps=8, rownorm_k=4),
     "dit_block": Workload("dit_block", _dit_block(), "bf16", 5, steps=8, rownorm_k=4),
-    "qwen7b_heads_layer": Workload("qwen7b_heads_layer", _qwen_heads_layer(), "bf16", 6),
+    "qwen7b_heads_5l": Workload("qwen7b_heads_5l", _qwen_heads_layers(5), "bf16", 6),
 }
 
 
