@@ -68,7 +68,16 @@ typedef struct {
     /* nonzero: matrices with min(m, n) <= 128 also take the batched products instead of
        the fused kernel that runs the whole step of such a matrix on one SM */
     int32_t generic_small;
-    int32_t reserved[4];
+    /* plans holding both fused (min(m, n) <= 128) and batched matrices run the
+       two concurrently: the fused kernel on all SMs but 2 x chain_clusters, the
+       batched products on a second stream forked from and joined back into the
+       caller's stream with events.  0: chosen from the plan's work estimate
+       (overlap only when the fused matrices hold most of the work); > 0: that
+       many CTA pairs for the batched products; < 0: no overlap (the fused
+       kernel, then the batched products, on the caller's stream).  Results do
+       not depend on this choice. */
+    int32_t chain_clusters;
+    int32_t reserved[3];
 } muon_plan_opts;
 
 typedef struct muon_plan_s* muon_plan;

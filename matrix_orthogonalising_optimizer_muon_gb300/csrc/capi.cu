@@ -86,6 +86,22 @@ bool make_out_map(CUtensorMap* map, void* base, bool bf16, uint64_t r, uint64_t 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// CTA pairs left to the batched products of a plan that also holds fused
+// (r <= 128) matrices, or 0 to run the two one after the other.  Estimates at
+// full GPU: the fused kernel moves its bytes at about 5.1 TB/s; the batched side
+// is a chain of 16 dependent launches (about 20 us each when small) plus its
+// FLOPs at about 1.2 PFLOP/s.  The batched side gets the share of CTA pairs its
+// estimate holds of the total, within [1/8, 1/2] of them; when it is the larger
+// part it runs after the fused kernel on every SM instead (a persistent launch
+// keeps its CTA pairs to the end, after the fused kernel has finished).
+int choose_chain_clusters(double fused_bytes, double chain_flops, int max_pairs) {
+    const double t_fused = fused_bytes / 5.1e12;
+    const double t_chain = 16 * 20e-6 + chain_flops / 1.2e15;
+    if (t_chain >= t_fused) return 0;
+    const int k = (int)std::lround(max_pairs * t_chain / (t_chain + t_fused));
+    return std::min(std::max(k, std::max(1, max_pairs / 8)), max_pairs / 2);
+}
+
 inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 inline long long round_up(long long a, long long b) { return ceil_div(a, b) * b; }
 
@@ -124,6 +140,11 @@ struct muon_plan_s {
     int device = 0;
     int sm_count = 0;
     int pair_clusters = 0;   // co-resident CTA pairs for the 2-SM kernel (0: 1-SM kernel only)
+    // fused (r <= 128) and batched matrices in one plan: CTA pairs left to the batched
+    // products while the fused kernel runs (0: no overlap), their stream and fork/join
+    int chain_clusters = 0;
+    cudaStream_t s2 = nullptr;
+    cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
     muon_dtype gdt = MUON_F32;
     muon_plan_opts opts{};
     std::vector<muon_shape> shapes;
@@ -153,9 +174,11 @@ struct muon_plan_s {
     // opts.timing: one event group per step since the last muon_stage_times call
     // NS: e[0] momentum | e[1] SYRK | e[2] fused r <= 128 | e[6] r x r | e[3] final | e[4];
     // RowNorm: e[0] .. e[5]
+    // (split: the batched products run on s2 from e[1], beside the fused kernel)
     struct StepEvents {
         cudaEvent_t e[7];
         bool ns;
+        bool split;
     };
     std::vector<StepEvents> evs;
     size_t n_timed = 0;
@@ -283,11 +306,14 @@ struct Grouper {
     muon_plan_s* p;
     cudaStream_t s;
     bool bf16;
+    int clusters = 0;   // CTA pairs for the pair kernel, CTAs for the one-SM kernel
+    int grid1 = 0;
     GemmLaunch L1;   // 1-SM kernel, 128 x 256 tiles
     GemmLaunch L2;   // CTA-pair kernel, 256 x 256 tiles
     muon_status st = MUON_OK;
     int launches = 0;
-    Grouper(muon_plan_s* plan, cudaStream_t stream, bool is_bf16) : p(plan), s(stream), bf16(is_bf16) {
+    Grouper(muon_plan_s* plan, cudaStream_t stream, bool is_bf16, int pair_clusters, int sm_grid)
+        : p(plan), s(stream), bf16(is_bf16), clusters(pair_clusters), grid1(sm_grid) {
         reset(L1);
         reset(L2);
     }
@@ -330,7 +356,7 @@ struct Grouper {
     void flush1() {
         if (L1.nprob == 0) return;
         if (st == MUON_OK) {
-            st = cuda_status(gemm_launch(L1, bf16, p->sm_count, s));
+            st = cuda_status(gemm_launch(L1, bf16, grid1, s));
             ++launches;
         }
         reset(L1);
@@ -338,7 +364,7 @@ struct Grouper {
     void flush2() {
         if (L2.nprob == 0) return;
         if (st == MUON_OK) {
-            st = cuda_status(gemm2_launch(L2, bf16, p->pair_clusters, s));
+            st = cuda_status(gemm2_launch(L2, bf16, clusters, s));
             ++launches;
         }
         reset(L2);
@@ -368,6 +394,9 @@ void free_plan(muon_plan_s* p) {
     if (p->ws) cudaFree(p->ws);
     if (p->h_pinned) cudaFreeHost(p->h_pinned);
     if (p->upload_ev) cudaEventDestroy(p->upload_ev);
+    if (p->fork_ev) cudaEventDestroy(p->fork_ev);
+    if (p->join_ev) cudaEventDestroy(p->join_ev);
+    if (p->s2) cudaStreamDestroy(p->s2);
     for (auto& g : p->evs)
         for (auto& e : g.e)
             if (e) cudaEventDestroy(e);
@@ -628,6 +657,27 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
         ok = gemm2_max_clusters(&clusters) == cudaSuccess;
         p->pair_clusters = clusters;
     }
+    if (ok && p->pair_clusters > 1 && p->opts.chain_clusters >= 0) {
+        double fused_bytes = 0, chain_flops = 0;
+        for (auto& b : p->buckets) {
+            const double r = b.r, c = b.c;
+            if (b.fused)
+                fused_bytes += 12.0 * r * c * b.batch;
+            else
+                chain_flops += (3.0 * r * r * c + 17.0 * r * r * r) * b.batch;
+        }
+        if (fused_bytes > 0 && chain_flops > 0) {
+            int k = p->opts.chain_clusters;
+            if (k == 0) k = choose_chain_clusters(fused_bytes, chain_flops, p->pair_clusters);
+            k = std::min(k, std::min(p->pair_clusters - 1, (p->sm_count - 2) / 2));
+            if (k > 0) {
+                p->chain_clusters = k;
+                ok = cudaStreamCreateWithFlags(&p->s2, cudaStreamNonBlocking) == cudaSuccess &&
+                     cudaEventCreateWithFlags(&p->fork_ev, cudaEventDisableTiming) == cudaSuccess &&
+                     cudaEventCreateWithFlags(&p->join_ev, cudaEventDisableTiming) == cudaSuccess;
+            }
+        }
+    }
     ok = ok && cudaDeviceSynchronize() == cudaSuccess;
     if (!ok) {
         cudaGetLastError();
@@ -732,28 +782,22 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
         p->flops[2] += fl_final;
     }
 
-    // ---- G0' = s alpha^2 X0 X0^T (lower triangle, mirrored), all buckets in one launch
-    {
-        Grouper g(p, s, true);
-        for (auto& b : p->buckets) {
-            if (b.fused) continue;
-            GemmProblem q = problem(b.r, b.r, b.c, b.batch, true, kEpiSyrk);
-            q.C = b.G[0];
-            q.strideC = (long long)b.r * b.ldr;
-            q.ldc = b.ldr;
-            q.alpha = p->alpha + b.slot_base;
-            q.out_scale = b.gscale;
-            q.tma_out = kTmaOutC;
-            g.add(b.ut_a, b.ut_b, b.ut_a, q, &b.og[0]);
-        }
-        g.flush();
-        if (g.st != MUON_OK) return g.st;
-        launches += g.launches;
+    // Plans with both fused and batched matrices run them side by side: the batched
+    // products on p->s2 (forked here, joined after the final product) with
+    // chain_clusters CTA pairs, the fused kernel on the remaining SMs.
+    const bool split = p->chain_clusters > 0;
+    cudaStream_t sc = split ? p->s2 : s;
+    const int gc_clusters = split ? p->chain_clusters : p->pair_clusters;
+    const int g_grid1 = split ? 2 * p->chain_clusters : p->sm_count;
+    const int fused_grid = split ? p->sm_count - 2 * p->chain_clusters : p->sm_count;
+    if (se) se->split = split;
+    if (split) {
+        MUON_TRY(cudaEventRecord(p->fork_ev, s));
+        MUON_TRY(cudaStreamWaitEvent(p->s2, p->fork_ev, 0));
     }
-    if (se) MUON_TRY(cudaEventRecord(se->e[2], s));
 
     // ---- r <= 128: the whole step of each matrix (SYRK, recursion, final product +
-    // update) in one fused launch; its time is counted in the r x r stage
+    // update) in one fused launch, on all SMs but those left to the batched products
     {
         GemmLaunch Ls;
         std::memset(&Ls, 0, sizeof(Ls));
@@ -761,7 +805,7 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
         float* const* W = reinterpret_cast<float* const*>(p->d_ptrs + 2 * n);
         auto flush_small = [&]() -> muon_status {
             if (Ls.nprob == 0) return MUON_OK;
-            const muon_status st2 = cuda_status(ns_small_launch(Ls, p->sm_count, s));
+            const muon_status st2 = cuda_status(ns_small_launch(Ls, fused_grid, s));
             ++launches;
             std::memset(&Ls, 0, sizeof(Ls));
             Ls.status = p->status;
@@ -796,6 +840,28 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
     }
     if (se) MUON_TRY(cudaEventRecord(se->e[6], s));
 
+
+    // ---- G0' = s alpha^2 X0 X0^T (lower triangle, mirrored), all buckets in one launch
+    {
+        Grouper g(p, sc, true, gc_clusters, g_grid1);
+        for (auto& b : p->buckets) {
+            if (b.fused) continue;
+            GemmProblem q = problem(b.r, b.r, b.c, b.batch, true, kEpiSyrk);
+            q.C = b.G[0];
+            q.strideC = (long long)b.r * b.ldr;
+            q.ldc = b.ldr;
+            q.alpha = p->alpha + b.slot_base;
+            q.out_scale = b.gscale;
+            q.tma_out = kTmaOutC;
+            g.add(b.ut_a, b.ut_b, b.ut_a, q, &b.og[0]);
+        }
+        g.flush();
+        if (g.st != MUON_OK) return g.st;
+        launches += g.launches;
+    }
+    if (se) MUON_TRY(cudaEventRecord(se->e[2], sc));
+
+
     // ---- Newton-Schulz in the Gram space (fp16 operands, G carried as s G)
     const int J = ns_steps;
     int gc = 0;   // current G buffer
@@ -808,7 +874,7 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
     };
     for (int k = 1; k <= J; ++k) {
         {   // P = aI + (b/s) G' + (c/s^2) G'^2 (at k = 1 this is also Q_1)
-            Grouper g(p, s, false);
+            Grouper g(p, sc, false, gc_clusters, g_grid1);
             for (auto& b : p->buckets) {
             if (b.fused) continue;
                 GemmProblem q = rr_problem(b, kEpiPoly);
@@ -828,7 +894,7 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
             launches += g.launches;
         }
         {   // Q' = P Q (k >= 2) and T = P P (k < J), independent: one launch
-            Grouper g(p, s, false);
+            Grouper g(p, sc, false, gc_clusters, g_grid1);
             for (auto& b : p->buckets) {
             if (b.fused) continue;
                 if (k >= 2) {
@@ -856,7 +922,7 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
             if (k >= 2) qc ^= 1;
         }
         if (k < J) {   // G'' = G' T
-            Grouper g(p, s, false);
+            Grouper g(p, sc, false, gc_clusters, g_grid1);
             for (auto& b : p->buckets) {
             if (b.fused) continue;
                 GemmProblem q = rr_problem(b, kEpiPlain);
@@ -873,15 +939,15 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
     if (J == 0) {
         for (auto& b : p->buckets) {
             if (b.fused) continue;
-            MUON_TRY(launch_identity_bf16(b.Qb, b.r, b.ldr, b.batch, s));
+            MUON_TRY(launch_identity_bf16(b.Qb, b.r, b.ldr, b.batch, sc));
             ++launches;
         }
     }
-    if (se) MUON_TRY(cudaEventRecord(se->e[3], s));
+    if (se) MUON_TRY(cudaEventRecord(se->e[3], sc));
 
     // ---- O = alpha Q X0, fused W <- W - lr (s O + wd W) in the stored layout
     {
-        Grouper g(p, s, true);
+        Grouper g(p, sc, true, gc_clusters, g_grid1);
         float* const* W = reinterpret_cast<float* const*>(p->d_ptrs + 2 * n);
         for (auto& b : p->buckets) {
             if (b.fused) continue;
@@ -901,7 +967,11 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
         if (g.st != MUON_OK) return g.st;
         launches += g.launches;
     }
-    if (se) MUON_TRY(cudaEventRecord(se->e[4], s));
+    if (se) MUON_TRY(cudaEventRecord(se->e[4], sc));
+    if (split) {
+        MUON_TRY(cudaEventRecord(p->join_ev, p->s2));
+        MUON_TRY(cudaStreamWaitEvent(s, p->join_ev, 0));
+    }
     p->last_launches = launches;
     return MUON_OK;
 }
@@ -972,19 +1042,20 @@ muon_status muon_stage_times(muon_plan p, float* ms, double* flops, int32_t n_st
     if (!p || !ms || n_stages < 0 || n_stages > 6) return MUON_ERR_INVALID_ARG;
     if (p->n_timed == 0) return MUON_ERR_INVALID_ARG;
     double acc[6] = {0, 0, 0, 0, 0, 0};
-    // stage k runs from event from[k] to event to[k] (NS steps)
-    const int from[4] = {0, 1, 6, 3}, to[4] = {1, 2, 3, 4};
+    // NS steps: momentum e[0] -> e[1]; fused e[1] -> e[6]; SYRK from e[6] (after the
+    // fused kernel) or, split, from e[1] (beside it) to e[2]; r x r e[2] -> e[3];
+    // final e[3] -> e[4]
     for (size_t g = 0; g < p->n_timed; ++g) {
         const auto& se = p->evs[g];
         float t = 0.f;
         if (se.ns) {
-            if (cudaEventSynchronize(se.e[4]) != cudaSuccess) return MUON_ERR_CUDA;
-            for (int k = 0; k < 4; ++k) {
+            if (cudaEventSynchronize(se.e[4]) != cudaSuccess || cudaEventSynchronize(se.e[6]) != cudaSuccess)
+                return MUON_ERR_CUDA;
+            const int from[5] = {0, se.split ? 1 : 6, 2, 3, 1}, to[5] = {1, 2, 3, 4, 6}, slot[5] = {0, 1, 2, 3, 5};
+            for (int k = 0; k < 5; ++k) {
                 if (cudaEventElapsedTime(&t, se.e[from[k]], se.e[to[k]]) != cudaSuccess) return MUON_ERR_CUDA;
-                acc[k] += t;
+                acc[slot[k]] += t;
             }
-            if (cudaEventElapsedTime(&t, se.e[2], se.e[6]) != cudaSuccess) return MUON_ERR_CUDA;
-            acc[5] += t;
         } else {
             if (cudaEventSynchronize(se.e[5]) != cudaSuccess) return MUON_ERR_CUDA;
             if (cudaEventElapsedTime(&t, se.e[0], se.e[5]) != cudaSuccess) return MUON_ERR_CUDA;

@@ -316,10 +316,12 @@ def test_invalid_arguments_are_rejected_without_touching_buffers():
     plan.sync()
 
 
-def test_stage_times_split_fused_and_gemm_stages():
+@pytest.mark.parametrize("chain_clusters", [-1, 6])
+def test_stage_times_split_fused_and_gemm_stages(chain_clusters):
     """muon_stage_times: six stages; the fused r <= 128 step has its own stage and
-    its matrices are left out of the GEMM stages' algorithmic FLOPs; the stages
-    of NS steps add up to the step time."""
+    its matrices are left out of the GEMM stages' algorithmic FLOPs.  Run in
+    sequence (chain_clusters -1) the stages of NS steps add up to the step time;
+    overlapped (6 CTA pairs for the batched products) they run beside the fused one."""
     import torch
     import matrix_orthogonalising_optimizer_muon_gb300 as lib
     from workloads import gen_tensor
@@ -327,7 +329,7 @@ def test_stage_times_split_fused_and_gemm_stages():
     W = [gen_tensor(s, 0.02, 7 + i, "cuda") for i, s in enumerate(shapes)]
     G = [gen_tensor(s, 1e-3, 17 + i, "cuda") for i, s in enumerate(shapes)]
     M = [gen_tensor(s, 1e-3, 27 + i, "cuda") for i, s in enumerate(shapes)]
-    plan = lib.MuonPlan(shapes, "f32", timing=True)
+    plan = lib.MuonPlan(shapes, "f32", timing=True, chain_clusters=chain_clusters)
     plan.step(W, G, M, LR, WD, MU, 5, "ns")
     plan.sync()
     plan.stage_times()
@@ -343,9 +345,29 @@ def test_stage_times_split_fused_and_gemm_stages():
     assert ms[4] == 0.0                      # no RowNorm step ran
     assert all(ms[k] > 0 for k in (0, 1, 2, 3, 5))
     total = ev0.elapsed_time(ev1)
-    assert 0.7 * total <= sum(ms) <= 1.05 * total, (ms, total)
+    batched = ms[1] + ms[2] + ms[3]
+    span = ms[0] + (ms[5] + batched if chain_clusters < 0 else max(ms[5], batched))
+    assert 0.7 * total <= span <= 1.05 * total, (ms, total)
     r, c = 300, 700                          # the two non-fused matrices (one per orientation)
     assert fl[0] == pytest.approx(3 * 2 * r * r * c)
     assert fl[1] == pytest.approx(3 * 2 * 17 * r ** 3)
     assert fl[2] == pytest.approx(3 * 2 * 2 * r * r * c)
     plan.close()
+
+
+def test_overlapped_fused_and_batched_match_sequential_bitwise():
+    """The fused and batched matrices of one plan run side by side on two streams
+    (automatic split) or one after the other (chain_clusters -1); every tile's
+    arithmetic is the same either way, so W, M and O agree bit for bit."""
+    import torch
+    shapes = [(128, 1000), (100, 3000), (300, 700), (700, 300), (64, 64), (520, 2100)]
+    inputs = host_inputs(shapes, "bf16", base_seed=77)
+    outs = []
+    for cc in (0, -1, 5):
+        res = run_step(shapes, "bf16", inputs=inputs, chain_clusters=cc)
+        outs.append(res)
+    for res in outs[1:]:
+        for i in range(len(shapes)):
+            assert torch.equal(res["W"][i], outs[0]["W"][i]), i
+            assert torch.equal(res["M"][i], outs[0]["M"][i]), i
+            assert torch.equal(res["O"][i], outs[0]["O"][i]), i
