@@ -134,6 +134,16 @@ muon_status muon_rownorm_step(muon_plan p, float* const* params, const void* con
 muon_status muon_sync(muon_plan p, void* stream);
 
 /*
+ * muon_debug_wait_timeout - test hook for the bounded device waits: enqueues on
+ * stream one mbarrier wait whose phase nothing completes, bounded at limit_us
+ * microseconds (1 .. 1e6).  The wait gives up, records the timeout in the plan's
+ * status word and the kernel returns, as every tensor-core kernel does when a
+ * TMA load or MMA commit never arrives; the next muon_sync returns
+ * MUON_ERR_TIMEOUT (and clears the word) and the plan stays usable.
+ */
+muon_status muon_debug_wait_timeout(muon_plan p, int32_t limit_us, void* stream);
+
+/*
  * muon_debug_copy_update - copy the orthogonalised update O of matrix i from
  * the last NS step (stored layout, m x n fp32) into dst (device memory, m*n
  * floats).  Needs opts.keep_update; synchronises stream.

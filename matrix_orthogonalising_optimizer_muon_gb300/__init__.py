@@ -59,6 +59,7 @@ EXPORTED = {
     "muon_plan_create": (ctypes.c_int, [ctypes.POINTER(MuonShape), ctypes.c_int32, ctypes.c_int,
                                         ctypes.POINTER(MuonPlanOpts), ctypes.POINTER(_P)]),
     "muon_plan_destroy": (None, [_P]),
+    "muon_debug_wait_timeout": (ctypes.c_int, [_P, ctypes.c_int32, _P]),
     "muon_step": (ctypes.c_int, [_P, _PP, _PP, _PP, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                  ctypes.c_int32, ctypes.c_int, _P]),
     "muon_rownorm_step": (ctypes.c_int, [_P, _PP, _PP, _PP, ctypes.c_float, ctypes.c_float,
@@ -220,6 +221,12 @@ class MuonPlan:
 
     def sync(self, stream=None):
         _check(self.lib.muon_sync(self.handle, _stream_handle(stream)), "muon_sync")
+
+    def debug_wait_timeout(self, limit_us: int, stream=None):
+        """Enqueue one bounded device wait that nothing completes (``muon_debug_wait_timeout``);
+        the next ``sync`` raises MuonError with MUON_ERR_TIMEOUT."""
+        _check(self.lib.muon_debug_wait_timeout(self.handle, int(limit_us), _stream_handle(stream)),
+               "muon_debug_wait_timeout")
 
     def debug_update(self, i: int, stream=None):
         """O of matrix i from the last NS step (needs keep_update), as a CUDA fp32 tensor."""

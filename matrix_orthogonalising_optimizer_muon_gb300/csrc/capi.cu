@@ -988,6 +988,13 @@ muon_status muon_sync(muon_plan p, void* stream) {
     return MUON_OK;
 }
 
+muon_status muon_debug_wait_timeout(muon_plan p, int32_t limit_us, void* stream) {
+    if (!p || limit_us < 1 || limit_us > 1000000) return MUON_ERR_INVALID_ARG;
+    if (check_device(p) != MUON_OK) return MUON_ERR_INVALID_ARG;
+    return cuda_status(
+        launch_wait_selftest(p->status, 1000ull * (unsigned long long)limit_us, static_cast<cudaStream_t>(stream)));
+}
+
 muon_status muon_debug_copy_update(muon_plan p, int32_t i, float* dst, void* stream) {
     if (!p || !dst || i < 0 || i >= (int)p->shapes.size()) return MUON_ERR_INVALID_ARG;
     if (!p->opts.keep_update) return MUON_ERR_INVALID_ARG;

@@ -9,6 +9,7 @@
 // Reductions never use floating-point atomics, so results are bitwise
 // reproducible run to run.
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace muon {
 
@@ -497,6 +498,26 @@ cudaError_t launch_rownorm_colapply(const ElemArgs& a, long long blocks, cudaStr
         k_rownorm_colapply<true><<<(unsigned)blocks, kElemThreads, 0, s>>>(a);
     else
         k_rownorm_colapply<false><<<(unsigned)blocks, kElemThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ bounded-wait self test
+// One wait on an mbarrier whose phase nothing completes: the bounded wait gives
+// up after limit_ns, raises the abort flag and records kStatusTimeoutSelftest in
+// the status word, and the kernel returns (the same path every tensor-core kernel
+// takes when a TMA load or an MMA commit never arrives).
+__global__ void k_wait_selftest(int* status, unsigned long long limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    mbar_wait(&bar, 0, &abort_flag, status, kStatusTimeoutSelftest, limit_ns);
+}
+
+cudaError_t launch_wait_selftest(int* status, unsigned long long limit_ns, cudaStream_t s) {
+    k_wait_selftest<<<1, 32, 0, s>>>(status, limit_ns);
     return cudaGetLastError();
 }
 

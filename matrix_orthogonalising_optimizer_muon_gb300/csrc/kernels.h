@@ -154,4 +154,7 @@ constexpr int kColSlab = 64;                                         // RowNorm 
 constexpr int kColWidth = 4 * kElemThreads;                          // columns per column-stat block
 constexpr long long kApplyElemsPerBlock = 4LL * kElemThreads * 4;    // RowNorm col apply
 
+// bounded-wait self test: one mbarrier wait that nothing completes (limit in ns)
+cudaError_t launch_wait_selftest(int* status, unsigned long long limit_ns, cudaStream_t s);
+
 }  // namespace muon

@@ -16,6 +16,7 @@ enum DeviceStatus : int {
     kStatusTimeoutProducer = 0x101,
     kStatusTimeoutMma = 0x102,
     kStatusTimeoutEpilogue = 0x103,
+    kStatusTimeoutSelftest = 0x1ff,   // muon_debug_wait_timeout
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -59,14 +60,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // `*abort` and records `code` in the global status word.  Returns true on
 // completion.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status,
-                                          int code) {
+                                          int code, unsigned long long limit_ns = kWaitTimeoutNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 0u) {
             if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+            if (globaltimer_ns() - t0 > limit_ns) {
                 *abort = 1;
                 atomicExch(status, code);
                 return false;

@@ -371,3 +371,24 @@ def test_overlapped_fused_and_batched_match_sequential_bitwise():
             assert torch.equal(res["W"][i], outs[0]["W"][i]), i
             assert torch.equal(res["M"][i], outs[0]["M"][i]), i
             assert torch.equal(res["O"][i], outs[0]["O"][i]), i
+
+
+def test_bounded_wait_expiry_is_reported_and_plan_recovers():
+    """Failure detection without a fault: a device wait that nothing completes gives
+    up after its limit, muon_sync reports MUON_ERR_TIMEOUT once, and the same plan
+    then steps correctly (checked against the oracle)."""
+    import matrix_orthogonalising_optimizer_muon_gb300 as lib
+    shapes = [(256, 1024), (100, 700)]
+    inputs = host_inputs(shapes, "f32", base_seed=91)
+    plan = lib.MuonPlan(shapes, "f32", keep_update=True)
+    plan.debug_wait_timeout(500)
+    with pytest.raises(lib.MuonError) as ei:
+        plan.sync()
+    assert ei.value.code == lib.MUON_ERR_TIMEOUT
+    plan.sync()                               # the status word was cleared
+    res = run_step(shapes, "f32", inputs=inputs, plan=plan)
+    for i in range(len(shapes)):
+        assert_ns(res, i)
+    with pytest.raises(lib.MuonError):
+        plan.debug_wait_timeout(0)            # limit outside [1, 1e6] us: refused on the host
+    plan.close()
