@@ -81,6 +81,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 // ------------------------------------------------------------------ momentum, m <= n
 template <bool BF16>
 __global__ void __launch_bounds__(kElemThreads) k_momentum_rows(const ElemArgs a) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float sred[33];
     const long long b = blockIdx.x;
     const int li = find_entry(a.list_blk, a.nlist, b);
@@ -140,6 +142,8 @@ __global__ void __launch_bounds__(kElemThreads) k_momentum_rows(const ElemArgs a
 // ------------------------------------------------------------------ momentum, m > n (transpose to r x c)
 template <bool BF16>
 __global__ void __launch_bounds__(kElemThreads) k_momentum_tiles(const ElemArgs a) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float tile[kTile][kTile + 1];   // [stored col][stored row]
     __shared__ float sred[33];
     const long long b = blockIdx.x;
@@ -224,6 +228,8 @@ __global__ void __launch_bounds__(kElemThreads) k_momentum_tiles(const ElemArgs 
 
 // ------------------------------------------------------------------ 1/||U||_F
 __global__ void k_norm_finalize(const ElemArgs a) {
+    pdl_trigger();
+    pdl_wait();
     const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (w >= a.nlist) return;
@@ -236,6 +242,8 @@ __global__ void k_norm_finalize(const ElemArgs a) {
 }
 
 __global__ void k_identity_bf16(__nv_bfloat16* q, int r, int ld, long long total) {
+    pdl_trigger();
+    pdl_wait();
     const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (e >= total) return;
     const long long per = (long long)r * ld;
@@ -249,6 +257,8 @@ constexpr int kRowMaxVec = 8;    // float4 groups per thread kept in registers (
 
 template <bool BF16>
 __global__ void __launch_bounds__(kElemThreads) k_rownorm_rows(const ElemArgs a) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float sred[33];
     const long long b = blockIdx.x;
     const int li = find_entry(a.list_blk, a.nlist, b);
@@ -327,6 +337,8 @@ __global__ void __launch_bounds__(kElemThreads) k_rownorm_rows(const ElemArgs a)
 // column sums of U^2 go to partials[cpart_off + slab * n + j].
 template <bool BF16>
 __global__ void __launch_bounds__(kElemThreads) k_rownorm_colstats(const ElemArgs a) {
+    pdl_trigger();
+    pdl_wait();
     const long long b = blockIdx.x;
     const int li = find_entry(a.list_blk, a.nlist, b);
     const int mi = a.list[li];
@@ -383,6 +395,8 @@ __global__ void __launch_bounds__(kElemThreads) k_rownorm_colstats(const ElemArg
 
 // inv[j] = 1 / max(||U[:, j]||_2, eps): fixed-order sum over the row slabs.
 __global__ void __launch_bounds__(kElemThreads) k_rownorm_colfinal(const ElemArgs a) {
+    pdl_trigger();
+    pdl_wait();
     const long long b = blockIdx.x;
     const int li = find_entry(a.list_blk, a.nlist, b);
     const MatDev md = a.mats[a.list[li]];
@@ -397,6 +411,8 @@ __global__ void __launch_bounds__(kElemThreads) k_rownorm_colfinal(const ElemArg
 // W <- W - lr (s * U * inv[col] + wd W), U recomputed from G and the stored new M.
 template <bool BF16>
 __global__ void __launch_bounds__(kElemThreads) k_rownorm_colapply(const ElemArgs a) {
+    pdl_trigger();
+    pdl_wait();
     const long long b = blockIdx.x;
     const int li = find_entry(a.list_blk, a.nlist, b);
     const int mi = a.list[li];
@@ -445,60 +461,52 @@ __global__ void __launch_bounds__(kElemThreads) k_rownorm_colapply(const ElemArg
 cudaError_t launch_momentum_rows(const ElemArgs& a, long long blocks, cudaStream_t s) {
     if (blocks <= 0) return cudaSuccess;
     if (a.grad_bf16)
-        k_momentum_rows<true><<<(unsigned)blocks, kElemThreads, 0, s>>>(a);
+        return launch_pdl(k_momentum_rows<true>, dim3((unsigned)blocks), dim3(kElemThreads), 0, s, a);
     else
-        k_momentum_rows<false><<<(unsigned)blocks, kElemThreads, 0, s>>>(a);
-    return cudaGetLastError();
+        return launch_pdl(k_momentum_rows<false>, dim3((unsigned)blocks), dim3(kElemThreads), 0, s, a);
 }
 cudaError_t launch_momentum_tiles(const ElemArgs& a, long long blocks, cudaStream_t s) {
     if (blocks <= 0) return cudaSuccess;
     if (a.grad_bf16)
-        k_momentum_tiles<true><<<(unsigned)blocks, kElemThreads, 0, s>>>(a);
+        return launch_pdl(k_momentum_tiles<true>, dim3((unsigned)blocks), dim3(kElemThreads), 0, s, a);
     else
-        k_momentum_tiles<false><<<(unsigned)blocks, kElemThreads, 0, s>>>(a);
-    return cudaGetLastError();
+        return launch_pdl(k_momentum_tiles<false>, dim3((unsigned)blocks), dim3(kElemThreads), 0, s, a);
 }
 cudaError_t launch_norm_finalize(const ElemArgs& a, cudaStream_t s) {
     if (a.nlist <= 0) return cudaSuccess;
     const int warps_per_block = kElemThreads / 32;
     const int blocks = (a.nlist + warps_per_block - 1) / warps_per_block;
-    k_norm_finalize<<<blocks, kElemThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(k_norm_finalize, dim3(blocks), dim3(kElemThreads), 0, s, a);
 }
 cudaError_t launch_identity_bf16(__nv_bfloat16* q, int r, int ld, int batch, cudaStream_t s) {
     const long long total = (long long)r * ld * batch;
     if (total <= 0) return cudaSuccess;
-    k_identity_bf16<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(q, r, ld, total);
-    return cudaGetLastError();
+    return launch_pdl(k_identity_bf16, dim3((unsigned)((total + 255) / 256)), dim3(256), 0, s, q, r, ld, total);
 }
 cudaError_t launch_rownorm_rows(const ElemArgs& a, long long blocks, cudaStream_t s) {
     if (blocks <= 0) return cudaSuccess;
     if (a.grad_bf16)
-        k_rownorm_rows<true><<<(unsigned)blocks, kElemThreads, 0, s>>>(a);
+        return launch_pdl(k_rownorm_rows<true>, dim3((unsigned)blocks), dim3(kElemThreads), 0, s, a);
     else
-        k_rownorm_rows<false><<<(unsigned)blocks, kElemThreads, 0, s>>>(a);
-    return cudaGetLastError();
+        return launch_pdl(k_rownorm_rows<false>, dim3((unsigned)blocks), dim3(kElemThreads), 0, s, a);
 }
 cudaError_t launch_rownorm_colstats(const ElemArgs& a, long long blocks, cudaStream_t s) {
     if (blocks <= 0) return cudaSuccess;
     if (a.grad_bf16)
-        k_rownorm_colstats<true><<<(unsigned)blocks, kElemThreads, 0, s>>>(a);
+        return launch_pdl(k_rownorm_colstats<true>, dim3((unsigned)blocks), dim3(kElemThreads), 0, s, a);
     else
-        k_rownorm_colstats<false><<<(unsigned)blocks, kElemThreads, 0, s>>>(a);
-    return cudaGetLastError();
+        return launch_pdl(k_rownorm_colstats<false>, dim3((unsigned)blocks), dim3(kElemThreads), 0, s, a);
 }
 cudaError_t launch_rownorm_colfinal(const ElemArgs& a, long long blocks, cudaStream_t s) {
     if (blocks <= 0) return cudaSuccess;
-    k_rownorm_colfinal<<<(unsigned)blocks, kElemThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(k_rownorm_colfinal, dim3((unsigned)blocks), dim3(kElemThreads), 0, s, a);
 }
 cudaError_t launch_rownorm_colapply(const ElemArgs& a, long long blocks, cudaStream_t s) {
     if (blocks <= 0) return cudaSuccess;
     if (a.grad_bf16)
-        k_rownorm_colapply<true><<<(unsigned)blocks, kElemThreads, 0, s>>>(a);
+        return launch_pdl(k_rownorm_colapply<true>, dim3((unsigned)blocks), dim3(kElemThreads), 0, s, a);
     else
-        k_rownorm_colapply<false><<<(unsigned)blocks, kElemThreads, 0, s>>>(a);
-    return cudaGetLastError();
+        return launch_pdl(k_rownorm_colapply<false>, dim3((unsigned)blocks), dim3(kElemThreads), 0, s, a);
 }
 
 // ------------------------------------------------------------------ bounded-wait self test

@@ -111,6 +111,8 @@ __global__ void __maxnreg__(168) gemm_kernel(const __grid_constant__ GemmLaunch 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_trigger();
+    pdl_wait();   // the previous kernel of the stream is complete from here on
 
     if (warp == 0) {
         if (lane == 0) {
@@ -338,6 +340,8 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
     cluster_sync();   // barriers of both CTAs initialised before any remote signal
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_trigger();
+    pdl_wait();   // the previous kernel of the stream is complete from here on
 
     if (warp == 0) {
         if (lane == 0) {
@@ -527,20 +531,18 @@ cudaError_t gemm2_launch(const GemmLaunch& L, bool bf16, int clusters, cudaStrea
     if (clusters > L.total_tiles) clusters = L.total_tiles;
     if (clusters < 1) clusters = 1;
     if (bf16)
-        gemm2_kernel<true><<<2 * clusters, kGemmThreads, Gemm2Cfg::SMEM_BYTES, s>>>(L);
+        return launch_pdl(gemm2_kernel<true>, dim3(2 * clusters), dim3(kGemmThreads), Gemm2Cfg::SMEM_BYTES, s, L);
     else
-        gemm2_kernel<false><<<2 * clusters, kGemmThreads, Gemm2Cfg::SMEM_BYTES, s>>>(L);
-    return cudaGetLastError();
+        return launch_pdl(gemm2_kernel<false>, dim3(2 * clusters), dim3(kGemmThreads), Gemm2Cfg::SMEM_BYTES, s, L);
 }
 
 cudaError_t gemm_launch(const GemmLaunch& L, bool bf16, int grid, cudaStream_t s) {
     if (L.total_tiles <= 0) return cudaSuccess;
     if (grid > L.total_tiles) grid = L.total_tiles;
     if (bf16)
-        gemm_kernel<true><<<grid, kGemmThreads, GemmCfg::SMEM_BYTES, s>>>(L);
+        return launch_pdl(gemm_kernel<true>, dim3(grid), dim3(kGemmThreads), GemmCfg::SMEM_BYTES, s, L);
     else
-        gemm_kernel<false><<<grid, kGemmThreads, GemmCfg::SMEM_BYTES, s>>>(L);
-    return cudaGetLastError();
+        return launch_pdl(gemm_kernel<false>, dim3(grid), dim3(kGemmThreads), GemmCfg::SMEM_BYTES, s, L);
 }
 
 }  // namespace muon

@@ -38,6 +38,23 @@ enum Epilogue : int {
 // the SYRK and the final product, fp16 for the r x r recursion.  With sym = 1
 // the output is symmetric (M = N): only tiles touching the lower triangle are
 // computed and each lower element is also written to its mirror position.
+// Launch with programmatic stream serialisation (see pdl_trigger / pdl_wait).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 struct GemmProblem {
     int M, N, K, batch;
     int tiles_m, tiles_n, tiles_per_item, tile_begin;

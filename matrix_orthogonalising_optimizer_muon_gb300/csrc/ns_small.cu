@@ -200,6 +200,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_trigger();
+    pdl_wait();   // the previous kernel of the stream is complete from here on
 
     if (warp == 0) {
         if (lane == 0) {
@@ -440,8 +442,7 @@ cudaError_t ns_small_prepare() {
 cudaError_t ns_small_launch(const GemmLaunch& L, int grid, cudaStream_t s) {
     if (L.total_tiles <= 0) return cudaSuccess;
     if (grid > L.total_tiles) grid = L.total_tiles;
-    ns_small_kernel<<<grid, kSmallThreads, SmallCfg::SMEM_BYTES, s>>>(L);
-    return cudaGetLastError();
+    return launch_pdl(ns_small_kernel, dim3(grid), dim3(kSmallThreads), SmallCfg::SMEM_BYTES, s, L);
 }
 
 }  // namespace muon

@@ -29,6 +29,17 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
     return t;
 }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+// Kernels of the step are launched with programmatic stream serialisation: each
+// CTA allows the next kernel of the stream to launch at once (pdl_trigger), and
+// waits for the previous kernel to complete and its memory to be visible
+// (pdl_wait) before its first global memory access, after its own set-up.  A CTA
+// can only trigger once it is resident, so a waiting dependent never takes an SM
+// from a kernel that still has CTAs to place.  Both are no-ops without the
+// launch attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
