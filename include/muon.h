@@ -77,7 +77,13 @@ typedef struct {
        kernel, then the batched products, on the caller's stream).  Results do
        not depend on this choice. */
     int32_t chain_clusters;
-    int32_t reserved[3];
+    int32_t reserved;
+    /* > 0: cap on the plan's device workspace in bytes.  The NS step then runs in
+       chunks of matrices (momentum, SYRK, recursion, final product + update per
+       chunk) whose X0 and r x r buffers share one region; results are the same.
+       muon_plan_create returns MUON_ERR_OOM if the cap cannot hold the per-matrix
+       tables plus the buffers of the largest single matrix.  0: no cap (one chunk). */
+    int64_t workspace_bytes;
 } muon_plan_opts;
 
 typedef struct muon_plan_s* muon_plan;
@@ -163,6 +169,9 @@ muon_status muon_debug_copy_update(muon_plan p, int32_t i, float* dst, void* str
  * is r*ld elements of 2 bytes (one 4-byte float for which = 8).
  * After a step with ns_steps = J, G buffer 0 holds s*G_0 when J <= 2, G
  * buffer 1 holds s*G_1 when J >= 2, buffer 3 holds P_J and buffer 7 holds Q_J.
+ * Matrices with min(m, n) <= 128 on the fused kernel have no r x r buffers
+ * (which 1-7 return MUON_ERR_UNSUPPORTED).  With a workspace cap the chunks
+ * share these buffers: they hold the last chunk's matrices.
  */
 muon_status muon_debug_copy_workspace(muon_plan p, int32_t i, int32_t which, void* dst, int32_t* ld,
                                       void* stream);

@@ -43,7 +43,8 @@ class MuonShape(ctypes.Structure):
 class MuonPlanOpts(ctypes.Structure):
     _fields_ = [("keep_update", ctypes.c_int32), ("timing", ctypes.c_int32),
                 ("single_sm_gemm", ctypes.c_int32), ("generic_small", ctypes.c_int32),
-                ("chain_clusters", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+                ("chain_clusters", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("workspace_bytes", ctypes.c_int64)]
 
 
 class MuonPlanInfo(ctypes.Structure):
@@ -139,13 +140,13 @@ class MuonPlan:
 
     def __init__(self, shapes, grad_dtype: str = "bf16", keep_update: bool = False,
                  timing: bool = False, single_sm_gemm: bool = False, generic_small: bool = False,
-                 chain_clusters: int = 0):
+                 chain_clusters: int = 0, workspace_bytes: int = 0):
         self.lib = load()
         self.shapes = [(int(m), int(n)) for m, n in shapes]
         self.grad_dtype = grad_dtype
         arr = (MuonShape * len(self.shapes))(*[MuonShape(m, n) for m, n in self.shapes])
         opts = MuonPlanOpts(1 if keep_update else 0, 1 if timing else 0, 1 if single_sm_gemm else 0,
-                            1 if generic_small else 0, int(chain_clusters))
+                            1 if generic_small else 0, int(chain_clusters), 0, int(workspace_bytes))
         h = ctypes.c_void_p()
         gd = {"bf16": MUON_BF16, "f32": MUON_F32}[grad_dtype]
         _check(self.lib.muon_plan_create(arr, len(self.shapes), gd, ctypes.byref(opts),

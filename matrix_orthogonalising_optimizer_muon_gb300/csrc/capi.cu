@@ -108,6 +108,7 @@ inline long long round_up(long long a, long long b) { return ceil_div(a, b) * b;
 struct Bucket {
     int r = 0, c = 0, batch = 0;
     bool fused = false;     // r <= 128: whole step in the fused one-matrix-per-CTA kernel
+    int chunk = 0;          // workspace chunk (see muon_plan_opts.workspace_bytes)
     int ldr = 0;   // leading dim of r x r buffers (multiple of 8)
     int ldu = 0;   // leading dim of X0 rows (multiple of 8)
     std::vector<int> mats;
@@ -140,9 +141,8 @@ struct muon_plan_s {
     int device = 0;
     int sm_count = 0;
     int pair_clusters = 0;   // co-resident CTA pairs for the 2-SM kernel (0: 1-SM kernel only)
-    // fused (r <= 128) and batched matrices in one plan: CTA pairs left to the batched
-    // products while the fused kernel runs (0: no overlap), their stream and fork/join
-    int chain_clusters = 0;
+    // fused (r <= 128) and batched matrices in one chunk: the batched products' stream
+    // and fork/join events (created when a chunk overlaps the two)
     cudaStream_t s2 = nullptr;
     cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
     muon_dtype gdt = MUON_F32;
@@ -164,7 +164,15 @@ struct muon_plan_s {
     unsigned char* d_transposed = nullptr;
     void** d_ptrs = nullptr;   // [G(n) | M(n) | W(n)]
 
-    ListDev mom_rows, mom_tiles, all, rn_rows, rn_stats, rn_final, rn_apply;
+    ListDev rn_rows, rn_stats, rn_final, rn_apply;
+    // NS steps run chunk by chunk; the chunks' X0 and r x r buffers share (alias) one
+    // workspace region.  One chunk unless opts.workspace_bytes caps the workspace.
+    struct Chunk {
+        std::vector<int> buckets;
+        ListDev mom_rows, mom_tiles, all;
+        int chain_clusters = 0;   // CTA pairs for the batched products beside the fused kernel
+    };
+    std::vector<Chunk> chunks;
 
     void** h_pinned = nullptr;
     std::vector<void*> h_cache;
@@ -172,13 +180,13 @@ struct muon_plan_s {
     bool uploaded = false;
 
     // opts.timing: one event group per step since the last muon_stage_times call
-    // NS: e[0] momentum | e[1] SYRK | e[2] fused r <= 128 | e[6] r x r | e[3] final | e[4];
-    // RowNorm: e[0] .. e[5]
-    // (split: the batched products run on s2 from e[1], beside the fused kernel)
+    // Per chunk c, events e[7c + k].  NS: e[0] momentum | e[1] fused r <= 128 | e[6],
+    // batched SYRK from e[6] (or, split, from e[1] beside the fused kernel) | e[2] r x r |
+    // e[3] final | e[4].  RowNorm: e[0] .. e[5] of chunk 0.
     struct StepEvents {
-        cudaEvent_t e[7];
-        bool ns;
-        bool split;
+        std::vector<cudaEvent_t> e;
+        std::vector<char> split;
+        bool ns = false;
     };
     std::vector<StepEvents> evs;
     size_t n_timed = 0;
@@ -382,8 +390,14 @@ muon_plan_s::StepEvents* next_events(muon_plan_s* p) {
     if (p->n_timed < p->evs.size()) return &p->evs[p->n_timed++];
     if (p->evs.size() >= kMaxTimedSteps) return &p->evs.back();
     muon_plan_s::StepEvents g{};
+    g.e.assign(7 * p->chunks.size(), nullptr);
+    g.split.assign(p->chunks.size(), 0);
     for (auto& e : g.e)
-        if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+        if (cudaEventCreate(&e) != cudaSuccess) {
+            for (auto& x : g.e)
+                if (x) cudaEventDestroy(x);
+            return nullptr;
+        }
     p->evs.push_back(g);
     p->n_timed = p->evs.size();
     return &p->evs.back();
@@ -453,10 +467,13 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
     if (opts) p->opts = *opts;
     p->shapes.assign(shapes, shapes + n);
 
-    // ---- orient + bucket by (r, c) (DiT paper sec. 3.1; DMuon batching)
+    // ---- orient; group by oriented shape (r, c) in order of first appearance
+    // (DiT paper sec. 3.1; DMuon batching)
     p->mats.resize(n);
     p->mat_bucket.resize(n);
     p->mat_item.resize(n);
+    std::vector<std::pair<int, int>> group_rc;
+    std::vector<std::vector<int>> group_mats;
     for (int i = 0; i < n; ++i) {
         MatDev& md = p->mats[i];
         std::memset(&md, 0, sizeof(md));
@@ -466,46 +483,35 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
         md.c = (int)std::max(md.m, md.n);
         md.transposed = md.m > md.n;
         md.scale = 0.2f * std::sqrt((float)md.c);   // blog eq. (4)
-        int b = -1;
-        for (size_t k = 0; k < p->buckets.size(); ++k)
-            if (p->buckets[k].r == md.r && p->buckets[k].c == md.c) b = (int)k;
-        if (b < 0) {
-            Bucket nb;
-            nb.r = md.r;
-            nb.c = md.c;
-            nb.ldr = (int)round_up(md.r, 8);
-            nb.ldu = (int)round_up(md.c, 8);
-            p->buckets.push_back(nb);
-            b = (int)p->buckets.size() - 1;
+        size_t g = 0;
+        while (g < group_rc.size() && !(group_rc[g].first == md.r && group_rc[g].second == md.c)) ++g;
+        if (g == group_rc.size()) {
+            group_rc.push_back({md.r, md.c});
+            group_mats.emplace_back();
         }
-        p->mat_bucket[i] = b;
-        p->mat_item[i] = (int)p->buckets[b].mats.size();
-        p->buckets[b].mats.push_back(i);
+        group_mats[g].push_back(i);
     }
 
-    // ---- workspace layout (256-byte aligned slices of one allocation)
+    // ---- workspace: a fixed part (per-matrix tables, partial sums, pointer tables,
+    // launch lists, debug copies of O) and a region for the X0 and r x r buffers of
+    // one chunk of matrices, shared by all chunks (they run one after the other)
+    const bool fused_ok = !p->opts.generic_small;
+    auto is_fused = [&](int r) { return fused_ok && r <= kSmallMaxR; };
+    auto mat_region_bytes = [&](int r, int c) {   // X0 slice + the seven r x r buffers
+        const double ldu = (double)round_up(c, 8), ldr = (double)round_up(r, 8);
+        return 2.0 * r * ldu + (is_fused(r) ? 0.0 : 7 * 2.0 * r * ldr);
+    };
     size_t off = 0;
     auto take = [&](size_t bytes) {
         const size_t o = off;
         off = (size_t)round_up((long long)(off + bytes), 256);
         return o;
     };
-    long long ut_elems = 0, slots = 0;
-    for (auto& b : p->buckets) {
-        b.batch = (int)b.mats.size();
-        b.slot_base = (int)slots;
-        slots += b.batch;
-        b.ut_off = ut_elems;
-        ut_elems += (long long)b.batch * b.r * b.ldu;
-    }
+    // momentum / RowNorm bookkeeping per matrix (not chunked)
     long long mom_part = 0, col_part = 0, inv_elems = 0;
-    std::vector<int> rows_list, tiles_list, all_list, rnr_list, rnc_list;
+    std::vector<int> rnr_list, rnc_list;
     for (int i = 0; i < n; ++i) {
         MatDev& md = p->mats[i];
-        const Bucket& b = p->buckets[p->mat_bucket[i]];
-        md.slot = b.slot_base + p->mat_item[i];
-        md.ldu = b.ldu;
-        md.ut_off = b.ut_off + (long long)p->mat_item[i] * b.r * b.ldu;
         md.nblk = (int)(md.transposed ? ceil_div(md.m, kTile) * ceil_div(md.n, kTile)
                                       : ceil_div(md.m * md.n, kMomElemsPerBlock));
         md.part_off = mom_part;
@@ -515,51 +521,113 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
             col_part += ceil_div(md.m, kColSlab) * md.n;
             md.inv_off = inv_elems;
             inv_elems += round_up(md.n, 4);
-            tiles_list.push_back(i);
             rnc_list.push_back(i);
         } else {
-            rows_list.push_back(i);
             rnr_list.push_back(i);
         }
-        all_list.push_back(i);
     }
-    const size_t o_ut = take((size_t)ut_elems * 2);
     const size_t o_mats = take(sizeof(MatDev) * n);
     const size_t o_part = take(sizeof(float) * std::max<long long>(mom_part, 1));
     const size_t o_cpart = take(sizeof(float) * std::max<long long>(col_part, 1));
     const size_t o_inv = take(sizeof(float) * std::max<long long>(inv_elems, 1));
-    const size_t o_alpha = take(sizeof(float) * std::max<long long>(slots, 1));
+    const size_t o_alpha = take(sizeof(float) * n);
     const size_t o_status = take(sizeof(int));
     const size_t o_tr = take((size_t)n);
     const size_t o_ptrs = take(sizeof(void*) * 3 * n);
-    std::vector<size_t> o_item(p->buckets.size()), o_rr(p->buckets.size()), o_qb(p->buckets.size()),
-        o_odbg(p->buckets.size());
-    for (size_t k = 0; k < p->buckets.size(); ++k) {
-        Bucket& b = p->buckets[k];
-        o_item[k] = take(sizeof(int) * b.batch);
-        const size_t rr = (size_t)b.batch * b.r * b.ldr;
-        o_rr[k] = take(rr * 2);   // G0 (fp16, scaled)
-        take(rr * 2);             // G1
-        take(rr * 2);             // P
-        take(rr * 2);             // T
-        take(rr * 2);             // Q0
-        take(rr * 2);             // Q1
-        o_qb[k] = take(rr * 2);   // bf16 Q for the final product
-        o_odbg[k] = p->opts.keep_update ? take((size_t)b.batch * b.r * b.c * 4) : 0;
+    const size_t o_items = take(sizeof(int) * n);   // item -> plan matrix, per bucket slice
+    const size_t o_odbg = p->opts.keep_update ? take([&] {
+        size_t t = 0;
+        for (int i = 0; i < n; ++i) t += (size_t)round_up(p->mats[i].m * p->mats[i].n * 4, 256);
+        return t;
+    }()) : 0;
+    // launch lists: per chunk the momentum rows / tiles / all lists, and the four
+    // RowNorm lists.  Chunks partition the matrices, so the entries total at most
+    // 2n + 3 per chunk (n chunks at most) plus 4n + 4: 10n + 8 ints and prefixes.
+    const size_t o_lists = take(sizeof(int) * (size_t)(10 * n + 8));
+    const size_t o_prefix = take(sizeof(long long) * (size_t)(10 * n + 8));
+    const size_t fixed_bytes = off;
+
+    // ---- chunks: matrices in group order, a new chunk whenever the region would
+    // exceed what the cap leaves after the fixed part (one chunk without a cap)
+    const long long cap = p->opts.workspace_bytes;
+    double region_cap = 1e300;
+    if (cap > 0) {
+        region_cap = (double)cap - (double)fixed_bytes;
+        double need = 0;
+        for (int i = 0; i < n; ++i) need = std::max(need, mat_region_bytes(p->mats[i].r, p->mats[i].c) + 8 * 256.0);
+        if (region_cap < need) {
+            delete p;
+            return MUON_ERR_OOM;   // the cap cannot hold even the largest single matrix
+        }
     }
-    // launch lists: int lists, then long long prefixes
-    struct HostList {
-        std::vector<int>* v;
-        ListDev* d;
-        int kind;
-    };
-    HostList hl[] = {{&rows_list, &p->mom_rows, 0}, {&tiles_list, &p->mom_tiles, 1}, {&all_list, &p->all, 2},
-                     {&rnr_list, &p->rn_rows, 3},   {&rnc_list, &p->rn_stats, 4},   {&rnc_list, &p->rn_final, 5},
-                     {&rnc_list, &p->rn_apply, 6}};
-    std::vector<size_t> o_list(7), o_blk(7);
-    for (int k = 0; k < 7; ++k) {
-        o_list[k] = take(sizeof(int) * std::max<size_t>(hl[k].v->size(), 1));
-        o_blk[k] = take(sizeof(long long) * (hl[k].v->size() + 1));
+    {
+        double used = 0;
+        p->chunks.emplace_back();
+        for (size_t g = 0; g < group_rc.size(); ++g) {
+            const int r = group_rc[g].first, c = group_rc[g].second;
+            int cur = -1;   // bucket of this group in the current chunk
+            for (int i : group_mats[g]) {
+                const double need = mat_region_bytes(r, c) + (cur < 0 ? 8 * 256.0 : 0.0);
+                if (used + need > region_cap && used > 0) {
+                    p->chunks.emplace_back();
+                    used = 0;
+                    cur = -1;
+                }
+                if (cur < 0) {
+                    Bucket nb;
+                    nb.r = r;
+                    nb.c = c;
+                    nb.ldr = (int)round_up(r, 8);
+                    nb.ldu = (int)round_up(c, 8);
+                    nb.fused = is_fused(r);
+                    nb.chunk = (int)p->chunks.size() - 1;
+                    p->buckets.push_back(nb);
+                    cur = (int)p->buckets.size() - 1;
+                    p->chunks.back().buckets.push_back(cur);
+                    used += 8 * 256.0;
+                }
+                used += mat_region_bytes(r, c);
+                p->mat_bucket[i] = cur;
+                p->mat_item[i] = (int)p->buckets[cur].mats.size();
+                p->buckets[cur].mats.push_back(i);
+            }
+        }
+    }
+    // region offsets: each chunk's buckets laid out from the start of the region
+    size_t region_bytes = 0;
+    std::vector<size_t> o_ut(p->buckets.size()), o_rr(p->buckets.size()), o_qb(p->buckets.size());
+    {
+        int slots = 0;
+        for (auto& ch : p->chunks) {
+            size_t roff = 0;
+            auto rtake = [&](size_t bytes) {
+                const size_t o = roff;
+                roff = (size_t)round_up((long long)(roff + bytes), 256);
+                return o;
+            };
+            for (int k : ch.buckets) {
+                Bucket& b = p->buckets[k];
+                b.batch = (int)b.mats.size();
+                b.slot_base = slots;
+                slots += b.batch;
+                o_ut[k] = rtake((size_t)b.batch * b.r * b.ldu * 2);
+                if (!b.fused) {
+                    const size_t rr = (size_t)b.batch * b.r * b.ldr * 2;
+                    o_rr[k] = rtake(rr);   // G0 (fp16, scaled)
+                    for (int q = 0; q < 5; ++q) rtake(rr);   // G1, P, T, Q0, Q1
+                    o_qb[k] = rtake(rr);   // bf16 Q for the final product
+                }
+            }
+            region_bytes = std::max(region_bytes, roff);
+        }
+    }
+    const size_t o_region = take(std::max<size_t>(region_bytes, 256));
+    for (int i = 0; i < n; ++i) {
+        MatDev& md = p->mats[i];
+        const Bucket& b = p->buckets[p->mat_bucket[i]];
+        md.slot = b.slot_base + p->mat_item[i];
+        md.ldu = b.ldu;
+        md.ut_off = (long long)(o_ut[p->mat_bucket[i]] / 2) + (long long)p->mat_item[i] * b.r * b.ldu;
     }
     p->ws_bytes = off;
     if (cudaMalloc(&p->ws, p->ws_bytes) != cudaSuccess) {
@@ -568,7 +636,7 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
         return MUON_ERR_OOM;
     }
     char* base = static_cast<char*>(p->ws);
-    p->ut = reinterpret_cast<__nv_bfloat16*>(base + o_ut);
+    p->ut = reinterpret_cast<__nv_bfloat16*>(base + o_region);
     p->d_mats = reinterpret_cast<MatDev*>(base + o_mats);
     p->partials = reinterpret_cast<float*>(base + o_part);
     p->cpartials = reinterpret_cast<float*>(base + o_cpart);
@@ -585,17 +653,20 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
     ok = ok && cudaMemset(p->status, 0, sizeof(int)) == cudaSuccess;
     ok = ok && cudaMemset(p->d_ptrs, 0, sizeof(void*) * 3 * n) == cudaSuccess;
 
-    for (int k = 0; ok && k < 7; ++k) {
-        std::vector<int>& v = *hl[k].v;
-        ListDev& d = *hl[k].d;
-        d.list = reinterpret_cast<int*>(base + o_list[k]);
-        d.blk = reinterpret_cast<long long*>(base + o_blk[k]);
+    // launch lists (int lists then long long prefixes, carved from their slices)
+    int* list_cursor = reinterpret_cast<int*>(base + o_lists);
+    long long* prefix_cursor = reinterpret_cast<long long*>(base + o_prefix);
+    auto upload_list = [&](const std::vector<int>& v, ListDev& d, int kind) {
+        d.list = list_cursor;
+        d.blk = prefix_cursor;
         d.n = (int)v.size();
+        list_cursor += std::max<size_t>(v.size(), 1);
+        prefix_cursor += v.size() + 1;
         std::vector<long long> pre(v.size() + 1, 0);
         for (size_t j = 0; j < v.size(); ++j) {
             const MatDev& md = p->mats[v[j]];
             long long nb = 0;
-            switch (hl[k].kind) {
+            switch (kind) {
                 case 0: case 1: nb = md.nblk; break;
                 case 2: nb = 1; break;
                 case 3: nb = md.m; break;
@@ -606,30 +677,53 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
             pre[j + 1] = pre[j] + nb;
         }
         d.blocks = pre.back();
-        if (!v.empty()) ok = cudaMemcpy(d.list, v.data(), sizeof(int) * v.size(), cudaMemcpyHostToDevice) == cudaSuccess;
-        ok = ok && cudaMemcpy(d.blk, pre.data(), sizeof(long long) * pre.size(), cudaMemcpyHostToDevice) == cudaSuccess;
+        if (ok && !v.empty()) ok = cudaMemcpy(d.list, v.data(), sizeof(int) * v.size(), cudaMemcpyHostToDevice) == cudaSuccess;
+        if (ok) ok = cudaMemcpy(d.blk, pre.data(), sizeof(long long) * pre.size(), cudaMemcpyHostToDevice) == cudaSuccess;
+    };
+    for (auto& ch : p->chunks) {
+        std::vector<int> rows, tiles, all;
+        for (int k : ch.buckets)
+            for (int i : p->buckets[k].mats) {
+                (p->mats[i].transposed ? tiles : rows).push_back(i);
+                all.push_back(i);
+            }
+        upload_list(rows, ch.mom_rows, 0);
+        upload_list(tiles, ch.mom_tiles, 1);
+        upload_list(all, ch.all, 2);
     }
+    upload_list(rnr_list, p->rn_rows, 3);
+    upload_list(rnc_list, p->rn_stats, 4);
+    upload_list(rnc_list, p->rn_final, 5);
+    upload_list(rnc_list, p->rn_apply, 6);
 
+    int* item_cursor = reinterpret_cast<int*>(base + o_items);
+    size_t odbg_off = o_odbg;
     for (size_t k = 0; ok && k < p->buckets.size(); ++k) {
         Bucket& b = p->buckets[k];
-        b.d_item_mat = reinterpret_cast<int*>(base + o_item[k]);
+        b.d_item_mat = item_cursor;
+        item_cursor += b.batch;
         ok = cudaMemcpy(b.d_item_mat, b.mats.data(), sizeof(int) * b.batch, cudaMemcpyHostToDevice) == cudaSuccess;
-        const size_t rr = (size_t)b.batch * b.r * b.ldr;
-        const size_t step = (size_t)round_up((long long)rr * 2, 256);
-        b.G[0] = reinterpret_cast<__half*>(base + o_rr[k]);
-        b.G[1] = reinterpret_cast<__half*>(base + o_rr[k] + step);
-        b.P = reinterpret_cast<__half*>(base + o_rr[k] + 2 * step);
-        b.T = reinterpret_cast<__half*>(base + o_rr[k] + 3 * step);
-        b.Q[0] = reinterpret_cast<__half*>(base + o_rr[k] + 4 * step);
-        b.Q[1] = reinterpret_cast<__half*>(base + o_rr[k] + 5 * step);
         b.gscale = std::ldexp(1.f, (int)std::lround(std::log2((double)b.r)));
-        b.fused = b.r <= kSmallMaxR && !p->opts.generic_small;
-        b.Qb = reinterpret_cast<__nv_bfloat16*>(base + o_qb[k]);
-        b.Odbg = p->opts.keep_update ? reinterpret_cast<float*>(base + o_odbg[k]) : nullptr;
+        b.ut_off = (long long)(o_ut[k] / 2);
+        if (p->opts.keep_update) {
+            b.Odbg = reinterpret_cast<float*>(base + odbg_off);
+            odbg_off += (size_t)round_up((long long)b.batch * b.r * b.c * 4, 256);
+        }
         __nv_bfloat16* ut = p->ut + b.ut_off;
         ok = ok && make_map(&b.ut_a, ut, true, b.c, b.r, b.batch, b.ldu, 64, kBM);
         ok = ok && make_map(&b.ut_b, ut, true, b.c, b.r, b.batch, b.ldu, 64, kBN);
         ok = ok && make_map(&b.ut_mn, ut, true, b.c, b.r, b.batch, b.ldu, 64, 64);
+        if (b.fused) continue;   // the fused kernel keeps its r x r operands on chip
+        const size_t rr = (size_t)b.batch * b.r * b.ldr;
+        const size_t step = (size_t)round_up((long long)rr * 2, 256);
+        char* rb = base + o_region + o_rr[k];
+        b.G[0] = reinterpret_cast<__half*>(rb);
+        b.G[1] = reinterpret_cast<__half*>(rb + step);
+        b.P = reinterpret_cast<__half*>(rb + 2 * step);
+        b.T = reinterpret_cast<__half*>(rb + 3 * step);
+        b.Q[0] = reinterpret_cast<__half*>(rb + 4 * step);
+        b.Q[1] = reinterpret_cast<__half*>(rb + 5 * step);
+        b.Qb = reinterpret_cast<__nv_bfloat16*>(base + o_region + o_qb[k]);
         ok = ok && make_map(&b.qb_a, b.Qb, true, b.r, b.r, b.batch, b.ldr, 64, kBM);
         for (int g = 0; g < 2; ++g) {
             ok = ok && make_map(&b.ga[g], b.G[g], false, b.r, b.r, b.batch, b.ldr, 64, kBM);
@@ -658,25 +752,29 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
         p->pair_clusters = clusters;
     }
     if (ok && p->pair_clusters > 1 && p->opts.chain_clusters >= 0) {
-        double fused_bytes = 0, chain_flops = 0;
-        for (auto& b : p->buckets) {
-            const double r = b.r, c = b.c;
-            if (b.fused)
-                fused_bytes += 12.0 * r * c * b.batch;
-            else
-                chain_flops += (3.0 * r * r * c + 17.0 * r * r * r) * b.batch;
-        }
-        if (fused_bytes > 0 && chain_flops > 0) {
-            int k = p->opts.chain_clusters;
-            if (k == 0) k = choose_chain_clusters(fused_bytes, chain_flops, p->pair_clusters);
-            k = std::min(k, std::min(p->pair_clusters - 1, (p->sm_count - 2) / 2));
-            if (k > 0) {
-                p->chain_clusters = k;
-                ok = cudaStreamCreateWithFlags(&p->s2, cudaStreamNonBlocking) == cudaSuccess &&
-                     cudaEventCreateWithFlags(&p->fork_ev, cudaEventDisableTiming) == cudaSuccess &&
-                     cudaEventCreateWithFlags(&p->join_ev, cudaEventDisableTiming) == cudaSuccess;
+        bool any = false;
+        for (auto& ch : p->chunks) {
+            double fused_bytes = 0, chain_flops = 0;
+            for (int k : ch.buckets) {
+                const Bucket& b = p->buckets[k];
+                const double r = b.r, c = b.c;
+                if (b.fused)
+                    fused_bytes += 12.0 * r * c * b.batch;
+                else
+                    chain_flops += (3.0 * r * r * c + 17.0 * r * r * r) * b.batch;
+            }
+            if (fused_bytes > 0 && chain_flops > 0) {
+                int k = p->opts.chain_clusters;
+                if (k == 0) k = choose_chain_clusters(fused_bytes, chain_flops, p->pair_clusters);
+                k = std::min(k, std::min(p->pair_clusters - 1, (p->sm_count - 2) / 2));
+                ch.chain_clusters = std::max(k, 0);
+                any = any || k > 0;
             }
         }
+        if (any)
+            ok = cudaStreamCreateWithFlags(&p->s2, cudaStreamNonBlocking) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&p->fork_ev, cudaEventDisableTiming) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&p->join_ev, cudaEventDisableTiming) == cudaSuccess;
     }
     ok = ok && cudaDeviceSynchronize() == cudaSuccess;
     if (!ok) {
@@ -748,22 +846,6 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
     const int n = (int)p->shapes.size();
     int launches = 0;
 
-    // ---- momentum, Nesterov, sum of squares, bf16 X0 (oriented)
-    if (se) {
-        se->ns = true;
-        MUON_TRY(cudaEventRecord(se->e[0], s));
-    }
-    ElemArgs a = elem_args(p, p->mom_rows, mu, lr, wd, 0.f);
-    MUON_TRY(launch_momentum_rows(a, p->mom_rows.blocks, s));
-    launches += p->mom_rows.blocks > 0;
-    a = elem_args(p, p->mom_tiles, mu, lr, wd, 0.f);
-    MUON_TRY(launch_momentum_tiles(a, p->mom_tiles.blocks, s));
-    launches += p->mom_tiles.blocks > 0;
-    a = elem_args(p, p->all, mu, lr, wd, 0.f);
-    MUON_TRY(launch_norm_finalize(a, s));
-    ++launches;
-    if (se) MUON_TRY(cudaEventRecord(se->e[1], s));
-
     // algorithmic tensor FLOPs of the GEMM stages (the fused r <= 128 step is
     // HBM-bound and timed as a stage of its own)
     double fl_syrk = 0, fl_rr = 0, fl_final = 0;
@@ -781,196 +863,221 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
         p->flops[1] += fl_rr;
         p->flops[2] += fl_final;
     }
+    if (se) se->ns = true;
+    for (size_t ci = 0; ci < p->chunks.size(); ++ci) {
+        const muon_plan_s::Chunk& ch = p->chunks[ci];
+        cudaEvent_t* ev = se ? &se->e[7 * ci] : nullptr;
+        // ---- momentum, Nesterov, sum of squares, bf16 X0 (oriented), for this chunk
+        if (ev) MUON_TRY(cudaEventRecord(ev[0], s));
+        ElemArgs a = elem_args(p, ch.mom_rows, mu, lr, wd, 0.f);
+        MUON_TRY(launch_momentum_rows(a, ch.mom_rows.blocks, s));
+        launches += ch.mom_rows.blocks > 0;
+        a = elem_args(p, ch.mom_tiles, mu, lr, wd, 0.f);
+        MUON_TRY(launch_momentum_tiles(a, ch.mom_tiles.blocks, s));
+        launches += ch.mom_tiles.blocks > 0;
+        a = elem_args(p, ch.all, mu, lr, wd, 0.f);
+        MUON_TRY(launch_norm_finalize(a, s));
+        ++launches;
+        if (ev) MUON_TRY(cudaEventRecord(ev[1], s));
 
-    // Plans with both fused and batched matrices run them side by side: the batched
-    // products on p->s2 (forked here, joined after the final product) with
-    // chain_clusters CTA pairs, the fused kernel on the remaining SMs.
-    const bool split = p->chain_clusters > 0;
-    cudaStream_t sc = split ? p->s2 : s;
-    const int gc_clusters = split ? p->chain_clusters : p->pair_clusters;
-    const int g_grid1 = split ? 2 * p->chain_clusters : p->sm_count;
-    const int fused_grid = split ? p->sm_count - 2 * p->chain_clusters : p->sm_count;
-    if (se) se->split = split;
-    if (split) {
-        MUON_TRY(cudaEventRecord(p->fork_ev, s));
-        MUON_TRY(cudaStreamWaitEvent(p->s2, p->fork_ev, 0));
-    }
 
-    // ---- r <= 128: the whole step of each matrix (SYRK, recursion, final product +
-    // update) in one fused launch, on all SMs but those left to the batched products
-    {
-        GemmLaunch Ls;
-        std::memset(&Ls, 0, sizeof(Ls));
-        Ls.status = p->status;
-        float* const* W = reinterpret_cast<float* const*>(p->d_ptrs + 2 * n);
-        auto flush_small = [&]() -> muon_status {
-            if (Ls.nprob == 0) return MUON_OK;
-            const muon_status st2 = cuda_status(ns_small_launch(Ls, fused_grid, s));
-            ++launches;
+        // Plans with both fused and batched matrices run them side by side: the batched
+        // products on p->s2 (forked here, joined after the final product) with
+        // chain_clusters CTA pairs, the fused kernel on the remaining SMs.
+        const bool split = ch.chain_clusters > 0;
+        cudaStream_t sc = split ? p->s2 : s;
+        const int gc_clusters = split ? ch.chain_clusters : p->pair_clusters;
+        const int g_grid1 = split ? 2 * ch.chain_clusters : p->sm_count;
+        const int fused_grid = split ? p->sm_count - 2 * ch.chain_clusters : p->sm_count;
+        if (se) se->split[ci] = split;
+        if (split) {
+            MUON_TRY(cudaEventRecord(p->fork_ev, s));
+            MUON_TRY(cudaStreamWaitEvent(p->s2, p->fork_ev, 0));
+        }
+
+        // ---- r <= 128: the whole step of each matrix (SYRK, recursion, final product +
+        // update) in one fused launch, on all SMs but those left to the batched products
+        {
+            GemmLaunch Ls;
             std::memset(&Ls, 0, sizeof(Ls));
             Ls.status = p->status;
-            return st2;
-        };
-        for (auto& b : p->buckets) {
-            if (!b.fused) continue;
-            if (Ls.nprob == kMaxProblems && (st = flush_small()) != MUON_OK) return st;
-            GemmProblem q = problem(b.r, b.c, b.r, b.batch, false, kEpiApply);
-            q.tiles_per_item = 1;
-            q.tile_begin = Ls.total_tiles;
-            q.alpha = p->alpha + b.slot_base;
-            q.item_mat = b.d_item_mat;
-            q.W = W;
-            q.transposed = p->d_transposed;
-            q.Odbg = b.Odbg;
-            q.lr = lr;
-            q.wd = wd;
-            q.scale = 0.2f * std::sqrt((float)b.c);
-            q.out_scale = b.gscale;
-            q.coef_a = kNsA;
-            q.coef_b = kNsB / b.gscale;
-            q.coef_c = kNsC / (b.gscale * b.gscale);
-            q.ns_steps = ns_steps;
-            Ls.mapA[Ls.nprob] = b.ut_a;
-            Ls.mapB[Ls.nprob] = b.ut_mn;
-            Ls.prob[Ls.nprob] = q;
-            Ls.nprob++;
-            Ls.total_tiles += b.batch;
-        }
-        if ((st = flush_small()) != MUON_OK) return st;
-    }
-    if (se) MUON_TRY(cudaEventRecord(se->e[6], s));
-
-
-    // ---- G0' = s alpha^2 X0 X0^T (lower triangle, mirrored), all buckets in one launch
-    {
-        Grouper g(p, sc, true, gc_clusters, g_grid1);
-        for (auto& b : p->buckets) {
-            if (b.fused) continue;
-            GemmProblem q = problem(b.r, b.r, b.c, b.batch, true, kEpiSyrk);
-            q.C = b.G[0];
-            q.strideC = (long long)b.r * b.ldr;
-            q.ldc = b.ldr;
-            q.alpha = p->alpha + b.slot_base;
-            q.out_scale = b.gscale;
-            q.tma_out = kTmaOutC;
-            g.add(b.ut_a, b.ut_b, b.ut_a, q, &b.og[0]);
-        }
-        g.flush();
-        if (g.st != MUON_OK) return g.st;
-        launches += g.launches;
-    }
-    if (se) MUON_TRY(cudaEventRecord(se->e[2], sc));
-
-
-    // ---- Newton-Schulz in the Gram space (fp16 operands, G carried as s G)
-    const int J = ns_steps;
-    int gc = 0;   // current G buffer
-    int qc = 0;   // current Q buffer
-    auto rr_problem = [](const Bucket& b, int epi) {
-        GemmProblem q = problem(b.r, b.r, b.r, b.batch, true, epi);
-        q.strideC = (long long)b.r * b.ldr;
-        q.ldc = b.ldr;
-        return q;
-    };
-    for (int k = 1; k <= J; ++k) {
-        {   // P = aI + (b/s) G' + (c/s^2) G'^2 (at k = 1 this is also Q_1)
-            Grouper g(p, sc, false, gc_clusters, g_grid1);
-            for (auto& b : p->buckets) {
-            if (b.fused) continue;
-                GemmProblem q = rr_problem(b, kEpiPoly);
-                q.C = b.P;
-                if (k == 1 && J > 1) q.C2 = b.Q[0];
-                if (k == 1 && J == 1) q.Cb = b.Qb;
-                q.Gin = b.G[gc];
+            float* const* W = reinterpret_cast<float* const*>(p->d_ptrs + 2 * n);
+            auto flush_small = [&]() -> muon_status {
+                if (Ls.nprob == 0) return MUON_OK;
+                const muon_status st2 = cuda_status(ns_small_launch(Ls, fused_grid, s));
+                ++launches;
+                std::memset(&Ls, 0, sizeof(Ls));
+                Ls.status = p->status;
+                return st2;
+            };
+            for (int bk : ch.buckets) {
+                Bucket& b = p->buckets[bk];
+                if (!b.fused) continue;
+                if (Ls.nprob == kMaxProblems && (st = flush_small()) != MUON_OK) return st;
+                GemmProblem q = problem(b.r, b.c, b.r, b.batch, false, kEpiApply);
+                q.tiles_per_item = 1;
+                q.tile_begin = Ls.total_tiles;
+                q.alpha = p->alpha + b.slot_base;
+                q.item_mat = b.d_item_mat;
+                q.W = W;
+                q.transposed = p->d_transposed;
+                q.Odbg = b.Odbg;
+                q.lr = lr;
+                q.wd = wd;
+                q.scale = 0.2f * std::sqrt((float)b.c);
+                q.out_scale = b.gscale;
                 q.coef_a = kNsA;
                 q.coef_b = kNsB / b.gscale;
                 q.coef_c = kNsC / (b.gscale * b.gscale);
-                // fp16 P (and the fp16 copy Q_1): TMA stores; P with a bf16 Q_1 (J = 1): per thread
-                q.tma_out = q.Cb ? 0 : (kTmaOutC | (q.C2 ? kTmaOutC2 : 0));
-                g.add(b.ga[gc], b.gb[gc], b.ga[gc], q, &b.op, q.C2 ? &b.oq[0] : nullptr);
+                q.ns_steps = ns_steps;
+                Ls.mapA[Ls.nprob] = b.ut_a;
+                Ls.mapB[Ls.nprob] = b.ut_mn;
+                Ls.prob[Ls.nprob] = q;
+                Ls.nprob++;
+                Ls.total_tiles += b.batch;
+            }
+            if ((st = flush_small()) != MUON_OK) return st;
+        }
+        if (ev) MUON_TRY(cudaEventRecord(ev[6], s));
+
+
+        // ---- G0' = s alpha^2 X0 X0^T (lower triangle, mirrored), all buckets in one launch
+        {
+            Grouper g(p, sc, true, gc_clusters, g_grid1);
+            for (int bk : ch.buckets) {
+                Bucket& b = p->buckets[bk];
+                if (b.fused) continue;
+                GemmProblem q = problem(b.r, b.r, b.c, b.batch, true, kEpiSyrk);
+                q.C = b.G[0];
+                q.strideC = (long long)b.r * b.ldr;
+                q.ldc = b.ldr;
+                q.alpha = p->alpha + b.slot_base;
+                q.out_scale = b.gscale;
+                q.tma_out = kTmaOutC;
+                g.add(b.ut_a, b.ut_b, b.ut_a, q, &b.og[0]);
             }
             g.flush();
             if (g.st != MUON_OK) return g.st;
             launches += g.launches;
         }
-        {   // Q' = P Q (k >= 2) and T = P P (k < J), independent: one launch
-            Grouper g(p, sc, false, gc_clusters, g_grid1);
-            for (auto& b : p->buckets) {
-            if (b.fused) continue;
-                if (k >= 2) {
-                    GemmProblem q = rr_problem(b, kEpiPlain);
+        if (ev) MUON_TRY(cudaEventRecord(ev[2], sc));
+
+
+        // ---- Newton-Schulz in the Gram space (fp16 operands, G carried as s G)
+        const int J = ns_steps;
+        int gc = 0;   // current G buffer
+        int qc = 0;   // current Q buffer
+        auto rr_problem = [](const Bucket& b, int epi) {
+            GemmProblem q = problem(b.r, b.r, b.r, b.batch, true, epi);
+            q.strideC = (long long)b.r * b.ldr;
+            q.ldc = b.ldr;
+            return q;
+        };
+        for (int k = 1; k <= J; ++k) {
+            {   // P = aI + (b/s) G' + (c/s^2) G'^2 (at k = 1 this is also Q_1)
+                Grouper g(p, sc, false, gc_clusters, g_grid1);
+                for (int bk : ch.buckets) {
+                Bucket& b = p->buckets[bk];
+                if (b.fused) continue;
+                    GemmProblem q = rr_problem(b, kEpiPoly);
+                    q.C = b.P;
+                    if (k == 1 && J > 1) q.C2 = b.Q[0];
+                    if (k == 1 && J == 1) q.Cb = b.Qb;
+                    q.Gin = b.G[gc];
+                    q.coef_a = kNsA;
+                    q.coef_b = kNsB / b.gscale;
+                    q.coef_c = kNsC / (b.gscale * b.gscale);
+                    // fp16 P (and the fp16 copy Q_1): TMA stores; P with a bf16 Q_1 (J = 1): per thread
+                    q.tma_out = q.Cb ? 0 : (kTmaOutC | (q.C2 ? kTmaOutC2 : 0));
+                    g.add(b.ga[gc], b.gb[gc], b.ga[gc], q, &b.op, q.C2 ? &b.oq[0] : nullptr);
+                }
+                g.flush();
+                if (g.st != MUON_OK) return g.st;
+                launches += g.launches;
+            }
+            {   // Q' = P Q (k >= 2) and T = P P (k < J), independent: one launch
+                Grouper g(p, sc, false, gc_clusters, g_grid1);
+                for (int bk : ch.buckets) {
+                Bucket& b = p->buckets[bk];
+                if (b.fused) continue;
+                    if (k >= 2) {
+                        GemmProblem q = rr_problem(b, kEpiPlain);
+                        if (k < J) {
+                            q.C = b.Q[qc ^ 1];
+                            q.tma_out = kTmaOutC;
+                            g.add(b.pa, b.qb[qc], b.qa[qc], q, &b.oq[qc ^ 1]);
+                        } else {
+                            q.Cb = b.Qb;
+                            q.tma_out = kTmaOutC | kTmaOutBf16;
+                            g.add(b.pa, b.qb[qc], b.qa[qc], q, &b.oqb);
+                        }
+                    }
                     if (k < J) {
-                        q.C = b.Q[qc ^ 1];
+                        GemmProblem q = rr_problem(b, kEpiPlain);
+                        q.C = b.T;
                         q.tma_out = kTmaOutC;
-                        g.add(b.pa, b.qb[qc], b.qa[qc], q, &b.oq[qc ^ 1]);
-                    } else {
-                        q.Cb = b.Qb;
-                        q.tma_out = kTmaOutC | kTmaOutBf16;
-                        g.add(b.pa, b.qb[qc], b.qa[qc], q, &b.oqb);
+                        g.add(b.pa, b.pb, b.pa, q, &b.ot);
                     }
                 }
-                if (k < J) {
+                g.flush();
+                if (g.st != MUON_OK) return g.st;
+                launches += g.launches;
+                if (k >= 2) qc ^= 1;
+            }
+            if (k < J) {   // G'' = G' T
+                Grouper g(p, sc, false, gc_clusters, g_grid1);
+                for (int bk : ch.buckets) {
+                Bucket& b = p->buckets[bk];
+                if (b.fused) continue;
                     GemmProblem q = rr_problem(b, kEpiPlain);
-                    q.C = b.T;
+                    q.C = b.G[gc ^ 1];
                     q.tma_out = kTmaOutC;
-                    g.add(b.pa, b.pb, b.pa, q, &b.ot);
+                    g.add(b.ga[gc], b.tb, b.ta, q, &b.og[gc ^ 1]);
                 }
+                g.flush();
+                if (g.st != MUON_OK) return g.st;
+                launches += g.launches;
+                gc ^= 1;
             }
-            g.flush();
-            if (g.st != MUON_OK) return g.st;
-            launches += g.launches;
-            if (k >= 2) qc ^= 1;
         }
-        if (k < J) {   // G'' = G' T
-            Grouper g(p, sc, false, gc_clusters, g_grid1);
-            for (auto& b : p->buckets) {
-            if (b.fused) continue;
-                GemmProblem q = rr_problem(b, kEpiPlain);
-                q.C = b.G[gc ^ 1];
-                q.tma_out = kTmaOutC;
-                g.add(b.ga[gc], b.tb, b.ta, q, &b.og[gc ^ 1]);
+        if (J == 0) {
+            for (int bk : ch.buckets) {
+                Bucket& b = p->buckets[bk];
+                if (b.fused) continue;
+                MUON_TRY(launch_identity_bf16(b.Qb, b.r, b.ldr, b.batch, sc));
+                ++launches;
             }
-            g.flush();
-            if (g.st != MUON_OK) return g.st;
-            launches += g.launches;
-            gc ^= 1;
         }
-    }
-    if (J == 0) {
-        for (auto& b : p->buckets) {
-            if (b.fused) continue;
-            MUON_TRY(launch_identity_bf16(b.Qb, b.r, b.ldr, b.batch, sc));
-            ++launches;
-        }
-    }
-    if (se) MUON_TRY(cudaEventRecord(se->e[3], sc));
+        if (ev) MUON_TRY(cudaEventRecord(ev[3], sc));
 
-    // ---- O = alpha Q X0, fused W <- W - lr (s O + wd W) in the stored layout
-    {
-        Grouper g(p, sc, true, gc_clusters, g_grid1);
-        float* const* W = reinterpret_cast<float* const*>(p->d_ptrs + 2 * n);
-        for (auto& b : p->buckets) {
-            if (b.fused) continue;
-            GemmProblem q = problem(b.r, b.c, b.r, b.batch, false, kEpiApply);
-            q.b_mn = 1;
-            q.alpha = p->alpha + b.slot_base;
-            q.item_mat = b.d_item_mat;
-            q.W = W;
-            q.transposed = p->d_transposed;
-            q.Odbg = b.Odbg;
-            q.lr = lr;
-            q.wd = wd;
-            q.scale = 0.2f * std::sqrt((float)b.c);
-            g.add(b.qb_a, b.ut_mn, b.ut_mn, q);
+        // ---- O = alpha Q X0, fused W <- W - lr (s O + wd W) in the stored layout
+        {
+            Grouper g(p, sc, true, gc_clusters, g_grid1);
+            float* const* W = reinterpret_cast<float* const*>(p->d_ptrs + 2 * n);
+            for (int bk : ch.buckets) {
+                Bucket& b = p->buckets[bk];
+                if (b.fused) continue;
+                GemmProblem q = problem(b.r, b.c, b.r, b.batch, false, kEpiApply);
+                q.b_mn = 1;
+                q.alpha = p->alpha + b.slot_base;
+                q.item_mat = b.d_item_mat;
+                q.W = W;
+                q.transposed = p->d_transposed;
+                q.Odbg = b.Odbg;
+                q.lr = lr;
+                q.wd = wd;
+                q.scale = 0.2f * std::sqrt((float)b.c);
+                g.add(b.qb_a, b.ut_mn, b.ut_mn, q);
+            }
+            g.flush();
+            if (g.st != MUON_OK) return g.st;
+            launches += g.launches;
         }
-        g.flush();
-        if (g.st != MUON_OK) return g.st;
-        launches += g.launches;
-    }
-    if (se) MUON_TRY(cudaEventRecord(se->e[4], sc));
-    if (split) {
-        MUON_TRY(cudaEventRecord(p->join_ev, p->s2));
-        MUON_TRY(cudaStreamWaitEvent(s, p->join_ev, 0));
+        if (ev) MUON_TRY(cudaEventRecord(ev[4], sc));
+        if (split) {
+            MUON_TRY(cudaEventRecord(p->join_ev, p->s2));
+            MUON_TRY(cudaStreamWaitEvent(s, p->join_ev, 0));
+        }
     }
     p->last_launches = launches;
     return MUON_OK;
@@ -1012,6 +1119,8 @@ muon_status muon_debug_copy_workspace(muon_plan p, int32_t i, int32_t which, voi
     if (!p || !dst || !ld || i < 0 || i >= (int)p->shapes.size() || which < 0 || which > 8)
         return MUON_ERR_INVALID_ARG;
     const Bucket& b = p->buckets[p->mat_bucket[i]];
+    // the fused kernel keeps its r x r operands on chip: only X0 and alpha exist
+    if (b.fused && which >= 1 && which <= 7) return MUON_ERR_UNSUPPORTED;
     const int item = p->mat_item[i];
     const size_t rr = (size_t)b.r * b.ldr;
     const void* src = nullptr;
@@ -1056,12 +1165,16 @@ muon_status muon_stage_times(muon_plan p, float* ms, double* flops, int32_t n_st
         const auto& se = p->evs[g];
         float t = 0.f;
         if (se.ns) {
-            if (cudaEventSynchronize(se.e[4]) != cudaSuccess || cudaEventSynchronize(se.e[6]) != cudaSuccess)
-                return MUON_ERR_CUDA;
-            const int from[5] = {0, se.split ? 1 : 6, 2, 3, 1}, to[5] = {1, 2, 3, 4, 6}, slot[5] = {0, 1, 2, 3, 5};
-            for (int k = 0; k < 5; ++k) {
-                if (cudaEventElapsedTime(&t, se.e[from[k]], se.e[to[k]]) != cudaSuccess) return MUON_ERR_CUDA;
-                acc[slot[k]] += t;
+            for (size_t c = 0; c < p->chunks.size(); ++c) {   // stages summed over the chunks
+                const cudaEvent_t* e = &se.e[7 * c];
+                if (cudaEventSynchronize(e[4]) != cudaSuccess || cudaEventSynchronize(e[6]) != cudaSuccess)
+                    return MUON_ERR_CUDA;
+                const int from[5] = {0, se.split[c] ? 1 : 6, 2, 3, 1}, to[5] = {1, 2, 3, 4, 6},
+                          slot[5] = {0, 1, 2, 3, 5};
+                for (int k = 0; k < 5; ++k) {
+                    if (cudaEventElapsedTime(&t, e[from[k]], e[to[k]]) != cudaSuccess) return MUON_ERR_CUDA;
+                    acc[slot[k]] += t;
+                }
             }
         } else {
             if (cudaEventSynchronize(se.e[5]) != cudaSuccess) return MUON_ERR_CUDA;

@@ -392,3 +392,43 @@ def test_bounded_wait_expiry_is_reported_and_plan_recovers():
     with pytest.raises(lib.MuonError):
         plan.debug_wait_timeout(0)            # limit outside [1, 1e6] us: refused on the host
     plan.close()
+
+
+def test_workspace_cap_runs_the_step_in_chunks_bitwise():
+    """opts.workspace_bytes: the NS step runs chunk by chunk on one shared region of
+    X0 and r x r buffers; every matrix gets bit for bit the update of the uncapped
+    plan, two steps in a row, and a cap below one matrix's needs is refused."""
+    import torch
+    import matrix_orthogonalising_optimizer_muon_gb300 as lib
+    shapes = [(520, 2100), (2100, 520), (384, 384), (130, 300), (300, 130), (128, 1000), (64, 64),
+              (256, 1024)] * 2
+    inputs = host_inputs(shapes, "bf16", base_seed=55)
+    ref = run_step(shapes, "bf16", inputs=inputs)
+    full = ref["plan"].info()
+    ref2 = run_step(shapes, "bf16", inputs=[(w, g, m) for w, (_, g, _), m in
+                                            zip(ref["W"], inputs, ref["M"])], plan=ref["plan"])
+    chunked = 0
+    for frac in (0.7, 0.5, 0.35):
+        cap = int(full["workspace_bytes"] * frac)
+        try:
+            res = run_step(shapes, "bf16", inputs=inputs, workspace_bytes=cap)
+        except lib.MuonError as e:
+            assert e.code == lib.MUON_ERR_OOM
+            continue
+        info = res["plan"].info()
+        assert info["workspace_bytes"] <= cap
+        chunked += info["n_buckets"] > full["n_buckets"]
+        for i in range(len(shapes)):
+            assert torch.equal(res["W"][i], ref["W"][i]), (frac, i)
+            assert torch.equal(res["M"][i], ref["M"][i]), (frac, i)
+            assert torch.equal(res["O"][i], ref["O"][i]), (frac, i)
+        res2 = run_step(shapes, "bf16", inputs=[(w, g, m) for w, (_, g, _), m in
+                                                zip(res["W"], inputs, res["M"])], plan=res["plan"])
+        for i in range(len(shapes)):
+            assert torch.equal(res2["W"][i], ref2["W"][i]), (frac, i)
+        res["plan"].close()
+    assert chunked >= 1
+    with pytest.raises(lib.MuonError) as ei:
+        lib.MuonPlan(shapes, "bf16", workspace_bytes=1 << 20)
+    assert ei.value.code == lib.MUON_ERR_OOM
+    ref["plan"].close()
