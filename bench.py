@@ -38,6 +38,8 @@ def parse_args():
     ap.add_argument("--workload", default="qwen7b_28l")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workspace-bytes", type=int, default=0,
+                    help="cap on the plan's device workspace (the step then runs in chunks); 0: none")
     return ap.parse_args()
 
 
@@ -267,7 +269,7 @@ def run_ours(args, rank, world, local):
         M.append(workloads.gen_tensor((m, n), workloads.M_STD, workloads.seed_of(wl.index, 0, i, "M"), dev))
         G.append(workloads.gen_tensor((m, n), workloads.G_STD, workloads.seed_of(wl.index, 0, i, "G"), dev,
                                       wl.grad_dtype))
-    plan = lib.MuonPlan(shapes, wl.grad_dtype, timing=True)
+    plan = lib.MuonPlan(shapes, wl.grad_dtype, timing=True, workspace_bytes=args.workspace_bytes)
     torch.cuda.synchronize()
     setup_s = time.time() - t0
     lr, wd, mu = workloads.LR, workloads.WD, workloads.MU
@@ -390,7 +392,8 @@ def report_ours(args, res, rank, world):
                    "ns_steps": 5, "rownorm_k": wl.rownorm_k,
                    "l2": "inputs larger than L2 (%.1f GB of W, G, M per step)" %
                          (sum(m * n for m, n in shapes) * (10 if wl.grad_dtype == "bf16" else 12) / 1e9),
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "workspace_bytes": res["plan"].info()["workspace_bytes"]},
         "stages_ms_per_ns_step": {"momentum_norm": round(per_ns[0], 3), "syrk": round(per_ns[1], 3),
                                   "ns_rxr": round(per_ns[2], 3), "final_apply": round(per_ns[3], 3),
                                   "fused_small": round(per_ns[5], 3)},
