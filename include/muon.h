@@ -77,7 +77,11 @@ typedef struct {
        kernel, then the batched products, on the caller's stream).  Results do
        not depend on this choice. */
     int32_t chain_clusters;
-    int32_t reserved;
+    /* > 0: the plan accepts muon_step_ex calls with up to max_ns_steps Newton-Schulz
+       steps (at most 100) and restart periods below ns_steps.  It reserves a second
+       X buffer per matrix and runs every matrix on the batched path.  0: ns_steps
+       <= 5 in one segment, matrices with min(m, n) <= 128 on the fused kernel. */
+    int32_t max_ns_steps;
     /* > 0: cap on the plan's device workspace in bytes.  The NS step then runs in
        chunks of matrices (momentum, SYRK, recursion, final product + update per
        chunk) whose X0 and r x r buffers share one region; results are the same.
@@ -121,6 +125,25 @@ void muon_plan_destroy(muon_plan p);
 muon_status muon_step(muon_plan p, float* const* params, const void* const* grads,
                       float* const* momentum, float lr, float wd, float mu,
                       int32_t ns_steps, muon_mode mode, void* stream);
+
+/*
+ * muon_step_ex - muon_step in NS mode with the Newton-Schulz coefficients and
+ * the evaluation schedule as arguments.
+ *   coeffs: (a, b, c) of the step X <- aX + b(XX^T)X + c(XX^T)^2 X (blog eq. (2));
+ *     NULL: the pages' (3.4445, -4.7750, 2.0315).  Cubic NS is (1.5, -0.5, 0).
+ *   restart: the Gram recursion (DMuon, "Gram Newton-Schulz") runs in segments of
+ *     at most `restart` steps (1..5; 0: 5).  After every segment but the last the
+ *     iterate X <- Q X is formed explicitly (bf16) and the next segment's Gram
+ *     matrix is computed from it: the same iteration in exact arithmetic, with the
+ *     fp16 recursion restarted before rounding errors in near-null directions of G
+ *     can grow.  restart = 1 is the direct form of eq. (2).
+ *   ns_steps: 0 .. 5, or up to opts.max_ns_steps on plans created with it.
+ * Runs with more than one segment need a plan created with opts.max_ns_steps > 0
+ * (MUON_ERR_UNSUPPORTED otherwise).  Other arguments and errors as muon_step.
+ */
+muon_status muon_step_ex(muon_plan p, float* const* params, const void* const* grads, float* const* momentum,
+                         float lr, float wd, float mu, int32_t ns_steps, const float* coeffs, int32_t restart,
+                         void* stream);
 
 /*
  * muon_rownorm_step - one RowNorm step (DiT paper sec. 3, "periodic RowNorm Muon"):

@@ -63,6 +63,8 @@ EXPORTED = {
     "muon_debug_wait_timeout": (ctypes.c_int, [_P, ctypes.c_int32, _P]),
     "muon_step": (ctypes.c_int, [_P, _PP, _PP, _PP, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                  ctypes.c_int32, ctypes.c_int, _P]),
+    "muon_step_ex": (ctypes.c_int, [_P, _PP, _PP, _PP, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                    ctypes.c_int32, ctypes.POINTER(ctypes.c_float), ctypes.c_int32, _P]),
     "muon_rownorm_step": (ctypes.c_int, [_P, _PP, _PP, _PP, ctypes.c_float, ctypes.c_float,
                                          ctypes.c_float, ctypes.c_float, _P]),
     "muon_sync": (ctypes.c_int, [_P, _P]),
@@ -140,13 +142,14 @@ class MuonPlan:
 
     def __init__(self, shapes, grad_dtype: str = "bf16", keep_update: bool = False,
                  timing: bool = False, single_sm_gemm: bool = False, generic_small: bool = False,
-                 chain_clusters: int = 0, workspace_bytes: int = 0):
+                 chain_clusters: int = 0, workspace_bytes: int = 0, max_ns_steps: int = 0):
         self.lib = load()
         self.shapes = [(int(m), int(n)) for m, n in shapes]
         self.grad_dtype = grad_dtype
         arr = (MuonShape * len(self.shapes))(*[MuonShape(m, n) for m, n in self.shapes])
         opts = MuonPlanOpts(1 if keep_update else 0, 1 if timing else 0, 1 if single_sm_gemm else 0,
-                            1 if generic_small else 0, int(chain_clusters), 0, int(workspace_bytes))
+                            1 if generic_small else 0, int(chain_clusters), int(max_ns_steps),
+                            int(workspace_bytes))
         h = ctypes.c_void_p()
         gd = {"bf16": MUON_BF16, "f32": MUON_F32}[grad_dtype]
         _check(self.lib.muon_plan_create(arr, len(self.shapes), gd, ctypes.byref(opts),
@@ -189,12 +192,25 @@ class MuonPlan:
                 _ptr_array([t.data_ptr() for t in momentum]))
 
     def step(self, params, grads, momentum, lr: float, wd: float, mu: float = DEFAULT_MU,
-             ns_steps: int = DEFAULT_NS_STEPS, mode: str = "ns", stream=None):
-        """One Muon step (``muon_step``)."""
+             ns_steps: int = DEFAULT_NS_STEPS, mode: str = "ns", stream=None, coeffs=None, restart: int = 0):
+        """One Muon step (``muon_step``; ``muon_step_ex`` when NS coefficients (a, b, c)
+        or a restart period are given)."""
         w, g, m = self._pointers(params, grads, momentum)
-        md = {"ns": MUON_MODE_NS, "rownorm": MUON_MODE_ROWNORM}[mode]
-        _check(self.lib.muon_step(self.handle, w, g, m, lr, wd, mu, ns_steps, md,
-                                  _stream_handle(stream)), "muon_step")
+        self._step(w, g, m, lr, wd, mu, ns_steps, mode, 1e-8, stream, coeffs, restart)
+
+    def _step(self, w, g, m, lr, wd, mu, ns_steps, mode, eps, stream, coeffs, restart):
+        if mode == "rownorm":
+            _check(self.lib.muon_rownorm_step(self.handle, w, g, m, lr, wd, mu, eps,
+                                              _stream_handle(stream)), "muon_rownorm_step")
+        elif mode != "ns":
+            raise ValueError("mode must be 'ns' or 'rownorm'")
+        elif coeffs is None and not restart:
+            _check(self.lib.muon_step(self.handle, w, g, m, lr, wd, mu, ns_steps, MUON_MODE_NS,
+                                      _stream_handle(stream)), "muon_step")
+        else:
+            abc = None if coeffs is None else (ctypes.c_float * 3)(*[float(x) for x in coeffs])
+            _check(self.lib.muon_step_ex(self.handle, w, g, m, lr, wd, mu, ns_steps, abc, int(restart),
+                                         _stream_handle(stream)), "muon_step_ex")
 
     def rownorm_step(self, params, grads, momentum, lr: float, wd: float, mu: float = DEFAULT_MU,
                      eps: float = 1e-8, stream=None):
@@ -210,15 +226,10 @@ class MuonPlan:
         self._bound_refs = (list(params), list(grads), list(momentum))
 
     def step_bound(self, lr: float, wd: float, mu: float = DEFAULT_MU, ns_steps: int = DEFAULT_NS_STEPS,
-                   mode: str = "ns", eps: float = 1e-8, stream=None):
-        """``muon_step`` / ``muon_rownorm_step`` on the tensors given to ``bind``."""
+                   mode: str = "ns", eps: float = 1e-8, stream=None, coeffs=None, restart: int = 0):
+        """``muon_step`` / ``muon_step_ex`` / ``muon_rownorm_step`` on the tensors given to ``bind``."""
         w, g, m = self._bound
-        if mode == "ns":
-            _check(self.lib.muon_step(self.handle, w, g, m, lr, wd, mu, ns_steps, MUON_MODE_NS,
-                                      _stream_handle(stream)), "muon_step")
-        else:
-            _check(self.lib.muon_rownorm_step(self.handle, w, g, m, lr, wd, mu, eps,
-                                              _stream_handle(stream)), "muon_rownorm_step")
+        self._step(w, g, m, lr, wd, mu, ns_steps, mode, eps, stream, coeffs, restart)
 
     def sync(self, stream=None):
         _check(self.lib.muon_sync(self.handle, _stream_handle(stream)), "muon_sync")

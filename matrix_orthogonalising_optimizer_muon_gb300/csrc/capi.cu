@@ -33,7 +33,8 @@ constexpr float kNsC = 2.0315f;
 // negative, and each step multiplies such an eigenvalue by about p(0)^2 = a^2 ~ 11.9,
 // so on rank-deficient or large square inputs it grows to O(1) and diverges after
 // about six steps.  Five steps (the pages' choice) keep it below 1e-2.
-constexpr int kMaxNsSteps = 5;
+constexpr int kMaxNsSteps = 5;            // one segment of the fp16 Gram recursion
+constexpr int kMaxNsStepsRestart = 100;    // with restarts (opts.max_ns_steps)
 constexpr int kMaxDim = 1 << 20;        // per-dimension limit of this build
 constexpr int kMaxR = 32768;            // r x r workspace limit of this build
 
@@ -109,6 +110,8 @@ struct Bucket {
     int r = 0, c = 0, batch = 0;
     bool fused = false;     // r <= 128: whole step in the fused one-matrix-per-CTA kernel
     int chunk = 0;          // workspace chunk (see muon_plan_opts.workspace_bytes)
+    long long ut1_off = -1; // second X buffer (restarted NS segments), element offset like ut_off
+    CUtensorMap ut1_a, ut1_b, ut1_mn;
     int ldr = 0;   // leading dim of r x r buffers (multiple of 8)
     int ldu = 0;   // leading dim of X0 rows (multiple of 8)
     std::vector<int> mats;
@@ -145,6 +148,7 @@ struct muon_plan_s {
     // and fork/join events (created when a chunk overlaps the two)
     cudaStream_t s2 = nullptr;
     cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
+    float* ones = nullptr;   // per matrix 1.0 (alpha of the iterates after a restart)
     muon_dtype gdt = MUON_F32;
     muon_plan_opts opts{};
     std::vector<muon_shape> shapes;
@@ -495,11 +499,16 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
     // ---- workspace: a fixed part (per-matrix tables, partial sums, pointer tables,
     // launch lists, debug copies of O) and a region for the X0 and r x r buffers of
     // one chunk of matrices, shared by all chunks (they run one after the other)
-    const bool fused_ok = !p->opts.generic_small;
+    if (p->opts.max_ns_steps < 0 || p->opts.max_ns_steps > kMaxNsStepsRestart) {
+        delete p;
+        return MUON_ERR_INVALID_ARG;
+    }
+    const bool restarts = p->opts.max_ns_steps > 0;   // second X buffer, batched path for all
+    const bool fused_ok = !p->opts.generic_small && !restarts;
     auto is_fused = [&](int r) { return fused_ok && r <= kSmallMaxR; };
     auto mat_region_bytes = [&](int r, int c) {   // X0 slice + the seven r x r buffers
         const double ldu = (double)round_up(c, 8), ldr = (double)round_up(r, 8);
-        return 2.0 * r * ldu + (is_fused(r) ? 0.0 : 7 * 2.0 * r * ldr);
+        return (restarts ? 4.0 : 2.0) * r * ldu + (is_fused(r) ? 0.0 : 7 * 2.0 * r * ldr);
     };
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -535,6 +544,7 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
     const size_t o_tr = take((size_t)n);
     const size_t o_ptrs = take(sizeof(void*) * 3 * n);
     const size_t o_items = take(sizeof(int) * n);   // item -> plan matrix, per bucket slice
+    const size_t o_ones = take(sizeof(float) * n);
     const size_t o_odbg = p->opts.keep_update ? take([&] {
         size_t t = 0;
         for (int i = 0; i < n; ++i) t += (size_t)round_up(p->mats[i].m * p->mats[i].n * 4, 256);
@@ -595,7 +605,8 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
     }
     // region offsets: each chunk's buckets laid out from the start of the region
     size_t region_bytes = 0;
-    std::vector<size_t> o_ut(p->buckets.size()), o_rr(p->buckets.size()), o_qb(p->buckets.size());
+    std::vector<size_t> o_ut(p->buckets.size()), o_ut1(p->buckets.size()), o_rr(p->buckets.size()),
+        o_qb(p->buckets.size());
     {
         int slots = 0;
         for (auto& ch : p->chunks) {
@@ -611,6 +622,7 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
                 b.slot_base = slots;
                 slots += b.batch;
                 o_ut[k] = rtake((size_t)b.batch * b.r * b.ldu * 2);
+                if (restarts) o_ut1[k] = rtake((size_t)b.batch * b.r * b.ldu * 2);
                 if (!b.fused) {
                     const size_t rr = (size_t)b.batch * b.r * b.ldr * 2;
                     o_rr[k] = rtake(rr);   // G0 (fp16, scaled)
@@ -645,6 +657,7 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
     p->status = reinterpret_cast<int*>(base + o_status);
     p->d_transposed = reinterpret_cast<unsigned char*>(base + o_tr);
     p->d_ptrs = reinterpret_cast<void**>(base + o_ptrs);
+    p->ones = reinterpret_cast<float*>(base + o_ones);
 
     std::vector<unsigned char> tr(n);
     for (int i = 0; i < n; ++i) tr[i] = (unsigned char)p->mats[i].transposed;
@@ -652,6 +665,10 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
     ok = ok && cudaMemcpy(p->d_transposed, tr.data(), n, cudaMemcpyHostToDevice) == cudaSuccess;
     ok = ok && cudaMemset(p->status, 0, sizeof(int)) == cudaSuccess;
     ok = ok && cudaMemset(p->d_ptrs, 0, sizeof(void*) * 3 * n) == cudaSuccess;
+    {
+        const std::vector<float> one(n, 1.f);
+        ok = ok && cudaMemcpy(p->ones, one.data(), sizeof(float) * n, cudaMemcpyHostToDevice) == cudaSuccess;
+    }
 
     // launch lists (int lists then long long prefixes, carved from their slices)
     int* list_cursor = reinterpret_cast<int*>(base + o_lists);
@@ -713,6 +730,13 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
         ok = ok && make_map(&b.ut_a, ut, true, b.c, b.r, b.batch, b.ldu, 64, kBM);
         ok = ok && make_map(&b.ut_b, ut, true, b.c, b.r, b.batch, b.ldu, 64, kBN);
         ok = ok && make_map(&b.ut_mn, ut, true, b.c, b.r, b.batch, b.ldu, 64, 64);
+        if (restarts) {
+            b.ut1_off = (long long)(o_ut1[k] / 2);
+            __nv_bfloat16* ut1 = p->ut + b.ut1_off;
+            ok = ok && make_map(&b.ut1_a, ut1, true, b.c, b.r, b.batch, b.ldu, 64, kBM);
+            ok = ok && make_map(&b.ut1_b, ut1, true, b.c, b.r, b.batch, b.ldu, 64, kBN);
+            ok = ok && make_map(&b.ut1_mn, ut1, true, b.c, b.r, b.batch, b.ldu, 64, 64);
+        }
         if (b.fused) continue;   // the fused kernel keeps its r x r operands on chip
         const size_t rr = (size_t)b.batch * b.r * b.ldr;
         const size_t step = (size_t)round_up((long long)rr * 2, 256);
@@ -833,9 +857,24 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
     if (!p) return MUON_ERR_INVALID_ARG;
     if (mode == MUON_MODE_ROWNORM) return muon_rownorm_step(p, params, grads, momentum, lr, wd, mu, 1e-8f, stream);
     if (mode != MUON_MODE_NS) return MUON_ERR_INVALID_ARG;
+    return muon_step_ex(p, params, grads, momentum, lr, wd, mu, ns_steps, nullptr, 0, stream);
+}
+
+muon_status muon_step_ex(muon_plan p, float* const* params, const void* const* grads, float* const* momentum,
+                         float lr, float wd, float mu, int32_t ns_steps, const float* coeffs, int32_t restart,
+                         void* stream) {
+    if (!p) return MUON_ERR_INVALID_ARG;
+    const int max_steps = p->opts.max_ns_steps > 0 ? p->opts.max_ns_steps : kMaxNsSteps;
     if (!finite_nonneg(lr) || !finite_nonneg(wd) || !std::isfinite(mu) || mu < 0.f || mu >= 1.f ||
-        ns_steps < 0 || ns_steps > kMaxNsSteps)
+        ns_steps < 0 || ns_steps > max_steps || restart < 0 || restart > kMaxNsSteps)
         return MUON_ERR_INVALID_ARG;
+    if (coeffs && !(std::isfinite(coeffs[0]) && std::isfinite(coeffs[1]) && std::isfinite(coeffs[2])))
+        return MUON_ERR_INVALID_ARG;
+    const float ca = coeffs ? coeffs[0] : kNsA, cb = coeffs ? coeffs[1] : kNsB, cc = coeffs ? coeffs[2] : kNsC;
+    // segments of at most `period` Gram steps (one segment unless restarted)
+    const int period = restart > 0 ? restart : kMaxNsSteps;
+    const int nseg = ns_steps == 0 ? 1 : (ns_steps + period - 1) / period;
+    if (nseg > 1 && p->opts.max_ns_steps <= 0) return MUON_ERR_UNSUPPORTED;
     muon_status st = check_pointers(p, params, grads, momentum);
     if (st != MUON_OK) return st;
     if ((st = check_device(p)) != MUON_OK) return st;
@@ -852,11 +891,13 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
     for (auto& b : p->buckets) {
         if (b.fused) continue;
         const double r = b.r, c = b.c;
-        fl_syrk += b.batch * r * r * c;
-        fl_final += b.batch * 2.0 * r * r * c;
-        const int J = ns_steps;
-        const int nrr = J == 0 ? 0 : (J == 1 ? 1 : 4 * J - 3);
-        fl_rr += b.batch * (double)nrr * r * r * r;
+        for (int sg = 0; sg < nseg; ++sg) {   // per segment: SYRK, 4Js-3 r x r products, r x c product
+            const int Js = sg == nseg - 1 ? ns_steps - sg * period : period;
+            fl_syrk += b.batch * r * r * c;
+            fl_final += b.batch * 2.0 * r * r * c;
+            const int nrr = Js == 0 ? 0 : (Js == 1 ? 1 : 4 * Js - 3);
+            fl_rr += b.batch * (double)nrr * r * r * r;
+        }
     }
     if (se) {
         p->flops[0] += fl_syrk;
@@ -926,9 +967,9 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
                 q.wd = wd;
                 q.scale = 0.2f * std::sqrt((float)b.c);
                 q.out_scale = b.gscale;
-                q.coef_a = kNsA;
-                q.coef_b = kNsB / b.gscale;
-                q.coef_c = kNsC / (b.gscale * b.gscale);
+                q.coef_a = ca;
+                q.coef_b = cb / b.gscale;
+                q.coef_c = cc / (b.gscale * b.gscale);
                 q.ns_steps = ns_steps;
                 Ls.mapA[Ls.nprob] = b.ut_a;
                 Ls.mapB[Ls.nprob] = b.ut_mn;
@@ -941,139 +982,156 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
         if (ev) MUON_TRY(cudaEventRecord(ev[6], s));
 
 
-        // ---- G0' = s alpha^2 X0 X0^T (lower triangle, mirrored), all buckets in one launch
-        {
-            Grouper g(p, sc, true, gc_clusters, g_grid1);
-            for (int bk : ch.buckets) {
-                Bucket& b = p->buckets[bk];
-                if (b.fused) continue;
-                GemmProblem q = problem(b.r, b.r, b.c, b.batch, true, kEpiSyrk);
-                q.C = b.G[0];
+        // ---- batched matrices: NS in segments of at most `period` Gram steps; between
+        // segments the iterate goes to the other X buffer (xc: 0 X0, 1 the second)
+        for (int sg = 0, xc = 0; sg < nseg; ++sg, xc ^= 1) {
+            const bool first = sg == 0, last = sg == nseg - 1;
+            const int Js = last ? ns_steps - sg * period : period;
+            // ---- G0' = s alpha^2 X0 X0^T (lower triangle, mirrored), all buckets in one launch
+            {
+                Grouper g(p, sc, true, gc_clusters, g_grid1);
+                for (int bk : ch.buckets) {
+                    Bucket& b = p->buckets[bk];
+                    if (b.fused) continue;
+                    GemmProblem q = problem(b.r, b.r, b.c, b.batch, true, kEpiSyrk);
+                    q.C = b.G[0];
+                    q.strideC = (long long)b.r * b.ldr;
+                    q.ldc = b.ldr;
+                    q.alpha = (first ? p->alpha : p->ones) + b.slot_base;
+                    q.out_scale = b.gscale;
+                    q.tma_out = kTmaOutC;
+                    if (xc == 0)
+                        g.add(b.ut_a, b.ut_b, b.ut_a, q, &b.og[0]);
+                    else
+                        g.add(b.ut1_a, b.ut1_b, b.ut1_a, q, &b.og[0]);
+                }
+                g.flush();
+                if (g.st != MUON_OK) return g.st;
+                launches += g.launches;
+            }
+            if (ev && first) MUON_TRY(cudaEventRecord(ev[2], sc));
+
+
+            // ---- Newton-Schulz in the Gram space (fp16 operands, G carried as s G)
+            const int J = Js;
+            int gc = 0;   // current G buffer
+            int qc = 0;   // current Q buffer
+            auto rr_problem = [](const Bucket& b, int epi) {
+                GemmProblem q = problem(b.r, b.r, b.r, b.batch, true, epi);
                 q.strideC = (long long)b.r * b.ldr;
                 q.ldc = b.ldr;
-                q.alpha = p->alpha + b.slot_base;
-                q.out_scale = b.gscale;
-                q.tma_out = kTmaOutC;
-                g.add(b.ut_a, b.ut_b, b.ut_a, q, &b.og[0]);
-            }
-            g.flush();
-            if (g.st != MUON_OK) return g.st;
-            launches += g.launches;
-        }
-        if (ev) MUON_TRY(cudaEventRecord(ev[2], sc));
-
-
-        // ---- Newton-Schulz in the Gram space (fp16 operands, G carried as s G)
-        const int J = ns_steps;
-        int gc = 0;   // current G buffer
-        int qc = 0;   // current Q buffer
-        auto rr_problem = [](const Bucket& b, int epi) {
-            GemmProblem q = problem(b.r, b.r, b.r, b.batch, true, epi);
-            q.strideC = (long long)b.r * b.ldr;
-            q.ldc = b.ldr;
-            return q;
-        };
-        for (int k = 1; k <= J; ++k) {
-            {   // P = aI + (b/s) G' + (c/s^2) G'^2 (at k = 1 this is also Q_1)
-                Grouper g(p, sc, false, gc_clusters, g_grid1);
-                for (int bk : ch.buckets) {
-                Bucket& b = p->buckets[bk];
-                if (b.fused) continue;
-                    GemmProblem q = rr_problem(b, kEpiPoly);
-                    q.C = b.P;
-                    if (k == 1 && J > 1) q.C2 = b.Q[0];
-                    if (k == 1 && J == 1) q.Cb = b.Qb;
-                    q.Gin = b.G[gc];
-                    q.coef_a = kNsA;
-                    q.coef_b = kNsB / b.gscale;
-                    q.coef_c = kNsC / (b.gscale * b.gscale);
-                    // fp16 P (and the fp16 copy Q_1): TMA stores; P with a bf16 Q_1 (J = 1): per thread
-                    q.tma_out = q.Cb ? 0 : (kTmaOutC | (q.C2 ? kTmaOutC2 : 0));
-                    g.add(b.ga[gc], b.gb[gc], b.ga[gc], q, &b.op, q.C2 ? &b.oq[0] : nullptr);
+                return q;
+            };
+            for (int k = 1; k <= J; ++k) {
+                {   // P = aI + (b/s) G' + (c/s^2) G'^2 (at k = 1 this is also Q_1)
+                    Grouper g(p, sc, false, gc_clusters, g_grid1);
+                    for (int bk : ch.buckets) {
+                    Bucket& b = p->buckets[bk];
+                    if (b.fused) continue;
+                        GemmProblem q = rr_problem(b, kEpiPoly);
+                        q.C = b.P;
+                        if (k == 1 && J > 1) q.C2 = b.Q[0];
+                        if (k == 1 && J == 1) q.Cb = b.Qb;
+                        q.Gin = b.G[gc];
+                        q.coef_a = ca;
+                        q.coef_b = cb / b.gscale;
+                        q.coef_c = cc / (b.gscale * b.gscale);
+                        // fp16 P (and the fp16 copy Q_1): TMA stores; P with a bf16 Q_1 (J = 1): per thread
+                        q.tma_out = q.Cb ? 0 : (kTmaOutC | (q.C2 ? kTmaOutC2 : 0));
+                        g.add(b.ga[gc], b.gb[gc], b.ga[gc], q, &b.op, q.C2 ? &b.oq[0] : nullptr);
+                    }
+                    g.flush();
+                    if (g.st != MUON_OK) return g.st;
+                    launches += g.launches;
                 }
-                g.flush();
-                if (g.st != MUON_OK) return g.st;
-                launches += g.launches;
-            }
-            {   // Q' = P Q (k >= 2) and T = P P (k < J), independent: one launch
-                Grouper g(p, sc, false, gc_clusters, g_grid1);
-                for (int bk : ch.buckets) {
-                Bucket& b = p->buckets[bk];
-                if (b.fused) continue;
-                    if (k >= 2) {
-                        GemmProblem q = rr_problem(b, kEpiPlain);
+                {   // Q' = P Q (k >= 2) and T = P P (k < J), independent: one launch
+                    Grouper g(p, sc, false, gc_clusters, g_grid1);
+                    for (int bk : ch.buckets) {
+                    Bucket& b = p->buckets[bk];
+                    if (b.fused) continue;
+                        if (k >= 2) {
+                            GemmProblem q = rr_problem(b, kEpiPlain);
+                            if (k < J) {
+                                q.C = b.Q[qc ^ 1];
+                                q.tma_out = kTmaOutC;
+                                g.add(b.pa, b.qb[qc], b.qa[qc], q, &b.oq[qc ^ 1]);
+                            } else {
+                                q.Cb = b.Qb;
+                                q.tma_out = kTmaOutC | kTmaOutBf16;
+                                g.add(b.pa, b.qb[qc], b.qa[qc], q, &b.oqb);
+                            }
+                        }
                         if (k < J) {
-                            q.C = b.Q[qc ^ 1];
+                            GemmProblem q = rr_problem(b, kEpiPlain);
+                            q.C = b.T;
                             q.tma_out = kTmaOutC;
-                            g.add(b.pa, b.qb[qc], b.qa[qc], q, &b.oq[qc ^ 1]);
-                        } else {
-                            q.Cb = b.Qb;
-                            q.tma_out = kTmaOutC | kTmaOutBf16;
-                            g.add(b.pa, b.qb[qc], b.qa[qc], q, &b.oqb);
+                            g.add(b.pa, b.pb, b.pa, q, &b.ot);
                         }
                     }
-                    if (k < J) {
+                    g.flush();
+                    if (g.st != MUON_OK) return g.st;
+                    launches += g.launches;
+                    if (k >= 2) qc ^= 1;
+                }
+                if (k < J) {   // G'' = G' T
+                    Grouper g(p, sc, false, gc_clusters, g_grid1);
+                    for (int bk : ch.buckets) {
+                    Bucket& b = p->buckets[bk];
+                    if (b.fused) continue;
                         GemmProblem q = rr_problem(b, kEpiPlain);
-                        q.C = b.T;
+                        q.C = b.G[gc ^ 1];
                         q.tma_out = kTmaOutC;
-                        g.add(b.pa, b.pb, b.pa, q, &b.ot);
+                        g.add(b.ga[gc], b.tb, b.ta, q, &b.og[gc ^ 1]);
                     }
+                    g.flush();
+                    if (g.st != MUON_OK) return g.st;
+                    launches += g.launches;
+                    gc ^= 1;
                 }
-                g.flush();
-                if (g.st != MUON_OK) return g.st;
-                launches += g.launches;
-                if (k >= 2) qc ^= 1;
             }
-            if (k < J) {   // G'' = G' T
-                Grouper g(p, sc, false, gc_clusters, g_grid1);
+            if (J == 0) {
                 for (int bk : ch.buckets) {
-                Bucket& b = p->buckets[bk];
-                if (b.fused) continue;
-                    GemmProblem q = rr_problem(b, kEpiPlain);
-                    q.C = b.G[gc ^ 1];
-                    q.tma_out = kTmaOutC;
-                    g.add(b.ga[gc], b.tb, b.ta, q, &b.og[gc ^ 1]);
+                    Bucket& b = p->buckets[bk];
+                    if (b.fused) continue;
+                    MUON_TRY(launch_identity_bf16(b.Qb, b.r, b.ldr, b.batch, sc));
+                    ++launches;
+                }
+            }
+            if (ev && last) MUON_TRY(cudaEventRecord(ev[3], sc));
+
+            // ---- last segment: O = alpha Q X, fused W <- W - lr (s O + wd W) in the stored
+            // layout; earlier segments: X' = alpha Q X (bf16) into the other X buffer
+            {
+                Grouper g(p, sc, true, gc_clusters, g_grid1);
+                float* const* W = reinterpret_cast<float* const*>(p->d_ptrs + 2 * n);
+                for (int bk : ch.buckets) {
+                    Bucket& b = p->buckets[bk];
+                    if (b.fused) continue;
+                    GemmProblem q = problem(b.r, b.c, b.r, b.batch, false, last ? kEpiApply : kEpiXout);
+                    q.b_mn = 1;
+                    q.alpha = (first ? p->alpha : p->ones) + b.slot_base;
+                    if (last) {
+                        q.item_mat = b.d_item_mat;
+                        q.W = W;
+                        q.transposed = p->d_transposed;
+                        q.Odbg = b.Odbg;
+                        q.lr = lr;
+                        q.wd = wd;
+                        q.scale = 0.2f * std::sqrt((float)b.c);
+                    } else {
+                        q.Cb = p->ut + (xc == 0 ? b.ut1_off : b.ut_off);
+                        q.ldc = b.ldu;
+                        q.strideC = (long long)b.r * b.ldu;
+                    }
+                    const CUtensorMap& xm = xc == 0 ? b.ut_mn : b.ut1_mn;
+                    g.add(b.qb_a, xm, xm, q);
                 }
                 g.flush();
                 if (g.st != MUON_OK) return g.st;
                 launches += g.launches;
-                gc ^= 1;
             }
+            if (ev && last) MUON_TRY(cudaEventRecord(ev[4], sc));
         }
-        if (J == 0) {
-            for (int bk : ch.buckets) {
-                Bucket& b = p->buckets[bk];
-                if (b.fused) continue;
-                MUON_TRY(launch_identity_bf16(b.Qb, b.r, b.ldr, b.batch, sc));
-                ++launches;
-            }
-        }
-        if (ev) MUON_TRY(cudaEventRecord(ev[3], sc));
-
-        // ---- O = alpha Q X0, fused W <- W - lr (s O + wd W) in the stored layout
-        {
-            Grouper g(p, sc, true, gc_clusters, g_grid1);
-            float* const* W = reinterpret_cast<float* const*>(p->d_ptrs + 2 * n);
-            for (int bk : ch.buckets) {
-                Bucket& b = p->buckets[bk];
-                if (b.fused) continue;
-                GemmProblem q = problem(b.r, b.c, b.r, b.batch, false, kEpiApply);
-                q.b_mn = 1;
-                q.alpha = p->alpha + b.slot_base;
-                q.item_mat = b.d_item_mat;
-                q.W = W;
-                q.transposed = p->d_transposed;
-                q.Odbg = b.Odbg;
-                q.lr = lr;
-                q.wd = wd;
-                q.scale = 0.2f * std::sqrt((float)b.c);
-                g.add(b.qb_a, b.ut_mn, b.ut_mn, q);
-            }
-            g.flush();
-            if (g.st != MUON_OK) return g.st;
-            launches += g.launches;
-        }
-        if (ev) MUON_TRY(cudaEventRecord(ev[4], sc));
         if (split) {
             MUON_TRY(cudaEventRecord(p->join_ev, p->s2));
             MUON_TRY(cudaStreamWaitEvent(s, p->join_ev, 0));

@@ -249,8 +249,36 @@ __device__ __forceinline__ void epilogue_values(const GemmProblem& P, int item, 
     }
 }
 
+// X' = alpha acc as bf16 rows (ldc, item stride strideC): the iterate handed from one
+// restarted Newton-Schulz segment to the next (not symmetric: rows only).
+__device__ __forceinline__ void store_xout(const GemmProblem& P, int item, int row, int col0,
+                                           const uint32_t (&raw)[32]) {
+    if (row >= P.M) return;
+    const float al = P.alpha[item];
+    __nv_bfloat16* dst = P.Cb + item * P.strideC + (long long)row * P.ldc + col0;
+    if (col0 + 31 < P.N && (P.ldc & 7) == 0) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t* r = raw + 8 * q;
+            reinterpret_cast<uint4*>(dst)[q] = make_uint4(
+                pack_bf162(al * __uint_as_float(r[0]), al * __uint_as_float(r[1])),
+                pack_bf162(al * __uint_as_float(r[2]), al * __uint_as_float(r[3])),
+                pack_bf162(al * __uint_as_float(r[4]), al * __uint_as_float(r[5])),
+                pack_bf162(al * __uint_as_float(r[6]), al * __uint_as_float(r[7])));
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (col0 + j < P.N) dst[j] = __float2bfloat16_rn(al * __uint_as_float(raw[j]));
+    }
+}
+
 __device__ __forceinline__ void epilogue_chunk(const GemmProblem& P, int item, int row, int col0,
                                                const uint32_t (&raw)[32]) {
+    if (P.epi == kEpiXout) {
+        store_xout(P, item, row, col0, raw);
+        return;
+    }
     float v[32];
     epilogue_values(P, item, row, col0, raw, v);
     store_sym(P, item, row, col0, v);

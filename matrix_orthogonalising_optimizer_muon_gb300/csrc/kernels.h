@@ -31,6 +31,7 @@ enum Epilogue : int {
     kEpiPoly = 1,    // C = a I + b' Gin + c' acc                  (P = aI + bG + cG^2 in scaled G')
     kEpiPlain = 2,   // C = acc                                    (P Q, P P, G' T)
     kEpiApply = 3,   // W -= lr (s_w alpha acc + wd W), stored layout (final O = Q X0)
+    kEpiXout = 4,    // Cb = alpha acc, bf16 r x c (X' = Q X between restarted NS segments)
 };
 
 // One batched product C_item = A_item * B_item^T (A: M x K, B: N x K as loaded

@@ -432,3 +432,84 @@ def test_workspace_cap_runs_the_step_in_chunks_bitwise():
         lib.MuonPlan(shapes, "bf16", workspace_bytes=1 << 20)
     assert ei.value.code == lib.MUON_ERR_OOM
     ref["plan"].close()
+
+
+# ---- NS coefficient and step variants (muon_step_ex)
+VARIANT_SHAPES = [(128, 1000), (100, 700), (300, 130), (520, 2100), (256, 1024)]
+
+
+def check_ns_variant(res, i, steps, coeffs, tol):
+    """M and W-given-O to 1e-5, O against the oracle's direct NS with these steps and coefficients."""
+    w, g, m = (t.double().numpy() for t in res["inputs"][i])
+    _, m_ref, o_ref = R.muon_step(w, g, m, LR, WD, MU, steps, "ns", 1e-8, coeffs)
+    o = res["O"][i].double().numpy()
+    assert rel(res["M"][i].numpy(), m_ref) <= TOL_FP32, i
+    mm, nn = o.shape
+    assert rel(res["W"][i].numpy(), R.apply_update(w, o, LR, WD, R.update_scale(mm, nn))) <= TOL_FP32, i
+    e = rel(o, o_ref)
+    assert e <= tol, (i, res["inputs"][i][0].shape, e)
+    return e
+
+
+@pytest.mark.parametrize("coeffs", [(1.5, -0.5, 0.0), (2.0, -1.5, 0.5)])
+def test_custom_coefficients_match_oracle(coeffs):
+    """Cubic NS and another quintic through muon_step_ex, on the fused r <= 128 kernel
+    and the CTA-pair path of one plan."""
+    res = run_step(VARIANT_SHAPES, "bf16", base_seed=61, coeffs=coeffs)
+    for i in range(len(VARIANT_SHAPES)):
+        check_ns_variant(res, i, 5, coeffs, TOL_O)
+
+
+@pytest.mark.parametrize("steps,restart", [(10, 0), (7, 3), (4, 1)])
+def test_restarted_segments_match_oracle(steps, restart):
+    """ns_steps beyond one segment (10 = 5 + 5, 7 = 3 + 3 + 1) and the direct form
+    (restart 1): the iterate is formed between segments and the next Gram matrix
+    recomputed from it."""
+    res = run_step(VARIANT_SHAPES, "bf16", base_seed=62, ns_steps=steps, restart=restart, max_ns_steps=10)
+    for i in range(len(VARIANT_SHAPES)):
+        check_ns_variant(res, i, steps, R.NS_COEFFS, TOL_O)
+
+
+def test_restart_every_step_on_ill_conditioned_input():
+    """Singular values spread from 1 to 1e-4: the Gram form carries fp16 rounding of
+    G into the small singular directions through Q (measured 0.17 on GB300); the
+    direct form (restart 1) recomputes X X^T from the iterate every step and cuts the
+    error to less than half (measured 0.073).  It stays above the 2e-2 bar: the
+    iterates are bf16 (X0 from the momentum pass, X' between steps), whose rounding
+    the small singular directions cannot carry."""
+    import torch
+    rng = np.random.default_rng(7)
+    r, c = 256, 1024
+    a, _ = np.linalg.qr(rng.standard_normal((r, r)))
+    b, _ = np.linalg.qr(rng.standard_normal((c, r)))
+    u = (a * np.logspace(0, -4, r)) @ b.T * 1e-3
+    g = torch.from_numpy(u / (1 + MU)).float()            # with M = 0: U = (1 + mu) G
+    w = torch.from_numpy(rng.standard_normal((r, c)) * 0.02).float()
+    inputs = [(w, g, torch.zeros(r, c))]
+    errs = {}
+    for restart in (5, 1):
+        res = run_step([(r, c)], "f32", inputs=inputs, restart=restart, max_ns_steps=5)
+        errs[restart] = check_ns_variant(res, 0, 5, R.NS_COEFFS, 1.0)
+    assert errs[1] < 0.6 * errs[5], errs
+
+
+def test_step_ex_argument_checks():
+    import torch
+    import matrix_orthogonalising_optimizer_muon_gb300 as lib
+    shapes = [(64, 256), (300, 700)]
+    W = [torch.zeros(s, device="cuda") for s in shapes]
+    G = [torch.zeros(s, device="cuda") for s in shapes]
+    M = [torch.zeros(s, device="cuda") for s in shapes]
+    plan = lib.MuonPlan(shapes, "f32")
+    cases = [(dict(ns_steps=6), lib.MUON_ERR_INVALID_ARG),              # beyond one segment, no restarts
+             (dict(ns_steps=5, restart=2), lib.MUON_ERR_UNSUPPORTED),   # needs max_ns_steps
+             (dict(ns_steps=5, restart=6), lib.MUON_ERR_INVALID_ARG),
+             (dict(ns_steps=5, coeffs=(float("nan"), 0.0, 0.0)), lib.MUON_ERR_INVALID_ARG)]
+    for kw, code in cases:
+        with pytest.raises(lib.MuonError) as ei:
+            plan.step(W, G, M, LR, WD, MU, kw.pop("ns_steps"), "ns", **kw)
+        assert ei.value.code == code, kw
+    plan.close()
+    with pytest.raises(lib.MuonError) as ei:
+        lib.MuonPlan(shapes, "f32", max_ns_steps=101)
+    assert ei.value.code == lib.MUON_ERR_INVALID_ARG
