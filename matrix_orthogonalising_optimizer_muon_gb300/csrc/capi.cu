@@ -521,7 +521,7 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
     std::vector<int> rnr_list, rnc_list;
     for (int i = 0; i < n; ++i) {
         MatDev& md = p->mats[i];
-        md.nblk = (int)(md.transposed ? ceil_div(md.m, kTile) * ceil_div(md.n, kTile)
+        md.nblk = (int)(md.transposed ? ceil_div(md.m, kTileRows) * ceil_div(md.n, kTile)
                                       : ceil_div(md.m * md.n, kMomElemsPerBlock));
         md.part_off = mom_part;
         mom_part += md.nblk;

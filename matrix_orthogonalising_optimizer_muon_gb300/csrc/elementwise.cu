@@ -144,7 +144,7 @@ template <bool BF16>
 __global__ void __launch_bounds__(kElemThreads) k_momentum_tiles(const ElemArgs a) {
     pdl_trigger();
     pdl_wait();
-    __shared__ float tile[kTile][kTile + 1];   // [stored col][stored row]
+    __shared__ float tile[kTile][kTileRows + 1];   // [stored col][stored row]
     __shared__ float sred[33];
     const long long b = blockIdx.x;
     const int li = find_entry(a.list_blk, a.nlist, b);
@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(kElemThreads) k_momentum_tiles(const ElemArgs 
     const MatDev md = a.mats[mi];
     const long long blk = b - a.list_blk[li];
     const long long tiles_n = (md.n + kTile - 1) / kTile;
-    const long long i0 = (blk / tiles_n) * kTile;
+    const long long i0 = (blk / tiles_n) * kTileRows;
     const long long j0 = (blk % tiles_n) * kTile;
     const void* G = a.G[mi];
     float* M = a.M[mi];
@@ -160,12 +160,12 @@ __global__ void __launch_bounds__(kElemThreads) k_momentum_tiles(const ElemArgs 
     const float mu = a.mu;
     const int t = threadIdx.x;
     float ss = 0.f;
-    const bool full = (i0 + kTile <= md.m) && (j0 + kTile <= md.n) && (md.n % 4 == 0) && g_vec_ok<BF16>(G) &&
+    const bool full = (i0 + kTileRows <= md.m) && (j0 + kTile <= md.n) && (md.n % 4 == 0) && g_vec_ok<BF16>(G) &&
                       aligned16(M);
     const int cq = t & 15, rr = t >> 4;
     if (full) {
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
+        for (int p = 0; p < kTileRows / 16; ++p) {
             const long long i = i0 + rr + 16 * p;
             const long long e = i * md.n + j0 + 4 * cq;
             const float4 g = load_g4<BF16>(G, e);
@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(kElemThreads) k_momentum_tiles(const ElemArgs 
         }
     } else {
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
+        for (int p = 0; p < kTileRows / 16; ++p) {
             const long long i = i0 + rr + 16 * p;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -200,25 +200,22 @@ __global__ void __launch_bounds__(kElemThreads) k_momentum_tiles(const ElemArgs 
         }
     }
     __syncthreads();
-    // X0 row jj = stored column j0 + jj; its elements are stored rows i0 .. i0 + 63
-    const int i8 = (t & 7) * 8;
+    // X0 row jj = stored column j0 + jj; its elements are stored rows i0 .. i0 + kTileRows - 1.
+    // Warp w writes X0 rows 8w .. 8w + 7; lane l takes elements l, l + 32, l + 64, l + 96,
+    // so the shared reads hit 32 banks and each store covers 64 contiguous bytes.
+    {
+        const int lane = t & 31, wid = t >> 5;
+#pragma unroll 2
+        for (int r = 0; r < kTile / (kElemThreads / 32); ++r) {
+            const int jj = wid * (kTile / (kElemThreads / 32)) + r;
+            const long long gj = j0 + jj;
+            if (gj < md.n) {
+                __nv_bfloat16* dst = U + gj * md.ldu + i0;
 #pragma unroll
-    for (int p = 0; p < 2; ++p) {
-        const int jj = (t >> 3) + 32 * p;
-        const long long gj = j0 + jj;
-        if (gj < md.n) {
-            const long long gi = i0 + i8;
-            __nv_bfloat16* dst = U + gj * md.ldu + gi;
-            if (gi + 8 <= md.m) {
-                uint4 pk;
-                pk.x = pack_bf16x2(tile[jj][i8 + 0], tile[jj][i8 + 1]);
-                pk.y = pack_bf16x2(tile[jj][i8 + 2], tile[jj][i8 + 3]);
-                pk.z = pack_bf16x2(tile[jj][i8 + 4], tile[jj][i8 + 5]);
-                pk.w = pack_bf16x2(tile[jj][i8 + 6], tile[jj][i8 + 7]);
-                *reinterpret_cast<uint4*>(dst) = pk;
-            } else {
-                for (int q = 0; q < 8; ++q)
-                    if (gi + q < md.m) dst[q] = __float2bfloat16_rn(tile[jj][i8 + q]);
+                for (int q = 0; q < kTileRows / 32; ++q) {
+                    const int ii = lane + 32 * q;
+                    if (i0 + ii < md.m) dst[ii] = __float2bfloat16_rn(tile[jj][ii]);
+                }
             }
         }
     }

@@ -167,7 +167,12 @@ cudaError_t launch_rownorm_colapply(const ElemArgs& a, long long blocks, cudaStr
 constexpr int kElemThreads = 256;
 constexpr int kMomVecPerThread = 4;                                  // 8-element vectors per thread
 constexpr long long kMomElemsPerBlock = 8LL * kElemThreads * kMomVecPerThread;   // rows kernel
-constexpr int kTile = 64;                                            // transpose tile (64 x 64)
+constexpr int kTile = 64;                                            // transpose tile: 64 stored columns
+#ifndef MUON_TILE_ROWS
+#define MUON_TILE_ROWS 128
+#endif
+constexpr int kTileRows = MUON_TILE_ROWS;                            // ... x kTileRows stored rows
+static_assert(kTileRows % 32 == 0 && kTileRows <= 128, "transpose tile rows");
 constexpr int kColSlab = 64;                                         // RowNorm column-stat rows per block
 constexpr int kColWidth = 4 * kElemThreads;                          // columns per column-stat block
 constexpr long long kApplyElemsPerBlock = 4LL * kElemThreads * 4;    // RowNorm col apply
