@@ -28,7 +28,8 @@ namespace muon {
 // warp streams its 32 x 32 fp32 pieces of W in with cp.async (three pieces in
 // flight), updates them from the accumulator, and writes them back with
 // coalesced 16-byte stores.  The staging uses the r x r operand buffers, which
-// the final product does not read.
+// the final product does not read; with one NS step the last on-chip epilogue
+// still reads and writes them, so the epilogue warps meet before staging W.
 constexpr int kSmallRing = 3;                       // X stream ring (SYRK k-blocks, final chunks)
 constexpr int kSmallThreads = 320;                  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-9 epilogue
 constexpr int kSmallEpiWarps = 8;
@@ -165,7 +166,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
     uint64_t* accf_empty = accf_full + 2;
     uint64_t* drain = accf_empty + 2;
     uint64_t* stage_free = drain + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stage_free + 1);
+    uint64_t* rr_free = stage_free + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rr_free + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -183,6 +185,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
         }
         mbar_init(drain, 1);
         mbar_init(stage_free, kSmallEpiWarps);
+        mbar_init(rr_free, kSmallEpiWarps);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -343,7 +346,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
         const uint32_t tmem_row = tmem_base + (static_cast<uint32_t>(wq * 32) << 16);
         uint8_t* stage = smem + Cfg::STAGE + (warp - 2) * kWBufs * kWPiece;
         const uint32_t stage_u32 = smem_u32(stage);
-        uint32_t sc = 0, fc = 0, mc = 0;
+        uint32_t sc = 0, fc = 0, mc = 0, jc = 0;
         bool ok = true;
         auto step = [&](int kind, int k, int J, const GemmProblem& P, int item) -> bool {
             if (!mbar_wait(mma_done, sc & 1u, abort_flag, L.status, kStatusTimeoutEpilogue)) return false;
@@ -370,6 +373,14 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
                 if (ok && k < J) ok = step(kSmGT, k, J, P, item);
             }
             if (ok && J == 0) ok = step(kSmIdentity, 0, J, P, item);
+            if (ok && J == 1) {
+                // the last on-chip epilogue (the polynomial) reads G' and writes P in the
+                // buffers the W staging reuses: every warp leaves it before any stages W
+                __syncwarp();
+                if (lane == 0) mbar_arrive(rr_free);
+                ok = mbar_wait(rr_free, jc & 1u, abort_flag, L.status, kStatusTimeoutEpilogue);
+                ++jc;
+            }
             if (!ok) break;
             // Final product: this warp's pieces are (chunk ch, half h) at oriented rows
             // [32 wq, 32 wq + 32) and columns 128 ch + c_begin + 32 h; piece i lives in

@@ -175,6 +175,33 @@ def test_fused_small_kernel_batched():
         assert_ns(res, i)
 
 
+@pytest.mark.parametrize("ns_steps", [1, 2])
+def test_fused_small_w_staging_waits_for_last_epilogue(ns_steps):
+    """Many short fused matrices per CTA at one and two NS steps, three steps on one plan;
+    every matrix's W must equal W0 updated with its own O.  With one step the last on-chip
+    epilogue reads G' and writes P in the shared-memory buffers that the W staging of the
+    final phase reuses; the epilogue warps meet on an mbarrier before staging.  Without it
+    W went wrong only when the W pieces came from L2 within a few hundred cycles (a kernel
+    that prefetched W into L2 during the recursion); on plain inputs the window is too short
+    to open, so this is a regression guard, not a reproducer."""
+    import matrix_orthogonalising_optimizer_muon_gb300 as lib
+    shapes = [(128, 256)] * 120 + [(100, 200)] * 100 + [(64, 128)] * 100
+    plan = lib.MuonPlan(shapes, "bf16", keep_update=True)
+    try:
+        for seed in (33, 34, 35):
+            res = run_step(shapes, "bf16", base_seed=seed, ns_steps=ns_steps, plan=plan)
+            for i in range(len(shapes)):
+                o = res["O"][i].double().numpy()
+                m_, n_ = o.shape
+                w0 = res["inputs"][i][0].double().numpy()
+                w_given_o = R.apply_update(w0, o, LR, WD, R.update_scale(m_, n_))
+                assert rel(res["W"][i].numpy(), w_given_o) <= TOL_FP32, (seed, i, shapes[i])
+        for i in [0, 119, 120, 219, 220, 319]:
+            assert_ns(res, i, ns_steps=ns_steps)
+    finally:
+        plan.close()
+
+
 def test_batched_bucket_ns5():
     """Several same-shape matrices batched in one bucket (grouped launch items)."""
     shapes = [(200, 520)] * 5 + [(520, 200)] * 3
