@@ -86,8 +86,16 @@ typedef struct {
        chunks of matrices (momentum, SYRK, recursion, final product + update per
        chunk) whose X0 and r x r buffers share one region; results are the same.
        muon_plan_create returns MUON_ERR_OOM if the cap cannot hold the per-matrix
-       tables plus the buffers of the largest single matrix.  0: no cap (one chunk). */
+       tables plus the buffers of the largest single matrix.  0: no cap (one chunk).
+       Negative: MUON_ERR_INVALID_ARG. */
     int64_t workspace_bytes;
+    /* > 1: split the matrices into about this many chunks (the region each chunk
+       needs is at most 1/chunks of the whole, and at least one matrix's), so that
+       muon_step_host can overlap one chunk's host copies with another chunk's
+       compute.  Results are the same.  0 or 1: chunks only as workspace_bytes
+       requires.  Negative: MUON_ERR_INVALID_ARG. */
+    int32_t chunks;
+    int32_t reserved;   /* must be 0 */
 } muon_plan_opts;
 
 typedef struct muon_plan_s* muon_plan;
@@ -144,6 +152,32 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
 muon_status muon_step_ex(muon_plan p, float* const* params, const void* const* grads, float* const* momentum,
                          float lr, float wd, float mu, int32_t ns_steps, const float* coeffs, int32_t restart,
                          void* stream);
+
+/*
+ * muon_step_host - muon_step for gradients that arrive from host memory and
+ * parameters that go back to it, with the copies overlapped with the compute.
+ *   grads_host   host array of n pointers to the gradients in host memory (grad
+ *                dtype, stored shape).  Pinned memory lets the copies run
+ *                asynchronously; with pageable memory each copy blocks the caller.
+ *   grads        host array of n device pointers the gradients are copied to
+ *                (caller-owned, as in muon_step); the step reads them there.
+ *   params_host  NULL (no copy back), or a host array of n pointers to host
+ *                buffers (fp32, stored shape) that receive the updated parameters.
+ *   params, momentum, lr, wd, mu, ns_steps, mode: as muon_step (RowNorm with eps 1e-8).
+ * NS mode runs chunk by chunk (opts.chunks, opts.workspace_bytes): one copy
+ * stream of the plan copies the gradients in chunk order, each chunk's momentum
+ * kernel waits only for its own chunk's gradients, and a second copy stream
+ * copies each chunk's parameters back as soon as that chunk's final product has
+ * run, while the next chunks compute.  RowNorm mode copies in, computes and
+ * copies back in sequence.  The copies in are ordered after the work already on
+ * `stream` (which may still read the previous gradients), and `stream` waits for
+ * the last copy back: once `stream` is synchronised, params_host holds the
+ * result.  Errors as muon_step; a null grads_host (or null entry of either host
+ * array) is MUON_ERR_INVALID_ARG, checked before anything is enqueued.
+ */
+muon_status muon_step_host(muon_plan p, float* const* params, const void* const* grads, float* const* momentum,
+                           const void* const* grads_host, float* const* params_host, float lr, float wd,
+                           float mu, int32_t ns_steps, muon_mode mode, void* stream);
 
 /*
  * muon_rownorm_step - one RowNorm step (DiT paper sec. 3, "periodic RowNorm Muon"):
@@ -234,6 +268,8 @@ typedef struct {
     int64_t workspace_bytes;
     int32_t launches_last_step;   /* kernels the last step enqueued */
     int32_t sm_count;
+    int32_t n_chunks;             /* chunks the NS step runs in (opts.chunks, opts.workspace_bytes) */
+    int32_t reserved;
 } muon_plan_info_t;
 
 muon_status muon_plan_info(muon_plan p, muon_plan_info_t* info);

@@ -43,14 +43,14 @@ class MuonShape(ctypes.Structure):
 class MuonPlanOpts(ctypes.Structure):
     _fields_ = [("keep_update", ctypes.c_int32), ("timing", ctypes.c_int32),
                 ("single_sm_gemm", ctypes.c_int32), ("generic_small", ctypes.c_int32),
-                ("chain_clusters", ctypes.c_int32), ("reserved", ctypes.c_int32),
-                ("workspace_bytes", ctypes.c_int64)]
+                ("chain_clusters", ctypes.c_int32), ("max_ns_steps", ctypes.c_int32),
+                ("workspace_bytes", ctypes.c_int64), ("chunks", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class MuonPlanInfo(ctypes.Structure):
     _fields_ = [("n_matrices", ctypes.c_int32), ("n_buckets", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64), ("launches_last_step", ctypes.c_int32),
-                ("sm_count", ctypes.c_int32)]
+                ("sm_count", ctypes.c_int32), ("n_chunks", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -65,6 +65,8 @@ EXPORTED = {
                                  ctypes.c_int32, ctypes.c_int, _P]),
     "muon_step_ex": (ctypes.c_int, [_P, _PP, _PP, _PP, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                     ctypes.c_int32, ctypes.POINTER(ctypes.c_float), ctypes.c_int32, _P]),
+    "muon_step_host": (ctypes.c_int, [_P, _PP, _PP, _PP, _PP, _PP, ctypes.c_float, ctypes.c_float,
+                                      ctypes.c_float, ctypes.c_int32, ctypes.c_int, _P]),
     "muon_rownorm_step": (ctypes.c_int, [_P, _PP, _PP, _PP, ctypes.c_float, ctypes.c_float,
                                          ctypes.c_float, ctypes.c_float, _P]),
     "muon_sync": (ctypes.c_int, [_P, _P]),
@@ -142,14 +144,14 @@ class MuonPlan:
 
     def __init__(self, shapes, grad_dtype: str = "bf16", keep_update: bool = False,
                  timing: bool = False, single_sm_gemm: bool = False, generic_small: bool = False,
-                 chain_clusters: int = 0, workspace_bytes: int = 0, max_ns_steps: int = 0):
+                 chain_clusters: int = 0, workspace_bytes: int = 0, max_ns_steps: int = 0, chunks: int = 0):
         self.lib = load()
         self.shapes = [(int(m), int(n)) for m, n in shapes]
         self.grad_dtype = grad_dtype
         arr = (MuonShape * len(self.shapes))(*[MuonShape(m, n) for m, n in self.shapes])
         opts = MuonPlanOpts(1 if keep_update else 0, 1 if timing else 0, 1 if single_sm_gemm else 0,
                             1 if generic_small else 0, int(chain_clusters), int(max_ns_steps),
-                            int(workspace_bytes))
+                            int(workspace_bytes), int(chunks), 0)
         h = ctypes.c_void_p()
         gd = {"bf16": MUON_BF16, "f32": MUON_F32}[grad_dtype]
         _check(self.lib.muon_plan_create(arr, len(self.shapes), gd, ctypes.byref(opts),
@@ -211,6 +213,34 @@ class MuonPlan:
             abc = None if coeffs is None else (ctypes.c_float * 3)(*[float(x) for x in coeffs])
             _check(self.lib.muon_step_ex(self.handle, w, g, m, lr, wd, mu, ns_steps, abc, int(restart),
                                          _stream_handle(stream)), "muon_step_ex")
+
+    def step_host(self, params, grads, momentum, grads_host, params_host, lr: float, wd: float,
+                  mu: float = DEFAULT_MU, ns_steps: int = DEFAULT_NS_STEPS, mode: str = "ns", stream=None):
+        """``muon_step_host``: gradients copied in from the CPU tensors ``grads_host`` (into the
+        CUDA tensors ``grads``), the updated params copied back into the CPU tensors
+        ``params_host`` (or not, if None), overlapped with the compute chunk by chunk.  Pinned
+        CPU tensors keep the copies asynchronous; synchronise the stream before reading
+        ``params_host``."""
+        import torch
+        w, g, m = self._pointers(params, grads, momentum)
+        n = len(self.shapes)
+        gdt = torch.bfloat16 if self.grad_dtype == "bf16" else torch.float32
+        outs = [] if params_host is None else list(params_host)
+        if len(grads_host) != n or (params_host is not None and len(outs) != n):
+            raise ValueError("expected %d host tensors" % n)
+        for i in range(n):
+            pairs = [(grads_host[i], gdt, "host grad")] + ([(outs[i], torch.float32, "host param")] if outs else [])
+            for t, dt, name in pairs:
+                if tuple(t.shape) != self.shapes[i] or t.dtype != dt or t.is_cuda or not t.is_contiguous():
+                    raise ValueError("%s %d: need a contiguous CPU %s tensor of shape %s" % (name, i, dt,
+                                                                                            self.shapes[i]))
+        gh = _ptr_array([t.data_ptr() for t in grads_host])
+        wh = _ptr_array([t.data_ptr() for t in outs]) if outs else None
+        md = {"ns": MUON_MODE_NS, "rownorm": MUON_MODE_ROWNORM}.get(mode)
+        if md is None:
+            raise ValueError("mode must be 'ns' or 'rownorm'")
+        _check(self.lib.muon_step_host(self.handle, w, g, m, gh, wh, lr, wd, mu, ns_steps, md,
+                                       _stream_handle(stream)), "muon_step_host")
 
     def rownorm_step(self, params, grads, momentum, lr: float, wd: float, mu: float = DEFAULT_MU,
                      eps: float = 1e-8, stream=None):

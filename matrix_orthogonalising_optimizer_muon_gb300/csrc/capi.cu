@@ -196,6 +196,16 @@ struct muon_plan_s {
     size_t n_timed = 0;
     double flops[3] = {0, 0, 0};   // summed over the timed steps
     int last_launches = 0;
+
+    // muon_step_host: copy streams (in, out) and events, created on first use.
+    // in_ev[c]: chunk c's gradients are on the device; out_ev[c]: chunk c's
+    // parameters are final; entry_ev: the caller's stream before the step;
+    // end_ev: the last copy back.
+    struct HostCopy {
+        cudaStream_t in = nullptr, out = nullptr;
+        std::vector<cudaEvent_t> in_ev, out_ev;
+        cudaEvent_t entry_ev = nullptr, end_ev = nullptr;
+    } hc;
 };
 
 namespace {
@@ -415,6 +425,14 @@ void free_plan(muon_plan_s* p) {
     if (p->fork_ev) cudaEventDestroy(p->fork_ev);
     if (p->join_ev) cudaEventDestroy(p->join_ev);
     if (p->s2) cudaStreamDestroy(p->s2);
+    if (p->hc.in) cudaStreamDestroy(p->hc.in);
+    if (p->hc.out) cudaStreamDestroy(p->hc.out);
+    for (cudaEvent_t e : p->hc.in_ev)
+        if (e) cudaEventDestroy(e);
+    for (cudaEvent_t e : p->hc.out_ev)
+        if (e) cudaEventDestroy(e);
+    if (p->hc.entry_ev) cudaEventDestroy(p->hc.entry_ev);
+    if (p->hc.end_ev) cudaEventDestroy(p->hc.end_ev);
     for (auto& g : p->evs)
         for (auto& e : g.e)
             if (e) cudaEventDestroy(e);
@@ -453,6 +471,9 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
         if (shapes[i].rows > kMaxDim || shapes[i].cols > kMaxDim) return MUON_ERR_UNSUPPORTED;
         if (std::min(shapes[i].rows, shapes[i].cols) > kMaxR) return MUON_ERR_UNSUPPORTED;
     }
+    if (opts && (opts->max_ns_steps < 0 || opts->max_ns_steps > kMaxNsStepsRestart || opts->chunks < 0 ||
+                 opts->reserved != 0 || opts->workspace_bytes < 0))
+        return MUON_ERR_INVALID_ARG;
     muon_plan_s* p = new (std::nothrow) muon_plan_s();
     if (!p) return MUON_ERR_OOM;
     if (cudaGetDevice(&p->device) != cudaSuccess) {
@@ -499,10 +520,6 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
     // ---- workspace: a fixed part (per-matrix tables, partial sums, pointer tables,
     // launch lists, debug copies of O) and a region for the X0 and r x r buffers of
     // one chunk of matrices, shared by all chunks (they run one after the other)
-    if (p->opts.max_ns_steps < 0 || p->opts.max_ns_steps > kMaxNsStepsRestart) {
-        delete p;
-        return MUON_ERR_INVALID_ARG;
-    }
     const bool restarts = p->opts.max_ns_steps > 0;   // second X buffer, batched path for all
     const bool fused_ok = !p->opts.generic_small && !restarts;
     auto is_fused = [&](int r) { return fused_ok && r <= kSmallMaxR; };
@@ -569,6 +586,16 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
             delete p;
             return MUON_ERR_OOM;   // the cap cannot hold even the largest single matrix
         }
+    }
+    if (p->opts.chunks > 1) {   // about opts.chunks chunks, each at least one matrix
+        double total = 0, largest = 0;
+        for (int i = 0; i < n; ++i) {
+            const double b = mat_region_bytes(p->mats[i].r, p->mats[i].c);
+            total += b;
+            largest = std::max(largest, b + 8 * 256.0);
+        }
+        const double per = total / p->opts.chunks + 8 * 256.0 * (double)group_rc.size();
+        region_cap = std::min(region_cap, std::max(per, largest));
     }
     {
         double used = 0;
@@ -860,9 +887,25 @@ muon_status muon_step(muon_plan p, float* const* params, const void* const* grad
     return muon_step_ex(p, params, grads, momentum, lr, wd, mu, ns_steps, nullptr, 0, stream);
 }
 
+// Host side of muon_step_host inside the NS step: the chunk's gradients arrive on
+// hc.in (in_ev), its parameters go back on hc.out.
+struct HostIO {
+    float* const* params_host;   // may be null
+};
+
+static muon_status ns_step(muon_plan p, float* const* params, const void* const* grads, float* const* momentum,
+                           float lr, float wd, float mu, int32_t ns_steps, const float* coeffs, int32_t restart,
+                           void* stream, const HostIO* io);
+
 muon_status muon_step_ex(muon_plan p, float* const* params, const void* const* grads, float* const* momentum,
                          float lr, float wd, float mu, int32_t ns_steps, const float* coeffs, int32_t restart,
                          void* stream) {
+    return ns_step(p, params, grads, momentum, lr, wd, mu, ns_steps, coeffs, restart, stream, nullptr);
+}
+
+static muon_status ns_step(muon_plan p, float* const* params, const void* const* grads, float* const* momentum,
+                           float lr, float wd, float mu, int32_t ns_steps, const float* coeffs, int32_t restart,
+                           void* stream, const HostIO* io) {
     if (!p) return MUON_ERR_INVALID_ARG;
     const int max_steps = p->opts.max_ns_steps > 0 ? p->opts.max_ns_steps : kMaxNsSteps;
     if (!finite_nonneg(lr) || !finite_nonneg(wd) || !std::isfinite(mu) || mu < 0.f || mu >= 1.f ||
@@ -908,6 +951,7 @@ muon_status muon_step_ex(muon_plan p, float* const* params, const void* const* g
     for (size_t ci = 0; ci < p->chunks.size(); ++ci) {
         const muon_plan_s::Chunk& ch = p->chunks[ci];
         cudaEvent_t* ev = se ? &se->e[7 * ci] : nullptr;
+        if (io) MUON_TRY(cudaStreamWaitEvent(s, p->hc.in_ev[ci], 0));   // this chunk's gradients
         // ---- momentum, Nesterov, sum of squares, bf16 X0 (oriented), for this chunk
         if (ev) MUON_TRY(cudaEventRecord(ev[0], s));
         ElemArgs a = elem_args(p, ch.mom_rows, mu, lr, wd, 0.f);
@@ -1136,8 +1180,107 @@ muon_status muon_step_ex(muon_plan p, float* const* params, const void* const* g
             MUON_TRY(cudaEventRecord(p->join_ev, p->s2));
             MUON_TRY(cudaStreamWaitEvent(s, p->join_ev, 0));
         }
+        if (io && io->params_host) {   // this chunk's parameters are final: copy them back
+            MUON_TRY(cudaEventRecord(p->hc.out_ev[ci], s));
+            MUON_TRY(cudaStreamWaitEvent(p->hc.out, p->hc.out_ev[ci], 0));
+            for (int bk : ch.buckets)
+                for (int i : p->buckets[bk].mats)
+                    MUON_TRY(cudaMemcpyAsync(io->params_host[i], params[i],
+                                             (size_t)(p->mats[i].m * p->mats[i].n) * sizeof(float),
+                                             cudaMemcpyDefault, p->hc.out));
+        }
     }
     p->last_launches = launches;
+    return MUON_OK;
+}
+
+// Copy streams and events of muon_step_host, created on first use.
+static muon_status host_copy_setup(muon_plan_s* p) {
+    auto& h = p->hc;
+    if (h.in) return MUON_OK;
+    const size_t nc = p->chunks.size();
+    bool ok = cudaStreamCreateWithFlags(&h.in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&h.entry_ev, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&h.end_ev, cudaEventDisableTiming) == cudaSuccess;
+    h.in_ev.assign(nc, nullptr);
+    h.out_ev.assign(nc, nullptr);
+    for (size_t c = 0; ok && c < nc; ++c)
+        ok = cudaEventCreateWithFlags(&h.in_ev[c], cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&h.out_ev[c], cudaEventDisableTiming) == cudaSuccess;
+    if (ok) return MUON_OK;
+    g_last_cuda_error = cudaGetLastError();
+    if (h.in) cudaStreamDestroy(h.in);
+    if (h.out) cudaStreamDestroy(h.out);
+    h.in = h.out = nullptr;
+    for (cudaEvent_t& e : h.in_ev)
+        if (e) cudaEventDestroy(e);
+    for (cudaEvent_t& e : h.out_ev)
+        if (e) cudaEventDestroy(e);
+    h.in_ev.clear();
+    h.out_ev.clear();
+    if (h.entry_ev) cudaEventDestroy(h.entry_ev);
+    if (h.end_ev) cudaEventDestroy(h.end_ev);
+    h.entry_ev = h.end_ev = nullptr;
+    return MUON_ERR_CUDA;
+}
+
+muon_status muon_step_host(muon_plan p, float* const* params, const void* const* grads, float* const* momentum,
+                           const void* const* grads_host, float* const* params_host, float lr, float wd,
+                           float mu, int32_t ns_steps, muon_mode mode, void* stream) {
+    if (!p || !grads_host) return MUON_ERR_INVALID_ARG;
+    const int n = (int)p->shapes.size();
+    for (int i = 0; i < n; ++i)
+        if (!grads_host[i] || (params_host && !params_host[i])) return MUON_ERR_INVALID_ARG;
+    // every check of the step itself before anything is enqueued
+    const int max_steps = p->opts.max_ns_steps > 0 ? p->opts.max_ns_steps : kMaxNsSteps;
+    if (!finite_nonneg(lr) || !finite_nonneg(wd) || !std::isfinite(mu) || mu < 0.f || mu >= 1.f)
+        return MUON_ERR_INVALID_ARG;
+    if (mode == MUON_MODE_NS) {
+        if (ns_steps < 0 || ns_steps > max_steps) return MUON_ERR_INVALID_ARG;
+    } else if (mode != MUON_MODE_ROWNORM) {
+        return MUON_ERR_INVALID_ARG;
+    }
+    muon_status st = check_pointers(p, params, grads, momentum);
+    if (st != MUON_OK) return st;
+    if ((st = check_device(p)) != MUON_OK) return st;
+    if ((st = host_copy_setup(p)) != MUON_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t gsz = p->gdt == MUON_BF16 ? 2 : 4;
+    auto& h = p->hc;
+    // gradients in, chunk by chunk, after the caller's earlier work (which may still read grads)
+    MUON_TRY(cudaEventRecord(h.entry_ev, s));
+    MUON_TRY(cudaStreamWaitEvent(h.in, h.entry_ev, 0));
+    const bool ns = mode == MUON_MODE_NS;
+    for (size_t ci = 0; ci < p->chunks.size(); ++ci) {
+        for (int bk : p->chunks[ci].buckets)
+            for (int i : p->buckets[bk].mats)
+                MUON_TRY(cudaMemcpyAsync(const_cast<void*>(grads[i]), grads_host[i],
+                                         (size_t)(p->mats[i].m * p->mats[i].n) * gsz, cudaMemcpyDefault, h.in));
+        if (ns) MUON_TRY(cudaEventRecord(h.in_ev[ci], h.in));
+    }
+    if (ns) {
+        const HostIO io{params_host};
+        st = ns_step(p, params, grads, momentum, lr, wd, mu, ns_steps, nullptr, 0, stream, &io);
+        if (st != MUON_OK) return st;
+    } else {
+        MUON_TRY(cudaEventRecord(h.in_ev[0], h.in));
+        MUON_TRY(cudaStreamWaitEvent(s, h.in_ev[0], 0));
+        st = muon_rownorm_step(p, params, grads, momentum, lr, wd, mu, 1e-8f, stream);
+        if (st != MUON_OK) return st;
+        if (params_host) {
+            MUON_TRY(cudaEventRecord(h.out_ev[0], s));
+            MUON_TRY(cudaStreamWaitEvent(h.out, h.out_ev[0], 0));
+            for (int i = 0; i < n; ++i)
+                MUON_TRY(cudaMemcpyAsync(params_host[i], params[i],
+                                         (size_t)(p->mats[i].m * p->mats[i].n) * sizeof(float), cudaMemcpyDefault,
+                                         h.out));
+        }
+    }
+    if (params_host) {   // the caller's stream covers the copies back
+        MUON_TRY(cudaEventRecord(h.end_ev, h.out));
+        MUON_TRY(cudaStreamWaitEvent(s, h.end_ev, 0));
+    }
     return MUON_OK;
 }
 
@@ -1208,6 +1351,8 @@ muon_status muon_plan_info(muon_plan p, muon_plan_info_t* info) {
     info->n_buckets = (int32_t)p->buckets.size();
     info->workspace_bytes = (int64_t)p->ws_bytes;
     info->launches_last_step = p->last_launches;
+    info->n_chunks = (int32_t)p->chunks.size();
+    info->reserved = 0;
     info->sm_count = p->sm_count;
     return MUON_OK;
 }

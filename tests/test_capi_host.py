@@ -24,6 +24,23 @@ def test_header_and_binding_agree():
     assert sorted(mu.EXPORTED) == names
 
 
+def struct_fields(name):
+    """(field, bytes) of a typedef struct in include/muon.h, in order."""
+    src = open(os.path.join(ROOT, "include", "muon.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    body = re.search(r"typedef struct \{([^}]*)\}\s*" + name + r"\s*;", src).group(1)
+    size = {"int32_t": 4, "int64_t": 8}
+    return [(f, size[t]) for t, f in re.findall(r"\b(int32_t|int64_t)\s+(\w+)\s*;", body)]
+
+
+def test_struct_layouts_match_the_header():
+    for name, cls in (("muon_plan_opts", mu.MuonPlanOpts), ("muon_plan_info_t", mu.MuonPlanInfo)):
+        fields = struct_fields(name)
+        assert [f for f, _ in fields] == [f for f, _ in cls._fields_], name
+        assert [b for _, b in fields] == [ctypes.sizeof(t) for _, t in cls._fields_], name
+        assert ctypes.sizeof(cls) == sum(b for _, b in fields), name
+
+
 def test_library_exports_every_declared_symbol():
     lib = mu.load()
     for name in declared_functions():
@@ -48,6 +65,12 @@ def test_plan_create_rejects_bad_arguments_before_cuda():
     assert lib.muon_plan_create(None, 1, mu.MUON_BF16, None, ctypes.byref(h)) == mu.MUON_ERR_INVALID_ARG
     assert lib.muon_step(None, None, None, None, 0.1, 0.1, 0.9, 5, 0, None) == mu.MUON_ERR_INVALID_ARG
     assert lib.muon_sync(None, None) == mu.MUON_ERR_INVALID_ARG
+    assert lib.muon_step_host(None, None, None, None, None, None, 0.1, 0.1, 0.9, 5, 0, None) == \
+        mu.MUON_ERR_INVALID_ARG
+    one = (mu.MuonShape * 1)(mu.MuonShape(4, 8))
+    for bad in (mu.MuonPlanOpts(chunks=-1), mu.MuonPlanOpts(reserved=1)):
+        assert lib.muon_plan_create(one, 1, mu.MUON_BF16, ctypes.byref(bad), ctypes.byref(h)) == \
+            mu.MUON_ERR_INVALID_ARG
     big = (mu.MuonShape * 1)(mu.MuonShape(1 << 21, 4))
     assert lib.muon_plan_create(big, 1, mu.MUON_F32, None, ctypes.byref(h)) == mu.MUON_ERR_UNSUPPORTED
 

@@ -540,3 +540,92 @@ def test_step_ex_argument_checks():
     with pytest.raises(lib.MuonError) as ei:
         lib.MuonPlan(shapes, "f32", max_ns_steps=101)
     assert ei.value.code == lib.MUON_ERR_INVALID_ARG
+
+
+HOST_SHAPES = [(128, 3584)] * 6 + [(300, 65), (7, 13)] + [(520, 200)] * 3 + [(200, 520)] * 2 + [(1024, 256)]
+
+
+def _two_steps_on_device(plan, shapes, grads, mode):
+    """Reference for muon_step_host: the same two steps with the gradients already on the device."""
+    import torch
+    inp = host_inputs(shapes, "bf16", 41)
+    W = [w.cuda() for w, _, _ in inp]
+    M = [m.cuda() for _, _, m in inp]
+    G = [torch.empty_like(g, device="cuda") for g in grads[0]]
+    for step_grads in grads:
+        for gd, gh in zip(G, step_grads):
+            gd.copy_(gh)
+        if mode == "ns":
+            plan.step(W, G, M, LR, WD, MU, 5, "ns")
+        else:
+            plan.rownorm_step(W, G, M, LR, WD, MU)
+    plan.sync()
+    return [w.cpu() for w in W], [m.cpu() for m in M]
+
+
+@pytest.mark.parametrize("mode", ["ns", "rownorm"])
+def test_step_host_overlapped_copies_match_device_step(mode):
+    """muon_step_host on a plan split into chunks (gradients copied in and params copied
+    back on the plan's copy streams, overlapped with the compute) gives bitwise the
+    results of the same two steps run on device buffers by an unchunked plan; the host
+    copies of the params equal the device params, and the second step's copies in wait
+    for the first step's reads of the gradient buffers."""
+    import torch
+    import matrix_orthogonalising_optimizer_muon_gb300 as lib
+    shapes = HOST_SHAPES
+    grads = [[g for _, g, _ in host_inputs(shapes, "bf16", 41, step=t)] for t in (0, 1)]
+    ref_plan = lib.MuonPlan(shapes, "bf16")
+    W_ref, M_ref = _two_steps_on_device(ref_plan, shapes, grads, mode)
+    ref_plan.close()
+
+    plan = lib.MuonPlan(shapes, "bf16", chunks=4)
+    assert plan.info()["n_chunks"] >= 3
+    inp = host_inputs(shapes, "bf16", 41)
+    W = [w.cuda() for w, _, _ in inp]
+    M = [m.cuda() for _, _, m in inp]
+    G = [torch.empty(s, dtype=torch.bfloat16, device="cuda") for s in shapes]
+    gh = [[g.pin_memory() for g in step_grads] for step_grads in grads]
+    wh = [torch.empty(s, dtype=torch.float32).pin_memory() for s in shapes]
+    for t in range(2):
+        plan.step_host(W, G, M, gh[t], wh, LR, WD, MU, 5, mode)
+    torch.cuda.current_stream().synchronize()
+    plan.sync()
+    for i in range(len(shapes)):
+        assert torch.equal(W[i].cpu(), W_ref[i]), (mode, i, shapes[i])
+        assert torch.equal(M[i].cpu(), M_ref[i]), (mode, i, shapes[i])
+        assert torch.equal(wh[i], W_ref[i]), (mode, i, shapes[i])
+        assert torch.equal(G[i].cpu(), grads[1][i]), (mode, i, shapes[i])
+    plan.close()
+
+
+def test_step_host_without_copy_back_and_argument_checks():
+    import ctypes
+    import torch
+    import matrix_orthogonalising_optimizer_muon_gb300 as lib
+    shapes = HOST_SHAPES
+    grads = [[g for _, g, _ in host_inputs(shapes, "bf16", 41, step=0)]]
+    ref_plan = lib.MuonPlan(shapes, "bf16")
+    W_ref, M_ref = _two_steps_on_device(ref_plan, shapes, grads, "ns")
+    ref_plan.close()
+    plan = lib.MuonPlan(shapes, "bf16")   # one chunk
+    inp = host_inputs(shapes, "bf16", 41)
+    W = [w.cuda() for w, _, _ in inp]
+    M = [m.cuda() for _, _, m in inp]
+    G = [torch.zeros(s, dtype=torch.bfloat16, device="cuda") for s in shapes]
+    w0 = [w.clone() for w in W]
+    # a null host gradient pointer: rejected before anything is enqueued
+    w, g, m = plan._pointers(W, G, M)
+    gh = (ctypes.c_void_p * len(shapes))(*([grads[0][0].data_ptr()] + [None] * (len(shapes) - 1)))
+    code = plan.lib.muon_step_host(plan.handle, w, g, m, gh, None, LR, WD, MU, 5, lib.MUON_MODE_NS, None)
+    assert code == lib.MUON_ERR_INVALID_ARG
+    gh = (ctypes.c_void_p * len(shapes))(*[t.data_ptr() for t in grads[0]])
+    code = plan.lib.muon_step_host(plan.handle, w, g, m, gh, None, LR, WD, MU, 6, lib.MUON_MODE_NS, None)
+    assert code == lib.MUON_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert all(torch.equal(a, b) for a, b in zip(W, w0)) and all(int(t.abs().sum()) == 0 for t in G)
+    plan.step_host(W, G, M, grads[0], None, LR, WD, MU, 5, "ns")   # pageable host memory
+    torch.cuda.synchronize()
+    plan.sync()
+    for i in range(len(shapes)):
+        assert torch.equal(W[i].cpu(), W_ref[i]) and torch.equal(M[i].cpu(), M_ref[i]), i
+    plan.close()
