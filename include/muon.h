@@ -168,8 +168,8 @@ muon_status muon_step_ex(muon_plan p, float* const* params, const void* const* g
  * stream of the plan copies the gradients in chunk order, each chunk's momentum
  * kernel waits only for its own chunk's gradients, and a second copy stream
  * copies each chunk's parameters back as soon as that chunk's final product has
- * run, while the next chunks compute.  RowNorm mode copies in, computes and
- * copies back in sequence.  The copies in are ordered after the work already on
+ * run, while the next chunks compute.  RowNorm mode runs chunk by chunk in the
+ * same way (eps = 1e-8).  The copies in are ordered after the work already on
  * `stream` (which may still read the previous gradients), and `stream` waits for
  * the last copy back: once `stream` is synchronised, params_host holds the
  * result.  Errors as muon_step; a null grads_host (or null entry of either host

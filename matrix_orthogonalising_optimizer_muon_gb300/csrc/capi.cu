@@ -174,6 +174,7 @@ struct muon_plan_s {
     struct Chunk {
         std::vector<int> buckets;
         ListDev mom_rows, mom_tiles, all;
+        ListDev rn_rows, rn_stats, rn_final, rn_apply;   // RowNorm of this chunk (muon_step_host)
         int chain_clusters = 0;   // CTA pairs for the batched products beside the fused kernel
     };
     std::vector<Chunk> chunks;
@@ -567,11 +568,14 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
         for (int i = 0; i < n; ++i) t += (size_t)round_up(p->mats[i].m * p->mats[i].n * 4, 256);
         return t;
     }()) : 0;
-    // launch lists: per chunk the momentum rows / tiles / all lists, and the four
-    // RowNorm lists.  Chunks partition the matrices, so the entries total at most
-    // 2n + 3 per chunk (n chunks at most) plus 4n + 4: 10n + 8 ints and prefixes.
-    const size_t o_lists = take(sizeof(int) * (size_t)(10 * n + 8));
-    const size_t o_prefix = take(sizeof(long long) * (size_t)(10 * n + 8));
+    // launch lists: per chunk the momentum rows / tiles / all lists and its four
+    // RowNorm lists, and the four RowNorm lists of the whole plan.  Chunks partition
+    // the matrices (n chunks at most); a list of k matrices takes max(k, 1) ints and
+    // k + 1 prefixes.  Momentum lists: 2 per matrix plus 3 per chunk, at most 5n; chunk
+    // RowNorm lists (rows once, column matrices three times): at most 3n + 4n; the
+    // plan's: 3n + 4.  15n + 4 <= 17n + 16 of each.
+    const size_t o_lists = take(sizeof(int) * (size_t)(17 * n + 16));
+    const size_t o_prefix = take(sizeof(long long) * (size_t)(17 * n + 16));
     const size_t fixed_bytes = off;
 
     // ---- chunks: matrices in group order, a new chunk whenever the region would
@@ -734,6 +738,10 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
         upload_list(rows, ch.mom_rows, 0);
         upload_list(tiles, ch.mom_tiles, 1);
         upload_list(all, ch.all, 2);
+        upload_list(rows, ch.rn_rows, 3);
+        upload_list(tiles, ch.rn_stats, 4);
+        upload_list(tiles, ch.rn_final, 5);
+        upload_list(tiles, ch.rn_apply, 6);
     }
     upload_list(rnr_list, p->rn_rows, 3);
     upload_list(rnc_list, p->rn_stats, 4);
@@ -844,6 +852,26 @@ void muon_plan_destroy(muon_plan p) {
     free_plan(p);
 }
 
+// The RowNorm kernels over one set of lists (m <= n rows; m > n column statistics,
+// finalize, apply).
+static muon_status rownorm_launch(muon_plan_s* p, const ListDev& rows, const ListDev& stats,
+                                  const ListDev& fin, const ListDev& apply, float lr, float wd, float mu, float eps,
+                                  cudaStream_t s, int* launches) {
+    ElemArgs a = elem_args(p, rows, mu, lr, wd, eps);
+    MUON_TRY(launch_rownorm_rows(a, rows.blocks, s));
+    *launches += rows.blocks > 0;
+    a = elem_args(p, stats, mu, lr, wd, eps);
+    a.partials = p->cpartials;
+    MUON_TRY(launch_rownorm_colstats(a, stats.blocks, s));
+    a = elem_args(p, fin, mu, lr, wd, eps);
+    a.partials = p->cpartials;
+    MUON_TRY(launch_rownorm_colfinal(a, fin.blocks, s));
+    a = elem_args(p, apply, mu, lr, wd, eps);
+    MUON_TRY(launch_rownorm_colapply(a, apply.blocks, s));
+    *launches += stats.blocks > 0 ? 3 : 0;
+    return MUON_OK;
+}
+
 muon_status muon_rownorm_step(muon_plan p, float* const* params, const void* const* grads, float* const* momentum,
                               float lr, float wd, float mu, float eps, void* stream) {
     if (!p) return MUON_ERR_INVALID_ARG;
@@ -862,18 +890,9 @@ muon_status muon_rownorm_step(muon_plan p, float* const* params, const void* con
         MUON_TRY(cudaEventRecord(se->e[0], s));
     }
     int launches = 0;
-    ElemArgs a = elem_args(p, p->rn_rows, mu, lr, wd, eps);
-    MUON_TRY(launch_rownorm_rows(a, p->rn_rows.blocks, s));
-    launches += p->rn_rows.blocks > 0;
-    a = elem_args(p, p->rn_stats, mu, lr, wd, eps);
-    a.partials = p->cpartials;
-    MUON_TRY(launch_rownorm_colstats(a, p->rn_stats.blocks, s));
-    a = elem_args(p, p->rn_final, mu, lr, wd, eps);
-    a.partials = p->cpartials;
-    MUON_TRY(launch_rownorm_colfinal(a, p->rn_final.blocks, s));
-    a = elem_args(p, p->rn_apply, mu, lr, wd, eps);
-    MUON_TRY(launch_rownorm_colapply(a, p->rn_apply.blocks, s));
-    launches += p->rn_stats.blocks > 0 ? 3 : 0;
+    if ((st = rownorm_launch(p, p->rn_rows, p->rn_stats, p->rn_final, p->rn_apply, lr, wd, mu, eps, s,
+                             &launches)) != MUON_OK)
+        return st;
     if (se) MUON_TRY(cudaEventRecord(se->e[5], s));
     p->last_launches = launches;
     return MUON_OK;
@@ -1251,31 +1270,36 @@ muon_status muon_step_host(muon_plan p, float* const* params, const void* const*
     // gradients in, chunk by chunk, after the caller's earlier work (which may still read grads)
     MUON_TRY(cudaEventRecord(h.entry_ev, s));
     MUON_TRY(cudaStreamWaitEvent(h.in, h.entry_ev, 0));
-    const bool ns = mode == MUON_MODE_NS;
     for (size_t ci = 0; ci < p->chunks.size(); ++ci) {
         for (int bk : p->chunks[ci].buckets)
             for (int i : p->buckets[bk].mats)
                 MUON_TRY(cudaMemcpyAsync(const_cast<void*>(grads[i]), grads_host[i],
                                          (size_t)(p->mats[i].m * p->mats[i].n) * gsz, cudaMemcpyDefault, h.in));
-        if (ns) MUON_TRY(cudaEventRecord(h.in_ev[ci], h.in));
+        MUON_TRY(cudaEventRecord(h.in_ev[ci], h.in));
     }
-    if (ns) {
+    if (mode == MUON_MODE_NS) {
         const HostIO io{params_host};
         st = ns_step(p, params, grads, momentum, lr, wd, mu, ns_steps, nullptr, 0, stream, &io);
         if (st != MUON_OK) return st;
-    } else {
-        MUON_TRY(cudaEventRecord(h.in_ev[0], h.in));
-        MUON_TRY(cudaStreamWaitEvent(s, h.in_ev[0], 0));
-        st = muon_rownorm_step(p, params, grads, momentum, lr, wd, mu, 1e-8f, stream);
-        if (st != MUON_OK) return st;
-        if (params_host) {
-            MUON_TRY(cudaEventRecord(h.out_ev[0], s));
-            MUON_TRY(cudaStreamWaitEvent(h.out, h.out_ev[0], 0));
-            for (int i = 0; i < n; ++i)
-                MUON_TRY(cudaMemcpyAsync(params_host[i], params[i],
-                                         (size_t)(p->mats[i].m * p->mats[i].n) * sizeof(float), cudaMemcpyDefault,
-                                         h.out));
+    } else {   // RowNorm, chunk by chunk like the NS step
+        if ((st = upload_pointers(p, params, grads, momentum, s)) != MUON_OK) return st;
+        int launches = 0;
+        for (size_t ci = 0; ci < p->chunks.size(); ++ci) {
+            const muon_plan_s::Chunk& ch = p->chunks[ci];
+            MUON_TRY(cudaStreamWaitEvent(s, h.in_ev[ci], 0));
+            if ((st = rownorm_launch(p, ch.rn_rows, ch.rn_stats, ch.rn_final, ch.rn_apply, lr, wd, mu, 1e-8f, s,
+                                     &launches)) != MUON_OK)
+                return st;
+            if (!params_host) continue;
+            MUON_TRY(cudaEventRecord(h.out_ev[ci], s));
+            MUON_TRY(cudaStreamWaitEvent(h.out, h.out_ev[ci], 0));
+            for (int bk : ch.buckets)
+                for (int i : p->buckets[bk].mats)
+                    MUON_TRY(cudaMemcpyAsync(params_host[i], params[i],
+                                             (size_t)(p->mats[i].m * p->mats[i].n) * sizeof(float),
+                                             cudaMemcpyDefault, h.out));
         }
+        p->last_launches = launches;
     }
     if (params_host) {   // the caller's stream covers the copies back
         MUON_TRY(cudaEventRecord(h.end_ev, h.out));
