@@ -37,6 +37,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen7b_28l")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--quad-clusters", action="store_true",
+                    help="final product in clusters of two CTA pairs sharing X0 by TMA multicast")
     ap.add_argument("--e2e-chunks", type=int, default=16,
                     help="chunks of the e2e plan (host copies of one chunk overlap another's compute)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -271,7 +273,8 @@ def run_ours(args, rank, world, local):
         M.append(workloads.gen_tensor((m, n), workloads.M_STD, workloads.seed_of(wl.index, 0, i, "M"), dev))
         G.append(workloads.gen_tensor((m, n), workloads.G_STD, workloads.seed_of(wl.index, 0, i, "G"), dev,
                                       wl.grad_dtype))
-    plan = lib.MuonPlan(shapes, wl.grad_dtype, timing=True, workspace_bytes=args.workspace_bytes)
+    plan = lib.MuonPlan(shapes, wl.grad_dtype, timing=True, workspace_bytes=args.workspace_bytes,
+                        quad_clusters=args.quad_clusters)
     torch.cuda.synchronize()
     setup_s = time.time() - t0
     lr, wd, mu = workloads.LR, workloads.WD, workloads.MU
@@ -407,7 +410,8 @@ def report_ours(args, res, rank, world):
                    "l2": "inputs larger than L2 (%.1f GB of W, G, M per step)" %
                          (sum(m * n for m, n in shapes) * (10 if wl.grad_dtype == "bf16" else 12) / 1e9),
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "workspace_bytes": res["plan"].info()["workspace_bytes"]},
+                   "workspace_bytes": res["plan"].info()["workspace_bytes"],
+                   "quad_clusters": res["plan"].info()["quad_clusters"]},
         "stages_ms_per_ns_step": {"momentum_norm": round(per_ns[0], 3), "syrk": round(per_ns[1], 3),
                                   "ns_rxr": round(per_ns[2], 3), "final_apply": round(per_ns[3], 3),
                                   "fused_small": round(per_ns[5], 3)},

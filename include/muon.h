@@ -95,7 +95,13 @@ typedef struct {
        compute.  Results are the same.  0 or 1: chunks only as workspace_bytes
        requires.  Negative: MUON_ERR_INVALID_ARG. */
     int32_t chunks;
-    int32_t reserved;   /* must be 0 */
+    /* nonzero: the final product O = Q X0 runs in clusters of two CTA pairs that load
+       their shared X0 columns once (TMA multicast), when every problem of its launch
+       has an even number of 256-row tiles (r a multiple of 512) and the launch has the
+       whole GPU.  Results are the same.  Off by default: only 36 such clusters fit on
+       the 152 SMs (144 SMs), and on GB300 the product ran 2-3 % slower than on 76
+       single-pair clusters.  0: every product in clusters of one CTA pair. */
+    int32_t quad_clusters;
 } muon_plan_opts;
 
 typedef struct muon_plan_s* muon_plan;
@@ -269,7 +275,7 @@ typedef struct {
     int32_t launches_last_step;   /* kernels the last step enqueued */
     int32_t sm_count;
     int32_t n_chunks;             /* chunks the NS step runs in (opts.chunks, opts.workspace_bytes) */
-    int32_t reserved;
+    int32_t quad_clusters;        /* co-resident clusters of two CTA pairs (0: not used) */
 } muon_plan_info_t;
 
 muon_status muon_plan_info(muon_plan p, muon_plan_info_t* info);

@@ -144,6 +144,7 @@ struct muon_plan_s {
     int device = 0;
     int sm_count = 0;
     int pair_clusters = 0;   // co-resident CTA pairs for the 2-SM kernel (0: 1-SM kernel only)
+    int quad_clusters = 0;   // co-resident clusters of two pairs (0: never used)
     // fused (r <= 128) and batched matrices in one chunk: the batched products' stream
     // and fork/join events (created when a chunk overlaps the two)
     cudaStream_t s2 = nullptr;
@@ -386,8 +387,26 @@ struct Grouper {
     }
     void flush2() {
         if (L2.nprob == 0) return;
+        // clusters of two pairs sharing B (multicast) when enabled, the launch has the
+        // whole GPU, and every problem is a non-symmetric product with an MN-major B and
+        // an even number of tile rows
+        const int quads = std::min(clusters / 2, p->quad_clusters);
+        bool quad = quads >= 1 && clusters == p->pair_clusters;
+        for (int i = 0; quad && i < L2.nprob; ++i) {
+            const GemmProblem& q = L2.prob[i];
+            quad = q.b_mn && !q.sym && q.tiles_m % 2 == 0;
+        }
+        if (quad) {   // count super-tiles of two pair tiles
+            L2.total_tiles = 0;
+            for (int i = 0; i < L2.nprob; ++i) {
+                GemmProblem& q = L2.prob[i];
+                q.tiles_per_item = q.tiles_m / 2 * q.tiles_n;
+                q.tile_begin = L2.total_tiles;
+                L2.total_tiles += q.tiles_per_item * q.batch;
+            }
+        }
         if (st == MUON_OK) {
-            st = cuda_status(gemm2_launch(L2, bf16, clusters, s));
+            st = cuda_status(gemm2_launch(L2, bf16, quad ? 2 * quads : clusters, s, quad));
             ++launches;
         }
         reset(L2);
@@ -473,7 +492,7 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
         if (std::min(shapes[i].rows, shapes[i].cols) > kMaxR) return MUON_ERR_UNSUPPORTED;
     }
     if (opts && (opts->max_ns_steps < 0 || opts->max_ns_steps > kMaxNsStepsRestart || opts->chunks < 0 ||
-                 opts->reserved != 0 || opts->workspace_bytes < 0))
+                 opts->workspace_bytes < 0))
         return MUON_ERR_INVALID_ARG;
     muon_plan_s* p = new (std::nothrow) muon_plan_s();
     if (!p) return MUON_ERR_OOM;
@@ -807,8 +826,13 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
     ok = ok && gemm_prepare(p->device) == cudaSuccess;
     if (ok && !p->opts.single_sm_gemm) {
         int clusters = 0;
-        ok = gemm2_max_clusters(&clusters) == cudaSuccess;
+        ok = gemm2_max_clusters(&clusters, 2) == cudaSuccess;
         p->pair_clusters = clusters;
+        if (ok && p->opts.quad_clusters) {
+            int quads = 0;
+            ok = gemm2_max_clusters(&quads, 4) == cudaSuccess;
+            p->quad_clusters = quads;
+        }
     }
     if (ok && p->pair_clusters > 1 && p->opts.chain_clusters >= 0) {
         bool any = false;
@@ -1376,7 +1400,7 @@ muon_status muon_plan_info(muon_plan p, muon_plan_info_t* info) {
     info->workspace_bytes = (int64_t)p->ws_bytes;
     info->launches_last_step = p->last_launches;
     info->n_chunks = (int32_t)p->chunks.size();
-    info->reserved = 0;
+    info->quad_clusters = p->quad_clusters;
     info->sm_count = p->sm_count;
     return MUON_OK;
 }

@@ -126,7 +126,7 @@ __global__ void __maxnreg__(168) gemm_kernel(const __grid_constant__ GemmLaunch 
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const uint32_t s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1u;
-                    if (!mbar_wait(empty + s, ph ^ 1u, abort_flag, L.status, kStatusTimeoutProducer)) {
+                    if (!mbar_wait_idle(empty + s, ph ^ 1u, abort_flag, L.status, kStatusTimeoutProducer, false)) {
                         ok = false;
                         break;
                     }
@@ -162,14 +162,14 @@ __global__ void __maxnreg__(168) gemm_kernel(const __grid_constant__ GemmLaunch 
                 const int kblocks = (P.K + Cfg::BK - 1) / Cfg::BK;
                 const uint32_t acc = local & 1;
                 const uint32_t aph = (local >> 1) & 1u;
-                if (!mbar_wait(tempty + acc, aph ^ 1u, abort_flag, L.status, kStatusTimeoutMma)) break;
+                if (!mbar_wait_idle(tempty + acc, aph ^ 1u, abort_flag, L.status, kStatusTimeoutMma, false)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * kBN;
                 const uint32_t idesc = idesc_make(BF16, kBM, kBN, false, P.b_mn != 0);
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const uint32_t s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1u;
-                    if (!mbar_wait(full + s, ph, abort_flag, L.status, kStatusTimeoutMma)) {
+                    if (!mbar_wait_idle(full + s, ph, abort_flag, L.status, kStatusTimeoutMma, false)) {
                         ok = false;
                         break;
                     }
@@ -206,7 +206,7 @@ __global__ void __maxnreg__(168) gemm_kernel(const __grid_constant__ GemmLaunch 
             const uint32_t aph = (local >> 1) & 1u;
             if (P.epi == kEpiApply || P.epi == kEpiPoly)
                 prefetch_epilogue_inputs(P, tc.item, tc.m0 + wq * 32, tc.n0 + c_begin, kBN * 4 / kEpiWarps, lane);
-            if (!mbar_wait(tfull + acc, aph, abort_flag, L.status, kStatusTimeoutEpilogue)) break;
+            if (!mbar_wait_idle(tfull + acc, aph, abort_flag, L.status, kStatusTimeoutEpilogue, false)) break;
             tc_fence_after();
             const int row = tc.m0 + wq * 32 + lane;
             const int warp_row_max = tc.m0 + wq * 32 + 31;
@@ -292,9 +292,28 @@ __device__ __forceinline__ TileCoord decode_pair_tile(const GemmLaunch& L, int t
     return {p, item, tm * 256 + 128 * (int)rank, tn * 256};
 }
 
-template <bool BF16>
-__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
-    gemm2_kernel(const __grid_constant__ GemmLaunch L) {
+// Clusters of four CTAs (two pairs) on non-symmetric problems with an MN-major B
+// and an even number of pair-tile rows: unit u is a super-tile (sm, tn) and pair
+// pr computes tile (2 sm + pr, tn), so both pairs read the same B columns.
+__device__ __forceinline__ TileCoord decode_quad_tile(const GemmLaunch& L, int u, uint32_t pr, uint32_t q) {
+    int p = 0;
+    while (p + 1 < L.nprob && u >= L.prob[p + 1].tile_begin) ++p;
+    const GemmProblem& P = L.prob[p];
+    const int local = u - P.tile_begin;
+    const int item = local / P.tiles_per_item;
+    const int tl = local - item * P.tiles_per_item;
+    const int half_m = P.tiles_m / 2;
+    const int sm = tl % half_m, tn = tl / half_m;
+    return {p, item, (2 * sm + (int)pr) * 256 + 128 * (int)q, tn * 256};
+}
+
+// CL = 2: one CTA pair per cluster.  CL = 4: two pairs per cluster sharing the B
+// operand of decode_quad_tile's super-tiles: each CTA loads one of the two 64-column
+// boxes of its B half and multicasts it to the CTA of the same parity in the other
+// pair; a stage is free again once both pairs' MMAs have read it.
+template <bool BF16, int CL>
+__global__ void __maxnreg__(168) gemm2_kernel(const __grid_constant__ GemmLaunch L) {
+    static_assert(CL == 2 || CL == 4, "clusters of one or two CTA pairs");
     using Cfg = Gemm2Cfg;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -309,14 +328,18 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
-    const bool leader = rank == 0;
-    const int cluster_id = blockIdx.x >> 1;
-    const int nclusters = gridDim.x >> 1;
+    const uint32_t q = rank & 1u;      // CTA within its pair
+    const uint32_t pr = rank >> 1;     // pair within the cluster
+    const uint32_t lead = rank & ~1u;  // the pair's even CTA: MMA issuer, owner of the full / tempty barriers
+    const bool leader = q == 0;
+    const int cluster_id = blockIdx.x / CL;
+    const int nclusters = gridDim.x / CL;
+    auto decode = [&](int t) { return CL == 2 ? decode_pair_tile(L, t, q) : decode_quad_tile(L, t, pr, q); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages2; ++s) {
             mbar_init(full + s, 1);    // leader: its expect_tx arrival + both CTAs' bytes
-            mbar_init(empty + s, 1);   // both: the leader's multicast commit
+            mbar_init(empty + s, CL / 2);   // every pair's leader: its multicast commit
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull + a, 1);   // both: the leader's multicast commit
@@ -349,23 +372,27 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
             uint32_t it = 0;
             bool ok = true;
             for (int t = cluster_id; ok && t < L.total_tiles; t += nclusters) {
-                const TileCoord tc = decode_pair_tile(L, t, rank);
+                const TileCoord tc = decode(t);
                 const GemmProblem& P = L.prob[tc.p];
                 const int kblocks = (P.K + Cfg::BK - 1) / Cfg::BK;
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const uint32_t s = it % kStages2;
                     const uint32_t ph = (it / kStages2) & 1u;
-                    if (!mbar_wait_cluster(empty + s, ph ^ 1u, abort_flag, L.status, kStatusTimeoutProducer)) {
+                    if (!mbar_wait_idle(empty + s, ph ^ 1u, abort_flag, L.status, kStatusTimeoutProducer, true)) {
                         ok = false;
                         break;
                     }
                     uint8_t* sa = smem + s * Cfg::STAGE_BYTES;
                     uint8_t* sb = sa + Cfg::A_BYTES;
-                    const uint32_t fb = mapa_shared(smem_u32(full + s), 0);
+                    const uint32_t fb = mapa_shared(smem_u32(full + s), lead);
                     if (leader) mbar_arrive_expect_tx(full + s, 2 * Cfg::STAGE_BYTES);
                     tma_load_3d_pair(sa, &L.mapA[tc.p], fb, kb * Cfg::BK, tc.m0, tc.item);
-                    const int nb = tc.n0 + 128 * (int)rank;
-                    if (!P.b_mn) {
+                    const int nb = tc.n0 + 128 * (int)q;
+                    if (CL == 4) {   // B MN-major, shared with the other pair
+                        const uint16_t mask = (uint16_t)((1u << q) | (1u << (2 + q)));
+                        tma_load_3d_pair_mc(sb + pr * Cfg::MN_CHUNK_BYTES, &L.mapB[tc.p], fb, nb + 64 * (int)pr,
+                                            kb * Cfg::BK, tc.item, mask);
+                    } else if (!P.b_mn) {
                         tma_load_3d_pair(sb, &L.mapB[tc.p], fb, kb * Cfg::BK, nb, tc.item);
                     } else {
                         tma_load_3d_pair(sb, &L.mapB[tc.p], fb, nb, kb * Cfg::BK, tc.item);
@@ -388,19 +415,19 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
             int local = 0;
             bool ok = true;
             for (int t = cluster_id; ok && t < L.total_tiles; t += nclusters, ++local) {
-                const TileCoord tc = decode_pair_tile(L, t, rank);
+                const TileCoord tc = decode(t);
                 const GemmProblem& P = L.prob[tc.p];
                 const int kblocks = (P.K + Cfg::BK - 1) / Cfg::BK;
                 const uint32_t acc = local & 1;
                 const uint32_t aph = (local >> 1) & 1u;
-                if (!mbar_wait_cluster(tempty + acc, aph ^ 1u, abort_flag, L.status, kStatusTimeoutMma)) break;
+                if (!mbar_wait_idle(tempty + acc, aph ^ 1u, abort_flag, L.status, kStatusTimeoutMma, true)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * kBN;
                 const uint32_t idesc = idesc_make(BF16, 256, kBN, false, P.b_mn != 0);
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const uint32_t s = it % kStages2;
                     const uint32_t ph = (it / kStages2) & 1u;
-                    if (!mbar_wait_cluster(full + s, ph, abort_flag, L.status, kStatusTimeoutMma)) {
+                    if (!mbar_wait_idle(full + s, ph, abort_flag, L.status, kStatusTimeoutMma, true)) {
                         ok = false;
                         break;
                     }
@@ -415,12 +442,12 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
                                    : sdesc_sw128(b_addr + kk * Cfg::UK * Cfg::ESZ, 0, 1024);
                         mma_f16kind_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0);
                     }
-                    mma_commit_pair(empty + s, 3);   // frees the stage in both CTAs
+                    mma_commit_pair(empty + s, CL == 4 ? 0xF : 0x3);   // this pair is done with the stage
                 }
                 if (!ok) break;
-                mma_commit_pair(tfull + acc, 3);     // both CTAs' accumulators ready
+                mma_commit_pair(tfull + acc, (uint16_t)(3u << lead));   // both CTAs' accumulators ready
             }
-            mma_commit_pair(drain, 1);
+            mma_commit_pair(drain, (uint16_t)(1u << rank));
             mbar_drain(drain, 0);
         }
     } else {
@@ -428,17 +455,17 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
         // warp % 4; warps 2-5 take columns 0-127 of the tile, warps 6-9 columns 128-255
         const int wq = warp & 3;
         const int c_begin = ((warp - 2) >> 2) * (kBN * 4 / kEpiWarps);
-        const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), 0);
+        const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), lead);
         uint8_t* stage_l = smem + Cfg::OUT_OFFSET + (warp - 2) * 4096;
         int local = 0;
         for (int t = cluster_id; t < L.total_tiles; t += nclusters, ++local) {
-            const TileCoord tc = decode_pair_tile(L, t, rank);
+            const TileCoord tc = decode(t);
             const GemmProblem& P = L.prob[tc.p];
             const uint32_t acc = local & 1;
             const uint32_t aph = (local >> 1) & 1u;
             if (P.epi == kEpiApply || P.epi == kEpiPoly)
                 prefetch_epilogue_inputs(P, tc.item, tc.m0 + wq * 32, tc.n0 + c_begin, kBN * 4 / kEpiWarps, lane);
-            if (!mbar_wait_cluster(tfull + acc, aph, abort_flag, L.status, kStatusTimeoutEpilogue)) break;
+            if (!mbar_wait_idle(tfull + acc, aph, abort_flag, L.status, kStatusTimeoutEpilogue, true)) break;
             tc_fence_after();
             const int row = tc.m0 + wq * 32 + lane;
             const int warp_row_max = tc.m0 + wq * 32 + 31;
@@ -501,39 +528,47 @@ cudaError_t gemm_prepare(int device) {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  GemmCfg::SMEM_BYTES);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(gemm2_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Gemm2Cfg::SMEM_BYTES);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(gemm2_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Gemm2Cfg::SMEM_BYTES);
+    const int n = Gemm2Cfg::SMEM_BYTES;
+    const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm2_kernel<true, 2>, a, n);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm2_kernel<false, 2>, a, n);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm2_kernel<true, 4>, a, n);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm2_kernel<false, 4>, a, n);
     if (e == cudaSuccess) e = ns_small_prepare();
     return e;
 }
 
-cudaError_t gemm2_max_clusters(int* out) {
+cudaError_t gemm2_max_clusters(int* out, int cluster_ctas) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = cluster_ctas;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(2, 1, 1);
+    cfg.gridDim = dim3(cluster_ctas, 1, 1);
     cfg.blockDim = dim3(kGemmThreads, 1, 1);
     cfg.dynamicSmemBytes = Gemm2Cfg::SMEM_BYTES;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaOccupancyMaxActiveClusters(out, gemm2_kernel<true>, &cfg);
+    if (cluster_ctas == 4) return cudaOccupancyMaxActiveClusters(out, gemm2_kernel<true, 4>, &cfg);
+    return cudaOccupancyMaxActiveClusters(out, gemm2_kernel<true, 2>, &cfg);
 }
 
-cudaError_t gemm2_launch(const GemmLaunch& L, bool bf16, int clusters, cudaStream_t s) {
+cudaError_t gemm2_launch(const GemmLaunch& L, bool bf16, int clusters, cudaStream_t s, bool quad) {
     if (L.total_tiles <= 0) return cudaSuccess;
+    const dim3 blk(kGemmThreads);
+    const size_t sm = Gemm2Cfg::SMEM_BYTES;
+    if (quad) {   // clusters of two pairs; L.total_tiles counts super-tiles
+        int quads = clusters / 2;
+        if (quads > L.total_tiles) quads = L.total_tiles;
+        if (quads < 1) quads = 1;
+        return bf16 ? launch_pdl_cluster(gemm2_kernel<true, 4>, dim3(4 * quads), blk, sm, s, 4u, L)
+                    : launch_pdl_cluster(gemm2_kernel<false, 4>, dim3(4 * quads), blk, sm, s, 4u, L);
+    }
     if (clusters > L.total_tiles) clusters = L.total_tiles;
     if (clusters < 1) clusters = 1;
-    if (bf16)
-        return launch_pdl(gemm2_kernel<true>, dim3(2 * clusters), dim3(kGemmThreads), Gemm2Cfg::SMEM_BYTES, s, L);
-    else
-        return launch_pdl(gemm2_kernel<false>, dim3(2 * clusters), dim3(kGemmThreads), Gemm2Cfg::SMEM_BYTES, s, L);
+    return bf16 ? launch_pdl_cluster(gemm2_kernel<true, 2>, dim3(2 * clusters), blk, sm, s, 2u, L)
+                : launch_pdl_cluster(gemm2_kernel<false, 2>, dim3(2 * clusters), blk, sm, s, 2u, L);
 }
 
 cudaError_t gemm_launch(const GemmLaunch& L, bool bf16, int grid, cudaStream_t s) {

@@ -56,6 +56,27 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
+// As launch_pdl, with clusters of cluster_x CTAs along x.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                      unsigned cluster_x, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 struct GemmProblem {
     int M, N, K, batch;
     int tiles_m, tiles_n, tiles_per_item, tile_begin;
@@ -103,8 +124,12 @@ cudaError_t gemm_prepare(int device);   // sets the dynamic shared-memory limit 
 cudaError_t gemm_launch(const GemmLaunch& L, bool bf16, int grid, cudaStream_t s);
 // CTA-pair kernel (cluster of 2, tcgen05 cta_group::2, 256 x 256 tiles); problems
 // use pair tiling: tiles_m = ceil(M / 256), tiles_n = ceil(N / 256).
-cudaError_t gemm2_max_clusters(int* out);
-cudaError_t gemm2_launch(const GemmLaunch& L, bool bf16, int clusters, cudaStream_t s);
+// quad: clusters of two pairs that share B by TMA multicast (non-symmetric problems
+// with an MN-major B and even tiles_m only); tiles_per_item then counts super-tiles
+// of two pair tiles, (tiles_m / 2) * tiles_n, and `clusters` is the number of pairs
+// (two per launched cluster).
+cudaError_t gemm2_max_clusters(int* out, int cluster_ctas);   // co-resident clusters of 2 or 4 CTAs
+cudaError_t gemm2_launch(const GemmLaunch& L, bool bf16, int clusters, cudaStream_t s, bool quad = false);
 // Whole NS step (SYRK, r x r recursion, final product + fused update) of matrices
 // with r <= 128, one matrix per CTA at a time.  One problem per bucket: M = r,
 // N = c, batch = matrices, tile_begin = prefix over matrices; mapA = X with

@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
                 for (int q = 0; ok && q < 2 * nch; ++q, ++it) {
                     const uint32_t s = it % kSmallRing;
                     const uint32_t ph = (it / kSmallRing) & 1u;
-                    if (!mbar_wait(empty + s, ph ^ 1u, abort_flag, L.status, kStatusTimeoutProducer)) {
+                    if (!mbar_wait_idle(empty + s, ph ^ 1u, abort_flag, L.status, kStatusTimeoutProducer, false)) {
                         ok = false;
                         break;
                     }
@@ -270,7 +270,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
             };
             auto finish_step = [&]() -> bool {   // commit, then wait for the epilogue of this step
                 mma_commit(mma_done);
-                const bool w = mbar_wait(epi_done, sc & 1u, abort_flag, L.status, kStatusTimeoutMma);
+                const bool w =
+                    mbar_wait_idle(epi_done, sc & 1u, abort_flag, L.status, kStatusTimeoutMma, false);
                 ++sc;
                 tc_fence_after();
                 return w;
@@ -284,7 +285,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
                 // G0 = X X^T (A and B are the same staged k-block)
                 for (int kb = 0; ok && kb < nch; ++kb, ++it) {
                     const uint32_t s = it % kSmallRing;
-                    if (!mbar_wait(full + s, (it / kSmallRing) & 1u, abort_flag, L.status, kStatusTimeoutMma)) {
+                    if (!mbar_wait_idle(full + s, (it / kSmallRing) & 1u, abort_flag, L.status, kStatusTimeoutMma,
+                                        false)) {
                         ok = false;
                         break;
                     }
@@ -316,9 +318,10 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
                 // O = Q X, 128 columns at a time, into alternating accumulators
                 for (int ch = 0; ch < nch; ++ch, ++it, ++fc) {
                     const uint32_t b = fc & 1u;
-                    if (!mbar_wait(accf_empty + b, ((fc >> 1) & 1u) ^ 1u, abort_flag, L.status, kStatusTimeoutMma) ||
-                        !mbar_wait(full + (it % kSmallRing), (it / kSmallRing) & 1u, abort_flag, L.status,
-                                   kStatusTimeoutMma)) {
+                    if (!mbar_wait_idle(accf_empty + b, ((fc >> 1) & 1u) ^ 1u, abort_flag, L.status,
+                                        kStatusTimeoutMma, false) ||
+                        !mbar_wait_idle(full + (it % kSmallRing), (it / kSmallRing) & 1u, abort_flag, L.status,
+                                        kStatusTimeoutMma, false)) {
                         ok = false;
                         break;
                     }
@@ -349,7 +352,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
         uint32_t sc = 0, fc = 0, mc = 0, jc = 0;
         bool ok = true;
         auto step = [&](int kind, int k, int J, const GemmProblem& P, int item) -> bool {
-            if (!mbar_wait(mma_done, sc & 1u, abort_flag, L.status, kStatusTimeoutEpilogue)) return false;
+            if (!mbar_wait_idle(mma_done, sc & 1u, abort_flag, L.status, kStatusTimeoutEpilogue, false))
+                return false;
             ++sc;
             tc_fence_after();
             small_step_epilogue(kind, k, J, P, item, smem, tmem_row, row, c_begin);
@@ -378,7 +382,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
                 // buffers the W staging reuses: every warp leaves it before any stages W
                 __syncwarp();
                 if (lane == 0) mbar_arrive(rr_free);
-                ok = mbar_wait(rr_free, jc & 1u, abort_flag, L.status, kStatusTimeoutEpilogue);
+                ok = mbar_wait_idle(rr_free, jc & 1u, abort_flag, L.status, kStatusTimeoutEpilogue, false);
                 ++jc;
             }
             if (!ok) break;
@@ -403,7 +407,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
                 if (ahead < npieces) w_piece_load(wc, rw, piece_col(ahead), stage_u32 + (ahead % kWBufs) * kWPiece, lane);
                 else cp_async_commit();
                 if (h == 0) {
-                    if (!mbar_wait(accf_full + b, (fc >> 1) & 1u, abort_flag, L.status, kStatusTimeoutEpilogue)) {
+                    if (!mbar_wait_idle(accf_full + b, (fc >> 1) & 1u, abort_flag, L.status, kStatusTimeoutEpilogue,
+                                        false)) {
                         ok = false;
                         break;
                     }
@@ -432,7 +437,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
             // all warps leave the final phase first
             __syncwarp();
             if (lane == 0) mbar_arrive(stage_free);
-            ok = mbar_wait(stage_free, mc & 1u, abort_flag, L.status, kStatusTimeoutEpilogue);
+            ok = mbar_wait_idle(stage_free, mc & 1u, abort_flag, L.status, kStatusTimeoutEpilogue, false);
             ++mc;
         }
         cp_async_wait<0>();

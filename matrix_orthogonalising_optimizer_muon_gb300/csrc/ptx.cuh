@@ -247,6 +247,49 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
         }
     }
 }
+// Waits of roles that have nothing to do until the phase completes (epilogue warps
+// between tiles, a producer waiting for a free stage, the MMA thread waiting for an
+// operand stage) pass a suspend-time hint: the thread sleeps in the barrier unit,
+// resuming when the phase completes or the hint expires, instead of re-issuing the
+// test and taking issue slots from the warps that share its scheduler.  On the
+// CTA-pair GEMM this made every stage 2-4 % faster than hot polling.
+constexpr uint32_t kIdleSuspendNs = 20000;
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, bool cluster_scope) {
+    uint32_t ok;
+    if (cluster_scope)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}\n"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity), "r"(kIdleSuspendNs)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}\n"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity), "r"(kIdleSuspendNs)
+            : "memory");
+    return ok != 0;
+}
+// As mbar_wait / mbar_wait_cluster for idle roles (see kIdleSuspendNs); the abort
+// flag and the time limit are checked after every suspended test.
+__device__ __forceinline__ bool mbar_wait_idle(uint64_t* bar, uint32_t parity, volatile int* abort, int* status,
+                                               int code, bool cluster_scope) {
+    if (mbar_try_wait_sleep(bar, parity, cluster_scope)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, cluster_scope)) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+            *abort = 1;
+            atomicExch(status, code);
+            return false;
+        }
+    }
+}
 // TMA load into this CTA's shared memory whose completion is signalled on an
 // mbarrier that may live in the peer CTA of the pair (shared::cluster address).
 __device__ __forceinline__ void tma_load_3d_pair(void* smem_dst, const CUtensorMap* map, uint32_t bar_cluster_saddr,
@@ -255,6 +298,17 @@ __device__ __forceinline__ void tma_load_3d_pair(void* smem_dst, const CUtensorM
         "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar_cluster_saddr)
+        : "memory");
+}
+// As tma_load_3d_pair, multicast: the box lands at the same shared-memory offset in
+// every CTA of ctaMask, and each landing signals the mbarrier at bar's offset in the
+// even CTA of the destination's pair.
+__device__ __forceinline__ void tma_load_3d_pair_mc(void* smem_dst, const CUtensorMap* map, uint32_t bar_cluster_saddr,
+                                                    int x, int y, int z, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        ".cta_group::2 [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar_cluster_saddr), "h"(mask)
         : "memory");
 }
 // TMEM allocation shared by the CTA pair: one warp of EACH CTA executes it.

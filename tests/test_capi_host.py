@@ -68,7 +68,7 @@ def test_plan_create_rejects_bad_arguments_before_cuda():
     assert lib.muon_step_host(None, None, None, None, None, None, 0.1, 0.1, 0.9, 5, 0, None) == \
         mu.MUON_ERR_INVALID_ARG
     one = (mu.MuonShape * 1)(mu.MuonShape(4, 8))
-    for bad in (mu.MuonPlanOpts(chunks=-1), mu.MuonPlanOpts(reserved=1)):
+    for bad in (mu.MuonPlanOpts(chunks=-1), mu.MuonPlanOpts(workspace_bytes=-1)):
         assert lib.muon_plan_create(one, 1, mu.MUON_BF16, ctypes.byref(bad), ctypes.byref(h)) == \
             mu.MUON_ERR_INVALID_ARG
     big = (mu.MuonShape * 1)(mu.MuonShape(1 << 21, 4))

@@ -629,3 +629,31 @@ def test_step_host_without_copy_back_and_argument_checks():
     for i in range(len(shapes)):
         assert torch.equal(W[i].cpu(), W_ref[i]) and torch.equal(M[i].cpu(), M_ref[i]), i
     plan.close()
+
+
+@pytest.mark.parametrize("shapes", [
+    [(512, 1024), (1024, 2000), (2000, 1024), (300, 700), (512, 4000)],   # even tile rows: clusters of two pairs
+    [(512, 1024), (700, 900), (128, 3584)],                              # an odd tile-row count: pairs only
+])
+def test_quad_clusters_match_pair_clusters_bitwise(shapes):
+    """The final product in clusters of two CTA pairs sharing X0 by TMA multicast gives
+    bitwise the results of clusters of one pair (same MMAs in the same order), and
+    matches the oracle."""
+    import matrix_orthogonalising_optimizer_muon_gb300 as lib
+    qplan = lib.MuonPlan(shapes, "bf16", keep_update=True, quad_clusters=True)
+    assert qplan.info()["quad_clusters"] >= 16
+    quad = run_step(shapes, "bf16", base_seed=51, plan=qplan)
+    plan = lib.MuonPlan(shapes, "bf16", keep_update=True)
+    assert plan.info()["quad_clusters"] == 0
+    pair = run_step(shapes, "bf16", inputs=quad["inputs"], plan=plan)
+    for i in range(len(shapes)):
+        assert torch_equal(quad["W"][i], pair["W"][i]), shapes[i]
+        assert torch_equal(quad["O"][i], pair["O"][i]), shapes[i]
+        assert_ns(quad, i)
+    plan.close()
+    qplan.close()
+
+
+def torch_equal(a, b):
+    import torch
+    return torch.equal(a, b)
