@@ -37,6 +37,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen7b_28l")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-tune", action="store_true",
+                    help="skip muon_plan_tune (the plan's launch choices from its work estimate)")
     ap.add_argument("--quad-clusters", action="store_true",
                     help="final product in clusters of two CTA pairs sharing X0 by TMA multicast")
     ap.add_argument("--e2e-chunks", type=int, default=16,
@@ -280,6 +282,8 @@ def run_ours(args, rank, world, local):
     lr, wd, mu = workloads.LR, workloads.WD, workloads.MU
     stream = torch.cuda.current_stream()
     plan.bind(W, G, M)
+    if not args.no_tune:   # plan-time tuning on the resident inputs (its steps precede the warm-up)
+        plan.tune(W, G, M, workloads.LR, workloads.WD, workloads.MU, reps=2, stream=torch.cuda.current_stream())
 
     def one_step(t):
         if wl.rownorm_k and t % wl.rownorm_k != 0:
@@ -411,7 +415,9 @@ def report_ours(args, res, rank, world):
                          (sum(m * n for m, n in shapes) * (10 if wl.grad_dtype == "bf16" else 12) / 1e9),
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "workspace_bytes": res["plan"].info()["workspace_bytes"],
-                   "quad_clusters": res["plan"].info()["quad_clusters"]},
+                   "quad_clusters": res["plan"].info()["quad_clusters"],
+                   "tuned_candidates": res["plan"].info()["tuned_candidates"],
+                   "chain_clusters": res["plan"].info()["chain_clusters"]},
         "stages_ms_per_ns_step": {"momentum_norm": round(per_ns[0], 3), "syrk": round(per_ns[1], 3),
                                   "ns_rxr": round(per_ns[2], 3), "final_apply": round(per_ns[3], 3),
                                   "fused_small": round(per_ns[5], 3)},

@@ -196,6 +196,22 @@ muon_status muon_rownorm_step(muon_plan p, float* const* params, const void* con
                               float eps, void* stream);
 
 /*
+ * muon_plan_tune - a profiled planner (DMuon's per-shape autotuning, on one GPU): times
+ * the plan's launch choices that change only speed on the caller's buffers and keeps
+ * the fastest.  Candidates: for chunks holding both fused (min(m, n) <= 128) and
+ * batched matrices, the CTA pairs the batched products get beside the fused kernel
+ * (none, the work estimate's choice, half and one and a half times it; only when
+ * opts.chain_clusters is 0), and final products in clusters of two CTA pairs or not.
+ * Every candidate gives bitwise the same results.  Each candidate runs one warm-up
+ * and `reps` timed NS steps (ns_steps 5): params and momentum are updated as by that
+ * many ordinary steps, so tune on scratch copies or count the calls as training
+ * steps.  reps in [1, 100]; *ms_out (may be NULL) receives the chosen candidate's ms
+ * per step.  Synchronises stream; errors as muon_step (MUON_ERR_INVALID_ARG for reps).
+ */
+muon_status muon_plan_tune(muon_plan p, float* const* params, const void* const* grads, float* const* momentum,
+                           float lr, float wd, float mu, int32_t reps, float* ms_out, void* stream);
+
+/*
  * muon_sync - wait for the plan's work on stream, then read and clear the
  * device status word.  Returns MUON_ERR_TIMEOUT if a bounded device wait
  * expired since the last muon_sync, MUON_ERR_CUDA on a CUDA error.
@@ -275,7 +291,9 @@ typedef struct {
     int32_t launches_last_step;   /* kernels the last step enqueued */
     int32_t sm_count;
     int32_t n_chunks;             /* chunks the NS step runs in (opts.chunks, opts.workspace_bytes) */
-    int32_t quad_clusters;        /* co-resident clusters of two CTA pairs (0: not used) */
+    int32_t quad_clusters;        /* clusters of two CTA pairs the final products use (0: not used) */
+    int32_t tuned_candidates;     /* launch choices muon_plan_tune measured (0: never tuned) */
+    int32_t chain_clusters;       /* CTA pairs the batched products get beside the fused kernel (0: none) */
 } muon_plan_info_t;
 
 muon_status muon_plan_info(muon_plan p, muon_plan_info_t* info);

@@ -51,7 +51,8 @@ class MuonPlanOpts(ctypes.Structure):
 class MuonPlanInfo(ctypes.Structure):
     _fields_ = [("n_matrices", ctypes.c_int32), ("n_buckets", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64), ("launches_last_step", ctypes.c_int32),
-                ("sm_count", ctypes.c_int32), ("n_chunks", ctypes.c_int32), ("quad_clusters", ctypes.c_int32)]
+                ("sm_count", ctypes.c_int32), ("n_chunks", ctypes.c_int32), ("quad_clusters", ctypes.c_int32),
+                ("tuned_candidates", ctypes.c_int32), ("chain_clusters", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -71,6 +72,8 @@ EXPORTED = {
     "muon_rownorm_step": (ctypes.c_int, [_P, _PP, _PP, _PP, ctypes.c_float, ctypes.c_float,
                                          ctypes.c_float, ctypes.c_float, _P]),
     "muon_sync": (ctypes.c_int, [_P, _P]),
+    "muon_plan_tune": (ctypes.c_int, [_P, _PP, _PP, _PP, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                      ctypes.c_int32, ctypes.POINTER(ctypes.c_float), _P]),
     "muon_debug_copy_update": (ctypes.c_int, [_P, ctypes.c_int32, _P, _P]),
     "muon_debug_copy_workspace": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int32, _P,
                                                  ctypes.POINTER(ctypes.c_int32), _P]),
@@ -262,6 +265,16 @@ class MuonPlan:
         """``muon_step`` / ``muon_step_ex`` / ``muon_rownorm_step`` on the tensors given to ``bind``."""
         w, g, m = self._bound
         self._step(w, g, m, lr, wd, mu, ns_steps, mode, eps, stream, coeffs, restart)
+
+    def tune(self, params, grads, momentum, lr: float, wd: float, mu: float = DEFAULT_MU, reps: int = 3,
+             stream=None) -> float:
+        """``muon_plan_tune``: time the plan's speed-only launch choices on these tensors (each
+        candidate runs 1 + reps NS steps on them) and keep the fastest; returns its ms per step."""
+        w, g, m = self._pointers(params, grads, momentum)
+        ms = ctypes.c_float()
+        _check(self.lib.muon_plan_tune(self.handle, w, g, m, lr, wd, mu, int(reps), ctypes.byref(ms),
+                                       _stream_handle(stream)), "muon_plan_tune")
+        return ms.value
 
     def sync(self, stream=None):
         _check(self.lib.muon_sync(self.handle, _stream_handle(stream)), "muon_sync")

@@ -144,7 +144,9 @@ struct muon_plan_s {
     int device = 0;
     int sm_count = 0;
     int pair_clusters = 0;   // co-resident CTA pairs for the 2-SM kernel (0: 1-SM kernel only)
-    int quad_clusters = 0;   // co-resident clusters of two pairs (0: never used)
+    int quad_max = 0;        // co-resident clusters of two pairs
+    bool use_quad = false;   // final products in clusters of two pairs (opts.quad_clusters or muon_plan_tune)
+    int tuned = 0;           // candidates muon_plan_tune measured (0: not tuned)
     // fused (r <= 128) and batched matrices in one chunk: the batched products' stream
     // and fork/join events (created when a chunk overlaps the two)
     cudaStream_t s2 = nullptr;
@@ -177,6 +179,8 @@ struct muon_plan_s {
         ListDev mom_rows, mom_tiles, all;
         ListDev rn_rows, rn_stats, rn_final, rn_apply;   // RowNorm of this chunk (muon_step_host)
         int chain_clusters = 0;   // CTA pairs for the batched products beside the fused kernel
+        int chain_est = 0;        // the work estimate's choice (chunks with fused and batched work)
+        bool mixed = false;       // the chunk holds both fused and batched matrices
     };
     std::vector<Chunk> chunks;
 
@@ -390,7 +394,7 @@ struct Grouper {
         // clusters of two pairs sharing B (multicast) when enabled, the launch has the
         // whole GPU, and every problem is a non-symmetric product with an MN-major B and
         // an even number of tile rows
-        const int quads = std::min(clusters / 2, p->quad_clusters);
+        const int quads = p->use_quad ? std::min(clusters / 2, p->quad_max) : 0;
         bool quad = quads >= 1 && clusters == p->pair_clusters;
         for (int i = 0; quad && i < L2.nprob; ++i) {
             const GemmProblem& q = L2.prob[i];
@@ -828,13 +832,14 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
         int clusters = 0;
         ok = gemm2_max_clusters(&clusters, 2) == cudaSuccess;
         p->pair_clusters = clusters;
-        if (ok && p->opts.quad_clusters) {
+        if (ok) {
             int quads = 0;
             ok = gemm2_max_clusters(&quads, 4) == cudaSuccess;
-            p->quad_clusters = quads;
+            p->quad_max = quads;
+            p->use_quad = p->opts.quad_clusters != 0 && quads > 0;
         }
     }
-    if (ok && p->pair_clusters > 1 && p->opts.chain_clusters >= 0) {
+    if (ok && p->pair_clusters > 1) {
         bool any = false;
         for (auto& ch : p->chunks) {
             double fused_bytes = 0, chain_flops = 0;
@@ -847,11 +852,14 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
                     chain_flops += (3.0 * r * r * c + 17.0 * r * r * r) * b.batch;
             }
             if (fused_bytes > 0 && chain_flops > 0) {
-                int k = p->opts.chain_clusters;
-                if (k == 0) k = choose_chain_clusters(fused_bytes, chain_flops, p->pair_clusters);
-                k = std::min(k, std::min(p->pair_clusters - 1, (p->sm_count - 2) / 2));
-                ch.chain_clusters = std::max(k, 0);
-                any = any || k > 0;
+                const int kmax = std::min(p->pair_clusters - 1, (p->sm_count - 2) / 2);
+                ch.mixed = true;
+                ch.chain_est = std::max(std::min(choose_chain_clusters(fused_bytes, chain_flops, p->pair_clusters),
+                                                 kmax), 0);
+                const int k = p->opts.chain_clusters == 0 ? ch.chain_est
+                                                          : std::min(std::max(p->opts.chain_clusters, 0), kmax);
+                ch.chain_clusters = k;
+                any = true;   // the second stream also serves muon_plan_tune's candidates
             }
         }
         if (any)
@@ -1332,6 +1340,68 @@ muon_status muon_step_host(muon_plan p, float* const* params, const void* const*
     return MUON_OK;
 }
 
+muon_status muon_plan_tune(muon_plan p, float* const* params, const void* const* grads, float* const* momentum,
+                           float lr, float wd, float mu, int32_t reps, float* ms_out, void* stream) {
+    if (!p || reps < 1 || reps > 100) return MUON_ERR_INVALID_ARG;
+    muon_status st = check_pointers(p, params, grads, momentum);
+    if (st != MUON_OK) return st;
+    // candidates: CTA pairs beside the fused kernel (none, the estimate, half and one and a
+    // half times it; only while opts.chain_clusters leaves the choice to the plan) and
+    // final products in clusters of two pairs or not
+    bool mixed = false;
+    for (const auto& ch : p->chunks) mixed = mixed || (ch.mixed && ch.chain_est > 0);
+    std::vector<float> scales = {1.f};
+    if (mixed && p->opts.chain_clusters == 0 && p->s2) scales = {1.f, 0.f, 0.5f, 1.5f};
+    std::vector<bool> quads = {p->use_quad};
+    if (p->quad_max > 0) quads = {false, true};
+    const int kmax = std::min(p->pair_clusters - 1, (p->sm_count - 2) / 2);
+    auto apply = [&](float sc, bool q) {
+        for (auto& ch : p->chunks)
+            if (ch.mixed && p->opts.chain_clusters == 0)
+                ch.chain_clusters = sc == 0.f ? 0 : std::min(std::max((int)std::lround(ch.chain_est * sc), 1), kmax);
+        p->use_quad = q;
+    };
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+        g_last_cuda_error = cudaGetLastError();
+        if (e0) cudaEventDestroy(e0);
+        return MUON_ERR_CUDA;
+    }
+    float best = 0.f, best_sc = 1.f;
+    bool best_q = p->use_quad;
+    int tried = 0;
+    for (float sc : scales) {
+        for (bool q : quads) {
+            apply(sc, q);
+            st = muon_step_ex(p, params, grads, momentum, lr, wd, mu, kMaxNsSteps, nullptr, 0, stream);   // warm-up
+            if (st == MUON_OK && cudaEventRecord(e0, s) != cudaSuccess) st = MUON_ERR_CUDA;
+            for (int i = 0; st == MUON_OK && i < reps; ++i)
+                st = muon_step_ex(p, params, grads, momentum, lr, wd, mu, kMaxNsSteps, nullptr, 0, stream);
+            float ms = 0.f;
+            if (st == MUON_OK && (cudaEventRecord(e1, s) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
+                                  cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess))
+                st = MUON_ERR_CUDA;
+            if (st != MUON_OK) break;
+            ms /= (float)reps;
+            if (tried == 0 || ms < best) {
+                best = ms;
+                best_sc = sc;
+                best_q = q;
+            }
+            ++tried;
+        }
+        if (st != MUON_OK) break;
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    apply(best_sc, best_q);
+    if (st != MUON_OK) return st;
+    p->tuned = tried;
+    if (ms_out) *ms_out = best;
+    return muon_sync(p, stream);
+}
+
 muon_status muon_sync(muon_plan p, void* stream) {
     if (!p) return MUON_ERR_INVALID_ARG;
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MUON_ERR_CUDA;
@@ -1400,7 +1470,11 @@ muon_status muon_plan_info(muon_plan p, muon_plan_info_t* info) {
     info->workspace_bytes = (int64_t)p->ws_bytes;
     info->launches_last_step = p->last_launches;
     info->n_chunks = (int32_t)p->chunks.size();
-    info->quad_clusters = p->quad_clusters;
+    info->quad_clusters = p->use_quad ? p->quad_max : 0;
+    info->tuned_candidates = p->tuned;
+    int chain = 0;
+    for (const auto& ch : p->chunks) chain = std::max(chain, ch.chain_clusters);
+    info->chain_clusters = chain;
     info->sm_count = p->sm_count;
     return MUON_OK;
 }

@@ -65,6 +65,7 @@ def test_plan_create_rejects_bad_arguments_before_cuda():
     assert lib.muon_plan_create(None, 1, mu.MUON_BF16, None, ctypes.byref(h)) == mu.MUON_ERR_INVALID_ARG
     assert lib.muon_step(None, None, None, None, 0.1, 0.1, 0.9, 5, 0, None) == mu.MUON_ERR_INVALID_ARG
     assert lib.muon_sync(None, None) == mu.MUON_ERR_INVALID_ARG
+    assert lib.muon_plan_tune(None, None, None, None, 0.1, 0.1, 0.9, 3, None, None) == mu.MUON_ERR_INVALID_ARG
     assert lib.muon_step_host(None, None, None, None, None, None, 0.1, 0.1, 0.9, 5, 0, None) == \
         mu.MUON_ERR_INVALID_ARG
     one = (mu.MuonShape * 1)(mu.MuonShape(4, 8))

@@ -657,3 +657,29 @@ def test_quad_clusters_match_pair_clusters_bitwise(shapes):
 def torch_equal(a, b):
     import torch
     return torch.equal(a, b)
+
+
+def test_plan_tune_keeps_results_bitwise():
+    """muon_plan_tune times the speed-only launch choices (CTA pairs beside the fused kernel,
+    clusters of two pairs for the final product) and keeps the fastest; a step of the tuned
+    plan gives bitwise the results of the untuned plan."""
+    import torch
+    import matrix_orthogonalising_optimizer_muon_gb300 as lib
+    shapes = [(128, 3584)] * 64 + [(3584, 512)] * 4 + [(1024, 2048)] * 2
+    inputs = host_inputs(shapes, "bf16", 71)
+    ref = run_step(shapes, "bf16", inputs=inputs)
+    plan = lib.MuonPlan(shapes, "bf16", keep_update=True)
+    W = [w.cuda() for w, _, _ in inputs]
+    G = [g.cuda() for _, g, _ in inputs]
+    M = [m.cuda() for _, _, m in inputs]
+    ms = plan.tune(W, G, M, LR, WD, MU, reps=2)
+    info = plan.info()
+    assert ms > 0 and info["tuned_candidates"] >= 2, (ms, info)
+    res = run_step(shapes, "bf16", inputs=inputs, plan=plan)
+    for i in range(len(shapes)):
+        assert torch.equal(res["W"][i], ref["W"][i]), (i, info)
+        assert torch.equal(res["M"][i], ref["M"][i]), (i, info)
+        assert torch.equal(res["O"][i], ref["O"][i]), (i, info)
+    with pytest.raises(lib.MuonError):
+        plan.tune(W, G, M, LR, WD, MU, reps=0)
+    plan.close()
