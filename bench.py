@@ -306,10 +306,12 @@ def run_ours(args, rank, world, local):
     barrier(world)
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev_step = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]   # end of each step
     launches = 0
     ev0.record(stream)
     for t in range(args.steps):
         one_step(args.warmup + t)
+        ev_step[t].record(stream)
         launches += plan.info()["launches_last_step"]
     ev1.record(stream)
     torch.cuda.synchronize()
@@ -319,7 +321,9 @@ def run_ours(args, rank, world, local):
     stage_ms, stage_fl = plan.stage_times()   # per-stage event times summed over the K steps
     elapsed_ms = ev0.elapsed_time(ev1)
     ms_step = max_over_ranks(elapsed_ms / args.steps, world)
-    return dict(wl=wl, shapes=shapes, plan=plan, W=W, G=G, M=M, ms_step=ms_step, stage_ms=stage_ms,
+    per_step = [(ev0 if t == 0 else ev_step[t - 1]).elapsed_time(ev_step[t]) for t in range(args.steps)]
+    return dict(wl=wl, shapes=shapes, plan=plan, W=W, G=G, M=M, ms_step=ms_step, per_step=per_step,
+                stage_ms=stage_ms,
                 stage_fl=stage_fl, launches=launches, clocks=clk, peaks=peaks, peak_src=peak_src,
                 setup_s=setup_s, one_step=one_step)
 
@@ -421,6 +425,8 @@ def report_ours(args, res, rank, world):
         "stages_ms_per_ns_step": {"momentum_norm": round(per_ns[0], 3), "syrk": round(per_ns[1], 3),
                                   "ns_rxr": round(per_ns[2], 3), "final_apply": round(per_ns[3], 3),
                                   "fused_small": round(per_ns[5], 3)},
+        "ms_per_step_median": round(statistics.median(res["per_step"]), 3),
+        "ms_per_step_min": round(min(res["per_step"]), 3),
         "ns_steps_timed": n_ns,
         "roofline": roofline,
         "gpu_launches": res["launches"],

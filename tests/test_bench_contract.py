@@ -57,4 +57,5 @@ def test_our_arm_line_has_roofline_baseline_e2e_and_clocks():
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] == 256 * 1024 * 4
     assert e2e["d2h_bytes_per_step"] == 256 * 1024 * 4
     assert d["gpu_launches"] > 0
+    assert 0 < d["ms_per_step_min"] <= d["ms_per_step_median"]
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
