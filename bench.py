@@ -39,8 +39,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-tune", action="store_true",
                     help="skip muon_plan_tune (the plan's launch choices from its work estimate)")
-    ap.add_argument("--quad-clusters", action="store_true",
-                    help="final product in clusters of two CTA pairs sharing X0 by TMA multicast")
+    ap.add_argument("--full-symmetric", action="store_true",
+                    help="symmetric r x r results stored whole (no lower-triangle storage)")
     ap.add_argument("--e2e-chunks", type=int, default=16,
                     help="chunks of the e2e plan (host copies of one chunk overlap another's compute)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -276,7 +276,7 @@ def run_ours(args, rank, world, local):
         G.append(workloads.gen_tensor((m, n), workloads.G_STD, workloads.seed_of(wl.index, 0, i, "G"), dev,
                                       wl.grad_dtype))
     plan = lib.MuonPlan(shapes, wl.grad_dtype, timing=True, workspace_bytes=args.workspace_bytes,
-                        quad_clusters=args.quad_clusters)
+                        full_symmetric=args.full_symmetric)
     torch.cuda.synchronize()
     setup_s = time.time() - t0
     lr, wd, mu = workloads.LR, workloads.WD, workloads.MU
@@ -419,7 +419,7 @@ def report_ours(args, res, rank, world):
                          (sum(m * n for m, n in shapes) * (10 if wl.grad_dtype == "bf16" else 12) / 1e9),
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "workspace_bytes": res["plan"].info()["workspace_bytes"],
-                   "quad_clusters": res["plan"].info()["quad_clusters"],
+                   "lower_chunks": res["plan"].info()["lower_chunks"],
                    "tuned_candidates": res["plan"].info()["tuned_candidates"],
                    "chain_clusters": res["plan"].info()["chain_clusters"]},
         "stages_ms_per_ns_step": {"momentum_norm": round(per_ns[0], 3), "syrk": round(per_ns[1], 3),

@@ -95,13 +95,12 @@ typedef struct {
        compute.  Results are the same.  0 or 1: chunks only as workspace_bytes
        requires.  Negative: MUON_ERR_INVALID_ARG. */
     int32_t chunks;
-    /* nonzero: the final product O = Q X0 runs in clusters of two CTA pairs that load
-       their shared X0 columns once (TMA multicast), when every problem of its launch
-       has an even number of 256-row tiles (r a multiple of 512) and the launch has the
-       whole GPU.  Results are the same.  Off by default: only 36 such clusters fit on
-       the 152 SMs (144 SMs), and on GB300 the product ran 2-3 % slower than on 76
-       single-pair clusters.  0: every product in clusters of one CTA pair. */
-    int32_t quad_clusters;
+    /* nonzero: symmetric r x r results (G, P, T, Q) stored whole on every launch.  0:
+       chunks whose batched matrices have r and c multiples of 64 store them as their
+       lower triangle (256 x 256 tiles at or below the diagonal; the products read the
+       blocks above it from the mirror position), which saves the mirrored half of the
+       epilogue's stores.  Results are the same. */
+    int32_t full_symmetric;
 } muon_plan_opts;
 
 typedef struct muon_plan_s* muon_plan;
@@ -201,7 +200,8 @@ muon_status muon_rownorm_step(muon_plan p, float* const* params, const void* con
  * the fastest.  Candidates: for chunks holding both fused (min(m, n) <= 128) and
  * batched matrices, the CTA pairs the batched products get beside the fused kernel
  * (none, the work estimate's choice, half and one and a half times it; only when
- * opts.chain_clusters is 0), and final products in clusters of two CTA pairs or not.
+ * opts.chain_clusters is 0), and symmetric results stored as the lower triangle or
+ * whole (chunks where opts.full_symmetric leaves the choice).
  * Every candidate gives bitwise the same results.  Each candidate runs one warm-up
  * and `reps` timed NS steps (ns_steps 5): params and momentum are updated as by that
  * many ordinary steps, so tune on scratch copies or count the calls as training
@@ -291,7 +291,7 @@ typedef struct {
     int32_t launches_last_step;   /* kernels the last step enqueued */
     int32_t sm_count;
     int32_t n_chunks;             /* chunks the NS step runs in (opts.chunks, opts.workspace_bytes) */
-    int32_t quad_clusters;        /* clusters of two CTA pairs the final products use (0: not used) */
+    int32_t lower_chunks;         /* chunks storing symmetric results as the lower triangle */
     int32_t tuned_candidates;     /* launch choices muon_plan_tune measured (0: never tuned) */
     int32_t chain_clusters;       /* CTA pairs the batched products get beside the fused kernel (0: none) */
 } muon_plan_info_t;

@@ -45,13 +45,13 @@ class MuonPlanOpts(ctypes.Structure):
                 ("single_sm_gemm", ctypes.c_int32), ("generic_small", ctypes.c_int32),
                 ("chain_clusters", ctypes.c_int32), ("max_ns_steps", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64), ("chunks", ctypes.c_int32),
-                ("quad_clusters", ctypes.c_int32)]
+                ("full_symmetric", ctypes.c_int32)]
 
 
 class MuonPlanInfo(ctypes.Structure):
     _fields_ = [("n_matrices", ctypes.c_int32), ("n_buckets", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64), ("launches_last_step", ctypes.c_int32),
-                ("sm_count", ctypes.c_int32), ("n_chunks", ctypes.c_int32), ("quad_clusters", ctypes.c_int32),
+                ("sm_count", ctypes.c_int32), ("n_chunks", ctypes.c_int32), ("lower_chunks", ctypes.c_int32),
                 ("tuned_candidates", ctypes.c_int32), ("chain_clusters", ctypes.c_int32)]
 
 
@@ -149,14 +149,14 @@ class MuonPlan:
     def __init__(self, shapes, grad_dtype: str = "bf16", keep_update: bool = False,
                  timing: bool = False, single_sm_gemm: bool = False, generic_small: bool = False,
                  chain_clusters: int = 0, workspace_bytes: int = 0, max_ns_steps: int = 0, chunks: int = 0,
-                 quad_clusters: bool = False):
+                 full_symmetric: bool = False):
         self.lib = load()
         self.shapes = [(int(m), int(n)) for m, n in shapes]
         self.grad_dtype = grad_dtype
         arr = (MuonShape * len(self.shapes))(*[MuonShape(m, n) for m, n in self.shapes])
         opts = MuonPlanOpts(1 if keep_update else 0, 1 if timing else 0, 1 if single_sm_gemm else 0,
                             1 if generic_small else 0, int(chain_clusters), int(max_ns_steps),
-                            int(workspace_bytes), int(chunks), 1 if quad_clusters else 0)
+                            int(workspace_bytes), int(chunks), 1 if full_symmetric else 0)
         h = ctypes.c_void_p()
         gd = {"bf16": MUON_BF16, "f32": MUON_F32}[grad_dtype]
         _check(self.lib.muon_plan_create(arr, len(self.shapes), gd, ctypes.byref(opts),

@@ -72,6 +72,23 @@ bool make_map(CUtensorMap* map, void* base, bool bf16, uint64_t inner, uint64_t 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D view (64 columns, rows, cols / 64 column chunks, batch) of `batch` row-major
+// matrices with cols % 64 == 0, so every box stays inside its rows: boxes (64, 128, 1, 1)
+// are K-major operand blocks at (0, row, k / 64, item), boxes (64, 64, 2, 1) two 64-column
+// chunks of 64 rows (an MN-major operand block, or a mirrored one) at (0, k, row / 64, item).
+bool make_map4(CUtensorMap* map, void* base, bool bf16, uint64_t cols, uint64_t rows, uint64_t batch, uint64_t ld,
+               uint32_t box_rows, uint32_t box_chunks) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || cols % 64 != 0) return false;
+    cuuint64_t dims[4] = {64, rows, cols / 64, batch};
+    cuuint64_t strides[3] = {ld * 2, 128, ld * rows * 2};
+    cuuint32_t box[4] = {64, box_rows, box_chunks, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, base, dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Store map over `batch` r x r row-major matrices (leading dim ld): 32 x 32 boxes
 // in the 64-byte-swizzled shared layout the pair kernel's epilogue stages.
 bool make_out_map(CUtensorMap* map, void* base, bool bf16, uint64_t r, uint64_t batch, uint64_t ld) {
@@ -129,6 +146,9 @@ struct Bucket {
     CUtensorMap ga[2], gb[2], pa, pb, tb, qb[2];
     CUtensorMap qa[2], ta;   // 128-row boxes of Q and T (B halves of the CTA-pair kernel)
     CUtensorMap og[2], op, ot, oq[2], oqb;   // store maps of G, P, T, Q (fp16) and Qb (bf16)
+    // 4-D maps of lower-triangle launches (r % 64 == 0 and c % 64 == 0): K-major (..k) and
+    // mirror / MN-major (..t) boxes of X0, the second X buffer and the r x r buffers
+    CUtensorMap utk, utt, ut1k, ut1t, gk[2], gt[2], pk, pt, tk, tt, qk[2], qt[2], qbk, qbt;
 };
 
 struct ListDev {
@@ -144,8 +164,6 @@ struct muon_plan_s {
     int device = 0;
     int sm_count = 0;
     int pair_clusters = 0;   // co-resident CTA pairs for the 2-SM kernel (0: 1-SM kernel only)
-    int quad_max = 0;        // co-resident clusters of two pairs
-    bool use_quad = false;   // final products in clusters of two pairs (opts.quad_clusters or muon_plan_tune)
     int tuned = 0;           // candidates muon_plan_tune measured (0: not tuned)
     // fused (r <= 128) and batched matrices in one chunk: the batched products' stream
     // and fork/join events (created when a chunk overlaps the two)
@@ -181,6 +199,8 @@ struct muon_plan_s {
         int chain_clusters = 0;   // CTA pairs for the batched products beside the fused kernel
         int chain_est = 0;        // the work estimate's choice (chunks with fused and batched work)
         bool mixed = false;       // the chunk holds both fused and batched matrices
+        bool lower_ok = false;    // every batched bucket on the pair kernel has r and c multiples of 64
+        bool lower = false;       // its pair-kernel products store symmetric results as the lower triangle
     };
     std::vector<Chunk> chunks;
 
@@ -329,19 +349,27 @@ GemmProblem problem(int M, int N, int K, int batch, bool sym, int epi) {
     return q;
 }
 
+// 4-D maps of one operand for lower-triangle launches.
+struct Maps4 {
+    const CUtensorMap* k = nullptr;   // K-major boxes (64, 128, 1, 1)
+    const CUtensorMap* t = nullptr;   // mirror / MN-major boxes (64, 64, 2, 1)
+    bool sym = false;                 // a symmetric buffer stored as its lower triangle
+};
+
 // Collects problems into grouped launches of up to kMaxProblems.
 struct Grouper {
     muon_plan_s* p;
     cudaStream_t s;
     bool bf16;
+    bool lower;         // lower-triangle launches (the chunk's Chunk::lower)
     int clusters = 0;   // CTA pairs for the pair kernel, CTAs for the one-SM kernel
     int grid1 = 0;
     GemmLaunch L1;   // 1-SM kernel, 128 x 256 tiles
     GemmLaunch L2;   // CTA-pair kernel, 256 x 256 tiles
     muon_status st = MUON_OK;
     int launches = 0;
-    Grouper(muon_plan_s* plan, cudaStream_t stream, bool is_bf16, int pair_clusters, int sm_grid)
-        : p(plan), s(stream), bf16(is_bf16), clusters(pair_clusters), grid1(sm_grid) {
+    Grouper(muon_plan_s* plan, cudaStream_t stream, bool is_bf16, bool lower_tri, int pair_clusters, int sm_grid)
+        : p(plan), s(stream), bf16(is_bf16), lower(lower_tri), clusters(pair_clusters), grid1(sm_grid) {
         reset(L1);
         reset(L2);
     }
@@ -362,8 +390,10 @@ struct Grouper {
     // CTA-pair kernel (each CTA loads 128 rows of A and 128 of B).
     // oc / oc2: store maps of a symmetric problem's outputs (tma_out set by the
     // caller); the pair kernel then writes them with TMA stores.
+    // a4 / b4: the operands' 4-D maps, used by lower-triangle launches (B of an
+    // MN-major problem through b4.t).
     void add(const CUtensorMap& a128, const CUtensorMap& b256, const CUtensorMap& b128, GemmProblem q,
-             const CUtensorMap* oc = nullptr, const CUtensorMap* oc2 = nullptr) {
+             const CUtensorMap* oc, const CUtensorMap* oc2, Maps4 a4, Maps4 b4) {
         if (q.M > kBM && p->pair_clusters > 0) {
             if (L2.nprob == kMaxProblems) flush2();
             q.tiles_m = (int)ceil_div(q.M, 256);
@@ -374,7 +404,16 @@ struct Grouper {
                 L2.mapC[L2.nprob] = *oc;
                 if (oc2) L2.mapC2[L2.nprob] = *oc2;
             }
-            push(L2, a128, b128, q);
+            if (lower) {
+                q.lower_out = q.sym;
+                q.sym_a = a4.sym;
+                q.sym_b = b4.sym && !q.b_mn;
+                L2.mapAt[L2.nprob] = a4.t ? *a4.t : *a4.k;
+                L2.mapBt[L2.nprob] = b4.t ? *b4.t : *b4.k;
+                push(L2, *a4.k, b4.k ? *b4.k : *b4.t, q);
+            } else {
+                push(L2, a128, b128, q);
+            }
         } else {
             if (L1.nprob == kMaxProblems) flush1();
             q.tma_out = 0;
@@ -391,26 +430,8 @@ struct Grouper {
     }
     void flush2() {
         if (L2.nprob == 0) return;
-        // clusters of two pairs sharing B (multicast) when enabled, the launch has the
-        // whole GPU, and every problem is a non-symmetric product with an MN-major B and
-        // an even number of tile rows
-        const int quads = p->use_quad ? std::min(clusters / 2, p->quad_max) : 0;
-        bool quad = quads >= 1 && clusters == p->pair_clusters;
-        for (int i = 0; quad && i < L2.nprob; ++i) {
-            const GemmProblem& q = L2.prob[i];
-            quad = q.b_mn && !q.sym && q.tiles_m % 2 == 0;
-        }
-        if (quad) {   // count super-tiles of two pair tiles
-            L2.total_tiles = 0;
-            for (int i = 0; i < L2.nprob; ++i) {
-                GemmProblem& q = L2.prob[i];
-                q.tiles_per_item = q.tiles_m / 2 * q.tiles_n;
-                q.tile_begin = L2.total_tiles;
-                L2.total_tiles += q.tiles_per_item * q.batch;
-            }
-        }
         if (st == MUON_OK) {
-            st = cuda_status(gemm2_launch(L2, bf16, quad ? 2 * quads : clusters, s, quad));
+            st = cuda_status(gemm2_launch(L2, bf16, clusters, s, lower));
             ++launches;
         }
         reset(L2);
@@ -788,12 +809,21 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
         ok = ok && make_map(&b.ut_a, ut, true, b.c, b.r, b.batch, b.ldu, 64, kBM);
         ok = ok && make_map(&b.ut_b, ut, true, b.c, b.r, b.batch, b.ldu, 64, kBN);
         ok = ok && make_map(&b.ut_mn, ut, true, b.c, b.r, b.batch, b.ldu, 64, 64);
+        const bool aligned4 = !b.fused && b.r % 64 == 0 && b.c % 64 == 0;
+        if (aligned4) {
+            ok = ok && make_map4(&b.utk, ut, true, b.c, b.r, b.batch, b.ldu, 128, 1);
+            ok = ok && make_map4(&b.utt, ut, true, b.c, b.r, b.batch, b.ldu, 64, 2);
+        }
         if (restarts) {
             b.ut1_off = (long long)(o_ut1[k] / 2);
             __nv_bfloat16* ut1 = p->ut + b.ut1_off;
             ok = ok && make_map(&b.ut1_a, ut1, true, b.c, b.r, b.batch, b.ldu, 64, kBM);
             ok = ok && make_map(&b.ut1_b, ut1, true, b.c, b.r, b.batch, b.ldu, 64, kBN);
             ok = ok && make_map(&b.ut1_mn, ut1, true, b.c, b.r, b.batch, b.ldu, 64, 64);
+            if (aligned4) {
+                ok = ok && make_map4(&b.ut1k, ut1, true, b.c, b.r, b.batch, b.ldu, 128, 1);
+                ok = ok && make_map4(&b.ut1t, ut1, true, b.c, b.r, b.batch, b.ldu, 64, 2);
+            }
         }
         if (b.fused) continue;   // the fused kernel keeps its r x r operands on chip
         const size_t rr = (size_t)b.batch * b.r * b.ldr;
@@ -824,20 +854,34 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
         ok = ok && make_out_map(&b.op, b.P, false, b.r, b.batch, b.ldr);
         ok = ok && make_out_map(&b.ot, b.T, false, b.r, b.batch, b.ldr);
         ok = ok && make_out_map(&b.oqb, b.Qb, true, b.r, b.batch, b.ldr);
+        if (aligned4) {
+            auto kt = [&](CUtensorMap* k, CUtensorMap* t, void* buf, bool bf) {
+                return make_map4(k, buf, bf, b.r, b.r, b.batch, b.ldr, 128, 1) &&
+                       make_map4(t, buf, bf, b.r, b.r, b.batch, b.ldr, 64, 2);
+            };
+            for (int g = 0; g < 2; ++g) {
+                ok = ok && kt(&b.gk[g], &b.gt[g], b.G[g], false);
+                ok = ok && kt(&b.qk[g], &b.qt[g], b.Q[g], false);
+            }
+            ok = ok && kt(&b.pk, &b.pt, b.P, false) && kt(&b.tk, &b.tt, b.T, false) && kt(&b.qbk, &b.qbt, b.Qb, true);
+        }
     }
     ok = ok && cudaMallocHost(&p->h_pinned, sizeof(void*) * 3 * n) == cudaSuccess;
     ok = ok && cudaEventCreateWithFlags(&p->upload_ev, cudaEventDisableTiming) == cudaSuccess;
     ok = ok && gemm_prepare(p->device) == cudaSuccess;
     if (ok && !p->opts.single_sm_gemm) {
         int clusters = 0;
-        ok = gemm2_max_clusters(&clusters, 2) == cudaSuccess;
+        ok = gemm2_max_clusters(&clusters) == cudaSuccess;
         p->pair_clusters = clusters;
-        if (ok) {
-            int quads = 0;
-            ok = gemm2_max_clusters(&quads, 4) == cudaSuccess;
-            p->quad_max = quads;
-            p->use_quad = p->opts.quad_clusters != 0 && quads > 0;
+    }
+    for (auto& ch : p->chunks) {   // lower-triangle storage where the 4-D operand view is exact
+        bool aligned = true;
+        for (int k : ch.buckets) {
+            const Bucket& b = p->buckets[k];
+            if (!b.fused && b.r > kBM) aligned = aligned && b.r % 64 == 0 && b.c % 64 == 0;
         }
+        ch.lower_ok = p->pair_clusters > 0 && aligned;
+        ch.lower = ch.lower_ok && !p->opts.full_symmetric;
     }
     if (ok && p->pair_clusters > 1) {
         bool any = false;
@@ -1084,7 +1128,7 @@ static muon_status ns_step(muon_plan p, float* const* params, const void* const*
             const int Js = last ? ns_steps - sg * period : period;
             // ---- G0' = s alpha^2 X0 X0^T (lower triangle, mirrored), all buckets in one launch
             {
-                Grouper g(p, sc, true, gc_clusters, g_grid1);
+                Grouper g(p, sc, true, ch.lower, gc_clusters, g_grid1);
                 for (int bk : ch.buckets) {
                     Bucket& b = p->buckets[bk];
                     if (b.fused) continue;
@@ -1096,9 +1140,9 @@ static muon_status ns_step(muon_plan p, float* const* params, const void* const*
                     q.out_scale = b.gscale;
                     q.tma_out = kTmaOutC;
                     if (xc == 0)
-                        g.add(b.ut_a, b.ut_b, b.ut_a, q, &b.og[0]);
+                        g.add(b.ut_a, b.ut_b, b.ut_a, q, &b.og[0], nullptr, {&b.utk}, {&b.utk});
                     else
-                        g.add(b.ut1_a, b.ut1_b, b.ut1_a, q, &b.og[0]);
+                        g.add(b.ut1_a, b.ut1_b, b.ut1_a, q, &b.og[0], nullptr, {&b.ut1k}, {&b.ut1k});
                 }
                 g.flush();
                 if (g.st != MUON_OK) return g.st;
@@ -1119,7 +1163,7 @@ static muon_status ns_step(muon_plan p, float* const* params, const void* const*
             };
             for (int k = 1; k <= J; ++k) {
                 {   // P = aI + (b/s) G' + (c/s^2) G'^2 (at k = 1 this is also Q_1)
-                    Grouper g(p, sc, false, gc_clusters, g_grid1);
+                    Grouper g(p, sc, false, ch.lower, gc_clusters, g_grid1);
                     for (int bk : ch.buckets) {
                     Bucket& b = p->buckets[bk];
                     if (b.fused) continue;
@@ -1133,14 +1177,15 @@ static muon_status ns_step(muon_plan p, float* const* params, const void* const*
                         q.coef_c = cc / (b.gscale * b.gscale);
                         // fp16 P (and the fp16 copy Q_1): TMA stores; P with a bf16 Q_1 (J = 1): per thread
                         q.tma_out = q.Cb ? 0 : (kTmaOutC | (q.C2 ? kTmaOutC2 : 0));
-                        g.add(b.ga[gc], b.gb[gc], b.ga[gc], q, &b.op, q.C2 ? &b.oq[0] : nullptr);
+                        const Maps4 g4{&b.gk[gc], &b.gt[gc], true};
+                        g.add(b.ga[gc], b.gb[gc], b.ga[gc], q, &b.op, q.C2 ? &b.oq[0] : nullptr, g4, g4);
                     }
                     g.flush();
                     if (g.st != MUON_OK) return g.st;
                     launches += g.launches;
                 }
                 {   // Q' = P Q (k >= 2) and T = P P (k < J), independent: one launch
-                    Grouper g(p, sc, false, gc_clusters, g_grid1);
+                    Grouper g(p, sc, false, ch.lower, gc_clusters, g_grid1);
                     for (int bk : ch.buckets) {
                     Bucket& b = p->buckets[bk];
                     if (b.fused) continue;
@@ -1149,18 +1194,20 @@ static muon_status ns_step(muon_plan p, float* const* params, const void* const*
                             if (k < J) {
                                 q.C = b.Q[qc ^ 1];
                                 q.tma_out = kTmaOutC;
-                                g.add(b.pa, b.qb[qc], b.qa[qc], q, &b.oq[qc ^ 1]);
+                                g.add(b.pa, b.qb[qc], b.qa[qc], q, &b.oq[qc ^ 1], nullptr, {&b.pk, &b.pt, true},
+                                      {&b.qk[qc], &b.qt[qc], true});
                             } else {
                                 q.Cb = b.Qb;
                                 q.tma_out = kTmaOutC | kTmaOutBf16;
-                                g.add(b.pa, b.qb[qc], b.qa[qc], q, &b.oqb);
+                                g.add(b.pa, b.qb[qc], b.qa[qc], q, &b.oqb, nullptr, {&b.pk, &b.pt, true},
+                                      {&b.qk[qc], &b.qt[qc], true});
                             }
                         }
                         if (k < J) {
                             GemmProblem q = rr_problem(b, kEpiPlain);
                             q.C = b.T;
                             q.tma_out = kTmaOutC;
-                            g.add(b.pa, b.pb, b.pa, q, &b.ot);
+                            g.add(b.pa, b.pb, b.pa, q, &b.ot, nullptr, {&b.pk, &b.pt, true}, {&b.pk, &b.pt, true});
                         }
                     }
                     g.flush();
@@ -1169,14 +1216,15 @@ static muon_status ns_step(muon_plan p, float* const* params, const void* const*
                     if (k >= 2) qc ^= 1;
                 }
                 if (k < J) {   // G'' = G' T
-                    Grouper g(p, sc, false, gc_clusters, g_grid1);
+                    Grouper g(p, sc, false, ch.lower, gc_clusters, g_grid1);
                     for (int bk : ch.buckets) {
                     Bucket& b = p->buckets[bk];
                     if (b.fused) continue;
                         GemmProblem q = rr_problem(b, kEpiPlain);
                         q.C = b.G[gc ^ 1];
                         q.tma_out = kTmaOutC;
-                        g.add(b.ga[gc], b.tb, b.ta, q, &b.og[gc ^ 1]);
+                        g.add(b.ga[gc], b.tb, b.ta, q, &b.og[gc ^ 1], nullptr, {&b.gk[gc], &b.gt[gc], true},
+                              {&b.tk, &b.tt, true});
                     }
                     g.flush();
                     if (g.st != MUON_OK) return g.st;
@@ -1197,7 +1245,7 @@ static muon_status ns_step(muon_plan p, float* const* params, const void* const*
             // ---- last segment: O = alpha Q X, fused W <- W - lr (s O + wd W) in the stored
             // layout; earlier segments: X' = alpha Q X (bf16) into the other X buffer
             {
-                Grouper g(p, sc, true, gc_clusters, g_grid1);
+                Grouper g(p, sc, true, ch.lower, gc_clusters, g_grid1);
                 float* const* W = reinterpret_cast<float* const*>(p->d_ptrs + 2 * n);
                 for (int bk : ch.buckets) {
                     Bucket& b = p->buckets[bk];
@@ -1219,7 +1267,8 @@ static muon_status ns_step(muon_plan p, float* const* params, const void* const*
                         q.strideC = (long long)b.r * b.ldu;
                     }
                     const CUtensorMap& xm = xc == 0 ? b.ut_mn : b.ut1_mn;
-                    g.add(b.qb_a, xm, xm, q);
+                    g.add(b.qb_a, xm, xm, q, nullptr, nullptr, {&b.qbk, &b.qbt, true},
+                          {nullptr, xc == 0 ? &b.utt : &b.ut1t});
                 }
                 g.flush();
                 if (g.st != MUON_OK) return g.st;
@@ -1347,19 +1396,21 @@ muon_status muon_plan_tune(muon_plan p, float* const* params, const void* const*
     if (st != MUON_OK) return st;
     // candidates: CTA pairs beside the fused kernel (none, the estimate, half and one and a
     // half times it; only while opts.chain_clusters leaves the choice to the plan) and
-    // final products in clusters of two pairs or not
+    // symmetric r x r results stored as the lower triangle or whole
     bool mixed = false;
     for (const auto& ch : p->chunks) mixed = mixed || (ch.mixed && ch.chain_est > 0);
     std::vector<float> scales = {1.f};
     if (mixed && p->opts.chain_clusters == 0 && p->s2) scales = {1.f, 0.f, 0.5f, 1.5f};
-    std::vector<bool> quads = {p->use_quad};
-    if (p->quad_max > 0) quads = {false, true};
+    bool lower_choice = false;   // chunks where lower-triangle storage is a choice
+    for (const auto& ch : p->chunks) lower_choice = lower_choice || ch.lower_ok;
+    std::vector<bool> quads = {true};
+    if (lower_choice && !p->opts.full_symmetric) quads = {true, false};
     const int kmax = std::min(p->pair_clusters - 1, (p->sm_count - 2) / 2);
     auto apply = [&](float sc, bool q) {
         for (auto& ch : p->chunks)
             if (ch.mixed && p->opts.chain_clusters == 0)
                 ch.chain_clusters = sc == 0.f ? 0 : std::min(std::max((int)std::lround(ch.chain_est * sc), 1), kmax);
-        p->use_quad = q;
+        for (auto& ch : p->chunks) ch.lower = ch.lower_ok && !p->opts.full_symmetric && q;
     };
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaEvent_t e0 = nullptr, e1 = nullptr;
@@ -1369,7 +1420,7 @@ muon_status muon_plan_tune(muon_plan p, float* const* params, const void* const*
         return MUON_ERR_CUDA;
     }
     float best = 0.f, best_sc = 1.f;
-    bool best_q = p->use_quad;
+    bool best_q = true;
     int tried = 0;
     for (float sc : scales) {
         for (bool q : quads) {
@@ -1459,6 +1510,18 @@ muon_status muon_debug_copy_workspace(muon_plan p, int32_t i, int32_t which, voi
         case 8: src = p->alpha + p->mats[i].slot; bytes = 4; *ld = 1; break;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (which >= 1 && which <= 7 && b.r > kBM && p->chunks[b.chunk].lower) {
+        // lower-triangle storage (256 x 256 tiles at or below the diagonal): rebuild the upper part
+        std::vector<uint16_t> h(rr);
+        if (cudaMemcpyAsync(h.data(), src, bytes, cudaMemcpyDefault, s) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess)
+            return MUON_ERR_CUDA;
+        for (int row = 0; row < b.r; ++row)
+            for (int col = (row / 256 + 1) * 256; col < b.r; ++col)
+                h[(size_t)row * b.ldr + col] = h[(size_t)col * b.ldr + row];
+        if (cudaMemcpyAsync(dst, h.data(), bytes, cudaMemcpyDefault, s) != cudaSuccess) return MUON_ERR_CUDA;
+        return cudaStreamSynchronize(s) == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
+    }
     if (cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDefault, s) != cudaSuccess) return MUON_ERR_CUDA;
     return cudaStreamSynchronize(s) == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
 }
@@ -1470,7 +1533,9 @@ muon_status muon_plan_info(muon_plan p, muon_plan_info_t* info) {
     info->workspace_bytes = (int64_t)p->ws_bytes;
     info->launches_last_step = p->last_launches;
     info->n_chunks = (int32_t)p->chunks.size();
-    info->quad_clusters = p->use_quad ? p->quad_max : 0;
+    int lower = 0;
+    for (const auto& ch : p->chunks) lower += ch.lower ? 1 : 0;
+    info->lower_chunks = lower;
     info->tuned_candidates = p->tuned;
     int chain = 0;
     for (const auto& ch : p->chunks) chain = std::max(chain, ch.chain_clusters);

@@ -292,28 +292,22 @@ __device__ __forceinline__ TileCoord decode_pair_tile(const GemmLaunch& L, int t
     return {p, item, tm * 256 + 128 * (int)rank, tn * 256};
 }
 
-// Clusters of four CTAs (two pairs) on non-symmetric problems with an MN-major B
-// and an even number of pair-tile rows: unit u is a super-tile (sm, tn) and pair
-// pr computes tile (2 sm + pr, tn), so both pairs read the same B columns.
-__device__ __forceinline__ TileCoord decode_quad_tile(const GemmLaunch& L, int u, uint32_t pr, uint32_t q) {
-    int p = 0;
-    while (p + 1 < L.nprob && u >= L.prob[p + 1].tile_begin) ++p;
-    const GemmProblem& P = L.prob[p];
-    const int local = u - P.tile_begin;
-    const int item = local / P.tiles_per_item;
-    const int tl = local - item * P.tiles_per_item;
-    const int half_m = P.tiles_m / 2;
-    const int sm = tl % half_m, tn = tl / half_m;
-    return {p, item, (2 * sm + (int)pr) * 256 + 128 * (int)q, tn * 256};
+// A k-block [k0, k0 + 64) of rows starting at `row0` of a lower-stored symmetric
+// operand lies beyond the rows' 256-row diagonal tile: it is read from the mirror
+// position (rows k0.., columns row0..), MN-major.
+__device__ __forceinline__ bool upper_block(bool sym, int k0, int row0) {
+    return sym && k0 >= (row0 & ~255) + 256;
 }
 
-// CL = 2: one CTA pair per cluster.  CL = 4: two pairs per cluster sharing the B
-// operand of decode_quad_tile's super-tiles: each CTA loads one of the two 64-column
-// boxes of its B half and multicasts it to the CTA of the same parity in the other
-// pair; a stage is free again once both pairs' MMAs have read it.
-template <bool BF16, int CL>
+// LOWER = false: operands through 3-D maps, symmetric outputs stored whole.
+// LOWER = true: every operand through a 4-D map of 64-column chunks, one box per
+// operand per stage whichever way it is read (the map and the coordinates are
+// selected per k-block, no branch around the TMA issue); symmetric outputs stored
+// as their lower triangle (lower_out) and read back through the mirror (sym_a /
+// sym_b).  The same MMAs on the same operand values in the same order: both give
+// bitwise the same results.
+template <bool BF16, bool LOWER>
 __global__ void __maxnreg__(168) gemm2_kernel(const __grid_constant__ GemmLaunch L) {
-    static_assert(CL == 2 || CL == 4, "clusters of one or two CTA pairs");
     using Cfg = Gemm2Cfg;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -328,18 +322,17 @@ __global__ void __maxnreg__(168) gemm2_kernel(const __grid_constant__ GemmLaunch
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
-    const uint32_t q = rank & 1u;      // CTA within its pair
-    const uint32_t pr = rank >> 1;     // pair within the cluster
-    const uint32_t lead = rank & ~1u;  // the pair's even CTA: MMA issuer, owner of the full / tempty barriers
+    const uint32_t q = rank & 1u;      // CTA within the pair
+    const uint32_t lead = 0;           // the even CTA: MMA issuer, owner of the full / tempty barriers
     const bool leader = q == 0;
-    const int cluster_id = blockIdx.x / CL;
-    const int nclusters = gridDim.x / CL;
-    auto decode = [&](int t) { return CL == 2 ? decode_pair_tile(L, t, q) : decode_quad_tile(L, t, pr, q); };
+    const int cluster_id = blockIdx.x >> 1;
+    const int nclusters = gridDim.x >> 1;
+    auto decode = [&](int t) { return decode_pair_tile(L, t, q); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages2; ++s) {
             mbar_init(full + s, 1);    // leader: its expect_tx arrival + both CTAs' bytes
-            mbar_init(empty + s, CL / 2);   // every pair's leader: its multicast commit
+            mbar_init(empty + s, 1);   // both: the leader's multicast commit
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull + a, 1);   // both: the leader's multicast commit
@@ -353,6 +346,8 @@ __global__ void __maxnreg__(168) gemm2_kernel(const __grid_constant__ GemmLaunch
         for (int p = 0; p < L.nprob; ++p) {
             tma_prefetch_desc(&L.mapA[p]);
             tma_prefetch_desc(&L.mapB[p]);
+            if (LOWER && L.prob[p].sym_a) tma_prefetch_desc(&L.mapAt[p]);
+            if (LOWER && (L.prob[p].sym_b || L.prob[p].b_mn)) tma_prefetch_desc(&L.mapBt[p]);
         }
     }
     if (warp == 1) {
@@ -375,6 +370,12 @@ __global__ void __maxnreg__(168) gemm2_kernel(const __grid_constant__ GemmLaunch
                 const TileCoord tc = decode(t);
                 const GemmProblem& P = L.prob[tc.p];
                 const int kblocks = (P.K + Cfg::BK - 1) / Cfg::BK;
+                // lower-triangle launches: the problem's fields and maps read once per tile
+                const bool sym_a = P.sym_a != 0, sym_b = P.sym_b != 0, bmn = P.b_mn != 0;
+                const CUtensorMap* mA = &L.mapA[tc.p];
+                const CUtensorMap* mAt = &L.mapAt[tc.p];
+                const CUtensorMap* mB = &L.mapB[tc.p];
+                const CUtensorMap* mBt = &L.mapBt[tc.p];
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const uint32_t s = it % kStages2;
                     const uint32_t ph = (it / kStages2) & 1u;
@@ -386,13 +387,18 @@ __global__ void __maxnreg__(168) gemm2_kernel(const __grid_constant__ GemmLaunch
                     uint8_t* sb = sa + Cfg::A_BYTES;
                     const uint32_t fb = mapa_shared(smem_u32(full + s), lead);
                     if (leader) mbar_arrive_expect_tx(full + s, 2 * Cfg::STAGE_BYTES);
-                    tma_load_3d_pair(sa, &L.mapA[tc.p], fb, kb * Cfg::BK, tc.m0, tc.item);
                     const int nb = tc.n0 + 128 * (int)q;
-                    if (CL == 4) {   // B MN-major, shared with the other pair
-                        const uint16_t mask = (uint16_t)((1u << q) | (1u << (2 + q)));
-                        tma_load_3d_pair_mc(sb + pr * Cfg::MN_CHUNK_BYTES, &L.mapB[tc.p], fb, nb + 64 * (int)pr,
-                                            kb * Cfg::BK, tc.item, mask);
-                    } else if (!P.b_mn) {
+                    if constexpr (LOWER) {
+                        // one 4-D box per operand: K-major at (0, row, kb) or the mirror at (0, k0, row / 64)
+                        const int k0 = kb * Cfg::BK;
+                        const bool at = upper_block(sym_a, k0, tc.m0);
+                        const bool bt = bmn || upper_block(sym_b, k0, tc.n0);
+                        tma_load_4d_pair(sa, at ? mAt : mA, fb, 0, at ? k0 : tc.m0, at ? (tc.m0 >> 6) : kb, tc.item);
+                        tma_load_4d_pair(sb, bt ? mBt : mB, fb, 0, bt ? k0 : nb, bt ? (nb >> 6) : kb, tc.item);
+                        continue;
+                    }
+                    tma_load_3d_pair(sa, &L.mapA[tc.p], fb, kb * Cfg::BK, tc.m0, tc.item);
+                    if (!P.b_mn) {
                         tma_load_3d_pair(sb, &L.mapB[tc.p], fb, kb * Cfg::BK, nb, tc.item);
                     } else {
                         tma_load_3d_pair(sb, &L.mapB[tc.p], fb, nb, kb * Cfg::BK, tc.item);
@@ -424,6 +430,9 @@ __global__ void __maxnreg__(168) gemm2_kernel(const __grid_constant__ GemmLaunch
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * kBN;
                 const uint32_t idesc = idesc_make(BF16, 256, kBN, false, P.b_mn != 0);
+                // lower-triangle launches: k-block where A / B switch to the mirror (MN-major)
+                const int a_sw = P.sym_a ? ((tc.m0 & ~255) + 256) / Cfg::BK : 1 << 30;
+                const int b_sw = P.b_mn ? 0 : (P.sym_b ? ((tc.n0 & ~255) + 256) / Cfg::BK : 1 << 30);
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const uint32_t s = it % kStages2;
                     const uint32_t ph = (it / kStages2) & 1u;
@@ -434,15 +443,29 @@ __global__ void __maxnreg__(168) gemm2_kernel(const __grid_constant__ GemmLaunch
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(smem + s * Cfg::STAGE_BYTES);
                     const uint32_t b_addr = a_addr + Cfg::A_BYTES;
+                    if constexpr (LOWER) {
+                        const bool a_mn = kb >= a_sw, b_mn = kb >= b_sw;
+                        const uint32_t id = idesc_make(BF16, 256, kBN, a_mn, b_mn);
 #pragma unroll
-                    for (int kk = 0; kk < Cfg::BK / Cfg::UK; ++kk) {
-                        const uint64_t ad = sdesc_sw128(a_addr + kk * Cfg::UK * Cfg::ESZ, 0, 1024);
-                        const uint64_t bd =
-                            P.b_mn ? sdesc_sw128(b_addr + kk * Cfg::UK * 128, Cfg::MN_CHUNK_BYTES, 1024)
-                                   : sdesc_sw128(b_addr + kk * Cfg::UK * Cfg::ESZ, 0, 1024);
-                        mma_f16kind_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+                        for (int kk = 0; kk < Cfg::BK / Cfg::UK; ++kk) {
+                            constexpr int MN = Cfg::MN_CHUNK_BYTES;
+                            const uint64_t ad = a_mn ? sdesc_sw128(a_addr + kk * Cfg::UK * 128, MN, 1024)
+                                                     : sdesc_sw128(a_addr + kk * Cfg::UK * Cfg::ESZ, 0, 1024);
+                            const uint64_t bd = b_mn ? sdesc_sw128(b_addr + kk * Cfg::UK * 128, MN, 1024)
+                                                     : sdesc_sw128(b_addr + kk * Cfg::UK * Cfg::ESZ, 0, 1024);
+                            mma_f16kind_pair(d_tmem, ad, bd, id, (kb | kk) != 0);
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < Cfg::BK / Cfg::UK; ++kk) {
+                            const uint64_t ad = sdesc_sw128(a_addr + kk * Cfg::UK * Cfg::ESZ, 0, 1024);
+                            const uint64_t bd =
+                                P.b_mn ? sdesc_sw128(b_addr + kk * Cfg::UK * 128, Cfg::MN_CHUNK_BYTES, 1024)
+                                       : sdesc_sw128(b_addr + kk * Cfg::UK * Cfg::ESZ, 0, 1024);
+                            mma_f16kind_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+                        }
                     }
-                    mma_commit_pair(empty + s, CL == 4 ? 0xF : 0x3);   // this pair is done with the stage
+                    mma_commit_pair(empty + s, 0x3);   // frees the stage in both CTAs
                 }
                 if (!ok) break;
                 mma_commit_pair(tfull + acc, (uint16_t)(3u << lead));   // both CTAs' accumulators ready
@@ -530,45 +553,40 @@ cudaError_t gemm_prepare(int device) {
                                  GemmCfg::SMEM_BYTES);
     const int n = Gemm2Cfg::SMEM_BYTES;
     const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm2_kernel<true, 2>, a, n);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm2_kernel<false, 2>, a, n);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm2_kernel<true, 4>, a, n);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm2_kernel<false, 4>, a, n);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm2_kernel<true, false>, a, n);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm2_kernel<false, false>, a, n);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm2_kernel<true, true>, a, n);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm2_kernel<false, true>, a, n);
     if (e == cudaSuccess) e = ns_small_prepare();
     return e;
 }
 
-cudaError_t gemm2_max_clusters(int* out, int cluster_ctas) {
+cudaError_t gemm2_max_clusters(int* out) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cluster_ctas;
+    attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(cluster_ctas, 1, 1);
+    cfg.gridDim = dim3(2, 1, 1);
     cfg.blockDim = dim3(kGemmThreads, 1, 1);
     cfg.dynamicSmemBytes = Gemm2Cfg::SMEM_BYTES;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cluster_ctas == 4) return cudaOccupancyMaxActiveClusters(out, gemm2_kernel<true, 4>, &cfg);
-    return cudaOccupancyMaxActiveClusters(out, gemm2_kernel<true, 2>, &cfg);
+    return cudaOccupancyMaxActiveClusters(out, gemm2_kernel<true, false>, &cfg);
 }
 
-cudaError_t gemm2_launch(const GemmLaunch& L, bool bf16, int clusters, cudaStream_t s, bool quad) {
+cudaError_t gemm2_launch(const GemmLaunch& L, bool bf16, int clusters, cudaStream_t s, bool lower) {
     if (L.total_tiles <= 0) return cudaSuccess;
-    const dim3 blk(kGemmThreads);
-    const size_t sm = Gemm2Cfg::SMEM_BYTES;
-    if (quad) {   // clusters of two pairs; L.total_tiles counts super-tiles
-        int quads = clusters / 2;
-        if (quads > L.total_tiles) quads = L.total_tiles;
-        if (quads < 1) quads = 1;
-        return bf16 ? launch_pdl_cluster(gemm2_kernel<true, 4>, dim3(4 * quads), blk, sm, s, 4u, L)
-                    : launch_pdl_cluster(gemm2_kernel<false, 4>, dim3(4 * quads), blk, sm, s, 4u, L);
-    }
     if (clusters > L.total_tiles) clusters = L.total_tiles;
     if (clusters < 1) clusters = 1;
-    return bf16 ? launch_pdl_cluster(gemm2_kernel<true, 2>, dim3(2 * clusters), blk, sm, s, 2u, L)
-                : launch_pdl_cluster(gemm2_kernel<false, 2>, dim3(2 * clusters), blk, sm, s, 2u, L);
+    const dim3 grid(2 * clusters), blk(kGemmThreads);
+    const size_t sm = Gemm2Cfg::SMEM_BYTES;
+    if (lower)
+        return bf16 ? launch_pdl_cluster(gemm2_kernel<true, true>, grid, blk, sm, s, 2u, L)
+                    : launch_pdl_cluster(gemm2_kernel<false, true>, grid, blk, sm, s, 2u, L);
+    return bf16 ? launch_pdl_cluster(gemm2_kernel<true, false>, grid, blk, sm, s, 2u, L)
+                : launch_pdl_cluster(gemm2_kernel<false, false>, grid, blk, sm, s, 2u, L);
 }
 
 cudaError_t gemm_launch(const GemmLaunch& L, bool bf16, int grid, cudaStream_t s) {

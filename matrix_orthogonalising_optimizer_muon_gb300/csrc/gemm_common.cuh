@@ -302,6 +302,9 @@ __device__ __forceinline__ void epilogue_chunk_tma(const GemmProblem& P, const C
     float v[32];
     epilogue_values(P, item, R0 + lane, col0, raw, v);
     const bool diag = col0 == R0;
+    // the transposed block goes to the mirror position unless the output is stored as
+    // its lower triangle and the block lies below the diagonal 256 x 256 tile
+    const bool mirror = !diag && (!P.lower_out || ((R0 ^ col0) & ~255) == 0);
     const bool bf = (P.tma_out & kTmaOutBf16) != 0;
     if (lane == 0) bulk_wait_read<0>();   // the previous chunk's stores have read the staging
     __syncwarp();
@@ -324,7 +327,7 @@ __device__ __forceinline__ void epilogue_chunk_tma(const GemmProblem& P, const C
                 *reinterpret_cast<unsigned short*>(stl + stage64_off(j, lane)) = h;
             }
         }
-    } else {
+    } else if (mirror) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
             const unsigned short h = bf ? __bfloat16_as_ushort(__float2bfloat16_rn(v[j]))
@@ -337,7 +340,7 @@ __device__ __forceinline__ void epilogue_chunk_tma(const GemmProblem& P, const C
     if (lane == 0) {
         if (P.tma_out & kTmaOutC) tma_store_3d(mc, stl, col0, R0, item);
         if (P.tma_out & kTmaOutC2) tma_store_3d(mc2, stl, col0, R0, item);
-        if (!diag) {
+        if (mirror) {
             if (P.tma_out & kTmaOutC) tma_store_3d(mc, stm, R0, col0, item);
             if (P.tma_out & kTmaOutC2) tma_store_3d(mc2, stm, R0, col0, item);
         }

@@ -102,7 +102,14 @@ struct GemmProblem {
     // symmetric outputs of the CTA-pair kernel written with TMA stores from shared
     // memory: kTmaOutC (staged values via mapC), kTmaOutC2 (also via mapC2),
     // kTmaOutBf16 (staged as bf16, else fp16); 0: per-thread stores
-    int tma_out, pad4;
+    int tma_out;
+    // CTA-pair kernel with lower-triangle storage (launches of chunks whose batched
+    // matrices have r and c multiples of 64): symmetric r x r results are stored as
+    // their 256 x 256 pair tiles at or below the diagonal, the diagonal tiles whole and
+    // exactly symmetric.  lower_out: this output is stored so (no mirror below the
+    // diagonal tile).  sym_a / sym_b: that operand is stored so; its 64-deep k-blocks
+    // beyond the operand rows' diagonal tile are read from the mirror position.
+    int lower_out, sym_a, sym_b;
 };
 constexpr int kTmaOutC = 1, kTmaOutC2 = 2, kTmaOutBf16 = 4;
 
@@ -111,12 +118,19 @@ struct GemmLaunch {
     CUtensorMap mapB[kMaxProblems];
     CUtensorMap mapC[kMaxProblems];    // 32 x 32 store boxes (64-byte swizzle) of the outputs
     CUtensorMap mapC2[kMaxProblems];
+    // Lower-triangle launches view every operand as (64 columns, rows, column chunks,
+    // batch): mapA / mapB then hold K-major boxes (64, 128, 1, 1) at (0, row, k / 64, item)
+    // and mapAt / mapBt mirror boxes (64, 64, 2, 1) at (0, k, row / 64, item), MN-major in
+    // shared memory (mapBt also serves an MN-major B such as X0 in the final product).
+    CUtensorMap mapAt[kMaxProblems];
+    CUtensorMap mapBt[kMaxProblems];
     GemmProblem prob[kMaxProblems];
     int nprob;
     int total_tiles;
     int* status;
     int pad;
 };
+static_assert(sizeof(GemmLaunch) <= 32764, "a GemmLaunch must fit the kernel parameter space");
 
 size_t gemm_smem_bytes();
 cudaError_t gemm_prepare(int device);   // sets the dynamic shared-memory limit once
@@ -124,12 +138,9 @@ cudaError_t gemm_prepare(int device);   // sets the dynamic shared-memory limit 
 cudaError_t gemm_launch(const GemmLaunch& L, bool bf16, int grid, cudaStream_t s);
 // CTA-pair kernel (cluster of 2, tcgen05 cta_group::2, 256 x 256 tiles); problems
 // use pair tiling: tiles_m = ceil(M / 256), tiles_n = ceil(N / 256).
-// quad: clusters of two pairs that share B by TMA multicast (non-symmetric problems
-// with an MN-major B and even tiles_m only); tiles_per_item then counts super-tiles
-// of two pair tiles, (tiles_m / 2) * tiles_n, and `clusters` is the number of pairs
-// (two per launched cluster).
-cudaError_t gemm2_max_clusters(int* out, int cluster_ctas);   // co-resident clusters of 2 or 4 CTAs
-cudaError_t gemm2_launch(const GemmLaunch& L, bool bf16, int clusters, cudaStream_t s, bool quad = false);
+// lower: the lower-triangle variant (4-D operand maps, lower_out / sym_a / sym_b honoured).
+cudaError_t gemm2_max_clusters(int* out);
+cudaError_t gemm2_launch(const GemmLaunch& L, bool bf16, int clusters, cudaStream_t s, bool lower);
 // Whole NS step (SYRK, r x r recursion, final product + fused update) of matrices
 // with r <= 128, one matrix per CTA at a time.  One problem per bucket: M = r,
 // N = c, batch = matrices, tile_begin = prefix over matrices; mapA = X with

@@ -300,15 +300,13 @@ __device__ __forceinline__ void tma_load_3d_pair(void* smem_dst, const CUtensorM
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar_cluster_saddr)
         : "memory");
 }
-// As tma_load_3d_pair, multicast: the box lands at the same shared-memory offset in
-// every CTA of ctaMask, and each landing signals the mbarrier at bar's offset in the
-// even CTA of the destination's pair.
-__device__ __forceinline__ void tma_load_3d_pair_mc(void* smem_dst, const CUtensorMap* map, uint32_t bar_cluster_saddr,
-                                                    int x, int y, int z, uint16_t mask) {
+// 4-D variant of tma_load_3d_pair (x innermost; x * element size a multiple of 16).
+__device__ __forceinline__ void tma_load_4d_pair(void* smem_dst, const CUtensorMap* map, uint32_t bar_cluster_saddr,
+                                                 int x, int y, int z, int w) {
     asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        ".cta_group::2 [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar_cluster_saddr), "h"(mask)
+        "cp.async.bulk.tensor.4d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar_cluster_saddr)
         : "memory");
 }
 // TMEM allocation shared by the CTA pair: one warp of EACH CTA executes it.

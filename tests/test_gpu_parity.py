@@ -632,26 +632,32 @@ def test_step_host_without_copy_back_and_argument_checks():
 
 
 @pytest.mark.parametrize("shapes", [
-    [(512, 1024), (1024, 2000), (2000, 1024), (300, 700), (512, 4000)],   # even tile rows: clusters of two pairs
-    [(512, 1024), (700, 900), (128, 3584)],                              # an odd tile-row count: pairs only
+    [(512, 1024), (1024, 2048), (2048, 1024), (768, 1536), (512, 4096)],   # r, c multiples of 64: lower triangle
+    [(512, 1024), (700, 900), (128, 3584)],                              # a ragged bucket: stored whole
 ])
-def test_quad_clusters_match_pair_clusters_bitwise(shapes):
-    """The final product in clusters of two CTA pairs sharing X0 by TMA multicast gives
-    bitwise the results of clusters of one pair (same MMAs in the same order), and
-    matches the oracle."""
+def test_lower_triangle_storage_matches_whole_storage_bitwise(shapes):
+    """Symmetric r x r results stored as their lower triangle (the products read the
+    blocks above the diagonal tile from the mirror position through 4-D maps) give
+    bitwise the results of whole storage: the same MMAs on the same operand values."""
     import matrix_orthogonalising_optimizer_muon_gb300 as lib
-    qplan = lib.MuonPlan(shapes, "bf16", keep_update=True, quad_clusters=True)
-    assert qplan.info()["quad_clusters"] >= 16
-    quad = run_step(shapes, "bf16", base_seed=51, plan=qplan)
-    plan = lib.MuonPlan(shapes, "bf16", keep_update=True)
-    assert plan.info()["quad_clusters"] == 0
-    pair = run_step(shapes, "bf16", inputs=quad["inputs"], plan=plan)
+    lplan = lib.MuonPlan(shapes, "bf16", keep_update=True)
+    aligned = all(min(m, n) % 64 == 0 and max(m, n) % 64 == 0 for m, n in shapes if min(m, n) > 128)
+    assert lplan.info()["lower_chunks"] == (1 if aligned else 0)
+    low = run_step(shapes, "bf16", base_seed=51, plan=lplan)
+    plan = lib.MuonPlan(shapes, "bf16", keep_update=True, full_symmetric=True)
+    assert plan.info()["lower_chunks"] == 0
+    whole = run_step(shapes, "bf16", inputs=low["inputs"], plan=plan)
     for i in range(len(shapes)):
-        assert torch_equal(quad["W"][i], pair["W"][i]), shapes[i]
-        assert torch_equal(quad["O"][i], pair["O"][i]), shapes[i]
-        assert_ns(quad, i)
+        assert torch_equal(low["W"][i], whole["W"][i]), shapes[i]
+        assert torch_equal(low["O"][i], whole["O"][i]), shapes[i]
+        assert_ns(low, i)
+    # the workspace copies rebuild the upper part: same G, P, Q as whole storage
+    for i, (m, n) in enumerate(shapes):
+        if min(m, n) > 128:
+            for which in (1, 2, 3, 5, 6, 7):
+                assert torch_equal(lplan.debug_workspace(i, which), plan.debug_workspace(i, which)), (i, which)
     plan.close()
-    qplan.close()
+    lplan.close()
 
 
 def torch_equal(a, b):
