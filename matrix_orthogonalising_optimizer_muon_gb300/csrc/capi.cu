@@ -1403,8 +1403,8 @@ muon_status muon_plan_tune(muon_plan p, float* const* params, const void* const*
     if (mixed && p->opts.chain_clusters == 0 && p->s2) scales = {1.f, 0.f, 0.5f, 1.5f};
     bool lower_choice = false;   // chunks where lower-triangle storage is a choice
     for (const auto& ch : p->chunks) lower_choice = lower_choice || ch.lower_ok;
-    std::vector<bool> quads = {true};
-    if (lower_choice && !p->opts.full_symmetric) quads = {true, false};
+    std::vector<bool> lowers = {true};
+    if (lower_choice && !p->opts.full_symmetric) lowers = {true, false};
     const int kmax = std::min(p->pair_clusters - 1, (p->sm_count - 2) / 2);
     auto apply = [&](float sc, bool q) {
         for (auto& ch : p->chunks)
@@ -1423,7 +1423,7 @@ muon_status muon_plan_tune(muon_plan p, float* const* params, const void* const*
     bool best_q = true;
     int tried = 0;
     for (float sc : scales) {
-        for (bool q : quads) {
+        for (bool q : lowers) {
             apply(sc, q);
             st = muon_step_ex(p, params, grads, momentum, lr, wd, mu, kMaxNsSteps, nullptr, 0, stream);   // warm-up
             if (st == MUON_OK && cudaEventRecord(e0, s) != cudaSuccess) st = MUON_ERR_CUDA;
