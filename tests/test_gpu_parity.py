@@ -689,3 +689,24 @@ def test_plan_tune_keeps_results_bitwise():
     with pytest.raises(lib.MuonError):
         plan.tune(W, G, M, LR, WD, MU, reps=0)
     plan.close()
+
+
+@pytest.mark.parametrize("ns_steps,restart", [(0, 0), (1, 0), (2, 0), (7, 3), (4, 1)])
+def test_lower_triangle_storage_other_steps_and_restarts(ns_steps, restart):
+    """Lower-triangle storage with J = 0 (identity Q), 1 (P and Q stored whole by the
+    per-thread epilogue), 2, and restarted segments (the second X buffer's 4-D maps, X'
+    formed between segments): bitwise the results of whole storage, and the oracle's."""
+    import matrix_orthogonalising_optimizer_muon_gb300 as lib
+    shapes = [(192, 576), (576, 192), (256, 1024)]
+    mx = 10 if restart else 0
+    lplan = lib.MuonPlan(shapes, "bf16", keep_update=True, max_ns_steps=mx)
+    assert lplan.info()["lower_chunks"] == 1
+    low = run_step(shapes, "bf16", base_seed=81, ns_steps=ns_steps, restart=restart, plan=lplan)
+    wplan = lib.MuonPlan(shapes, "bf16", keep_update=True, max_ns_steps=mx, full_symmetric=True)
+    whole = run_step(shapes, "bf16", inputs=low["inputs"], ns_steps=ns_steps, restart=restart, plan=wplan)
+    for i in range(len(shapes)):
+        assert torch_equal(low["W"][i], whole["W"][i]), (i, ns_steps, restart)
+        assert torch_equal(low["O"][i], whole["O"][i]), (i, ns_steps, restart)
+        assert_ns(low, i, ns_steps=ns_steps)
+    lplan.close()
+    wplan.close()
