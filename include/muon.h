@@ -43,7 +43,7 @@ extern "C" {
 typedef enum {
     MUON_OK = 0,
     MUON_ERR_INVALID_ARG = 1,   /* bad shape, null pointer, overlap, hyperparameter out of range */
-    MUON_ERR_UNSUPPORTED = 2,   /* dtype / size this build does not handle */
+    MUON_ERR_UNSUPPORTED = 2,   /* dtype / size the library does not handle */
     MUON_ERR_OOM = 3,           /* workspace allocation failed */
     MUON_ERR_CUDA = 4,          /* a CUDA runtime or launch error */
     MUON_ERR_TIMEOUT = 5,       /* a device-side bounded wait expired */

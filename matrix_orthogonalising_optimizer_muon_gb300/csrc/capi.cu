@@ -35,8 +35,8 @@ constexpr float kNsC = 2.0315f;
 // about six steps.  Five steps (the pages' choice) keep it below 1e-2.
 constexpr int kMaxNsSteps = 5;            // one segment of the fp16 Gram recursion
 constexpr int kMaxNsStepsRestart = 100;    // with restarts (opts.max_ns_steps)
-constexpr int kMaxDim = 1 << 20;        // per-dimension limit of this build
-constexpr int kMaxR = 32768;            // r x r workspace limit of this build
+constexpr int kMaxDim = 1 << 20;        // per-dimension limit of the library
+constexpr int kMaxR = 32768;            // r x r workspace limit of the library
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,

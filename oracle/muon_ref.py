@@ -18,7 +18,7 @@ Everything is float64 numpy, written to be read against the pages it follows:
   technical summary section 2 "Gram Newton-Schulz": the recursion is run in the
   r x r Gram space G = X X^T.
 
-Readings taken where the pages are silent (each also listed in the design doc):
+Readings taken where the pages are silent:
 
 * Nesterov: the NS (and RowNorm) input is U = mu*M_t + G_t with
   M_t = mu*M_{t-1} + G_t (no dampening); the stored state is M_t.
