@@ -21,8 +21,14 @@
  *    pointers, in the order of the shapes given to muon_plan_create.  They may
  *    change from call to call; the array itself is read before the call returns.
  *  - stream is a cudaStream_t passed as void* (NULL = legacy default stream).
- *    All device work is enqueued on it; no call synchronises the host except
- *    muon_sync and muon_debug_copy_update.
+ *    All device work is enqueued on it (muon_step_host and the overlapped
+ *    fused/batched products also use streams of the plan, joined back into it);
+ *    no call synchronises the host except muon_sync, muon_plan_tune, the
+ *    muon_debug_copy_* calls, and muon_step_host with pageable host memory.
+ *  - A plan is not thread-safe: its calls share one workspace, pinned pointer
+ *    table and event set, so calls on one plan must not overlap, and steps of one
+ *    plan issued to different streams must be ordered by the caller.  Separate
+ *    plans are independent.
  *  - Errors: every argument is validated on the host before anything is
  *    launched, and an invalid call returns MUON_ERR_INVALID_ARG (or
  *    MUON_ERR_UNSUPPORTED) with no buffer touched.  A failed launch returns
