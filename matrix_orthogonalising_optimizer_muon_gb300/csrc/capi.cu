@@ -659,7 +659,7 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
                     cur = -1;
                 }
                 if (cur < 0) {
-                    Bucket nb;
+                    Bucket nb{};   // value-initialised: the tensor maps are filled in later
                     nb.r = r;
                     nb.c = c;
                     nb.ldr = (int)round_up(r, 8);
