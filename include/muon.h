@@ -120,12 +120,29 @@ typedef struct muon_plan_s* muon_plan;
  * Orients every shape to r x c (r = min, c = max; DiT paper sec. 3.1),
  * buckets equal (r, c) so each Gram Newton-Schulz product runs as one grouped
  * launch over all matrices of all buckets (DMuon, batching same-shape matrices),
- * and allocates the workspace once (bf16 X0, fp32 r x r Gram buffers, pointer
- * tables, status word) on the current device.  The plan owns the workspace;
- * muon_plan_destroy frees it.  Returns MUON_ERR_OOM if cudaMalloc fails.
+ * and allocates the workspace once (bf16 X0, the fp16 r x r Gram-space buffers
+ * and a bf16 copy of Q, per-matrix tables, launch lists, status word) on the
+ * current device.  The plan owns the workspace; muon_plan_destroy frees it.
+ * Returns MUON_ERR_OOM if cudaMalloc (or a host allocation) fails.
  */
 muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype grad_dtype,
                              const muon_plan_opts* opts, muon_plan* out);
+
+/*
+ * muon_plan_workspace_size - size the plan muon_plan_create would build for the
+ * same shapes, grad_dtype and opts, on the host alone: no CUDA call is made, so
+ * it works without a GPU.
+ *   bytes      receives the device workspace muon_plan_create would allocate (its
+ *              one cudaMalloc; muon_plan_info reports the same figure).
+ *   n_buckets  receives the number of (r, c) buckets, counted per chunk.
+ *   n_chunks   receives the number of chunks the NS step would run in.
+ * Any output pointer may be NULL.  Same argument checks and codes as
+ * muon_plan_create, including MUON_ERR_OOM when opts->workspace_bytes cannot
+ * hold the per-matrix tables plus the buffers of the largest single matrix.
+ */
+muon_status muon_plan_workspace_size(const muon_shape* shapes, int32_t n, muon_dtype grad_dtype,
+                                     const muon_plan_opts* opts, int64_t* bytes, int32_t* n_buckets,
+                                     int32_t* n_chunks);
 
 void muon_plan_destroy(muon_plan p);
 

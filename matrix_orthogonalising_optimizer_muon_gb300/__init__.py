@@ -7,8 +7,9 @@ fallback: if the library cannot be loaded, every entry point raises.
 The C entry points keep their names (``muon_plan_create``, ``muon_step``,
 ``muon_rownorm_step``, ``muon_sync``, ``muon_debug_copy_update``,
 ``muon_debug_copy_workspace``, ``muon_plan_info``, ``muon_stage_times``,
-``muon_status_string``, ``muon_plan_destroy``); ``MuonPlan`` wraps them for
-torch tensors and ``PeriodicRowNormMuon`` adds the step schedule of periodic
+``muon_status_string``, ``muon_plan_destroy`` and the rest of the header);
+``MuonPlan`` wraps them for torch tensors, ``plan_workspace_size`` sizes a plan on
+the host alone (``muon_plan_workspace_size``), and ``PeriodicRowNormMuon`` adds the step schedule of periodic
 RowNorm Muon (full NS5 every K steps, RowNorm otherwise; "Scaling Muon for
 Diffusion Transformers", sec. 3).
 """
@@ -20,7 +21,7 @@ import os
 from .build import LIB, build, up_to_date
 
 __all__ = [
-    "MuonError", "MuonPlan", "PeriodicRowNormMuon", "load", "build",
+    "MuonError", "MuonPlan", "PeriodicRowNormMuon", "plan_workspace_size", "load", "build",
     "MUON_OK", "MUON_ERR_INVALID_ARG", "MUON_ERR_UNSUPPORTED", "MUON_ERR_OOM",
     "MUON_ERR_CUDA", "MUON_ERR_TIMEOUT", "MUON_F32", "MUON_BF16",
     "MUON_MODE_NS", "MUON_MODE_ROWNORM", "EXPORTED",
@@ -62,6 +63,9 @@ EXPORTED = {
     "muon_plan_create": (ctypes.c_int, [ctypes.POINTER(MuonShape), ctypes.c_int32, ctypes.c_int,
                                         ctypes.POINTER(MuonPlanOpts), ctypes.POINTER(_P)]),
     "muon_plan_destroy": (None, [_P]),
+    "muon_plan_workspace_size": (ctypes.c_int, [ctypes.POINTER(MuonShape), ctypes.c_int32, ctypes.c_int,
+                                                ctypes.POINTER(MuonPlanOpts), ctypes.POINTER(ctypes.c_int64),
+                                                ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]),
     "muon_debug_wait_timeout": (ctypes.c_int, [_P, ctypes.c_int32, _P]),
     "muon_step": (ctypes.c_int, [_P, _PP, _PP, _PP, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                  ctypes.c_int32, ctypes.c_int, _P]),
@@ -139,6 +143,30 @@ def _ptr_array(ptrs):
     return (ctypes.c_void_p * len(ptrs))(*ptrs)
 
 
+def _plan_args(shapes, grad_dtype, keep_update=False, timing=False, single_sm_gemm=False,
+               generic_small=False, chain_clusters=0, workspace_bytes=0, max_ns_steps=0, chunks=0,
+               full_symmetric=False):
+    """(shape list, MuonShape array, dtype code, MuonPlanOpts) of a plan's arguments."""
+    shapes = [(int(m), int(n)) for m, n in shapes]
+    arr = (MuonShape * len(shapes))(*[MuonShape(m, n) for m, n in shapes])
+    opts = MuonPlanOpts(1 if keep_update else 0, 1 if timing else 0, 1 if single_sm_gemm else 0,
+                        1 if generic_small else 0, int(chain_clusters), int(max_ns_steps),
+                        int(workspace_bytes), int(chunks), 1 if full_symmetric else 0)
+    return shapes, arr, {"bf16": MUON_BF16, "f32": MUON_F32}[grad_dtype], opts
+
+
+def plan_workspace_size(shapes, grad_dtype: str = "bf16", **opts) -> dict:
+    """What ``MuonPlan(shapes, grad_dtype, **opts)`` would build, computed on the host alone
+    (``muon_plan_workspace_size``; no GPU needed): the device workspace bytes it would
+    allocate, its (r, c) buckets and its chunks."""
+    lib = load()
+    shapes, arr, gd, o = _plan_args(shapes, grad_dtype, **opts)
+    nbytes, nb, nc = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32()
+    _check(lib.muon_plan_workspace_size(arr, len(shapes), gd, ctypes.byref(o), ctypes.byref(nbytes),
+                                        ctypes.byref(nb), ctypes.byref(nc)), "muon_plan_workspace_size")
+    return {"workspace_bytes": nbytes.value, "n_buckets": nb.value, "n_chunks": nc.value}
+
+
 class MuonPlan:
     """A planned Muon step over a fixed list of matrix shapes (``muon_plan_create``).
 
@@ -151,14 +179,11 @@ class MuonPlan:
                  chain_clusters: int = 0, workspace_bytes: int = 0, max_ns_steps: int = 0, chunks: int = 0,
                  full_symmetric: bool = False):
         self.lib = load()
-        self.shapes = [(int(m), int(n)) for m, n in shapes]
+        self.shapes, arr, gd, opts = _plan_args(shapes, grad_dtype, keep_update, timing, single_sm_gemm,
+                                                generic_small, chain_clusters, workspace_bytes, max_ns_steps,
+                                                chunks, full_symmetric)
         self.grad_dtype = grad_dtype
-        arr = (MuonShape * len(self.shapes))(*[MuonShape(m, n) for m, n in self.shapes])
-        opts = MuonPlanOpts(1 if keep_update else 0, 1 if timing else 0, 1 if single_sm_gemm else 0,
-                            1 if generic_small else 0, int(chain_clusters), int(max_ns_steps),
-                            int(workspace_bytes), int(chunks), 1 if full_symmetric else 0)
         h = ctypes.c_void_p()
-        gd = {"bf16": MUON_BF16, "f32": MUON_F32}[grad_dtype]
         _check(self.lib.muon_plan_create(arr, len(self.shapes), gd, ctypes.byref(opts),
                                          ctypes.byref(h)), "muon_plan_create")
         self.handle = h

@@ -449,15 +449,20 @@ muon_plan_s::StepEvents* next_events(muon_plan_s* p) {
     if (p->n_timed < p->evs.size()) return &p->evs[p->n_timed++];
     if (p->evs.size() >= kMaxTimedSteps) return &p->evs.back();
     muon_plan_s::StepEvents g{};
-    g.e.assign(7 * p->chunks.size(), nullptr);
-    g.split.assign(p->chunks.size(), 0);
+    try {
+        g.e.assign(7 * p->chunks.size(), nullptr);
+        g.split.assign(p->chunks.size(), 0);
+        p->evs.reserve(p->evs.size() + 1);   // the push_back below cannot throw
+    } catch (...) {
+        return nullptr;   // host memory
+    }
     for (auto& e : g.e)
         if (cudaEventCreate(&e) != cudaSuccess) {
             for (auto& x : g.e)
                 if (x) cudaEventDestroy(x);
             return nullptr;
         }
-    p->evs.push_back(g);
+    p->evs.push_back(std::move(g));
     p->n_timed = p->evs.size();
     return &p->evs.back();
 }
@@ -484,31 +489,18 @@ void free_plan(muon_plan_s* p) {
     delete p;
 }
 
-}  // namespace
+// Workspace offsets and per-chunk RowNorm lists of a plan, from plan_layout.
+struct Layout {
+    bool restarts = false;   // opts.max_ns_steps > 0: second X buffer, every matrix batched
+    size_t o_mats = 0, o_part = 0, o_cpart = 0, o_inv = 0, o_alpha = 0, o_status = 0, o_tr = 0, o_ptrs = 0,
+           o_items = 0, o_ones = 0, o_odbg = 0, o_lists = 0, o_prefix = 0, o_region = 0;
+    std::vector<size_t> o_ut, o_ut1, o_rr, o_qb;   // per bucket: X0, second X, r x r, bf16 Q (in the region)
+    std::vector<int> rnr_list, rnc_list;           // RowNorm: row-wise and column-wise matrices
+};
 
-extern "C" {
-
-const char* muon_last_error_detail(void) {
-    return g_last_cuda_error == cudaSuccess ? "no CUDA error recorded" : cudaGetErrorString(g_last_cuda_error);
-}
-
-const char* muon_status_string(muon_status s) {
-    switch (s) {
-        case MUON_OK: return "MUON_OK";
-        case MUON_ERR_INVALID_ARG: return "MUON_ERR_INVALID_ARG: invalid argument";
-        case MUON_ERR_UNSUPPORTED: return "MUON_ERR_UNSUPPORTED: unsupported dtype or size";
-        case MUON_ERR_OOM: return "MUON_ERR_OOM: workspace allocation failed";
-        case MUON_ERR_CUDA: return "MUON_ERR_CUDA: CUDA runtime or launch error";
-        case MUON_ERR_TIMEOUT: return "MUON_ERR_TIMEOUT: a bounded device wait expired";
-        case MUON_ERR_NONFINITE: return "MUON_ERR_NONFINITE";
-    }
-    return "MUON_ERR_UNKNOWN";
-}
-
-muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype grad_dtype, const muon_plan_opts* opts,
-                             muon_plan* out) {
-    if (!out) return MUON_ERR_INVALID_ARG;
-    *out = nullptr;
+// Argument checks of muon_plan_create and muon_plan_workspace_size.
+muon_status check_plan_args(const muon_shape* shapes, int32_t n, muon_dtype grad_dtype,
+                            const muon_plan_opts* opts) {
     if (!shapes || n <= 0) return MUON_ERR_INVALID_ARG;
     if (grad_dtype != MUON_F32 && grad_dtype != MUON_BF16) return MUON_ERR_UNSUPPORTED;
     for (int i = 0; i < n; ++i) {
@@ -519,24 +511,15 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
     if (opts && (opts->max_ns_steps < 0 || opts->max_ns_steps > kMaxNsStepsRestart || opts->chunks < 0 ||
                  opts->workspace_bytes < 0))
         return MUON_ERR_INVALID_ARG;
-    muon_plan_s* p = new (std::nothrow) muon_plan_s();
-    if (!p) return MUON_ERR_OOM;
-    if (cudaGetDevice(&p->device) != cudaSuccess) {
-        delete p;
-        return MUON_ERR_CUDA;
-    }
-    if (cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess) {
-        delete p;
-        return MUON_ERR_CUDA;
-    }
-    if (!encode_fn()) {
-        delete p;
-        return MUON_ERR_CUDA;
-    }
-    p->gdt = grad_dtype;
-    if (opts) p->opts = *opts;
-    p->shapes.assign(shapes, shapes + n);
+    return MUON_OK;
+}
 
+// The host part of planning, from p->shapes and p->opts alone (no CUDA call):
+// orientation, buckets, chunks and the workspace layout; sets p->mats, p->buckets,
+// p->chunks, p->mat_bucket, p->mat_item and p->ws_bytes.  MUON_ERR_OOM when
+// opts.workspace_bytes cannot hold the largest single matrix.
+muon_status plan_layout(muon_plan_s* p, Layout& L) {
+    const int n = (int)p->shapes.size();
     // ---- orient; group by oriented shape (r, c) in order of first appearance
     // (DiT paper sec. 3.1; DMuon batching)
     p->mats.resize(n);
@@ -547,8 +530,8 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
     for (int i = 0; i < n; ++i) {
         MatDev& md = p->mats[i];
         std::memset(&md, 0, sizeof(md));
-        md.m = shapes[i].rows;
-        md.n = shapes[i].cols;
+        md.m = p->shapes[i].rows;
+        md.n = p->shapes[i].cols;
         md.r = (int)std::min(md.m, md.n);
         md.c = (int)std::max(md.m, md.n);
         md.transposed = md.m > md.n;
@@ -565,12 +548,15 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
     // ---- workspace: a fixed part (per-matrix tables, partial sums, pointer tables,
     // launch lists, debug copies of O) and a region for the X0 and r x r buffers of
     // one chunk of matrices, shared by all chunks (they run one after the other)
-    const bool restarts = p->opts.max_ns_steps > 0;   // second X buffer, batched path for all
+    const bool restarts = L.restarts = p->opts.max_ns_steps > 0;   // second X buffer, batched path for all
     const bool fused_ok = !p->opts.generic_small && !restarts;
     auto is_fused = [&](int r) { return fused_ok && r <= kSmallMaxR; };
-    auto mat_region_bytes = [&](int r, int c) {   // X0 slice + the seven r x r buffers
-        const double ldu = (double)round_up(c, 8), ldr = (double)round_up(r, 8);
-        return (restarts ? 4.0 : 2.0) * r * ldu + (is_fused(r) ? 0.0 : 7 * 2.0 * r * ldr);
+    // region bytes of a bucket of `batch` matrices, exactly as laid out below: its X0
+    // (and second X) buffer and, batched, its seven r x r buffers, each rounded to 256
+    auto bucket_bytes = [&](int r, int c, long long batch) -> long long {
+        const long long x = round_up(batch * r * round_up(c, 8) * 2, 256);
+        const long long rr = round_up(batch * r * round_up(r, 8) * 2, 256);
+        return (restarts ? 2 : 1) * x + (is_fused(r) ? 0 : 7 * rr);
     };
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -580,7 +566,6 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
     };
     // momentum / RowNorm bookkeeping per matrix (not chunked)
     long long mom_part = 0, col_part = 0, inv_elems = 0;
-    std::vector<int> rnr_list, rnc_list;
     for (int i = 0; i < n; ++i) {
         MatDev& md = p->mats[i];
         md.nblk = (int)(md.transposed ? ceil_div(md.m, kTileRows) * ceil_div(md.n, kTile)
@@ -592,22 +577,22 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
             col_part += ceil_div(md.m, kColSlab) * md.n;
             md.inv_off = inv_elems;
             inv_elems += round_up(md.n, 4);
-            rnc_list.push_back(i);
+            L.rnc_list.push_back(i);
         } else {
-            rnr_list.push_back(i);
+            L.rnr_list.push_back(i);
         }
     }
-    const size_t o_mats = take(sizeof(MatDev) * n);
-    const size_t o_part = take(sizeof(float) * std::max<long long>(mom_part, 1));
-    const size_t o_cpart = take(sizeof(float) * std::max<long long>(col_part, 1));
-    const size_t o_inv = take(sizeof(float) * std::max<long long>(inv_elems, 1));
-    const size_t o_alpha = take(sizeof(float) * n);
-    const size_t o_status = take(sizeof(int));
-    const size_t o_tr = take((size_t)n);
-    const size_t o_ptrs = take(sizeof(void*) * 3 * n);
-    const size_t o_items = take(sizeof(int) * n);   // item -> plan matrix, per bucket slice
-    const size_t o_ones = take(sizeof(float) * n);
-    const size_t o_odbg = p->opts.keep_update ? take([&] {
+    L.o_mats = take(sizeof(MatDev) * n);
+    L.o_part = take(sizeof(float) * std::max<long long>(mom_part, 1));
+    L.o_cpart = take(sizeof(float) * std::max<long long>(col_part, 1));
+    L.o_inv = take(sizeof(float) * std::max<long long>(inv_elems, 1));
+    L.o_alpha = take(sizeof(float) * n);
+    L.o_status = take(sizeof(int));
+    L.o_tr = take((size_t)n);
+    L.o_ptrs = take(sizeof(void*) * 3 * n);
+    L.o_items = take(sizeof(int) * n);   // item -> plan matrix, per bucket slice
+    L.o_ones = take(sizeof(float) * n);
+    L.o_odbg = p->opts.keep_update ? take([&] {
         size_t t = 0;
         for (int i = 0; i < n; ++i) t += (size_t)round_up(p->mats[i].m * p->mats[i].n * 4, 256);
         return t;
@@ -618,8 +603,8 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
     // k + 1 prefixes.  Momentum lists: 2 per matrix plus 3 per chunk, at most 5n; chunk
     // RowNorm lists (rows once, column matrices three times): at most 3n + 4n; the
     // plan's: 3n + 4.  15n + 4 <= 17n + 16 of each.
-    const size_t o_lists = take(sizeof(int) * (size_t)(17 * n + 16));
-    const size_t o_prefix = take(sizeof(long long) * (size_t)(17 * n + 16));
+    L.o_lists = take(sizeof(int) * (size_t)(17 * n + 16));
+    L.o_prefix = take(sizeof(long long) * (size_t)(17 * n + 16));
     const size_t fixed_bytes = off;
 
     // ---- chunks: matrices in group order, a new chunk whenever the region would
@@ -629,34 +614,33 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
     if (cap > 0) {
         region_cap = (double)cap - (double)fixed_bytes;
         double need = 0;
-        for (int i = 0; i < n; ++i) need = std::max(need, mat_region_bytes(p->mats[i].r, p->mats[i].c) + 8 * 256.0);
-        if (region_cap < need) {
-            delete p;
-            return MUON_ERR_OOM;   // the cap cannot hold even the largest single matrix
-        }
+        for (int i = 0; i < n; ++i) need = std::max(need, (double)bucket_bytes(p->mats[i].r, p->mats[i].c, 1));
+        if (region_cap < need) return MUON_ERR_OOM;   // the cap cannot hold even the largest single matrix
     }
     if (p->opts.chunks > 1) {   // about opts.chunks chunks, each at least one matrix
         double total = 0, largest = 0;
         for (int i = 0; i < n; ++i) {
-            const double b = mat_region_bytes(p->mats[i].r, p->mats[i].c);
+            const double b = (double)bucket_bytes(p->mats[i].r, p->mats[i].c, 1);
             total += b;
-            largest = std::max(largest, b + 8 * 256.0);
+            largest = std::max(largest, b);
         }
-        const double per = total / p->opts.chunks + 8 * 256.0 * (double)group_rc.size();
+        const double per = total / p->opts.chunks;
         region_cap = std::min(region_cap, std::max(per, largest));
     }
     {
-        double used = 0;
+        long long used = 0;   // region bytes of the current chunk, exactly
         p->chunks.emplace_back();
         for (size_t g = 0; g < group_rc.size(); ++g) {
             const int r = group_rc[g].first, c = group_rc[g].second;
             int cur = -1;   // bucket of this group in the current chunk
             for (int i : group_mats[g]) {
-                const double need = mat_region_bytes(r, c) + (cur < 0 ? 8 * 256.0 : 0.0);
-                if (used + need > region_cap && used > 0) {
+                const long long k = cur < 0 ? 0 : (long long)p->buckets[cur].mats.size();
+                long long grow = bucket_bytes(r, c, k + 1) - (k > 0 ? bucket_bytes(r, c, k) : 0);
+                if ((double)(used + grow) > region_cap && used > 0) {
                     p->chunks.emplace_back();
                     used = 0;
                     cur = -1;
+                    grow = bucket_bytes(r, c, 1);
                 }
                 if (cur < 0) {
                     Bucket nb{};   // value-initialised: the tensor maps are filled in later
@@ -669,9 +653,8 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
                     p->buckets.push_back(nb);
                     cur = (int)p->buckets.size() - 1;
                     p->chunks.back().buckets.push_back(cur);
-                    used += 8 * 256.0;
                 }
-                used += mat_region_bytes(r, c);
+                used += grow;
                 p->mat_bucket[i] = cur;
                 p->mat_item[i] = (int)p->buckets[cur].mats.size();
                 p->buckets[cur].mats.push_back(i);
@@ -680,8 +663,14 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
     }
     // region offsets: each chunk's buckets laid out from the start of the region
     size_t region_bytes = 0;
-    std::vector<size_t> o_ut(p->buckets.size()), o_ut1(p->buckets.size()), o_rr(p->buckets.size()),
-        o_qb(p->buckets.size());
+    std::vector<size_t>& o_ut = L.o_ut;
+    std::vector<size_t>& o_ut1 = L.o_ut1;
+    std::vector<size_t>& o_rr = L.o_rr;
+    std::vector<size_t>& o_qb = L.o_qb;
+    o_ut.assign(p->buckets.size(), 0);
+    o_ut1.assign(p->buckets.size(), 0);
+    o_rr.assign(p->buckets.size(), 0);
+    o_qb.assign(p->buckets.size(), 0);
     {
         int slots = 0;
         for (auto& ch : p->chunks) {
@@ -708,7 +697,7 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
             region_bytes = std::max(region_bytes, roff);
         }
     }
-    const size_t o_region = take(std::max<size_t>(region_bytes, 256));
+    L.o_region = take(std::max<size_t>(region_bytes, 256));
     for (int i = 0; i < n; ++i) {
         MatDev& md = p->mats[i];
         const Bucket& b = p->buckets[p->mat_bucket[i]];
@@ -717,22 +706,71 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
         md.ut_off = (long long)(o_ut[p->mat_bucket[i]] / 2) + (long long)p->mat_item[i] * b.r * b.ldu;
     }
     p->ws_bytes = off;
+    // the packing counts the region exactly, so a cap is never exceeded; kept as a guard
+    if (cap > 0 && (long long)off > cap) return MUON_ERR_OOM;
+    return MUON_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* muon_last_error_detail(void) {
+    return g_last_cuda_error == cudaSuccess ? "no CUDA error recorded" : cudaGetErrorString(g_last_cuda_error);
+}
+
+const char* muon_status_string(muon_status s) {
+    switch (s) {
+        case MUON_OK: return "MUON_OK";
+        case MUON_ERR_INVALID_ARG: return "MUON_ERR_INVALID_ARG: invalid argument";
+        case MUON_ERR_UNSUPPORTED: return "MUON_ERR_UNSUPPORTED: unsupported dtype or size";
+        case MUON_ERR_OOM: return "MUON_ERR_OOM: workspace allocation failed";
+        case MUON_ERR_CUDA: return "MUON_ERR_CUDA: CUDA runtime or launch error";
+        case MUON_ERR_TIMEOUT: return "MUON_ERR_TIMEOUT: a bounded device wait expired";
+        case MUON_ERR_NONFINITE: return "MUON_ERR_NONFINITE";
+    }
+    return "MUON_ERR_UNKNOWN";
+}
+
+// Everything of muon_plan_create after the argument checks.  On failure it frees p;
+// a host allocation that throws leaves p to the caller.
+static muon_status plan_build(muon_plan_s* p, const muon_shape* shapes, int32_t n, muon_dtype grad_dtype,
+                              const muon_plan_opts* opts, muon_plan* out) {
+    if (cudaGetDevice(&p->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess ||
+        !encode_fn()) {
+        free_plan(p);
+        return MUON_ERR_CUDA;
+    }
+    p->gdt = grad_dtype;
+    if (opts) p->opts = *opts;
+    p->shapes.assign(shapes, shapes + n);
+
+    Layout L;
+    {
+        const muon_status st = plan_layout(p, L);
+        if (st != MUON_OK) {
+            free_plan(p);
+            return st;
+        }
+    }
+    const bool restarts = L.restarts;
     if (cudaMalloc(&p->ws, p->ws_bytes) != cudaSuccess) {
         cudaGetLastError();
         free_plan(p);
         return MUON_ERR_OOM;
     }
     char* base = static_cast<char*>(p->ws);
-    p->ut = reinterpret_cast<__nv_bfloat16*>(base + o_region);
-    p->d_mats = reinterpret_cast<MatDev*>(base + o_mats);
-    p->partials = reinterpret_cast<float*>(base + o_part);
-    p->cpartials = reinterpret_cast<float*>(base + o_cpart);
-    p->rowinv = reinterpret_cast<float*>(base + o_inv);
-    p->alpha = reinterpret_cast<float*>(base + o_alpha);
-    p->status = reinterpret_cast<int*>(base + o_status);
-    p->d_transposed = reinterpret_cast<unsigned char*>(base + o_tr);
-    p->d_ptrs = reinterpret_cast<void**>(base + o_ptrs);
-    p->ones = reinterpret_cast<float*>(base + o_ones);
+    p->ut = reinterpret_cast<__nv_bfloat16*>(base + L.o_region);
+    p->d_mats = reinterpret_cast<MatDev*>(base + L.o_mats);
+    p->partials = reinterpret_cast<float*>(base + L.o_part);
+    p->cpartials = reinterpret_cast<float*>(base + L.o_cpart);
+    p->rowinv = reinterpret_cast<float*>(base + L.o_inv);
+    p->alpha = reinterpret_cast<float*>(base + L.o_alpha);
+    p->status = reinterpret_cast<int*>(base + L.o_status);
+    p->d_transposed = reinterpret_cast<unsigned char*>(base + L.o_tr);
+    p->d_ptrs = reinterpret_cast<void**>(base + L.o_ptrs);
+    p->ones = reinterpret_cast<float*>(base + L.o_ones);
 
     std::vector<unsigned char> tr(n);
     for (int i = 0; i < n; ++i) tr[i] = (unsigned char)p->mats[i].transposed;
@@ -746,8 +784,8 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
     }
 
     // launch lists (int lists then long long prefixes, carved from their slices)
-    int* list_cursor = reinterpret_cast<int*>(base + o_lists);
-    long long* prefix_cursor = reinterpret_cast<long long*>(base + o_prefix);
+    int* list_cursor = reinterpret_cast<int*>(base + L.o_lists);
+    long long* prefix_cursor = reinterpret_cast<long long*>(base + L.o_prefix);
     auto upload_list = [&](const std::vector<int>& v, ListDev& d, int kind) {
         d.list = list_cursor;
         d.blk = prefix_cursor;
@@ -787,20 +825,20 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
         upload_list(tiles, ch.rn_final, 5);
         upload_list(tiles, ch.rn_apply, 6);
     }
-    upload_list(rnr_list, p->rn_rows, 3);
-    upload_list(rnc_list, p->rn_stats, 4);
-    upload_list(rnc_list, p->rn_final, 5);
-    upload_list(rnc_list, p->rn_apply, 6);
+    upload_list(L.rnr_list, p->rn_rows, 3);
+    upload_list(L.rnc_list, p->rn_stats, 4);
+    upload_list(L.rnc_list, p->rn_final, 5);
+    upload_list(L.rnc_list, p->rn_apply, 6);
 
-    int* item_cursor = reinterpret_cast<int*>(base + o_items);
-    size_t odbg_off = o_odbg;
+    int* item_cursor = reinterpret_cast<int*>(base + L.o_items);
+    size_t odbg_off = L.o_odbg;
     for (size_t k = 0; ok && k < p->buckets.size(); ++k) {
         Bucket& b = p->buckets[k];
         b.d_item_mat = item_cursor;
         item_cursor += b.batch;
         ok = cudaMemcpy(b.d_item_mat, b.mats.data(), sizeof(int) * b.batch, cudaMemcpyHostToDevice) == cudaSuccess;
         b.gscale = std::ldexp(1.f, (int)std::lround(std::log2((double)b.r)));
-        b.ut_off = (long long)(o_ut[k] / 2);
+        b.ut_off = (long long)(L.o_ut[k] / 2);
         if (p->opts.keep_update) {
             b.Odbg = reinterpret_cast<float*>(base + odbg_off);
             odbg_off += (size_t)round_up((long long)b.batch * b.r * b.c * 4, 256);
@@ -815,7 +853,7 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
             ok = ok && make_map4(&b.utt, ut, true, b.c, b.r, b.batch, b.ldu, 64, 2);
         }
         if (restarts) {
-            b.ut1_off = (long long)(o_ut1[k] / 2);
+            b.ut1_off = (long long)(L.o_ut1[k] / 2);
             __nv_bfloat16* ut1 = p->ut + b.ut1_off;
             ok = ok && make_map(&b.ut1_a, ut1, true, b.c, b.r, b.batch, b.ldu, 64, kBM);
             ok = ok && make_map(&b.ut1_b, ut1, true, b.c, b.r, b.batch, b.ldu, 64, kBN);
@@ -828,14 +866,14 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
         if (b.fused) continue;   // the fused kernel keeps its r x r operands on chip
         const size_t rr = (size_t)b.batch * b.r * b.ldr;
         const size_t step = (size_t)round_up((long long)rr * 2, 256);
-        char* rb = base + o_region + o_rr[k];
+        char* rb = base + L.o_region + L.o_rr[k];
         b.G[0] = reinterpret_cast<__half*>(rb);
         b.G[1] = reinterpret_cast<__half*>(rb + step);
         b.P = reinterpret_cast<__half*>(rb + 2 * step);
         b.T = reinterpret_cast<__half*>(rb + 3 * step);
         b.Q[0] = reinterpret_cast<__half*>(rb + 4 * step);
         b.Q[1] = reinterpret_cast<__half*>(rb + 5 * step);
-        b.Qb = reinterpret_cast<__nv_bfloat16*>(base + o_region + o_qb[k]);
+        b.Qb = reinterpret_cast<__nv_bfloat16*>(base + L.o_region + L.o_qb[k]);
         ok = ok && make_map(&b.qb_a, b.Qb, true, b.r, b.r, b.batch, b.ldr, 64, kBM);
         for (int g = 0; g < 2; ++g) {
             ok = ok && make_map(&b.ga[g], b.G[g], false, b.r, b.r, b.batch, b.ldr, 64, kBM);
@@ -920,6 +958,43 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
     p->h_cache.assign(3 * n, nullptr);
     *out = p;
     return MUON_OK;
+}
+
+muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype grad_dtype, const muon_plan_opts* opts,
+                             muon_plan* out) {
+    if (!out) return MUON_ERR_INVALID_ARG;
+    *out = nullptr;
+    const muon_status bad = check_plan_args(shapes, n, grad_dtype, opts);
+    if (bad != MUON_OK) return bad;
+    muon_plan_s* p = new (std::nothrow) muon_plan_s();
+    if (!p) return MUON_ERR_OOM;
+    try {
+        return plan_build(p, shapes, n, grad_dtype, opts, out);
+    } catch (...) {   // std::vector's bad_alloc / length_error: host memory
+        free_plan(p);
+        return MUON_ERR_OOM;
+    }
+}
+
+muon_status muon_plan_workspace_size(const muon_shape* shapes, int32_t n, muon_dtype grad_dtype,
+                                     const muon_plan_opts* opts, int64_t* bytes, int32_t* n_buckets,
+                                     int32_t* n_chunks) {
+    const muon_status bad = check_plan_args(shapes, n, grad_dtype, opts);
+    if (bad != MUON_OK) return bad;
+    try {
+        muon_plan_s plan;   // host fields only: nothing is created on the device
+        if (opts) plan.opts = *opts;
+        plan.shapes.assign(shapes, shapes + n);
+        Layout L;
+        const muon_status st = plan_layout(&plan, L);
+        if (st != MUON_OK) return st;
+        if (bytes) *bytes = (int64_t)plan.ws_bytes;
+        if (n_buckets) *n_buckets = (int32_t)plan.buckets.size();
+        if (n_chunks) *n_chunks = (int32_t)plan.chunks.size();
+        return MUON_OK;
+    } catch (...) {   // host memory
+        return MUON_ERR_OOM;
+    }
 }
 
 void muon_plan_destroy(muon_plan p) {
@@ -1303,13 +1378,18 @@ static muon_status host_copy_setup(muon_plan_s* p) {
               cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking) == cudaSuccess &&
               cudaEventCreateWithFlags(&h.entry_ev, cudaEventDisableTiming) == cudaSuccess &&
               cudaEventCreateWithFlags(&h.end_ev, cudaEventDisableTiming) == cudaSuccess;
-    h.in_ev.assign(nc, nullptr);
-    h.out_ev.assign(nc, nullptr);
+    bool host_ok = true;
+    try {
+        h.in_ev.assign(nc, nullptr);
+        h.out_ev.assign(nc, nullptr);
+    } catch (...) {
+        ok = host_ok = false;   // host memory
+    }
     for (size_t c = 0; ok && c < nc; ++c)
         ok = cudaEventCreateWithFlags(&h.in_ev[c], cudaEventDisableTiming) == cudaSuccess &&
              cudaEventCreateWithFlags(&h.out_ev[c], cudaEventDisableTiming) == cudaSuccess;
     if (ok) return MUON_OK;
-    g_last_cuda_error = cudaGetLastError();
+    if (host_ok) g_last_cuda_error = cudaGetLastError();
     if (h.in) cudaStreamDestroy(h.in);
     if (h.out) cudaStreamDestroy(h.out);
     h.in = h.out = nullptr;
@@ -1322,7 +1402,7 @@ static muon_status host_copy_setup(muon_plan_s* p) {
     if (h.entry_ev) cudaEventDestroy(h.entry_ev);
     if (h.end_ev) cudaEventDestroy(h.end_ev);
     h.entry_ev = h.end_ev = nullptr;
-    return MUON_ERR_CUDA;
+    return host_ok ? MUON_ERR_CUDA : MUON_ERR_OOM;
 }
 
 muon_status muon_step_host(muon_plan p, float* const* params, const void* const* grads, float* const* momentum,
@@ -1399,12 +1479,12 @@ muon_status muon_plan_tune(muon_plan p, float* const* params, const void* const*
     // symmetric r x r results stored as the lower triangle or whole
     bool mixed = false;
     for (const auto& ch : p->chunks) mixed = mixed || (ch.mixed && ch.chain_est > 0);
-    std::vector<float> scales = {1.f};
-    if (mixed && p->opts.chain_clusters == 0 && p->s2) scales = {1.f, 0.f, 0.5f, 1.5f};
+    const float scales[4] = {1.f, 0.f, 0.5f, 1.5f};
+    const int n_scales = mixed && p->opts.chain_clusters == 0 && p->s2 ? 4 : 1;
     bool lower_choice = false;   // chunks where lower-triangle storage is a choice
     for (const auto& ch : p->chunks) lower_choice = lower_choice || ch.lower_ok;
-    std::vector<bool> lowers = {true};
-    if (lower_choice && !p->opts.full_symmetric) lowers = {true, false};
+    const bool lowers[2] = {true, false};
+    const int n_lowers = lower_choice && !p->opts.full_symmetric ? 2 : 1;
     const int kmax = std::min(p->pair_clusters - 1, (p->sm_count - 2) / 2);
     auto apply = [&](float sc, bool q) {
         for (auto& ch : p->chunks)
@@ -1422,8 +1502,10 @@ muon_status muon_plan_tune(muon_plan p, float* const* params, const void* const*
     float best = 0.f, best_sc = 1.f;
     bool best_q = true;
     int tried = 0;
-    for (float sc : scales) {
-        for (bool q : lowers) {
+    for (int si = 0; si < n_scales; ++si) {
+        for (int qi = 0; qi < n_lowers; ++qi) {
+            const float sc = scales[si];
+            const bool q = lowers[qi];
             apply(sc, q);
             st = muon_step_ex(p, params, grads, momentum, lr, wd, mu, kMaxNsSteps, nullptr, 0, stream);   // warm-up
             if (st == MUON_OK && cudaEventRecord(e0, s) != cudaSuccess) st = MUON_ERR_CUDA;
@@ -1512,7 +1594,12 @@ muon_status muon_debug_copy_workspace(muon_plan p, int32_t i, int32_t which, voi
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (which >= 1 && which <= 7 && b.r > kBM && p->chunks[b.chunk].lower) {
         // lower-triangle storage (256 x 256 tiles at or below the diagonal): rebuild the upper part
-        std::vector<uint16_t> h(rr);
+        std::vector<uint16_t> h;
+        try {
+            h.resize(rr);
+        } catch (...) {
+            return MUON_ERR_OOM;   // host memory
+        }
         if (cudaMemcpyAsync(h.data(), src, bytes, cudaMemcpyDefault, s) != cudaSuccess ||
             cudaStreamSynchronize(s) != cudaSuccess)
             return MUON_ERR_CUDA;

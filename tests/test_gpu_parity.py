@@ -710,3 +710,24 @@ def test_lower_triangle_storage_other_steps_and_restarts(ns_steps, restart):
         assert_ns(low, i, ns_steps=ns_steps)
     lplan.close()
     wplan.close()
+
+
+def test_plan_allocates_what_host_sizing_reports():
+    """muon_plan_workspace_size (host only) and a real plan agree on the workspace
+    bytes, buckets and chunks, with and without caps, chunks, restarts and the O copy."""
+    import matrix_orthogonalising_optimizer_muon_gb300 as lib
+    layer = [(3584, 3584), (512, 3584), (512, 3584), (3584, 3584), (18944, 3584), (18944, 3584), (3584, 18944)]
+    mixed = [(300, 1000), (1000, 300), (64, 64), (129, 4096), (4096, 256)] * 3
+    cases = [(layer, {}), (layer, {"chunks": 3}), (layer, {"max_ns_steps": 10}),
+             (mixed, {}), (mixed, {"keep_update": True}), (mixed, {"generic_small": True, "chunks": 4})]
+    full = lib.plan_workspace_size(layer)["workspace_bytes"]
+    cases.append((layer, {"workspace_bytes": full - 1}))
+    for shapes, opts in cases:
+        est = lib.plan_workspace_size(shapes, "bf16", **opts)
+        plan = lib.MuonPlan(shapes, "bf16", **opts)
+        info = plan.info()
+        plan.close()
+        got = {"workspace_bytes": info["workspace_bytes"], "n_buckets": info["n_buckets"],
+               "n_chunks": info["n_chunks"]}
+        assert got == est, (opts, got, est)
+    assert lib.plan_workspace_size(layer, workspace_bytes=full - 1)["n_chunks"] >= 2
