@@ -113,7 +113,8 @@ typedef struct muon_plan_s* muon_plan;
 
 /*
  * muon_plan_create - plan a step for a fixed list of matrix shapes ("muon_plan(shapes)").
- *   shapes     host array of n shapes (rows, cols >= 1).
+ *   shapes     host array of n shapes: 1 <= rows, cols <= 2^20 and
+ *              min(rows, cols) <= 32768, else MUON_ERR_UNSUPPORTED.
  *   grad_dtype dtype of every gradient: MUON_F32 or MUON_BF16.
  *   opts       may be NULL (all zero).
  *   out        receives the plan.

@@ -731,3 +731,20 @@ def test_plan_allocates_what_host_sizing_reports():
                "n_chunks": info["n_chunks"]}
         assert got == est, (opts, got, est)
     assert lib.plan_workspace_size(layer, workspace_bytes=full - 1)["n_chunks"] >= 2
+
+
+LONGEST = [(1, 1 << 20), (1 << 20, 8), (1 << 20, 136)]
+
+
+@pytest.mark.parametrize("mode", ["ns", "rownorm"])
+def test_longest_side_the_library_accepts(mode):
+    """Long side 2^20, the per-dimension limit: a row vector and a thin transposed matrix
+    on the fused kernel, and r = 136 on the CTA-pair kernel (one ragged 256 x 256 pair
+    tile whose SYRK runs 2^14 k-blocks)."""
+    res = run_step(LONGEST, "bf16", base_seed=77, mode=mode)
+    for i in range(len(LONGEST)):
+        if mode == "ns":
+            assert_ns(res, i)
+        else:
+            e = check_rownorm_matrix(res, i)
+            assert e["m"] <= TOL_FP32 and e["w"] <= TOL_FP32, (i, e)

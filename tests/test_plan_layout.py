@@ -155,3 +155,12 @@ def test_sizing_rejects_what_plan_create_rejects():
         assert f(bad, 1, mu.MUON_BF16, ctypes.byref(o), None, None, None) == mu.MUON_ERR_INVALID_ARG
     # NULL outputs are allowed
     assert f(bad, 1, mu.MUON_BF16, None, None, None, None) == mu.MUON_OK
+
+
+def test_size_limits():
+    # each side up to 2^20, r = min(m, n) up to 32768; sizing needs no memory
+    assert ws([(1 << 20, 32768), (32768, 1 << 20), (1, 1 << 20)])["n_buckets"] == 2
+    for bad in ([((1 << 20) + 1, 8)], [(8, (1 << 20) + 1)], [(32769, 40000)]):
+        with pytest.raises(mu.MuonError) as e:
+            ws(bad)
+        assert e.value.code == mu.MUON_ERR_UNSUPPORTED
