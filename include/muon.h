@@ -23,8 +23,10 @@
  *  - stream is a cudaStream_t passed as void* (NULL = legacy default stream).
  *    All device work is enqueued on it (muon_step_host and the overlapped
  *    fused/batched products also use streams of the plan, joined back into it);
- *    no call synchronises the host except muon_sync, muon_plan_tune, the
- *    muon_debug_copy_* calls, and muon_step_host with pageable host memory.
+ *    no call synchronises the host except muon_plan_create and
+ *    muon_plan_destroy (the whole device: they allocate and free the workspace),
+ *    muon_sync, muon_plan_tune, the muon_debug_copy_* calls, and muon_step_host
+ *    with pageable host memory.
  *  - A plan is not thread-safe: its calls share one workspace, pinned pointer
  *    table and event set, so calls on one plan must not overlap, and steps of one
  *    plan issued to different streams must be ordered by the caller.  Separate
@@ -145,6 +147,12 @@ muon_status muon_plan_workspace_size(const muon_shape* shapes, int32_t n, muon_d
                                      const muon_plan_opts* opts, int64_t* bytes, int32_t* n_buckets,
                                      int32_t* n_chunks);
 
+/*
+ * muon_plan_destroy - wait for the device to go idle (cudaDeviceSynchronize, so
+ * no step of the plan is still running), then free everything the plan owns: its
+ * workspace, streams, events and pinned pointer table.  NULL is ignored.  The
+ * handle must not be used afterwards.
+ */
 void muon_plan_destroy(muon_plan p);
 
 /*
