@@ -382,3 +382,17 @@ class PeriodicRowNormMuon:
             self.plan.rownorm_step(params, grads, momentum, lr, wd, mu, self.eps, stream)
         self.t += 1
         return mode
+
+    def state_dict(self) -> dict:
+        """The schedule's state for a checkpoint: the next step's index and its settings.
+        (Momentum buffers belong to the caller and are checkpointed with the model.)"""
+        return {"t": self.t, "k": self.k, "eps": self.eps, "ns_steps": self.ns_steps}
+
+    def load_state_dict(self, state: dict) -> None:
+        """Resume from ``state_dict()``: the next step runs as step ``t`` of the saved run."""
+        t, k = int(state["t"]), int(state["k"])
+        if t < 0 or k <= 0:
+            raise ValueError("bad schedule state: t = %d, K = %d" % (t, k))
+        self.t, self.k = t, k
+        self.eps = float(state.get("eps", self.eps))
+        self.ns_steps = int(state.get("ns_steps", self.ns_steps))

@@ -94,3 +94,29 @@ def test_schedule_helper():
     assert p.calls == modes
     with pytest.raises(ValueError):
         mu.PeriodicRowNormMuon(p, k=0)
+
+
+def test_schedule_resumes_from_its_state():
+    class FakePlan:
+        def __init__(self):
+            self.calls = []
+
+        def step(self, *a, **k):
+            self.calls.append("ns")
+
+        def rownorm_step(self, *a, **k):
+            self.calls.append("rownorm")
+
+    whole = mu.PeriodicRowNormMuon(FakePlan(), k=4, eps=1e-7)
+    ref = [whole.step([], [], [], 0.02, 0.1) for _ in range(11)]
+    first = mu.PeriodicRowNormMuon(FakePlan(), k=4, eps=1e-7)
+    got = [first.step([], [], [], 0.02, 0.1) for _ in range(6)]
+    state = dict(first.state_dict())
+    resumed = mu.PeriodicRowNormMuon(FakePlan(), k=9)   # settings come from the state
+    resumed.load_state_dict(state)
+    assert (resumed.k, resumed.eps, resumed.t) == (4, 1e-7, 6)
+    got += [resumed.step([], [], [], 0.02, 0.1) for _ in range(5)]
+    assert got == ref
+    for bad in ({"t": -1, "k": 4}, {"t": 0, "k": 0}):
+        with pytest.raises(ValueError):
+            resumed.load_state_dict(bad)
