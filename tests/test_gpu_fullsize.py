@@ -104,14 +104,16 @@ def test_qwen7b_28l_layers_0_and_27():
     assert len(rms) == 196 and all(0.6 < x < 1.2 for x in rms)
 
 
-def test_dit_periodic_rownorm_8_steps_block0():
-    """28 DiT blocks, K = 4 over 8 steps with fresh grads; block 0 followed by the oracle."""
+def test_dit_periodic_rownorm_8_steps():
+    """28 DiT blocks, K = 4 over 8 steps with fresh grads; blocks 0 and 27 followed by the
+    oracle, and at the RowNorm step t = 1 every matrix's update direction, recovered from W
+    before and after, has unit oriented rows (a property of R_eps at any size)."""
     import torch
     import workloads
     import matrix_orthogonalising_optimizer_muon_gb300 as lib
     wl = workloads.WORKLOADS["dit1p3b"]
     W, G, M = device_inputs(wl)
-    sample = list(range(5))
+    sample = list(range(5)) + list(range(135, 140))
     w_ref = {i: W[i].double().cpu().numpy() for i in sample}
     m_ref = {i: M[i].double().cpu().numpy() for i in sample}
     plan = lib.MuonPlan(list(wl.shapes), wl.grad_dtype)
@@ -121,7 +123,18 @@ def test_dit_periodic_rownorm_8_steps_block0():
             for i, (m, n) in enumerate(wl.shapes):
                 G[i] = workloads.gen_tensor((m, n), workloads.G_STD, workloads.seed_of(wl.index, t, i, "G"),
                                             "cuda", wl.grad_dtype)
+        w_before = [w.clone() for w in W] if t == 1 else None
         mode = sched.step(W, G, M, LR, WD)
+        if w_before is not None:
+            plan.sync()
+            assert mode == "rownorm"
+            worst = 0.0
+            for i, (m, n) in enumerate(wl.shapes):
+                d = ((1.0 - LR * WD) * w_before[i].double() - W[i].double()) / (LR * R.update_scale(m, n))
+                norms = d.norm(dim=1) if m <= n else d.norm(dim=0)
+                worst = max(worst, float((norms - 1.0).abs().max()))
+            del w_before
+            assert worst <= 1e-4, worst
         for i in sample:
             g = G[i].double().cpu().numpy()
             w_ref[i], m_ref[i], _ = R.muon_step(w_ref[i], g, m_ref[i], LR, WD, MU, 5, mode, wl.eps, form="gram")
