@@ -748,3 +748,38 @@ def test_longest_side_the_library_accepts(mode):
         else:
             e = check_rownorm_matrix(res, i)
             assert e["m"] <= TOL_FP32 and e["w"] <= TOL_FP32, (i, e)
+
+
+@pytest.mark.parametrize("shapes,lower", [
+    (RAGGED, False),
+    ([(640, 1280), (1280, 640), (256, 1024), (128, 2048), (2048, 64)], True),
+], ids=["ragged", "lower_triangle"])
+def test_steps_write_nothing_outside_the_callers_buffers(shapes, lower):
+    """Every W, G and M is a view into a larger allocation, 4096 elements of guard on each
+    side (the views stay 256-byte aligned, so the kernels take their usual paths).  After
+    an NS step and a RowNorm step every guard is bit-identical and G is untouched."""
+    import torch
+    import matrix_orthogonalising_optimizer_muon_gb300 as lib
+    guard = 4096
+    inputs = host_inputs(shapes, "bf16", base_seed=91)
+    bufs, views = [], {"W": [], "G": [], "M": []}
+    for w, g, m in inputs:
+        for name, t in (("W", w), ("G", g), ("M", m)):
+            n = t.numel()
+            buf = torch.randn(n + 2 * guard, device="cuda").to(t.dtype)
+            view = buf[guard:guard + n].view(t.shape)
+            view.copy_(t.cuda())
+            assert view.is_contiguous() and view.data_ptr() % 256 == buf.data_ptr() % 256
+            bufs.append((buf, n, buf.clone()))
+            views[name].append(view)
+    g_before = [g.clone() for g in views["G"]]
+    plan = lib.MuonPlan(shapes, "bf16")
+    plan.step(views["W"], views["G"], views["M"], LR, WD, MU, 5, "ns")
+    plan.rownorm_step(views["W"], views["G"], views["M"], LR, WD, MU, 1e-8)
+    plan.sync()
+    for buf, n, ref in bufs:
+        assert torch.equal(buf[:guard], ref[:guard]) and torch.equal(buf[guard + n:], ref[guard + n:])
+    for g, g0 in zip(views["G"], g_before):
+        assert torch.equal(g, g0)
+    if lower:
+        assert plan.info()["lower_chunks"] == 1
