@@ -783,3 +783,43 @@ def test_steps_write_nothing_outside_the_callers_buffers(shapes, lower):
         assert torch.equal(g, g0)
     if lower:
         assert plan.info()["lower_chunks"] == 1
+
+
+def test_resume_from_saved_state_is_bitwise():
+    """Eight periodic RowNorm Muon steps (K = 4, fresh gradients each step) run straight
+    equal, bitwise, four steps, a save of W, M and the schedule to host memory, a new plan
+    restored from the save, and four more steps.  The optimizer's state is the momentum
+    and the step index; the plan keeps nothing else between steps."""
+    import torch
+    import matrix_orthogonalising_optimizer_muon_gb300 as lib
+    shapes = [(300, 1000), (1000, 300), (128, 512), (640, 1280), (64, 4096)]
+    base = host_inputs(shapes, "bf16", base_seed=55)
+    grads = [[g for _, g, _ in host_inputs(shapes, "bf16", base_seed=55, step=t)] for t in range(8)]
+
+    def run(steps, W, M, state=None):
+        plan = lib.MuonPlan(shapes, "bf16")
+        sched = lib.PeriodicRowNormMuon(plan, k=4)
+        if state is not None:
+            sched.load_state_dict(state)
+        for t in steps:
+            assert sched.t == t
+            sched.step(W, [g.cuda() for g in grads[t]], M, LR, WD)
+        plan.sync()
+        out = sched.state_dict()
+        plan.close()
+        return out
+
+    W1 = [w.cuda() for w, _, _ in base]
+    M1 = [m.cuda() for _, _, m in base]
+    run(range(8), W1, M1)
+    W2 = [w.cuda() for w, _, _ in base]
+    M2 = [m.cuda() for _, _, m in base]
+    state = run(range(4), W2, M2)
+    saved = ([w.cpu() for w in W2], [m.cpu() for m in M2], dict(state))
+    del W2, M2
+    W3 = [w.cuda() for w in saved[0]]
+    M3 = [m.cuda() for m in saved[1]]
+    run(range(4, 8), W3, M3, saved[2])
+    for i in range(len(shapes)):
+        assert torch.equal(W1[i], W3[i]), ("W", i)
+        assert torch.equal(M1[i], M3[i]), ("M", i)
