@@ -55,7 +55,7 @@ typedef enum {
     MUON_ERR_OOM = 3,           /* workspace allocation failed */
     MUON_ERR_CUDA = 4,          /* a CUDA runtime or launch error */
     MUON_ERR_TIMEOUT = 5,       /* a device-side bounded wait expired */
-    MUON_ERR_NONFINITE = 6      /* reserved */
+    MUON_ERR_NONFINITE = 6      /* a non-finite input norm (opts.check_finite), reported by muon_sync */
 } muon_status;
 
 typedef enum { MUON_F32 = 0, MUON_BF16 = 1 } muon_dtype;
@@ -109,6 +109,22 @@ typedef struct {
        blocks above it from the mirror position), which saves the mirrored half of the
        epilogue's stores.  Results are the same. */
     int32_t full_symmetric;
+    /* Which matrices with min(m, n) <= 128 run the NS step in fp32 on CUDA cores (one
+       matrix per CTA, the Gram recursion of DMuon's "Gram Newton-Schulz" with every
+       product in fp32) instead of on the tensor cores.  A nearly square Gaussian
+       matrix has singular values near zero, which the quintic amplifies by about
+       a^5 ~ 485; the tensor-core recipe (bf16 X0 and Q, fp16 Gram recursion) moves
+       its O by 1.3e-2 to 8e-2, the fp32 path by about 1e-5.  0: matrices with
+       max(m, n) < 1.25 min(m, n); > 0: every matrix with min(m, n) <= 128 (slower for
+       long matrices: the fp32 products run at CUDA-core rate); < 0: none.  Plans with
+       max_ns_steps > 0 never use it.  generic_small does not apply to these matrices. */
+    int32_t small_fp32;
+    /* nonzero: every step also checks its inputs for NaN and infinity: the squared norm
+       of each matrix's Nesterov input U (NS steps) and of each RowNorm row (RowNorm
+       steps) must be finite.  A non-finite one is recorded in the plan's device status
+       word and the next muon_sync returns MUON_ERR_NONFINITE.  The step still runs (the
+       update of such a matrix is then not finite).  0: no check. */
+    int32_t check_finite;
 } muon_plan_opts;
 
 typedef struct muon_plan_s* muon_plan;
@@ -246,7 +262,9 @@ muon_status muon_plan_tune(muon_plan p, float* const* params, const void* const*
 /*
  * muon_sync - wait for the plan's work on stream, then read and clear the
  * device status word.  Returns MUON_ERR_TIMEOUT if a bounded device wait
- * expired since the last muon_sync, MUON_ERR_CUDA on a CUDA error.
+ * expired since the last muon_sync, else MUON_ERR_NONFINITE if a step of a plan
+ * created with opts.check_finite met a non-finite input norm since then,
+ * MUON_ERR_CUDA on a CUDA error.
  */
 muon_status muon_sync(muon_plan p, void* stream);
 
@@ -299,9 +317,12 @@ muon_status muon_debug_copy_workspace(muon_plan p, int32_t i, int32_t which, voi
  * Scratch: when rows > cols the column statistics live in a 4 MiB array that is
  * part of the library image (every GPU that loads the library holds it until
  * the process exits); ceil(rows/64)*cols + cols floats must fit in 2^20, else
- * MUON_ERR_UNSUPPORTED is returned and nothing is launched.  The first call on
- * a device looks the array's device address up once (make that first call
- * before any stream capture).  Calls share the array, so calls that overlap
+ * MUON_ERR_UNSUPPORTED is returned and nothing is launched.  Every call looks
+ * the array's device address up in the current context (a host-side query with
+ * no allocation and no synchronisation, so a context that was reset gets the
+ * new address); the first call on a device may load the library's device code,
+ * so make it before any stream capture.  A failed lookup or launch returns
+ * MUON_ERR_CUDA and is reported by muon_last_error_detail.  Calls share the array, so calls that overlap
  * on the GPU (other streams, other host threads) race.  Nothing in the array
  * needs clearing: each call writes every word it reads.
  */

@@ -23,7 +23,7 @@ from .build import LIB, build, up_to_date
 __all__ = [
     "MuonError", "MuonPlan", "PeriodicRowNormMuon", "plan_workspace_size", "load", "build",
     "MUON_OK", "MUON_ERR_INVALID_ARG", "MUON_ERR_UNSUPPORTED", "MUON_ERR_OOM",
-    "MUON_ERR_CUDA", "MUON_ERR_TIMEOUT", "MUON_F32", "MUON_BF16",
+    "MUON_ERR_CUDA", "MUON_ERR_TIMEOUT", "MUON_ERR_NONFINITE", "MUON_F32", "MUON_BF16",
     "MUON_MODE_NS", "MUON_MODE_ROWNORM", "EXPORTED",
 ]
 
@@ -46,7 +46,8 @@ class MuonPlanOpts(ctypes.Structure):
                 ("single_sm_gemm", ctypes.c_int32), ("generic_small", ctypes.c_int32),
                 ("chain_clusters", ctypes.c_int32), ("max_ns_steps", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64), ("chunks", ctypes.c_int32),
-                ("full_symmetric", ctypes.c_int32)]
+                ("full_symmetric", ctypes.c_int32), ("small_fp32", ctypes.c_int32),
+                ("check_finite", ctypes.c_int32)]
 
 
 class MuonPlanInfo(ctypes.Structure):
@@ -145,13 +146,14 @@ def _ptr_array(ptrs):
 
 def _plan_args(shapes, grad_dtype, keep_update=False, timing=False, single_sm_gemm=False,
                generic_small=False, chain_clusters=0, workspace_bytes=0, max_ns_steps=0, chunks=0,
-               full_symmetric=False):
+               full_symmetric=False, small_fp32=0, check_finite=False):
     """(shape list, MuonShape array, dtype code, MuonPlanOpts) of a plan's arguments."""
     shapes = [(int(m), int(n)) for m, n in shapes]
     arr = (MuonShape * len(shapes))(*[MuonShape(m, n) for m, n in shapes])
     opts = MuonPlanOpts(1 if keep_update else 0, 1 if timing else 0, 1 if single_sm_gemm else 0,
                         1 if generic_small else 0, int(chain_clusters), int(max_ns_steps),
-                        int(workspace_bytes), int(chunks), 1 if full_symmetric else 0)
+                        int(workspace_bytes), int(chunks), 1 if full_symmetric else 0, int(small_fp32),
+                        1 if check_finite else 0)
     return shapes, arr, {"bf16": MUON_BF16, "f32": MUON_F32}[grad_dtype], opts
 
 
@@ -177,11 +179,11 @@ class MuonPlan:
     def __init__(self, shapes, grad_dtype: str = "bf16", keep_update: bool = False,
                  timing: bool = False, single_sm_gemm: bool = False, generic_small: bool = False,
                  chain_clusters: int = 0, workspace_bytes: int = 0, max_ns_steps: int = 0, chunks: int = 0,
-                 full_symmetric: bool = False):
+                 full_symmetric: bool = False, small_fp32: int = 0, check_finite: bool = False):
         self.lib = load()
         self.shapes, arr, gd, opts = _plan_args(shapes, grad_dtype, keep_update, timing, single_sm_gemm,
                                                 generic_small, chain_clusters, workspace_bytes, max_ns_steps,
-                                                chunks, full_symmetric)
+                                                chunks, full_symmetric, small_fp32, check_finite)
         self.grad_dtype = grad_dtype
         h = ctypes.c_void_p()
         _check(self.lib.muon_plan_create(arr, len(self.shapes), gd, ctypes.byref(opts),

@@ -126,6 +126,8 @@ inline long long round_up(long long a, long long b) { return ceil_div(a, b) * b;
 struct Bucket {
     int r = 0, c = 0, batch = 0;
     bool fused = false;     // r <= 128: whole step in the fused one-matrix-per-CTA kernel
+    bool f32 = false;       // r <= 128, nearly square: whole step in fp32 on CUDA cores (ns_f32_kernel)
+    bool batched() const { return !fused && !f32; }   // r x r buffers in the workspace, grouped products
     int chunk = 0;          // workspace chunk (see muon_plan_opts.workspace_bytes)
     long long ut1_off = -1; // second X buffer (restarted NS segments), element offset like ut_off
     CUtensorMap ut1_a, ut1_b, ut1_mn;
@@ -235,8 +237,12 @@ struct muon_plan_s {
 };
 
 namespace {
-
 thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+}  // namespace
+
+void muon::record_cuda_error(cudaError_t e) { g_last_cuda_error = e; }
+
+namespace {
 
 muon_status cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return MUON_OK;
@@ -325,6 +331,8 @@ ElemArgs elem_args(const muon_plan_s* p, const ListDev& l, float mu, float lr, f
     a.wd = wd;
     a.eps = eps;
     a.grad_bf16 = p->gdt == MUON_BF16;
+    a.check_finite = p->opts.check_finite ? 1 : 0;
+    a.status = p->status;
     return a;
 }
 
@@ -549,14 +557,20 @@ muon_status plan_layout(muon_plan_s* p, Layout& L) {
     // launch lists, debug copies of O) and a region for the X0 and r x r buffers of
     // one chunk of matrices, shared by all chunks (they run one after the other)
     const bool restarts = L.restarts = p->opts.max_ns_steps > 0;   // second X buffer, batched path for all
+    // fp32 path (opts.small_fp32): 0 nearly square (c < 1.25 r) matrices with r <= 128,
+    // > 0 every matrix with r <= 128, < 0 none; never in plans with restarts
+    auto is_f32 = [&](int r, int c) {
+        if (restarts || p->opts.small_fp32 < 0 || r > kF32MaxR) return false;
+        return p->opts.small_fp32 > 0 || 4LL * c < 5LL * r;
+    };
     const bool fused_ok = !p->opts.generic_small && !restarts;
-    auto is_fused = [&](int r) { return fused_ok && r <= kSmallMaxR; };
+    auto is_fused = [&](int r, int c) { return fused_ok && r <= kSmallMaxR && !is_f32(r, c); };
     // region bytes of a bucket of `batch` matrices, exactly as laid out below: its X0
     // (and second X) buffer and, batched, its seven r x r buffers, each rounded to 256
     auto bucket_bytes = [&](int r, int c, long long batch) -> long long {
         const long long x = round_up(batch * r * round_up(c, 8) * 2, 256);
         const long long rr = round_up(batch * r * round_up(r, 8) * 2, 256);
-        return (restarts ? 2 : 1) * x + (is_fused(r) ? 0 : 7 * rr);
+        return (restarts ? 2 : 1) * x + (is_fused(r, c) || is_f32(r, c) ? 0 : 7 * rr);
     };
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -648,7 +662,8 @@ muon_status plan_layout(muon_plan_s* p, Layout& L) {
                     nb.c = c;
                     nb.ldr = (int)round_up(r, 8);
                     nb.ldu = (int)round_up(c, 8);
-                    nb.fused = is_fused(r);
+                    nb.fused = is_fused(r, c);
+                    nb.f32 = is_f32(r, c);
                     nb.chunk = (int)p->chunks.size() - 1;
                     p->buckets.push_back(nb);
                     cur = (int)p->buckets.size() - 1;
@@ -687,7 +702,7 @@ muon_status plan_layout(muon_plan_s* p, Layout& L) {
                 slots += b.batch;
                 o_ut[k] = rtake((size_t)b.batch * b.r * b.ldu * 2);
                 if (restarts) o_ut1[k] = rtake((size_t)b.batch * b.r * b.ldu * 2);
-                if (!b.fused) {
+                if (b.batched()) {
                     const size_t rr = (size_t)b.batch * b.r * b.ldr * 2;
                     o_rr[k] = rtake(rr);   // G0 (fp16, scaled)
                     for (int q = 0; q < 5; ++q) rtake(rr);   // G1, P, T, Q0, Q1
@@ -727,7 +742,7 @@ const char* muon_status_string(muon_status s) {
         case MUON_ERR_OOM: return "MUON_ERR_OOM: workspace allocation failed";
         case MUON_ERR_CUDA: return "MUON_ERR_CUDA: CUDA runtime or launch error";
         case MUON_ERR_TIMEOUT: return "MUON_ERR_TIMEOUT: a bounded device wait expired";
-        case MUON_ERR_NONFINITE: return "MUON_ERR_NONFINITE";
+        case MUON_ERR_NONFINITE: return "MUON_ERR_NONFINITE: a non-finite input norm (opts.check_finite)";
     }
     return "MUON_ERR_UNKNOWN";
 }
@@ -847,7 +862,7 @@ static muon_status plan_build(muon_plan_s* p, const muon_shape* shapes, int32_t 
         ok = ok && make_map(&b.ut_a, ut, true, b.c, b.r, b.batch, b.ldu, 64, kBM);
         ok = ok && make_map(&b.ut_b, ut, true, b.c, b.r, b.batch, b.ldu, 64, kBN);
         ok = ok && make_map(&b.ut_mn, ut, true, b.c, b.r, b.batch, b.ldu, 64, 64);
-        const bool aligned4 = !b.fused && b.r % 64 == 0 && b.c % 64 == 0;
+        const bool aligned4 = b.batched() && b.r % 64 == 0 && b.c % 64 == 0;
         if (aligned4) {
             ok = ok && make_map4(&b.utk, ut, true, b.c, b.r, b.batch, b.ldu, 128, 1);
             ok = ok && make_map4(&b.utt, ut, true, b.c, b.r, b.batch, b.ldu, 64, 2);
@@ -863,7 +878,7 @@ static muon_status plan_build(muon_plan_s* p, const muon_shape* shapes, int32_t 
                 ok = ok && make_map4(&b.ut1t, ut1, true, b.c, b.r, b.batch, b.ldu, 64, 2);
             }
         }
-        if (b.fused) continue;   // the fused kernel keeps its r x r operands on chip
+        if (!b.batched()) continue;   // the one-CTA kernels keep their r x r operands on chip
         const size_t rr = (size_t)b.batch * b.r * b.ldr;
         const size_t step = (size_t)round_up((long long)rr * 2, 256);
         char* rb = base + L.o_region + L.o_rr[k];
@@ -907,6 +922,7 @@ static muon_status plan_build(muon_plan_s* p, const muon_shape* shapes, int32_t 
     ok = ok && cudaMallocHost(&p->h_pinned, sizeof(void*) * 3 * n) == cudaSuccess;
     ok = ok && cudaEventCreateWithFlags(&p->upload_ev, cudaEventDisableTiming) == cudaSuccess;
     ok = ok && gemm_prepare(p->device) == cudaSuccess;
+    ok = ok && ns_f32_prepare() == cudaSuccess;
     if (ok && !p->opts.single_sm_gemm) {
         int clusters = 0;
         ok = gemm2_max_clusters(&clusters) == cudaSuccess;
@@ -916,7 +932,7 @@ static muon_status plan_build(muon_plan_s* p, const muon_shape* shapes, int32_t 
         bool aligned = true;
         for (int k : ch.buckets) {
             const Bucket& b = p->buckets[k];
-            if (!b.fused && b.r > kBM) aligned = aligned && b.r % 64 == 0 && b.c % 64 == 0;
+            if (b.batched() && b.r > kBM) aligned = aligned && b.r % 64 == 0 && b.c % 64 == 0;
         }
         ch.lower_ok = p->pair_clusters > 0 && aligned;
         ch.lower = ch.lower_ok && !p->opts.full_symmetric;
@@ -930,7 +946,7 @@ static muon_status plan_build(muon_plan_s* p, const muon_shape* shapes, int32_t 
                 const double r = b.r, c = b.c;
                 if (b.fused)
                     fused_bytes += 12.0 * r * c * b.batch;
-                else
+                else if (b.batched())
                     chain_flops += (3.0 * r * r * c + 17.0 * r * r * r) * b.batch;
             }
             if (fused_bytes > 0 && chain_flops > 0) {
@@ -1102,7 +1118,7 @@ static muon_status ns_step(muon_plan p, float* const* params, const void* const*
     // HBM-bound and timed as a stage of its own)
     double fl_syrk = 0, fl_rr = 0, fl_final = 0;
     for (auto& b : p->buckets) {
-        if (b.fused) continue;
+        if (!b.batched()) continue;
         const double r = b.r, c = b.c;
         for (int sg = 0; sg < nseg; ++sg) {   // per segment: SYRK, 4Js-3 r x r products, r x c product
             const int Js = sg == nseg - 1 ? ns_steps - sg * period : period;
@@ -1193,6 +1209,50 @@ static muon_status ns_step(muon_plan p, float* const* params, const void* const*
             }
             if ((st = flush_small()) != MUON_OK) return st;
         }
+        // ---- small nearly square matrices: the whole step in fp32 on CUDA cores
+        {
+            F32Launch Lf;
+            std::memset(&Lf, 0, sizeof(Lf));
+            auto reset_f32 = [&]() {
+                std::memset(&Lf, 0, sizeof(Lf));
+                Lf.mats = p->d_mats;
+                Lf.G = const_cast<const void* const*>(p->d_ptrs);
+                Lf.M = reinterpret_cast<float* const*>(p->d_ptrs + n);
+                Lf.W = reinterpret_cast<float* const*>(p->d_ptrs + 2 * n);
+                Lf.mu = mu;
+                Lf.lr = lr;
+                Lf.wd = wd;
+                Lf.grad_bf16 = p->gdt == MUON_BF16;
+            };
+            auto flush_f32 = [&]() -> muon_status {
+                if (Lf.nprob == 0) return MUON_OK;
+                const muon_status st2 = cuda_status(ns_f32_launch(Lf, fused_grid, s));
+                ++launches;
+                reset_f32();
+                return st2;
+            };
+            reset_f32();
+            for (int bk : ch.buckets) {
+                Bucket& b = p->buckets[bk];
+                if (!b.f32) continue;
+                if (Lf.nprob == kMaxProblems && (st = flush_f32()) != MUON_OK) return st;
+                F32Problem& q = Lf.prob[Lf.nprob++];
+                q.r = b.r;
+                q.c = b.c;
+                q.batch = b.batch;
+                q.item_begin = Lf.total;
+                q.ns_steps = ns_steps;
+                q.item_mat = b.d_item_mat;
+                q.alpha = p->alpha + b.slot_base;
+                q.Odbg = b.Odbg;
+                q.coef_a = ca;
+                q.coef_b = cb;
+                q.coef_c = cc;
+                q.scale = 0.2f * std::sqrt((float)b.c);
+                Lf.total += b.batch;
+            }
+            if ((st = flush_f32()) != MUON_OK) return st;
+        }
         if (ev) MUON_TRY(cudaEventRecord(ev[6], s));
 
 
@@ -1206,7 +1266,7 @@ static muon_status ns_step(muon_plan p, float* const* params, const void* const*
                 Grouper g(p, sc, true, ch.lower, gc_clusters, g_grid1);
                 for (int bk : ch.buckets) {
                     Bucket& b = p->buckets[bk];
-                    if (b.fused) continue;
+                    if (!b.batched()) continue;
                     GemmProblem q = problem(b.r, b.r, b.c, b.batch, true, kEpiSyrk);
                     q.C = b.G[0];
                     q.strideC = (long long)b.r * b.ldr;
@@ -1241,7 +1301,7 @@ static muon_status ns_step(muon_plan p, float* const* params, const void* const*
                     Grouper g(p, sc, false, ch.lower, gc_clusters, g_grid1);
                     for (int bk : ch.buckets) {
                     Bucket& b = p->buckets[bk];
-                    if (b.fused) continue;
+                    if (!b.batched()) continue;
                         GemmProblem q = rr_problem(b, kEpiPoly);
                         q.C = b.P;
                         if (k == 1 && J > 1) q.C2 = b.Q[0];
@@ -1263,7 +1323,7 @@ static muon_status ns_step(muon_plan p, float* const* params, const void* const*
                     Grouper g(p, sc, false, ch.lower, gc_clusters, g_grid1);
                     for (int bk : ch.buckets) {
                     Bucket& b = p->buckets[bk];
-                    if (b.fused) continue;
+                    if (!b.batched()) continue;
                         if (k >= 2) {
                             GemmProblem q = rr_problem(b, kEpiPlain);
                             if (k < J) {
@@ -1294,7 +1354,7 @@ static muon_status ns_step(muon_plan p, float* const* params, const void* const*
                     Grouper g(p, sc, false, ch.lower, gc_clusters, g_grid1);
                     for (int bk : ch.buckets) {
                     Bucket& b = p->buckets[bk];
-                    if (b.fused) continue;
+                    if (!b.batched()) continue;
                         GemmProblem q = rr_problem(b, kEpiPlain);
                         q.C = b.G[gc ^ 1];
                         q.tma_out = kTmaOutC;
@@ -1310,7 +1370,7 @@ static muon_status ns_step(muon_plan p, float* const* params, const void* const*
             if (J == 0) {
                 for (int bk : ch.buckets) {
                     Bucket& b = p->buckets[bk];
-                    if (b.fused) continue;
+                    if (!b.batched()) continue;
                     MUON_TRY(launch_identity_bf16(b.Qb, b.r, b.ldr, b.batch, sc));
                     ++launches;
                 }
@@ -1324,7 +1384,7 @@ static muon_status ns_step(muon_plan p, float* const* params, const void* const*
                 float* const* W = reinterpret_cast<float* const*>(p->d_ptrs + 2 * n);
                 for (int bk : ch.buckets) {
                     Bucket& b = p->buckets[bk];
-                    if (b.fused) continue;
+                    if (!b.batched()) continue;
                     GemmProblem q = problem(b.r, b.c, b.r, b.batch, false, last ? kEpiApply : kEpiXout);
                     q.b_mn = 1;
                     q.alpha = (first ? p->alpha : p->ones) + b.slot_base;
@@ -1539,10 +1599,11 @@ muon_status muon_sync(muon_plan p, void* stream) {
     if (!p) return MUON_ERR_INVALID_ARG;
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MUON_ERR_CUDA;
     int st = 0;
-    if (cudaMemcpy(&st, p->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MUON_ERR_CUDA;
+    MUON_TRY(cudaMemcpy(&st, p->status, sizeof(int), cudaMemcpyDeviceToHost));
     if (st != 0) {
-        if (cudaMemset(p->status, 0, sizeof(int)) != cudaSuccess) return MUON_ERR_CUDA;
-        return MUON_ERR_TIMEOUT;
+        MUON_TRY(cudaMemset(p->status, 0, sizeof(int)));
+        // a timeout replaces the word; non-finite norms are or-ed into it
+        return (st & kStatusTimeoutMask) ? MUON_ERR_TIMEOUT : MUON_ERR_NONFINITE;
     }
     return MUON_OK;
 }
@@ -1572,7 +1633,7 @@ muon_status muon_debug_copy_workspace(muon_plan p, int32_t i, int32_t which, voi
         return MUON_ERR_INVALID_ARG;
     const Bucket& b = p->buckets[p->mat_bucket[i]];
     // the fused kernel keeps its r x r operands on chip: only X0 and alpha exist
-    if (b.fused && which >= 1 && which <= 7) return MUON_ERR_UNSUPPORTED;
+    if (!b.batched() && which >= 1 && which <= 7) return MUON_ERR_UNSUPPORTED;
     const int item = p->mat_item[i];
     const size_t rr = (size_t)b.r * b.ldr;
     const void* src = nullptr;

@@ -235,7 +235,10 @@ __global__ void k_norm_finalize(const ElemArgs a) {
     for (int k = lane; k < md.nblk; k += 32) s += (double)a.partials[md.part_off + k];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) a.alpha[md.slot] = s > 0.0 ? (float)(1.0 / sqrt(s)) : 0.f;
+    if (lane == 0) {
+        a.alpha[md.slot] = s > 0.0 ? (float)(1.0 / sqrt(s)) : 0.f;
+        if (a.check_finite && !isfinite(s)) atomicOr(a.status, kStatusNonFinite);
+    }
 }
 
 __global__ void k_identity_bf16(__nv_bfloat16* q, int r, int ld, long long total) {
@@ -294,6 +297,7 @@ __global__ void __launch_bounds__(kElemThreads) k_rownorm_rows(const ElemArgs a)
             }
         }
         const float tot = block_sum_all(ss, sred);
+        if (a.check_finite && t == 0 && !isfinite(tot)) atomicOr(a.status, kStatusNonFinite);
         const float inv = 1.f / fmaxf(sqrtf(tot), a.eps);
         const float k = s * inv;
 #pragma unroll
@@ -318,6 +322,7 @@ __global__ void __launch_bounds__(kElemThreads) k_rownorm_rows(const ElemArgs a)
             ss += u * u;
         }
         const float tot = block_sum_all(ss, sred);
+        if (a.check_finite && t == 0 && !isfinite(tot)) atomicOr(a.status, kStatusNonFinite);
         const float inv = 1.f / fmaxf(sqrtf(tot), a.eps);
         const float k = s * inv;
         for (long long j = t; j < n; j += kElemThreads) {
@@ -402,6 +407,7 @@ __global__ void __launch_bounds__(kElemThreads) k_rownorm_colfinal(const ElemArg
     const long long slabs = (md.m + kColSlab - 1) / kColSlab;
     float s = 0.f;
     for (long long k = 0; k < slabs; ++k) s += a.partials[md.cpart_off + k * md.n + j];
+    if (a.check_finite && !isfinite(s)) atomicOr(a.status, kStatusNonFinite);
     a.rowinv[md.inv_off + j] = 1.f / fmaxf(sqrtf(s), a.eps);
 }
 

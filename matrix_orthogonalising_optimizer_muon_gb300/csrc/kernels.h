@@ -9,6 +9,17 @@
 
 namespace muon {
 
+// Codes of the plan's device status word (read and cleared by muon_sync).
+enum DeviceStatus : int {
+    kStatusOk = 0,
+    kStatusTimeoutProducer = 0x101,
+    kStatusTimeoutMma = 0x102,
+    kStatusTimeoutEpilogue = 0x103,
+    kStatusTimeoutSelftest = 0x1ff,   // muon_debug_wait_timeout
+    kStatusTimeoutMask = 0xfff,       // timeouts replace the word (atomicExch)
+    kStatusNonFinite = 0x10000,       // a non-finite input norm (atomicOr; opts.check_finite)
+};
+
 // ------------------------------------------------------------------ GEMM
 // Tile of one tensor-core product: BM x BN output, one tcgen05.mma M=128 N=256.
 constexpr int kBM = 128;
@@ -182,7 +193,8 @@ struct ElemArgs {
     float* rowinv;             // per-row inverse norms (RowNorm, transposed matrices)
     float mu, lr, wd, eps;
     int grad_bf16;
-    int pad2;
+    int check_finite;          // record a non-finite norm in *status (kStatusNonFinite)
+    int* status;
 };
 
 // Momentum + Nesterov + partial sum of squares + bf16 X0 in the oriented layout.
@@ -212,6 +224,35 @@ static_assert(kTileRows % 32 == 0 && kTileRows <= 128, "transpose tile rows");
 constexpr int kColSlab = 64;                                         // RowNorm column-stat rows per block
 constexpr int kColWidth = 4 * kElemThreads;                          // columns per column-stat block
 constexpr long long kApplyElemsPerBlock = 4LL * kElemThreads * 4;    // RowNorm col apply
+
+// ------------------------------------------------------------------ fp32 step of small near-square matrices
+// Whole NS step (SYRK, r x r recursion, final product + update) in fp32 on CUDA
+// cores, one matrix per CTA, for matrices with r <= kF32MaxR.  U is recomputed
+// from the new momentum and the gradient (mu M + G), so the X0 workspace is not read.
+constexpr int kF32MaxR = 128;
+struct F32Problem {
+    int r, c, batch, item_begin;   // oriented shape, matrices, first launch item
+    int ns_steps, pad;
+    const int* item_mat;           // item -> plan matrix index
+    const float* alpha;            // per item 1/||U||_F
+    float* Odbg;                   // optional O (fp32, stored layout), item stride r*c
+    float coef_a, coef_b, coef_c, scale;
+};
+struct F32Launch {
+    F32Problem prob[kMaxProblems];
+    int nprob, total;
+    const MatDev* mats;
+    const void* const* G;
+    float* const* M;
+    float* const* W;
+    float mu, lr, wd;
+    int grad_bf16;
+};
+cudaError_t ns_f32_prepare();   // sets the kernel's dynamic shared-memory limit
+cudaError_t ns_f32_launch(const F32Launch& L, int grid, cudaStream_t s);
+
+// Remembers a CUDA error for muon_last_error_detail (this host thread's last one).
+void record_cuda_error(cudaError_t e);
 
 // bounded-wait self test: one mbarrier wait that nothing completes (limit in ns)
 cudaError_t launch_wait_selftest(int* status, unsigned long long limit_ns, cudaStream_t s);

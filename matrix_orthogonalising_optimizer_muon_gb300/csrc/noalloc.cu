@@ -12,14 +12,14 @@
 //
 // Scratch: `g_rownorm_scratch`, a file-scope __device__ array of
 // kNoAllocScratchFloats floats (4 MiB) that every GPU which loads the library
-// keeps until the process exits.  When m > n the RowNorm rows are the stored
-// columns, so their norms need a second pass: per-slab column sums of U^2 and
+// keeps until the process exits; its device address is looked up on every
+// call.  When m > n the RowNorm rows are the stored columns, so their norms need
+// a second pass: per-slab column sums of U^2 and
 // the per-column inverse norms are kept in this array.  Every scratch word a
 // call reads is written earlier in the same call, so nothing has to be
 // cleared between calls; calls that overlap on the GPU (different streams, or
 // several host threads) share the array and race.
 #include <cmath>
-#include <mutex>
 
 #include "../../include/muon.h"
 #include "kernels.h"
@@ -31,22 +31,16 @@ constexpr long long kNoAllocScratchFloats = 1LL << 20;   // 4 MiB
 
 static __device__ __align__(256) float g_rownorm_scratch[kNoAllocScratchFloats];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mutex;
-float* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on `dev` (the current device); looked up
-// once per device.  In host code the array's name is only a stand-in, so the
-// kernels always receive this address.
-cudaError_t scratch_address(int dev, float** out) {
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_ptr[dev]) {
-        void* p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_rownorm_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_ptr[dev] = static_cast<float*>(p);
-    }
-    *out = g_scratch_ptr[dev];
+// Device address of the scratch array in the current context.  In host code the
+// array's name is only a stand-in, so the kernels always receive this address.
+// It is looked up on every call (a host-side query: no allocation, no
+// synchronisation), so a context that was reset and re-created gets the array's
+// new address; the first lookup on a device may load the library's device code.
+cudaError_t scratch_address(float** out) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_rownorm_scratch);
+    if (e != cudaSuccess) return e;
+    *out = static_cast<float*>(p);
     return cudaSuccess;
 }
 
@@ -181,13 +175,18 @@ extern "C" muon_status muon_rownorm_matrix_noalloc(float* param, const void* gra
     if (overlap(w, numel * 4, mo, numel * 4) || overlap(w, numel * 4, g, numel * gsz) ||
         overlap(mo, numel * 4, g, numel * gsz))
         return MUON_ERR_INVALID_ARG;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MUON_ERR_CUDA;
     float* scratch = nullptr;
-    if (scratch_address(dev, &scratch) != cudaSuccess) return MUON_ERR_CUDA;
+    cudaError_t e = scratch_address(&scratch);
+    if (e != cudaSuccess) {
+        record_cuda_error(e);
+        return MUON_ERR_CUDA;
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const cudaError_t e = grad_dtype == MUON_BF16
-                              ? launch_all<true>(param, grad, momentum, rows, cols, lr, wd, mu, eps, scratch, s)
-                              : launch_all<false>(param, grad, momentum, rows, cols, lr, wd, mu, eps, scratch, s);
-    return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
+    e = grad_dtype == MUON_BF16 ? launch_all<true>(param, grad, momentum, rows, cols, lr, wd, mu, eps, scratch, s)
+                                : launch_all<false>(param, grad, momentum, rows, cols, lr, wd, mu, eps, scratch, s);
+    if (e != cudaSuccess) {
+        record_cuda_error(e);
+        return MUON_ERR_CUDA;
+    }
+    return MUON_OK;
 }

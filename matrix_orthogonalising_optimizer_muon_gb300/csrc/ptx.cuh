@@ -11,14 +11,6 @@ namespace muon {
 // status word and gives up (the kernel then drains and exits).
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
 
-enum DeviceStatus : int {
-    kStatusOk = 0,
-    kStatusTimeoutProducer = 0x101,
-    kStatusTimeoutMma = 0x102,
-    kStatusTimeoutEpilogue = 0x103,
-    kStatusTimeoutSelftest = 0x1ff,   // muon_debug_wait_timeout
-};
-
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -21,6 +21,8 @@ int main(void) {
     FIELD(muon_plan_opts, workspace_bytes);
     FIELD(muon_plan_opts, chunks);
     FIELD(muon_plan_opts, full_symmetric);
+    FIELD(muon_plan_opts, small_fp32);
+    FIELD(muon_plan_opts, check_finite);
     printf("sizeof.muon_plan_info_t %zu\n", sizeof(muon_plan_info_t));
     FIELD(muon_plan_info_t, n_matrices);
     FIELD(muon_plan_info_t, n_buckets);
