@@ -7,8 +7,11 @@ matrix parameters, bf16 grads, fp32 weights and momentum), NS5, 3 warm-up and
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
 
-With N > 1 (torchrun), every rank runs its own replica of the workload (the
-step has no cross-matrix exchange); the time is the max over ranks.
+With N > 1 (torchrun), the matrices are partitioned over the ranks, one owner
+per matrix (DistributedMuon, longest processing time first); each rank steps its
+own matrices and every owner then broadcasts its updated parameters to the other
+ranks.  The work is fixed as N grows (strong scaling); the time is the max over
+ranks.
 """
 from __future__ import annotations
 
@@ -212,6 +215,18 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
+def sum_over_ranks(x: int, world: int) -> int:
+    """Sum of a host integer over ranks (identity at world size 1)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.int64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return int(t.item())
+
+
 # ------------------------------------------------------------------ workload accounting
 def algorithmic_ns_flops(shapes, ns_steps=5):
     """Tensor FLOPs of the Gram-form NS step, symmetric products counted at half:
@@ -267,37 +282,62 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     peaks, peak_src = load_peaks()
 
-    # ---- inputs resident in HBM (seeded on the device); fresh grads per step
+    # ---- inputs resident in HBM (seeded on the device).  One gradient per matrix
+    # serves every step (the step's cost does not depend on the gradient's values).
+    # With N > 1 ranks each matrix has one owner (DistributedMuon: LPT over the
+    # ranks); a rank keeps every parameter but only its own matrices' G and M.
     t0 = time.time()
-    W, G, M = [], [], []
-    for i, (m, n) in enumerate(shapes):
-        W.append(workloads.gen_tensor((m, n), workloads.W_STD, workloads.seed_of(wl.index, 0, i, "W"), dev))
-        M.append(workloads.gen_tensor((m, n), workloads.M_STD, workloads.seed_of(wl.index, 0, i, "M"), dev))
-        G.append(workloads.gen_tensor((m, n), workloads.G_STD, workloads.seed_of(wl.index, 0, i, "G"), dev,
-                                      wl.grad_dtype))
-    plan = lib.MuonPlan(shapes, wl.grad_dtype, timing=True, workspace_bytes=args.workspace_bytes,
-                        full_symmetric=args.full_symmetric)
+    opt = None
+    if world > 1:
+        opt = lib.DistributedMuon(shapes, wl.grad_dtype, timing=True, workspace_bytes=args.workspace_bytes,
+                                  full_symmetric=args.full_symmetric)
+        owned = list(opt.owned)
+        W = opt.allocate_params(dev)
+        for i, (m, n) in enumerate(shapes):
+            W[i].copy_(workloads.gen_tensor((m, n), workloads.W_STD, workloads.seed_of(wl.index, 0, i, "W"), dev))
+    else:
+        owned = list(range(len(shapes)))
+        W = [workloads.gen_tensor((m, n), workloads.W_STD, workloads.seed_of(wl.index, 0, i, "W"), dev)
+             for i, (m, n) in enumerate(shapes)]
+    G, M = [None] * len(shapes), [None] * len(shapes)
+    for i in owned:
+        m, n = shapes[i]
+        M[i] = workloads.gen_tensor((m, n), workloads.M_STD, workloads.seed_of(wl.index, 0, i, "M"), dev)
+        G[i] = workloads.gen_tensor((m, n), workloads.G_STD, workloads.seed_of(wl.index, 0, i, "G"), dev,
+                                    wl.grad_dtype)
+    Wl, Gl, Ml = [W[i] for i in owned], [G[i] for i in owned], [M[i] for i in owned]
+    if opt is not None:
+        plan = opt.plan
+    else:
+        plan = lib.MuonPlan(shapes, wl.grad_dtype, timing=True, workspace_bytes=args.workspace_bytes,
+                            full_symmetric=args.full_symmetric)
     torch.cuda.synchronize()
     setup_s = time.time() - t0
     lr, wd, mu = workloads.LR, workloads.WD, workloads.MU
     stream = torch.cuda.current_stream()
-    plan.bind(W, G, M)
-    if not args.no_tune:   # plan-time tuning on the resident inputs (its steps precede the warm-up)
-        plan.tune(W, G, M, workloads.LR, workloads.WD, workloads.MU, reps=2, stream=torch.cuda.current_stream())
+    if plan is not None:
+        plan.bind(Wl, Gl, Ml)
+        if not args.no_tune:   # plan-time tuning on the resident inputs (its steps precede the warm-up)
+            plan.tune(Wl, Gl, Ml, workloads.LR, workloads.WD, workloads.MU, reps=2, stream=stream)
 
     def one_step(t):
-        if wl.rownorm_k and t % wl.rownorm_k != 0:
+        rownorm = bool(wl.rownorm_k and t % wl.rownorm_k != 0)
+        if opt is not None:
+            opt.step(W, G, M, lr, wd, mu, 5, "rownorm" if rownorm else "ns", eps=wl.eps, stream=stream)
+        elif rownorm:
             plan.step_bound(lr, wd, mu, mode="rownorm", eps=wl.eps, stream=stream)
         else:
             plan.step_bound(lr, wd, mu, 5, "ns", stream=stream)
 
     for t in range(args.warmup):
         one_step(t)
-    plan.sync()
-    try:
-        plan.stage_times()               # drop the warm-up steps' event groups
-    except lib.MuonError:
-        pass
+    torch.cuda.synchronize()
+    if plan is not None:
+        plan.sync()
+        try:
+            plan.stage_times()               # drop the warm-up steps' event groups
+        except lib.MuonError:
+            pass
 
     # ---- timed region: K steps, CUDA events on the launching stream
     clocks = ClockSampler(local)
@@ -312,18 +352,21 @@ def run_ours(args, rank, world, local):
     for t in range(args.steps):
         one_step(args.warmup + t)
         ev_step[t].record(stream)
-        launches += plan.info()["launches_last_step"]
+        launches += plan.info()["launches_last_step"] if plan is not None else 0
     ev1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
-    plan.sync()
-    stage_ms, stage_fl = plan.stage_times()   # per-stage event times summed over the K steps
+    if plan is not None:
+        plan.sync()
+        stage_ms, stage_fl = plan.stage_times()   # per-stage event times summed over the K steps
+    else:
+        stage_ms, stage_fl = [0.0] * 6, [0.0] * 3
     elapsed_ms = ev0.elapsed_time(ev1)
     ms_step = max_over_ranks(elapsed_ms / args.steps, world)
     per_step = [(ev0 if t == 0 else ev_step[t - 1]).elapsed_time(ev_step[t]) for t in range(args.steps)]
-    return dict(wl=wl, shapes=shapes, plan=plan, W=W, G=G, M=M, ms_step=ms_step, per_step=per_step,
-                stage_ms=stage_ms,
+    return dict(wl=wl, shapes=shapes, local_shapes=[shapes[i] for i in owned], plan=plan, opt=opt,
+                W=Wl, G=Gl, M=Ml, ms_step=ms_step, per_step=per_step, stage_ms=stage_ms,
                 stage_fl=stage_fl, launches=launches, clocks=clk, peaks=peaks, peak_src=peak_src,
                 setup_s=setup_s, one_step=one_step)
 
@@ -336,8 +379,10 @@ def run_e2e(res, args):
     import torch
     import matrix_orthogonalising_optimizer_muon_gb300 as lib
     import workloads
-    wl, shapes = res["wl"], res["shapes"]
+    wl, shapes = res["wl"], res["local_shapes"]
     W, G, M = res["W"], res["G"], res["M"]
+    if not shapes:
+        return 0.0, 0, 0, 0, 0
     host_g = [torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in G]
     host_w = [torch.empty(w.shape, dtype=w.dtype, pin_memory=True) for w in W]
     for hg, g in zip(host_g, G):
@@ -379,7 +424,8 @@ def report_ours(args, res, rank, world):
     gemm_ms = per_ns[1] + per_ns[2] + per_ns[3]
     gemm_fl = (st_fl[0] + st_fl[1] + st_fl[2]) / n_ns if n_ns else 0.0
     gbytes = 2 if wl.grad_dtype == "bf16" else 4
-    small = [(m, n) for m, n in shapes if min(m, n) <= 128]
+    local = res["local_shapes"]   # this rank's matrices (all of them on one GPU)
+    small = [(m, n) for m, n in local if min(m, n) <= 128]
     small_bytes = sum(m * n * 12 for m, n in small)   # X read twice (bf16), W read + written (fp32)
     # The roofline object describes the step's dominant kernel: the tensor-core
     # products (algorithmic FLOPs over their event time, against the measured
@@ -410,18 +456,19 @@ def report_ours(args, res, rank, world):
     line = {
         "metric": METRIC, "value": round(ms_step, 3), "unit": "ms", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": False,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16/fp16 tensor (fp32 accumulate), fp32 elementwise",
+        "scaling": "strong" if world > 1 else "weak", "vs_baseline": None,
+        "dtype": "bf16/fp16 tensor (fp32 accumulate), fp32 elementwise",
         "data": "synthetic (seeded Gaussian, shapes of the workload)",
         "config": {"workload": wl.name, "matrices": len(shapes),
                    "params": int(sum(m * n for m, n in shapes)), "grad_dtype": wl.grad_dtype,
                    "ns_steps": 5, "rownorm_k": wl.rownorm_k,
                    "l2": "inputs larger than L2 (%.1f GB of W, G, M per step)" %
                          (sum(m * n for m, n in shapes) * (10 if wl.grad_dtype == "bf16" else 12) / 1e9),
-                   "parallelism": "replicas" if world > 1 else "single GPU",
-                   "workspace_bytes": res["plan"].info()["workspace_bytes"],
-                   "lower_chunks": res["plan"].info()["lower_chunks"],
-                   "tuned_candidates": res["plan"].info()["tuned_candidates"],
-                   "chain_clusters": res["plan"].info()["chain_clusters"]},
+                   "parallelism": ("owner partition over %d GPUs (LPT), one fp32 parameter broadcast per "
+                                   "owner" % world) if world > 1 else "single GPU",
+                   **({k: res["plan"].info()[k] for k in ("workspace_bytes", "lower_chunks", "tuned_candidates",
+                                                          "chain_clusters")} if res["plan"] is not None else {}),
+                   **({"rank0_matrices": len(local)} if world > 1 else {})},
         "stages_ms_per_ns_step": {"momentum_norm": round(per_ns[0], 3), "syrk": round(per_ns[1], 3),
                                   "ns_rxr": round(per_ns[2], 3), "final_apply": round(per_ns[3], 3),
                                   "fused_small": round(per_ns[5], 3)},
@@ -435,11 +482,11 @@ def report_ours(args, res, rank, world):
     if n_rn:
         line["rownorm_ms_per_rownorm_step"] = round(st_ms[4] / n_rn, 3)
         line["rownorm_steps_timed"] = n_rn
-        rn_bytes = sum(m * n * (gbytes + 8 + 8) for m, n in shapes)   # G, M read + write, W read + write
+        rn_bytes = sum(m * n * (gbytes + 8 + 8) for m, n in local)   # G, M read + write, W read + write
         line["rownorm_step_gbs"] = round(rn_bytes / (st_ms[4] / n_rn * 1e-3) / 1e9, 1)
     line.update(ns5)
     if per_ns[0] > 0:
-        mom_bytes = sum(m * n * (gbytes + 8 + 2) for m, n in shapes)
+        mom_bytes = sum(m * n * (gbytes + 8 + 2) for m, n in local)
         line["momentum_kernel_gbs"] = round(mom_bytes / (per_ns[0] * 1e-3) / 1e9, 1)
         line["momentum_kernel_hbm_frac"] = round(line["momentum_kernel_gbs"] / peaks["hbm_gbs"], 4)
     return line
@@ -505,10 +552,12 @@ def main():
     if not args.no_e2e:
         e2e_ms, h2d, d2h, nsteps, e2e_chunks = run_e2e(res, args)
         e2e_ms = max_over_ranks(e2e_ms, world)
+        h2d, d2h = sum_over_ranks(h2d, world), sum_over_ranks(d2h, world)
         line["e2e"] = {"value": round(e2e_ms, 3), "unit": "ms", "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "steps": nsteps, "plan_chunks": e2e_chunks,
                        "what": "muon_step_host: grads host->device (pinned) and updated weights "
-                               "device->host, overlapped chunk by chunk with the step"}
+                               "device->host, overlapped chunk by chunk with the step" +
+                               ("; each rank its own matrices, bytes summed over ranks" if world > 1 else "")}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         t, detail = oracle_sample(res["shapes"], res["wl"].grad_dtype, seed=res["wl"].index)
         line["cpu_baseline"] = {"value": round(t * 1e3, 1), "unit": "ms", "cores": os.cpu_count(),

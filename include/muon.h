@@ -125,6 +125,19 @@ typedef struct {
        word and the next muon_sync returns MUON_ERR_NONFINITE.  The step still runs (the
        update of such a matrix is then not finite).  0: no check. */
     int32_t check_finite;
+    /* Precision of the batched products (matrices on neither one-CTA kernel).  Level 1
+       carries every r x r buffer (G, P, T, Q) as two fp16 parts and the final Q as
+       two bf16 parts (value = hi + lo, about 21 and 16 significant bits), each product
+       running as K-concatenated passes over the parts (3 for two split operands);
+       level 2 also splits X0 into two bf16 parts (the SYRK and the final product read
+       both).  Level 1 triples the r x r products' tensor work, level 2 also the SYRK
+       and the final product.  Symmetric results of split buckets are stored whole.
+       0: level 1 for nearly square buckets (max(m, n) < 1.25 min(m, n)) with
+       min(m, n) <= split_max_r, whose O the plain recipe moves by 1e-2 to 2.5e-2;
+       1 or 2: that level for every batched bucket; < 0: never. */
+    int32_t precision;
+    /* Largest min(m, n) that precision 0 splits (0: 1024). */
+    int32_t split_max_r;
 } muon_plan_opts;
 
 typedef struct muon_plan_s* muon_plan;
@@ -162,6 +175,29 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
 muon_status muon_plan_workspace_size(const muon_shape* shapes, int32_t n, muon_dtype grad_dtype,
                                      const muon_plan_opts* opts, int64_t* bytes, int32_t* n_buckets,
                                      int32_t* n_chunks);
+
+/*
+ * muon_partition - owner assignment of matrices to `world` GPUs (DMuon technical
+ * summary sec. 2: every matrix has exactly one owner rank, which keeps its momentum
+ * and runs its Newton-Schulz step once; the other ranks receive the updated
+ * parameters).  Host only, no CUDA call; deterministic, so every rank computes the
+ * same assignment from the same arguments without communicating.
+ *   shapes, n  the matrices, as for muon_plan_create (same limits).
+ *   world      number of ranks, 1 .. 65536.
+ *   cost       NULL, or n non-negative finite costs (for example measured seconds per
+ *              matrix).  NULL: a model of one GB300 step, per matrix the larger of
+ *              its tensor work ((3 r^2 c + 17 r^3) FLOPs at 1.5e15 FLOP/s, symmetric
+ *              products counted at half; none for min(m, n) <= 128) and its memory
+ *              traffic (24 bytes per element at 6.8e12 B/s), where r = min(m, n) and
+ *              c = max(m, n).
+ *   owner      receives n ranks in [0, world).
+ *   load       NULL, or receives `world` summed costs.
+ * The assignment is longest-processing-time first (DMuon's greedy fallback to its
+ * MILP): matrices in decreasing cost (ties by index) each go to the rank with the
+ * least load so far (ties by rank).  MUON_ERR_INVALID_ARG on a bad argument.
+ */
+muon_status muon_partition(const muon_shape* shapes, int32_t n, int32_t world, const double* cost, int32_t* owner,
+                           double* load);
 
 /*
  * muon_plan_destroy - wait for the device to go idle (cudaDeviceSynchronize, so
@@ -347,6 +383,8 @@ typedef struct {
     int32_t lower_chunks;         /* chunks storing symmetric results as the lower triangle */
     int32_t tuned_candidates;     /* launch choices muon_plan_tune measured (0: never tuned) */
     int32_t chain_clusters;       /* CTA pairs the batched products get beside the fused kernel (0: none) */
+    int32_t split_buckets;        /* batched buckets in split precision (opts.precision) */
+    int32_t fp32_buckets;         /* buckets on the fp32 kernel (opts.small_fp32) */
 } muon_plan_info_t;
 
 muon_status muon_plan_info(muon_plan p, muon_plan_info_t* info);

@@ -11,7 +11,9 @@ The C entry points keep their names (``muon_plan_create``, ``muon_step``,
 ``MuonPlan`` wraps them for torch tensors, ``plan_workspace_size`` sizes a plan on
 the host alone (``muon_plan_workspace_size``), and ``PeriodicRowNormMuon`` adds the step schedule of periodic
 RowNorm Muon (full NS5 every K steps, RowNorm otherwise; "Scaling Muon for
-Diffusion Transformers", sec. 3).
+Diffusion Transformers", sec. 3).  ``DistributedMuon`` runs the step across the
+ranks of a torch.distributed group with one owner per matrix (``partition_owners``,
+the library's ``muon_partition``) and broadcasts the updated parameters.
 """
 from __future__ import annotations
 
@@ -21,7 +23,8 @@ import os
 from .build import LIB, build, up_to_date
 
 __all__ = [
-    "MuonError", "MuonPlan", "PeriodicRowNormMuon", "plan_workspace_size", "load", "build",
+    "MuonError", "MuonPlan", "PeriodicRowNormMuon", "DistributedMuon", "partition_owners",
+    "plan_workspace_size", "load", "build",
     "MUON_OK", "MUON_ERR_INVALID_ARG", "MUON_ERR_UNSUPPORTED", "MUON_ERR_OOM",
     "MUON_ERR_CUDA", "MUON_ERR_TIMEOUT", "MUON_ERR_NONFINITE", "MUON_F32", "MUON_BF16",
     "MUON_MODE_NS", "MUON_MODE_ROWNORM", "EXPORTED",
@@ -47,14 +50,15 @@ class MuonPlanOpts(ctypes.Structure):
                 ("chain_clusters", ctypes.c_int32), ("max_ns_steps", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64), ("chunks", ctypes.c_int32),
                 ("full_symmetric", ctypes.c_int32), ("small_fp32", ctypes.c_int32),
-                ("check_finite", ctypes.c_int32)]
+                ("check_finite", ctypes.c_int32), ("precision", ctypes.c_int32), ("split_max_r", ctypes.c_int32)]
 
 
 class MuonPlanInfo(ctypes.Structure):
     _fields_ = [("n_matrices", ctypes.c_int32), ("n_buckets", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64), ("launches_last_step", ctypes.c_int32),
                 ("sm_count", ctypes.c_int32), ("n_chunks", ctypes.c_int32), ("lower_chunks", ctypes.c_int32),
-                ("tuned_candidates", ctypes.c_int32), ("chain_clusters", ctypes.c_int32)]
+                ("tuned_candidates", ctypes.c_int32), ("chain_clusters", ctypes.c_int32),
+                ("split_buckets", ctypes.c_int32), ("fp32_buckets", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -87,6 +91,9 @@ EXPORTED = {
     "muon_plan_info": (ctypes.c_int, [_P, ctypes.POINTER(MuonPlanInfo)]),
     "muon_stage_times": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_float),
                                         ctypes.POINTER(ctypes.c_double), ctypes.c_int32]),
+    "muon_partition": (ctypes.c_int, [ctypes.POINTER(MuonShape), ctypes.c_int32, ctypes.c_int32,
+                                      ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int32),
+                                      ctypes.POINTER(ctypes.c_double)]),
     "muon_rownorm_matrix_noalloc": (ctypes.c_int, [_P, _P, _P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                                                    ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                                    ctypes.c_float, _P]),
@@ -146,14 +153,14 @@ def _ptr_array(ptrs):
 
 def _plan_args(shapes, grad_dtype, keep_update=False, timing=False, single_sm_gemm=False,
                generic_small=False, chain_clusters=0, workspace_bytes=0, max_ns_steps=0, chunks=0,
-               full_symmetric=False, small_fp32=0, check_finite=False):
+               full_symmetric=False, small_fp32=0, check_finite=False, precision=0, split_max_r=0):
     """(shape list, MuonShape array, dtype code, MuonPlanOpts) of a plan's arguments."""
     shapes = [(int(m), int(n)) for m, n in shapes]
     arr = (MuonShape * len(shapes))(*[MuonShape(m, n) for m, n in shapes])
     opts = MuonPlanOpts(1 if keep_update else 0, 1 if timing else 0, 1 if single_sm_gemm else 0,
                         1 if generic_small else 0, int(chain_clusters), int(max_ns_steps),
                         int(workspace_bytes), int(chunks), 1 if full_symmetric else 0, int(small_fp32),
-                        1 if check_finite else 0)
+                        1 if check_finite else 0, int(precision), int(split_max_r))
     return shapes, arr, {"bf16": MUON_BF16, "f32": MUON_F32}[grad_dtype], opts
 
 
@@ -179,11 +186,13 @@ class MuonPlan:
     def __init__(self, shapes, grad_dtype: str = "bf16", keep_update: bool = False,
                  timing: bool = False, single_sm_gemm: bool = False, generic_small: bool = False,
                  chain_clusters: int = 0, workspace_bytes: int = 0, max_ns_steps: int = 0, chunks: int = 0,
-                 full_symmetric: bool = False, small_fp32: int = 0, check_finite: bool = False):
+                 full_symmetric: bool = False, small_fp32: int = 0, check_finite: bool = False,
+                 precision: int = 0, split_max_r: int = 0):
         self.lib = load()
         self.shapes, arr, gd, opts = _plan_args(shapes, grad_dtype, keep_update, timing, single_sm_gemm,
                                                 generic_small, chain_clusters, workspace_bytes, max_ns_steps,
-                                                chunks, full_symmetric, small_fp32, check_finite)
+                                                chunks, full_symmetric, small_fp32, check_finite, precision,
+                                                split_max_r)
         self.grad_dtype = grad_dtype
         h = ctypes.c_void_p()
         _check(self.lib.muon_plan_create(arr, len(self.shapes), gd, ctypes.byref(opts),
@@ -398,3 +407,132 @@ class PeriodicRowNormMuon:
         self.t, self.k = t, k
         self.eps = float(state.get("eps", self.eps))
         self.ns_steps = int(state.get("ns_steps", self.ns_steps))
+
+
+def partition_owners(shapes, world: int, costs=None):
+    """Owner rank of every matrix for ``world`` GPUs (``muon_partition``: longest
+    processing time first over per-matrix costs, DMuon's greedy owner assignment).
+    Returns (owners, loads)."""
+    lib = load()
+    shapes = [(int(m), int(n)) for m, n in shapes]
+    n = len(shapes)
+    arr = (MuonShape * n)(*[MuonShape(m, k) for m, k in shapes])
+    c = None if costs is None else (ctypes.c_double * n)(*[float(x) for x in costs])
+    owner = (ctypes.c_int32 * n)()
+    loads = (ctypes.c_double * int(world))()
+    _check(lib.muon_partition(arr, n, int(world), c, owner, loads), "muon_partition")
+    return list(owner), list(loads)
+
+
+class DistributedMuon:
+    """Owner-partitioned Muon step over the ranks of a torch.distributed group
+    (DMuon technical summary sec. 2: each matrix has one owner rank, which keeps
+    its momentum and runs its Newton-Schulz step exactly once; the updated
+    parameters are then published to every other rank).
+
+    Every rank holds every parameter matrix.  Gradients are the already reduced
+    full gradients; a rank reads only the gradients and momentum of the matrices
+    it owns (``owned``), so the other entries of ``grads`` and ``momentum`` may be
+    None.  After its local step each owner broadcasts its updated fp32
+    parameters (one NCCL broadcast per owner, from a flat buffer): the one data
+    exchange of the step.  Parameters allocated by ``allocate_params`` are views
+    into those flat buffers and are broadcast in place; other tensors go through
+    a staging buffer (one copy on each side).  With one rank this is a plain
+    ``MuonPlan`` step."""
+
+    def __init__(self, shapes, grad_dtype: str = "bf16", group=None, costs=None, **plan_opts):
+        import torch.distributed as dist
+        if dist.is_available() and dist.is_initialized():
+            self.rank, self.world = dist.get_rank(group), dist.get_world_size(group)
+        else:
+            self.rank, self.world = 0, 1
+        self.group = group
+        self.grad_dtype = grad_dtype
+        self.shapes = [(int(m), int(n)) for m, n in shapes]
+        self.owner, self.loads = partition_owners(self.shapes, self.world, costs)
+        self.owned_by = [[i for i, o in enumerate(self.owner) if o == r] for r in range(self.world)]
+        self.owned = self.owned_by[self.rank]
+        self.plan = self._make_plan(plan_opts) if self.owned else None
+        self._flat = None        # per owner: flat fp32 buffer of its parameters (allocate_params)
+        self._views = None
+        self._staging = None
+
+    def _make_plan(self, plan_opts):
+        return MuonPlan([self.shapes[i] for i in self.owned], self.grad_dtype, **plan_opts)
+
+    def _local_step(self, params, grads, momentum, lr, wd, mu, ns_steps, mode, eps, stream):
+        if mode == "ns":
+            self.plan.step(params, grads, momentum, lr, wd, mu, ns_steps, "ns", stream)
+        else:
+            self.plan.rownorm_step(params, grads, momentum, lr, wd, mu, eps, stream)
+
+    def allocate_params(self, device=None):
+        """Parameter tensors (fp32, every matrix) laid out as one flat buffer per owner,
+        so the exchange broadcasts each owner's parameters in place."""
+        import torch
+        self._flat, self._views = [], [None] * len(self.shapes)
+        for r in range(self.world):
+            idx = self.owned_by[r]
+            buf = torch.empty(sum(self.shapes[i][0] * self.shapes[i][1] for i in idx), dtype=torch.float32,
+                              device=device)
+            off = 0
+            for i in idx:
+                m, n = self.shapes[i]
+                self._views[i] = buf[off:off + m * n].view(m, n)
+                off += m * n
+            self._flat.append(buf)
+        return list(self._views)
+
+    def step(self, params, grads, momentum, lr: float, wd: float, mu: float = DEFAULT_MU,
+             ns_steps: int = DEFAULT_NS_STEPS, mode: str = "ns", eps: float = 1e-8, stream=None):
+        """The owned matrices' Muon step (NS or RowNorm), then the parameter exchange."""
+        if mode not in ("ns", "rownorm"):
+            raise ValueError("mode must be 'ns' or 'rownorm'")
+        if len(params) != len(self.shapes):
+            raise ValueError("expected %d parameter tensors" % len(self.shapes))
+        own = self.owned
+        if own:
+            self._local_step([params[i] for i in own], [grads[i] for i in own], [momentum[i] for i in own],
+                             lr, wd, mu, ns_steps, mode, eps, stream)
+        self.exchange(params)
+
+    def exchange(self, params):
+        """Every owner broadcasts its matrices' parameters to the other ranks."""
+        if self.world == 1:
+            return
+        import torch
+        import torch.distributed as dist
+        in_place = self._views is not None and all(
+            p.data_ptr() == v.data_ptr() and p.shape == v.shape for p, v in zip(params, self._views))
+        for r in range(self.world):
+            idx = self.owned_by[r]
+            if not idx:
+                continue
+            if in_place:
+                dist.broadcast(self._flat[r], src=r, group=self.group)
+                continue
+            numel = sum(params[i].numel() for i in idx)
+            dev = params[idx[0]].device
+            if self._staging is None or self._staging.numel() < numel or self._staging.device != dev:
+                self._staging = torch.empty(max(numel, max(
+                    sum(self.shapes[i][0] * self.shapes[i][1] for i in ix) for ix in self.owned_by)),
+                    dtype=torch.float32, device=dev)
+            buf = self._staging[:numel]
+            if r == self.rank:
+                torch.cat([params[i].reshape(-1) for i in idx], out=buf)
+            dist.broadcast(buf, src=r, group=self.group)
+            if r != self.rank:
+                off = 0
+                for i in idx:
+                    k = params[i].numel()
+                    params[i].view(-1).copy_(buf[off:off + k])
+                    off += k
+
+    def sync(self, stream=None):
+        if self.plan is not None:
+            self.plan.sync(stream)
+
+    def close(self):
+        if self.plan is not None:
+            self.plan.close()
+            self.plan = None

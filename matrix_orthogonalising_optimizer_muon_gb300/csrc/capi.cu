@@ -127,6 +127,7 @@ struct Bucket {
     int r = 0, c = 0, batch = 0;
     bool fused = false;     // r <= 128: whole step in the fused one-matrix-per-CTA kernel
     bool f32 = false;       // r <= 128, nearly square: whole step in fp32 on CUDA cores (ns_f32_kernel)
+    int split = 0;          // batched precision: 0 plain, 1 r x r buffers and Q in two parts, 2 also X0
     bool batched() const { return !fused && !f32; }   // r x r buffers in the workspace, grouped products
     int chunk = 0;          // workspace chunk (see muon_plan_opts.workspace_bytes)
     long long ut1_off = -1; // second X buffer (restarted NS segments), element offset like ut_off
@@ -402,6 +403,7 @@ struct Grouper {
     // MN-major problem through b4.t).
     void add(const CUtensorMap& a128, const CUtensorMap& b256, const CUtensorMap& b128, GemmProblem q,
              const CUtensorMap* oc, const CUtensorMap* oc2, Maps4 a4, Maps4 b4) {
+        if (q.a_split || q.b_split || q.out_split) q.tma_out = 0;   // split parts: per-thread stores
         if (q.M > kBM && p->pair_clusters > 0) {
             if (L2.nprob == kMaxProblems) flush2();
             q.tiles_m = (int)ceil_div(q.M, 256);
@@ -565,11 +567,20 @@ muon_status plan_layout(muon_plan_s* p, Layout& L) {
     };
     const bool fused_ok = !p->opts.generic_small && !restarts;
     auto is_fused = [&](int r, int c) { return fused_ok && r <= kSmallMaxR && !is_f32(r, c); };
+    // split precision of a batched bucket (opts.precision, opts.split_max_r)
+    auto split_of = [&](int r, int c) -> int {
+        if (is_fused(r, c) || is_f32(r, c) || p->opts.precision < 0) return 0;
+        if (p->opts.precision > 0) return p->opts.precision >= 2 ? 2 : 1;
+        const int rmax = p->opts.split_max_r > 0 ? p->opts.split_max_r : 1024;
+        return (4LL * c < 5LL * r && r <= rmax) ? 1 : 0;
+    };
     // region bytes of a bucket of `batch` matrices, exactly as laid out below: its X0
     // (and second X) buffer and, batched, its seven r x r buffers, each rounded to 256
+    // (split buffers hold two parts per matrix)
     auto bucket_bytes = [&](int r, int c, long long batch) -> long long {
-        const long long x = round_up(batch * r * round_up(c, 8) * 2, 256);
-        const long long rr = round_up(batch * r * round_up(r, 8) * 2, 256);
+        const int sp = split_of(r, c);
+        const long long x = round_up(batch * r * round_up(c, 8) * 2 * (sp == 2 ? 2 : 1), 256);
+        const long long rr = round_up(batch * r * round_up(r, 8) * 2 * (sp ? 2 : 1), 256);
         return (restarts ? 2 : 1) * x + (is_fused(r, c) || is_f32(r, c) ? 0 : 7 * rr);
     };
     size_t off = 0;
@@ -664,6 +675,7 @@ muon_status plan_layout(muon_plan_s* p, Layout& L) {
                     nb.ldu = (int)round_up(c, 8);
                     nb.fused = is_fused(r, c);
                     nb.f32 = is_f32(r, c);
+                    nb.split = split_of(r, c);
                     nb.chunk = (int)p->chunks.size() - 1;
                     p->buckets.push_back(nb);
                     cur = (int)p->buckets.size() - 1;
@@ -700,10 +712,11 @@ muon_status plan_layout(muon_plan_s* p, Layout& L) {
                 b.batch = (int)b.mats.size();
                 b.slot_base = slots;
                 slots += b.batch;
-                o_ut[k] = rtake((size_t)b.batch * b.r * b.ldu * 2);
-                if (restarts) o_ut1[k] = rtake((size_t)b.batch * b.r * b.ldu * 2);
+                const size_t xparts = b.split == 2 ? 2 : 1, rparts = b.split ? 2 : 1;
+                o_ut[k] = rtake((size_t)b.batch * b.r * b.ldu * 2 * xparts);
+                if (restarts) o_ut1[k] = rtake((size_t)b.batch * b.r * b.ldu * 2 * xparts);
                 if (b.batched()) {
-                    const size_t rr = (size_t)b.batch * b.r * b.ldr * 2;
+                    const size_t rr = (size_t)b.batch * b.r * b.ldr * 2 * rparts;
                     o_rr[k] = rtake(rr);   // G0 (fp16, scaled)
                     for (int q = 0; q < 5; ++q) rtake(rr);   // G1, P, T, Q0, Q1
                     o_qb[k] = rtake(rr);   // bf16 Q for the final product
@@ -718,7 +731,9 @@ muon_status plan_layout(muon_plan_s* p, Layout& L) {
         const Bucket& b = p->buckets[p->mat_bucket[i]];
         md.slot = b.slot_base + p->mat_item[i];
         md.ldu = b.ldu;
-        md.ut_off = (long long)(o_ut[p->mat_bucket[i]] / 2) + (long long)p->mat_item[i] * b.r * b.ldu;
+        md.x_split = b.split == 2 ? 1 : 0;   // hi part of item i at 2i, lo at 2i + 1
+        md.ut_off = (long long)(o_ut[p->mat_bucket[i]] / 2) +
+                    (long long)p->mat_item[i] * b.r * b.ldu * (md.x_split ? 2 : 1);
     }
     p->ws_bytes = off;
     // the packing counts the region exactly, so a cap is never exceeded; kept as a guard
@@ -859,10 +874,12 @@ static muon_status plan_build(muon_plan_s* p, const muon_shape* shapes, int32_t 
             odbg_off += (size_t)round_up((long long)b.batch * b.r * b.c * 4, 256);
         }
         __nv_bfloat16* ut = p->ut + b.ut_off;
-        ok = ok && make_map(&b.ut_a, ut, true, b.c, b.r, b.batch, b.ldu, 64, kBM);
-        ok = ok && make_map(&b.ut_b, ut, true, b.c, b.r, b.batch, b.ldu, 64, kBN);
-        ok = ok && make_map(&b.ut_mn, ut, true, b.c, b.r, b.batch, b.ldu, 64, 64);
-        const bool aligned4 = b.batched() && b.r % 64 == 0 && b.c % 64 == 0;
+        const int xb = b.batch * (b.split == 2 ? 2 : 1);   // X items (two parts per matrix at level 2)
+        const int rb = b.batch * (b.split ? 2 : 1);        // r x r items
+        ok = ok && make_map(&b.ut_a, ut, true, b.c, b.r, xb, b.ldu, 64, kBM);
+        ok = ok && make_map(&b.ut_b, ut, true, b.c, b.r, xb, b.ldu, 64, kBN);
+        ok = ok && make_map(&b.ut_mn, ut, true, b.c, b.r, xb, b.ldu, 64, 64);
+        const bool aligned4 = b.batched() && !b.split && b.r % 64 == 0 && b.c % 64 == 0;
         if (aligned4) {
             ok = ok && make_map4(&b.utk, ut, true, b.c, b.r, b.batch, b.ldu, 128, 1);
             ok = ok && make_map4(&b.utt, ut, true, b.c, b.r, b.batch, b.ldu, 64, 2);
@@ -870,43 +887,43 @@ static muon_status plan_build(muon_plan_s* p, const muon_shape* shapes, int32_t 
         if (restarts) {
             b.ut1_off = (long long)(L.o_ut1[k] / 2);
             __nv_bfloat16* ut1 = p->ut + b.ut1_off;
-            ok = ok && make_map(&b.ut1_a, ut1, true, b.c, b.r, b.batch, b.ldu, 64, kBM);
-            ok = ok && make_map(&b.ut1_b, ut1, true, b.c, b.r, b.batch, b.ldu, 64, kBN);
-            ok = ok && make_map(&b.ut1_mn, ut1, true, b.c, b.r, b.batch, b.ldu, 64, 64);
+            ok = ok && make_map(&b.ut1_a, ut1, true, b.c, b.r, xb, b.ldu, 64, kBM);
+            ok = ok && make_map(&b.ut1_b, ut1, true, b.c, b.r, xb, b.ldu, 64, kBN);
+            ok = ok && make_map(&b.ut1_mn, ut1, true, b.c, b.r, xb, b.ldu, 64, 64);
             if (aligned4) {
                 ok = ok && make_map4(&b.ut1k, ut1, true, b.c, b.r, b.batch, b.ldu, 128, 1);
                 ok = ok && make_map4(&b.ut1t, ut1, true, b.c, b.r, b.batch, b.ldu, 64, 2);
             }
         }
         if (!b.batched()) continue;   // the one-CTA kernels keep their r x r operands on chip
-        const size_t rr = (size_t)b.batch * b.r * b.ldr;
+        const size_t rr = (size_t)rb * b.r * b.ldr;
         const size_t step = (size_t)round_up((long long)rr * 2, 256);
-        char* rb = base + L.o_region + L.o_rr[k];
-        b.G[0] = reinterpret_cast<__half*>(rb);
-        b.G[1] = reinterpret_cast<__half*>(rb + step);
-        b.P = reinterpret_cast<__half*>(rb + 2 * step);
-        b.T = reinterpret_cast<__half*>(rb + 3 * step);
-        b.Q[0] = reinterpret_cast<__half*>(rb + 4 * step);
-        b.Q[1] = reinterpret_cast<__half*>(rb + 5 * step);
+        char* rbase = base + L.o_region + L.o_rr[k];
+        b.G[0] = reinterpret_cast<__half*>(rbase);
+        b.G[1] = reinterpret_cast<__half*>(rbase + step);
+        b.P = reinterpret_cast<__half*>(rbase + 2 * step);
+        b.T = reinterpret_cast<__half*>(rbase + 3 * step);
+        b.Q[0] = reinterpret_cast<__half*>(rbase + 4 * step);
+        b.Q[1] = reinterpret_cast<__half*>(rbase + 5 * step);
         b.Qb = reinterpret_cast<__nv_bfloat16*>(base + L.o_region + L.o_qb[k]);
-        ok = ok && make_map(&b.qb_a, b.Qb, true, b.r, b.r, b.batch, b.ldr, 64, kBM);
+        ok = ok && make_map(&b.qb_a, b.Qb, true, b.r, b.r, rb, b.ldr, 64, kBM);
         for (int g = 0; g < 2; ++g) {
-            ok = ok && make_map(&b.ga[g], b.G[g], false, b.r, b.r, b.batch, b.ldr, 64, kBM);
-            ok = ok && make_map(&b.gb[g], b.G[g], false, b.r, b.r, b.batch, b.ldr, 64, kBN);
-            ok = ok && make_map(&b.qb[g], b.Q[g], false, b.r, b.r, b.batch, b.ldr, 64, kBN);
-            ok = ok && make_map(&b.qa[g], b.Q[g], false, b.r, b.r, b.batch, b.ldr, 64, kBM);
+            ok = ok && make_map(&b.ga[g], b.G[g], false, b.r, b.r, rb, b.ldr, 64, kBM);
+            ok = ok && make_map(&b.gb[g], b.G[g], false, b.r, b.r, rb, b.ldr, 64, kBN);
+            ok = ok && make_map(&b.qb[g], b.Q[g], false, b.r, b.r, rb, b.ldr, 64, kBN);
+            ok = ok && make_map(&b.qa[g], b.Q[g], false, b.r, b.r, rb, b.ldr, 64, kBM);
         }
-        ok = ok && make_map(&b.pa, b.P, false, b.r, b.r, b.batch, b.ldr, 64, kBM);
-        ok = ok && make_map(&b.pb, b.P, false, b.r, b.r, b.batch, b.ldr, 64, kBN);
-        ok = ok && make_map(&b.tb, b.T, false, b.r, b.r, b.batch, b.ldr, 64, kBN);
-        ok = ok && make_map(&b.ta, b.T, false, b.r, b.r, b.batch, b.ldr, 64, kBM);
+        ok = ok && make_map(&b.pa, b.P, false, b.r, b.r, rb, b.ldr, 64, kBM);
+        ok = ok && make_map(&b.pb, b.P, false, b.r, b.r, rb, b.ldr, 64, kBN);
+        ok = ok && make_map(&b.tb, b.T, false, b.r, b.r, rb, b.ldr, 64, kBN);
+        ok = ok && make_map(&b.ta, b.T, false, b.r, b.r, rb, b.ldr, 64, kBM);
         for (int g = 0; g < 2; ++g) {
-            ok = ok && make_out_map(&b.og[g], b.G[g], false, b.r, b.batch, b.ldr);
-            ok = ok && make_out_map(&b.oq[g], b.Q[g], false, b.r, b.batch, b.ldr);
+            ok = ok && make_out_map(&b.og[g], b.G[g], false, b.r, rb, b.ldr);
+            ok = ok && make_out_map(&b.oq[g], b.Q[g], false, b.r, rb, b.ldr);
         }
-        ok = ok && make_out_map(&b.op, b.P, false, b.r, b.batch, b.ldr);
-        ok = ok && make_out_map(&b.ot, b.T, false, b.r, b.batch, b.ldr);
-        ok = ok && make_out_map(&b.oqb, b.Qb, true, b.r, b.batch, b.ldr);
+        ok = ok && make_out_map(&b.op, b.P, false, b.r, rb, b.ldr);
+        ok = ok && make_out_map(&b.ot, b.T, false, b.r, rb, b.ldr);
+        ok = ok && make_out_map(&b.oqb, b.Qb, true, b.r, rb, b.ldr);
         if (aligned4) {
             auto kt = [&](CUtensorMap* k, CUtensorMap* t, void* buf, bool bf) {
                 return make_map4(k, buf, bf, b.r, b.r, b.batch, b.ldr, 128, 1) &&
@@ -932,7 +949,7 @@ static muon_status plan_build(muon_plan_s* p, const muon_shape* shapes, int32_t 
         bool aligned = true;
         for (int k : ch.buckets) {
             const Bucket& b = p->buckets[k];
-            if (b.batched() && b.r > kBM) aligned = aligned && b.r % 64 == 0 && b.c % 64 == 0;
+            if (b.batched() && b.r > kBM) aligned = aligned && !b.split && b.r % 64 == 0 && b.c % 64 == 0;
         }
         ch.lower_ok = p->pair_clusters > 0 && aligned;
         ch.lower = ch.lower_ok && !p->opts.full_symmetric;
@@ -988,6 +1005,46 @@ muon_status muon_plan_create(const muon_shape* shapes, int32_t n, muon_dtype gra
         return plan_build(p, shapes, n, grad_dtype, opts, out);
     } catch (...) {   // std::vector's bad_alloc / length_error: host memory
         free_plan(p);
+        return MUON_ERR_OOM;
+    }
+}
+
+muon_status muon_partition(const muon_shape* shapes, int32_t n, int32_t world, const double* cost, int32_t* owner,
+                           double* load) {
+    if (!shapes || n <= 0 || !owner || world < 1 || world > 65536) return MUON_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i) {
+        if (shapes[i].rows <= 0 || shapes[i].cols <= 0 || shapes[i].rows > kMaxDim || shapes[i].cols > kMaxDim)
+            return MUON_ERR_INVALID_ARG;
+        if (cost && !(std::isfinite(cost[i]) && cost[i] >= 0.0)) return MUON_ERR_INVALID_ARG;
+    }
+    try {
+        std::vector<double> c(n);
+        for (int i = 0; i < n; ++i) {
+            if (cost) {
+                c[i] = cost[i];
+                continue;
+            }
+            const double r = (double)std::min(shapes[i].rows, shapes[i].cols);
+            const double cc = (double)std::max(shapes[i].rows, shapes[i].cols);
+            const double t_mem = 24.0 * r * cc / 6.8e12;
+            const double t_tc = r <= kSmallMaxR ? 0.0 : (3.0 * r * r * cc + 17.0 * r * r * r) / 1.5e15;
+            c[i] = std::max(t_mem, t_tc);
+        }
+        std::vector<int> order(n);
+        for (int i = 0; i < n; ++i) order[i] = i;
+        std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return c[a] > c[b]; });
+        std::vector<double> l(world, 0.0);
+        for (int i : order) {
+            int best = 0;
+            for (int r = 1; r < world; ++r)
+                if (l[r] < l[best]) best = r;
+            owner[i] = best;
+            l[best] += c[i];
+        }
+        if (load)
+            for (int r = 0; r < world; ++r) load[r] = l[r];
+        return MUON_OK;
+    } catch (...) {   // host memory
         return MUON_ERR_OOM;
     }
 }
@@ -1268,6 +1325,8 @@ static muon_status ns_step(muon_plan p, float* const* params, const void* const*
                     Bucket& b = p->buckets[bk];
                     if (!b.batched()) continue;
                     GemmProblem q = problem(b.r, b.r, b.c, b.batch, true, kEpiSyrk);
+                    q.a_split = q.b_split = b.split == 2;
+                    q.out_split = b.split != 0;
                     q.C = b.G[0];
                     q.strideC = (long long)b.r * b.ldr;
                     q.ldc = b.ldr;
@@ -1294,6 +1353,7 @@ static muon_status ns_step(muon_plan p, float* const* params, const void* const*
                 GemmProblem q = problem(b.r, b.r, b.r, b.batch, true, epi);
                 q.strideC = (long long)b.r * b.ldr;
                 q.ldc = b.ldr;
+                q.a_split = q.b_split = q.out_split = b.split != 0;   // every r x r operand and result
                 return q;
             };
             for (int k = 1; k <= J; ++k) {
@@ -1371,7 +1431,7 @@ static muon_status ns_step(muon_plan p, float* const* params, const void* const*
                 for (int bk : ch.buckets) {
                     Bucket& b = p->buckets[bk];
                     if (!b.batched()) continue;
-                    MUON_TRY(launch_identity_bf16(b.Qb, b.r, b.ldr, b.batch, sc));
+                    MUON_TRY(launch_identity_bf16(b.Qb, b.r, b.ldr, b.batch, b.split != 0, sc));
                     ++launches;
                 }
             }
@@ -1387,6 +1447,9 @@ static muon_status ns_step(muon_plan p, float* const* params, const void* const*
                     if (!b.batched()) continue;
                     GemmProblem q = problem(b.r, b.c, b.r, b.batch, false, last ? kEpiApply : kEpiXout);
                     q.b_mn = 1;
+                    q.a_split = b.split != 0;             // Q in two bf16 parts
+                    q.b_split = b.split == 2;             // X in two bf16 parts
+                    q.out_split = !last && b.split == 2;  // X' between segments
                     q.alpha = (first ? p->alpha : p->ones) + b.slot_base;
                     if (last) {
                         q.item_mat = b.d_item_mat;
@@ -1634,14 +1697,16 @@ muon_status muon_debug_copy_workspace(muon_plan p, int32_t i, int32_t which, voi
     const Bucket& b = p->buckets[p->mat_bucket[i]];
     // the fused kernel keeps its r x r operands on chip: only X0 and alpha exist
     if (!b.batched() && which >= 1 && which <= 7) return MUON_ERR_UNSUPPORTED;
-    const int item = p->mat_item[i];
+    // split buffers hold two parts per matrix (hi at 2 item, lo at 2 item + 1): the hi part is copied
+    const int item = p->mat_item[i] * (which >= 1 && which <= 7 && b.split ? 2 : 1);
+    const int xitem = p->mat_item[i] * (b.split == 2 ? 2 : 1);
     const size_t rr = (size_t)b.r * b.ldr;
     const void* src = nullptr;
     size_t bytes = 0;
     *ld = b.ldr;
     switch (which) {
         case 0:
-            src = p->ut + b.ut_off + (size_t)item * b.r * b.ldu;
+            src = p->ut + b.ut_off + (size_t)xitem * b.r * b.ldu;
             bytes = (size_t)b.r * b.ldu * 2;
             *ld = b.ldu;
             break;
@@ -1689,6 +1754,13 @@ muon_status muon_plan_info(muon_plan p, muon_plan_info_t* info) {
     for (const auto& ch : p->chunks) chain = std::max(chain, ch.chain_clusters);
     info->chain_clusters = chain;
     info->sm_count = p->sm_count;
+    int nsplit = 0, nf32 = 0;
+    for (const auto& b : p->buckets) {
+        nsplit += b.split ? 1 : 0;
+        nf32 += b.f32 ? 1 : 0;
+    }
+    info->split_buckets = nsplit;
+    info->fp32_buckets = nf32;
     return MUON_OK;
 }
 

@@ -119,6 +119,17 @@ __global__ void __launch_bounds__(kElemThreads) k_momentum_rows(const ElemArgs a
                 pk.z = pack_bf16x2(u4, u5);
                 pk.w = pack_bf16x2(u6, u7);
                 *reinterpret_cast<uint4*>(U + e) = pk;
+                if (md.x_split) {   // lo part: u - bf16(u), itself rounded to bf16
+                    const float v[8] = {u0, u1, u2, u3, u4, u5, u6, u7};
+                    const uint32_t h[4] = {pk.x, pk.y, pk.z, pk.w};
+                    uint32_t l[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float2 hf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&h[q]));
+                        l[q] = pack_bf16x2(v[2 * q] - hf.x, v[2 * q + 1] - hf.y);
+                    }
+                    *reinterpret_cast<uint4*>(U + (long long)md.r * md.ldu + e) = make_uint4(l[0], l[1], l[2], l[3]);
+                }
             }
         }
     } else {
@@ -131,7 +142,9 @@ __global__ void __launch_bounds__(kElemThreads) k_momentum_rows(const ElemArgs a
                 M[e] = m;
                 const float u = mu * m + g;
                 ss += u * u;
-                U[i * md.ldu + j] = __float2bfloat16_rn(u);
+                const __nv_bfloat16 h = __float2bfloat16_rn(u);
+                U[i * md.ldu + j] = h;
+                if (md.x_split) U[(long long)md.r * md.ldu + i * md.ldu + j] = __float2bfloat16_rn(u - __bfloat162float(h));
             }
         }
     }
@@ -214,7 +227,12 @@ __global__ void __launch_bounds__(kElemThreads) k_momentum_tiles(const ElemArgs 
 #pragma unroll
                 for (int q = 0; q < kTileRows / 32; ++q) {
                     const int ii = lane + 32 * q;
-                    if (i0 + ii < md.m) dst[ii] = __float2bfloat16_rn(tile[jj][ii]);
+                    if (i0 + ii < md.m) {
+                        const float u = tile[jj][ii];
+                        const __nv_bfloat16 h = __float2bfloat16_rn(u);
+                        dst[ii] = h;
+                        if (md.x_split) dst[(long long)md.r * md.ldu + ii] = __float2bfloat16_rn(u - __bfloat162float(h));
+                    }
                 }
             }
         }
@@ -241,7 +259,7 @@ __global__ void k_norm_finalize(const ElemArgs a) {
     }
 }
 
-__global__ void k_identity_bf16(__nv_bfloat16* q, int r, int ld, long long total) {
+__global__ void k_identity_bf16(__nv_bfloat16* q, int r, int ld, long long total, int split) {
     pdl_trigger();
     pdl_wait();
     const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -249,7 +267,8 @@ __global__ void k_identity_bf16(__nv_bfloat16* q, int r, int ld, long long total
     const long long per = (long long)r * ld;
     const long long w = e % per;
     const long long i = w / ld, j = w % ld;
-    q[e] = __float2bfloat16_rn((i == j) ? 1.f : 0.f);
+    const bool lo_part = split && ((e / per) & 1);
+    q[e] = __float2bfloat16_rn((i == j && !lo_part) ? 1.f : 0.f);
 }
 
 // ------------------------------------------------------------------ RowNorm, m <= n (stored rows)
@@ -481,10 +500,11 @@ cudaError_t launch_norm_finalize(const ElemArgs& a, cudaStream_t s) {
     const int blocks = (a.nlist + warps_per_block - 1) / warps_per_block;
     return launch_pdl(k_norm_finalize, dim3(blocks), dim3(kElemThreads), 0, s, a);
 }
-cudaError_t launch_identity_bf16(__nv_bfloat16* q, int r, int ld, int batch, cudaStream_t s) {
-    const long long total = (long long)r * ld * batch;
+cudaError_t launch_identity_bf16(__nv_bfloat16* q, int r, int ld, int batch, bool split, cudaStream_t s) {
+    const long long total = (long long)r * ld * batch * (split ? 2 : 1);
     if (total <= 0) return cudaSuccess;
-    return launch_pdl(k_identity_bf16, dim3((unsigned)((total + 255) / 256)), dim3(256), 0, s, q, r, ld, total);
+    return launch_pdl(k_identity_bf16, dim3((unsigned)((total + 255) / 256)), dim3(256), 0, s, q, r, ld, total,
+                      split ? 1 : 0);
 }
 cudaError_t launch_rownorm_rows(const ElemArgs& a, long long blocks, cudaStream_t s) {
     if (blocks <= 0) return cudaSuccess;

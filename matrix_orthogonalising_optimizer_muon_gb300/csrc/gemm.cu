@@ -122,25 +122,28 @@ __global__ void __maxnreg__(168) gemm_kernel(const __grid_constant__ GemmLaunch 
             for (int t = blockIdx.x; ok && t < L.total_tiles; t += gridDim.x) {
                 const TileCoord tc = decode_tile(L, t);
                 const GemmProblem& P = L.prob[tc.p];
-                const int kblocks = (P.K + Cfg::BK - 1) / Cfg::BK;
-                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                const int nkb = (P.K + Cfg::BK - 1) / Cfg::BK;
+                const int kblocks = nkb * split_passes(P);
+                for (int kbt = 0; kbt < kblocks; ++kbt, ++it) {
                     const uint32_t s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1u;
                     if (!mbar_wait_idle(empty + s, ph ^ 1u, abort_flag, L.status, kStatusTimeoutProducer, false)) {
                         ok = false;
                         break;
                     }
+                    int kb, za, zb;   // split passes: the part of A and B this k-block reads
+                    split_coords(P, kbt, nkb, tc.item, &kb, &za, &zb);
                     uint8_t* sa = smem + s * Cfg::STAGE_BYTES;
                     uint8_t* sb = sa + Cfg::A_BYTES;
                     mbar_arrive_expect_tx(full + s, Cfg::STAGE_BYTES);
-                    tma_load_3d(sa, &L.mapA[tc.p], full + s, kb * Cfg::BK, tc.m0, tc.item);
+                    tma_load_3d(sa, &L.mapA[tc.p], full + s, kb * Cfg::BK, tc.m0, za);
                     if (!P.b_mn) {
-                        tma_load_3d(sb, &L.mapB[tc.p], full + s, kb * Cfg::BK, tc.n0, tc.item);
+                        tma_load_3d(sb, &L.mapB[tc.p], full + s, kb * Cfg::BK, tc.n0, zb);
                     } else {
 #pragma unroll
                         for (int q = 0; q < kBN / 64; ++q)
                             tma_load_3d(sb + q * Cfg::MN_CHUNK_BYTES, &L.mapB[tc.p], full + s, tc.n0 + 64 * q,
-                                        kb * Cfg::BK, tc.item);
+                                        kb * Cfg::BK, zb);
                     }
                 }
             }
@@ -159,7 +162,7 @@ __global__ void __maxnreg__(168) gemm_kernel(const __grid_constant__ GemmLaunch 
             for (int t = blockIdx.x; ok && t < L.total_tiles; t += gridDim.x, ++local) {
                 const TileCoord tc = decode_tile(L, t);
                 const GemmProblem& P = L.prob[tc.p];
-                const int kblocks = (P.K + Cfg::BK - 1) / Cfg::BK;
+                const int kblocks = (P.K + Cfg::BK - 1) / Cfg::BK * split_passes(P);
                 const uint32_t acc = local & 1;
                 const uint32_t aph = (local >> 1) & 1u;
                 if (!mbar_wait_idle(tempty + acc, aph ^ 1u, abort_flag, L.status, kStatusTimeoutMma, false)) break;
@@ -369,7 +372,8 @@ __global__ void __maxnreg__(168) gemm2_kernel(const __grid_constant__ GemmLaunch
             for (int t = cluster_id; ok && t < L.total_tiles; t += nclusters) {
                 const TileCoord tc = decode(t);
                 const GemmProblem& P = L.prob[tc.p];
-                const int kblocks = (P.K + Cfg::BK - 1) / Cfg::BK;
+                const int nkb = (P.K + Cfg::BK - 1) / Cfg::BK;
+                const int kblocks = LOWER ? nkb : nkb * split_passes(P);
                 // lower-triangle launches: the problem's fields and maps read once per tile
                 const bool sym_a = P.sym_a != 0, sym_b = P.sym_b != 0, bmn = P.b_mn != 0;
                 const CUtensorMap* mA = &L.mapA[tc.p];
@@ -397,13 +401,14 @@ __global__ void __maxnreg__(168) gemm2_kernel(const __grid_constant__ GemmLaunch
                         tma_load_4d_pair(sb, bt ? mBt : mB, fb, 0, bt ? k0 : nb, bt ? (nb >> 6) : kb, tc.item);
                         continue;
                     }
-                    tma_load_3d_pair(sa, &L.mapA[tc.p], fb, kb * Cfg::BK, tc.m0, tc.item);
+                    int kr, za, zb;   // split passes: the part of A and B this k-block reads
+                    split_coords(P, kb, nkb, tc.item, &kr, &za, &zb);
+                    tma_load_3d_pair(sa, &L.mapA[tc.p], fb, kr * Cfg::BK, tc.m0, za);
                     if (!P.b_mn) {
-                        tma_load_3d_pair(sb, &L.mapB[tc.p], fb, kb * Cfg::BK, nb, tc.item);
+                        tma_load_3d_pair(sb, &L.mapB[tc.p], fb, kr * Cfg::BK, nb, zb);
                     } else {
-                        tma_load_3d_pair(sb, &L.mapB[tc.p], fb, nb, kb * Cfg::BK, tc.item);
-                        tma_load_3d_pair(sb + Cfg::MN_CHUNK_BYTES, &L.mapB[tc.p], fb, nb + 64, kb * Cfg::BK,
-                                         tc.item);
+                        tma_load_3d_pair(sb, &L.mapB[tc.p], fb, nb, kr * Cfg::BK, zb);
+                        tma_load_3d_pair(sb + Cfg::MN_CHUNK_BYTES, &L.mapB[tc.p], fb, nb + 64, kr * Cfg::BK, zb);
                     }
                 }
             }
@@ -423,7 +428,7 @@ __global__ void __maxnreg__(168) gemm2_kernel(const __grid_constant__ GemmLaunch
             for (int t = cluster_id; ok && t < L.total_tiles; t += nclusters, ++local) {
                 const TileCoord tc = decode(t);
                 const GemmProblem& P = L.prob[tc.p];
-                const int kblocks = (P.K + Cfg::BK - 1) / Cfg::BK;
+                const int kblocks = (P.K + Cfg::BK - 1) / Cfg::BK * (LOWER ? 1 : split_passes(P));
                 const uint32_t acc = local & 1;
                 const uint32_t aph = (local >> 1) & 1u;
                 if (!mbar_wait_idle(tempty + acc, aph ^ 1u, abort_flag, L.status, kStatusTimeoutMma, true)) break;

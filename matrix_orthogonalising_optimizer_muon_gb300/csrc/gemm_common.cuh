@@ -36,12 +36,47 @@ __device__ __forceinline__ uint32_t pack_bf162(float a, float b) {
 // v[j] is element (row, col0 + j) of a symmetric result.  The lower part goes to
 // (row, col), its mirror to (col, row).  Rows beyond M are masked (their lanes
 // still took part in the collective TMEM load).
+// Writes the chunk to the outputs C, C2 (fp16) and Cb (bf16) given (any may be null),
+// at batch item `item`, with the problem's shape and strides.
+__device__ __forceinline__ void store_sym_to(const GemmProblem& P, __half* C0, __half* C20, __nv_bfloat16* Cb0,
+                                             int item, int row, int col0, const float (&v)[32]);
+
+// out_split: hi = round(v) to item 2i, lo = round(v - hi) to item 2i + 1 (fp16 for C
+// and C2, bf16 for Cb, each rounded in its own format).
 __device__ __forceinline__ void store_sym(const GemmProblem& P, int item, int row, int col0, const float (&v)[32]) {
+    if (!P.out_split) {
+        store_sym_to(P, P.C, P.C2, P.Cb, item, row, col0, v);
+        return;
+    }
+    if (row >= P.M) return;
+    float hi[32], lo[32];
+    if (P.C || P.C2) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            hi[j] = __half2float(to_half(v[j]));
+            lo[j] = v[j] - hi[j];
+        }
+        store_sym_to(P, P.C, P.C2, nullptr, 2 * item, row, col0, hi);
+        store_sym_to(P, P.C, P.C2, nullptr, 2 * item + 1, row, col0, lo);
+    }
+    if (P.Cb) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            hi[j] = __bfloat162float(__float2bfloat16_rn(v[j]));
+            lo[j] = v[j] - hi[j];
+        }
+        store_sym_to(P, nullptr, nullptr, P.Cb, 2 * item, row, col0, hi);
+        store_sym_to(P, nullptr, nullptr, P.Cb, 2 * item + 1, row, col0, lo);
+    }
+}
+
+__device__ __forceinline__ void store_sym_to(const GemmProblem& P, __half* C0, __half* C20, __nv_bfloat16* Cb0,
+                                             int item, int row, int col0, const float (&v)[32]) {
     if (row >= P.M) return;
     const long long ib = item * P.strideC;
-    __half* C = P.C ? P.C + ib : nullptr;
-    __half* C2 = P.C2 ? P.C2 + ib : nullptr;
-    __nv_bfloat16* Cb = P.Cb ? P.Cb + ib : nullptr;
+    __half* C = C0 ? C0 + ib : nullptr;
+    __half* C2 = C20 ? C20 + ib : nullptr;
+    __nv_bfloat16* Cb = Cb0 ? Cb0 + ib : nullptr;
     const long long rbase = (long long)row * P.ldc + col0;
     const bool full = (col0 + 31 <= row) && (col0 + 31 < P.N);
     if (full) {
@@ -203,7 +238,8 @@ __device__ __forceinline__ void prefetch_epilogue_inputs(const GemmProblem& P, i
         const int row = row0 + lane;
         if (row >= P.M || (P.ldc & 7)) return;
         const uint32_t bytes = (uint32_t)(nc & ~7) * 2u;
-        if (bytes) prefetch_l2_bulk(P.Gin + item * P.strideC + (long long)row * P.ldc + col0, bytes);
+        const int gi = P.a_split ? 2 * item : item;
+        if (bytes) prefetch_l2_bulk(P.Gin + gi * P.strideC + (long long)row * P.ldc + col0, bytes);
     }
 }
 
@@ -221,7 +257,8 @@ __device__ __forceinline__ void epilogue_values(const GemmProblem& P, int item, 
     } else if (P.epi == kEpiPoly) {
         // P = a I + b' G' + c' G'^2, with G' read (8 values at a time) from the fp16
         // input the MMA used
-        const __half* Grow = P.Gin + item * P.strideC + (long long)(row < P.M ? row : 0) * P.ldc + col0;
+        const int gi = P.a_split ? 2 * item : item;   // split: G' = hi (item 2i) + lo (item 2i + 1)
+        const __half* Grow = P.Gin + gi * P.strideC + (long long)(row < P.M ? row : 0) * P.ldc + col0;
         const bool vec = (row < P.M) && (col0 + 31 < P.N);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -240,6 +277,11 @@ __device__ __forceinline__ void epilogue_values(const GemmProblem& P, int item, 
                 for (int e = 0; e < 8; ++e)
                     g[e] = (row < P.M && col0 + 8 * q + e < P.N) ? __half2float(Grow[8 * q + e]) : 0.f;
             }
+            if (P.a_split) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    g[e] += (row < P.M && col0 + 8 * q + e < P.N) ? __half2float(Grow[P.strideC + 8 * q + e]) : 0.f;
+            }
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int j = 8 * q + e;
@@ -255,6 +297,19 @@ __device__ __forceinline__ void store_xout(const GemmProblem& P, int item, int r
                                            const uint32_t (&raw)[32]) {
     if (row >= P.M) return;
     const float al = P.alpha[item];
+    if (P.out_split) {   // X' as bf16 hi (item 2i) and lo (item 2i + 1)
+        __nv_bfloat16* hi = P.Cb + 2 * item * P.strideC + (long long)row * P.ldc + col0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (col0 + j < P.N) {
+                const float x = al * __uint_as_float(raw[j]);
+                const __nv_bfloat16 h = __float2bfloat16_rn(x);
+                hi[j] = h;
+                hi[P.strideC + j] = __float2bfloat16_rn(x - __bfloat162float(h));
+            }
+        }
+        return;
+    }
     __nv_bfloat16* dst = P.Cb + item * P.strideC + (long long)row * P.ldc + col0;
     if (col0 + 31 < P.N && (P.ldc & 7) == 0) {
 #pragma unroll

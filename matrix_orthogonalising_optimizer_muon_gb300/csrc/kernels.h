@@ -121,8 +121,33 @@ struct GemmProblem {
     // diagonal tile).  sym_a / sym_b: that operand is stored so; its 64-deep k-blocks
     // beyond the operand rows' diagonal tile are read from the mirror position.
     int lower_out, sym_a, sym_b;
+    // Split precision (launches of plans that carry an operand as two 2-byte parts,
+    // value = hi + lo): a split buffer holds 2 x batch items, hi of item i at 2i and lo
+    // at 2i + 1.  a_split / b_split: that operand is split, and the product runs as
+    // K-concatenated passes over the parts, (hi, hi), (hi, lo), (lo, hi) when both are
+    // split, (hi), (lo) of the split one otherwise, all into one fp32 accumulator.
+    // out_split: the output (C, C2, Cb) is written as hi = round(v), lo = round(v - hi).
+    // kEpiPoly reads its G' input split when a_split is set.  Per-thread stores only.
+    int a_split, b_split, out_split;
 };
 constexpr int kTmaOutC = 1, kTmaOutC2 = 2, kTmaOutBf16 = 4;
+
+// K-concatenated passes of a (possibly split) product and the parts each reads.
+__host__ __device__ __forceinline__ int split_passes(const GemmProblem& P) {
+    return (P.a_split && P.b_split) ? 3 : ((P.a_split || P.b_split) ? 2 : 1);
+}
+// For k-block kbt of the concatenated product (nkb k-blocks per pass): the k-block
+// within the pass and the batch coordinates of A and B (item, or 2 item + part).
+__host__ __device__ __forceinline__ void split_coords(const GemmProblem& P, int kbt, int nkb, int item, int* kb,
+                                                      int* za, int* zb) {
+    const int pass = kbt / nkb;
+    *kb = kbt - pass * nkb;
+    const bool both = P.a_split && P.b_split;
+    const int a_lo = P.a_split ? (both ? pass == 2 : pass == 1) : 0;
+    const int b_lo = P.b_split ? (pass == 1) : 0;
+    *za = P.a_split ? 2 * item + a_lo : item;
+    *zb = P.b_split ? 2 * item + b_lo : item;
+}
 
 struct GemmLaunch {
     CUtensorMap mapA[kMaxProblems];
@@ -175,7 +200,7 @@ struct MatDev {
     long long cpart_off;     // offset of its RowNorm column partial sums (m > n)
     long long inv_off;       // offset of its RowNorm per-column inverse norms (m > n)
     float scale;             // 0.2 * sqrt(c)
-    int pad;
+    int x_split;             // X0 kept as bf16 hi and lo parts (lo at ut_off + r * ldu)
 };
 
 struct ElemArgs {
@@ -203,7 +228,8 @@ cudaError_t launch_momentum_tiles(const ElemArgs& a, long long blocks, cudaStrea
 // alpha[slot] = 1 / sqrt(sum of partials) (0 for a zero input); one warp per matrix.
 cudaError_t launch_norm_finalize(const ElemArgs& a, cudaStream_t s);
 // Fill a batch of r x r bf16 identities (ns_steps = 0).
-cudaError_t launch_identity_bf16(__nv_bfloat16* q, int r, int ld, int batch, cudaStream_t s);
+// split: q holds 2 x batch items (hi, lo per matrix); the lo parts are filled with zeros.
+cudaError_t launch_identity_bf16(__nv_bfloat16* q, int r, int ld, int batch, bool split, cudaStream_t s);
 // RowNorm: rows of the stored matrix (m <= n), one block per row, fused apply.
 cudaError_t launch_rownorm_rows(const ElemArgs& a, long long blocks, cudaStream_t s);
 // RowNorm, m > n: column statistics, finalize, apply.

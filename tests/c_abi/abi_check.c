@@ -23,6 +23,8 @@ int main(void) {
     FIELD(muon_plan_opts, full_symmetric);
     FIELD(muon_plan_opts, small_fp32);
     FIELD(muon_plan_opts, check_finite);
+    FIELD(muon_plan_opts, precision);
+    FIELD(muon_plan_opts, split_max_r);
     printf("sizeof.muon_plan_info_t %zu\n", sizeof(muon_plan_info_t));
     FIELD(muon_plan_info_t, n_matrices);
     FIELD(muon_plan_info_t, n_buckets);
@@ -33,6 +35,8 @@ int main(void) {
     FIELD(muon_plan_info_t, lower_chunks);
     FIELD(muon_plan_info_t, tuned_candidates);
     FIELD(muon_plan_info_t, chain_clusters);
+    FIELD(muon_plan_info_t, split_buckets);
+    FIELD(muon_plan_info_t, fp32_buckets);
     printf("sizeof.muon_shape %zu\n", sizeof(muon_shape));
 
     for (int s = MUON_OK; s <= MUON_ERR_NONFINITE; ++s) printf("status.%d %s\n", s, muon_status_string((muon_status)s));

@@ -257,6 +257,11 @@ def test_other_ns_step_counts(ns_steps):
         assert_ns(res, i, ns_steps=ns_steps)
 
 
+# Measured O errors of the rank-3 inputs below on GB300 (precision 0), by (J, generic_small):
+# (3, fused) 0.068-0.083, (3, batched) 0.081-0.089, (5, fused) 0.90-1.85, (5, batched) 1.85-2.61.
+RANK3_BOUND = {3: 0.12, 5: 3.4}
+
+
 @pytest.mark.parametrize("ns_steps", [3, 5])
 @pytest.mark.parametrize("generic_small", [False, True])
 def test_rank_deficient_input_stays_finite(ns_steps, generic_small):
@@ -264,7 +269,8 @@ def test_rank_deficient_input_stays_finite(ns_steps, generic_small):
     0), and bf16 rounding of X0 leaves ~1e-4 singular values in U's null space, so a
     bf16 NS of an exactly low-rank U is not close to the exact one (the fp64 oracle
     maps those directions to 0).  What must hold up to the largest supported J (5):
-    no NaN or inf, O bounded, and the momentum and the update given O exact."""
+    no NaN or inf, O bounded, O within the measured error plus 30 %, and the momentum
+    and the update given O exact."""
     import torch
     shapes = [(96, 300), (300, 96), (200, 700)]
     inputs = []
@@ -276,8 +282,9 @@ def test_rank_deficient_input_stays_finite(ns_steps, generic_small):
     res = run_step(shapes, "f32", inputs=inputs, ns_steps=ns_steps, generic_small=generic_small)
     for i in range(len(shapes)):
         assert bool(torch.isfinite(res["O"][i]).all()) and bool(torch.isfinite(res["W"][i]).all()), shapes[i]
-        assert float(res["O"][i].abs().max()) < 10.0, shapes[i]
-        e = check_ns_matrix(res, i, ns_steps, 1.0)
+        assert float(res["O"][i].abs().max()) < 1.0, shapes[i]
+        e = check_ns_matrix(res, i, ns_steps, RANK3_BOUND[ns_steps])
+        assert e["o"] <= RANK3_BOUND[ns_steps], (shapes[i], e)
         assert e["m"] <= TOL_FP32 and e["w_given_o"] <= TOL_FP32, (shapes[i], e)
 
 
@@ -577,12 +584,14 @@ def test_restarted_segments_match_oracle(steps, restart):
 
 
 def test_restart_every_step_on_ill_conditioned_input():
-    """Singular values spread from 1 to 1e-4: the Gram form carries fp16 rounding of
-    G into the small singular directions through Q (measured 0.17 on GB300); the
-    direct form (restart 1) recomputes X X^T from the iterate every step and cuts the
-    error to less than half (measured 0.073).  It stays above the 2e-2 bar: the
-    iterates are bf16 (X0 from the momentum pass, X' between steps), whose rounding
-    the small singular directions cannot carry."""
+    """Singular values spread from 1 to 1e-4 on the plain recipe (precision -1): the Gram
+    form carries fp16 rounding of G into the small singular directions through Q
+    (measured 0.17 on GB300); the direct form (restart 1) recomputes X X^T from the
+    iterate every step and cuts the error to less than half (measured 0.073).  It stays
+    above the 2e-2 bar: the iterates are bf16 (X0 from the momentum pass, X' between
+    steps), whose rounding the small singular directions cannot carry; precision 2
+    (test_split_level_2_on_an_ill_conditioned_input) removes that limit.  The bounds
+    pinned here are the measured values plus 30 %."""
     import torch
     rng = np.random.default_rng(7)
     r, c = 256, 1024
@@ -593,9 +602,9 @@ def test_restart_every_step_on_ill_conditioned_input():
     w = torch.from_numpy(rng.standard_normal((r, c)) * 0.02).float()
     inputs = [(w, g, torch.zeros(r, c))]
     errs = {}
-    for restart in (5, 1):
-        res = run_step([(r, c)], "f32", inputs=inputs, restart=restart, max_ns_steps=5)
-        errs[restart] = check_ns_variant(res, 0, 5, R.NS_COEFFS, 1.0)
+    for restart, bound in ((5, 0.22), (1, 0.095)):
+        res = run_step([(r, c)], "f32", inputs=inputs, restart=restart, max_ns_steps=5, precision=-1)
+        errs[restart] = check_ns_variant(res, 0, 5, R.NS_COEFFS, bound)
     assert errs[1] < 0.6 * errs[5], errs
 
 
@@ -902,3 +911,106 @@ def test_resume_from_saved_state_is_bitwise():
     for i in range(len(shapes)):
         assert torch.equal(W1[i], W3[i]), ("W", i)
         assert torch.equal(M1[i], M3[i]), ("M", i)
+
+
+def test_distributed_muon_on_one_rank_is_the_plan_step_bitwise():
+    """DistributedMuon without a process group (one rank owns every matrix): its step is
+    the plan's step, bitwise, in both modes; with allocate_params the parameters are views
+    into one flat buffer."""
+    import torch
+    import matrix_orthogonalising_optimizer_muon_gb300 as lib
+    shapes = [(300, 700), (700, 300), (128, 512), (96, 96)]
+    inputs = host_inputs(shapes, "bf16", base_seed=71)
+    opt = lib.DistributedMuon(shapes, "bf16")
+    assert opt.world == 1 and opt.owned == list(range(len(shapes)))
+    W1 = opt.allocate_params("cuda")
+    for w, (w0, _, _) in zip(W1, inputs):
+        w.copy_(w0.cuda())
+    M1 = [m.cuda() for _, _, m in inputs]
+    plan = lib.MuonPlan(shapes, "bf16")
+    W2 = [w.cuda() for w, _, _ in inputs]
+    M2 = [m.cuda() for _, _, m in inputs]
+    for mode in ("ns", "rownorm", "ns"):
+        G = [g.cuda() for _, g, _ in inputs]
+        opt.step(W1, G, M1, LR, WD, MU, 5, mode)
+        if mode == "ns":
+            plan.step(W2, G, M2, LR, WD, MU, 5, "ns")
+        else:
+            plan.rownorm_step(W2, G, M2, LR, WD, MU, 1e-8)
+    opt.sync()
+    plan.sync()
+    for i in range(len(shapes)):
+        assert torch.equal(W1[i], W2[i]) and torch.equal(M1[i], M2[i]), i
+    opt.close()
+    plan.close()
+
+
+# --------------------------------------------------------------- split precision (opts.precision)
+NEAR_SQUARE = [(256, 256), (384, 384), (512, 512), (200, 210), (300, 256), (576, 640)]
+
+
+def test_near_square_batched_buckets_split_by_default():
+    """Nearly square batched buckets (r > 128) carry the r x r recursion and Q in two parts
+    (precision 0 picks level 1 for them): O within the bar with margin (emulated 3-4e-3;
+    the plain recipe measured 2.1e-2 on 256 x 256), next to rectangular buckets that stay
+    plain in the same plan."""
+    shapes = NEAR_SQUARE + [(300, 700), (700, 300)]
+    res = run_step(shapes, "bf16", base_seed=33)
+    assert res["plan"].info()["split_buckets"] == len(NEAR_SQUARE)
+    for i in range(len(NEAR_SQUARE)):
+        e = assert_ns(res, i)
+        assert e["o"] <= 1e-2, (shapes[i], e)
+    for i in range(len(NEAR_SQUARE), len(shapes)):
+        assert_ns(res, i)
+    plain = run_step(shapes, "bf16", base_seed=33, precision=-1)
+    assert plain["plan"].info()["split_buckets"] == 0
+
+
+@pytest.mark.parametrize("ns_steps", [0, 1, 2, 5])
+def test_small_squares_on_the_batched_split_path(ns_steps):
+    """r <= 128 squares on the batched products (generic_small, small_fp32 = -1) with
+    precision 1: the one-SM kernel's split passes meet the bar at every step count."""
+    shapes = [(64, 64), (96, 96), (128, 128), (100, 100), (128, 3584)]
+    res = run_step(shapes, "bf16", base_seed=34, ns_steps=ns_steps, generic_small=True, small_fp32=-1,
+                   precision=1)
+    assert res["plan"].info()["split_buckets"] == len(shapes)
+    for i in range(len(shapes)):
+        e = assert_ns(res, i, ns_steps=ns_steps)
+        assert e["o"] <= 1e-2, (shapes[i], e)
+
+
+@pytest.mark.parametrize("precision", [1, 2])
+def test_split_levels_on_the_ragged_plan(precision):
+    """Every batched bucket of the ragged plan split (level 1, or 2 with X0 in two parts as
+    well): both orientations, ragged tails, the one-SM and the CTA-pair kernels."""
+    res = run_step(RAGGED, "bf16", base_seed=21, precision=precision)
+    for i in range(len(RAGGED)):
+        e = assert_ns(res, i)
+        assert e["o"] <= 1e-2, (RAGGED[i], e)
+
+
+def test_split_level_2_on_an_ill_conditioned_input():
+    """Singular values spread from 1 to 1e-4 (as in the restart test): the plain recipe
+    measured 0.17 (Gram form) and 0.073 (restart every step); with X0, the recursion and
+    Q all in two parts the error falls below the 2e-2 bar (emulated: 9e-5 with fp32 X0,
+    4.8e-2 with a one-part bf16 X0)."""
+    import torch
+    rng = np.random.default_rng(7)
+    r, c = 256, 1024
+    a, _ = np.linalg.qr(rng.standard_normal((r, r)))
+    b, _ = np.linalg.qr(rng.standard_normal((c, r)))
+    u = (a * np.logspace(0, -4, r)) @ b.T * 1e-3
+    g = torch.from_numpy(u / (1 + MU)).float()
+    w = torch.from_numpy(rng.standard_normal((r, c)) * 0.02).float()
+    res = run_step([(r, c)], "f32", inputs=[(w, g, torch.zeros(r, c))], precision=2)
+    e = assert_ns(res, 0)
+    assert e["o"] <= 2e-2, e
+
+
+@pytest.mark.parametrize("precision", [1, 2])
+def test_split_levels_with_restarted_segments(precision):
+    """Ten steps in two restarted segments: the iterate between them is written in two
+    parts at level 2 and read back by the next SYRK."""
+    res = run_step(VARIANT_SHAPES, "bf16", base_seed=62, ns_steps=10, max_ns_steps=10, precision=precision)
+    for i in range(len(VARIANT_SHAPES)):
+        check_ns_variant(res, i, 10, R.NS_COEFFS, TOL_O)

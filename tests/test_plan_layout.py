@@ -164,3 +164,34 @@ def test_size_limits():
         with pytest.raises(mu.MuonError) as e:
             ws(bad)
         assert e.value.code == mu.MUON_ERR_UNSUPPORTED
+
+
+def test_near_square_small_matrices_hold_no_gram_buffers():
+    """Nearly square matrices with r <= 128 run in fp32 on chip (small_fp32 = 0): no r x r
+    buffers, with or without generic_small; small_fp32 = -1 puts them back on the tensor
+    cores (batched with generic_small: seven r x r buffers, split in two parts by
+    precision 0 since they are nearly square)."""
+    sq = [(96, 96)] * 4
+    base = ws(sq)["workspace_bytes"]
+    assert ws(sq, generic_small=True)["workspace_bytes"] == base
+    rr = r256(4 * 96 * r8(96) * 2)
+    extra = ws(sq, generic_small=True, small_fp32=-1)["workspace_bytes"] - base
+    assert extra == 7 * r256(2 * 4 * 96 * r8(96) * 2)    # split: two parts per matrix
+    extra_plain = ws(sq, generic_small=True, small_fp32=-1, precision=-1)["workspace_bytes"] - base
+    assert extra_plain == 7 * rr
+
+
+def test_split_precision_doubles_the_split_buffers():
+    """precision 0 splits nearly square batched buckets only (r <= split_max_r): their seven
+    r x r buffers hold two parts per matrix; level 2 also doubles X0."""
+    sq, rect = (256, 256), (256, 1024)
+    rr = r256(256 * 256 * 2)
+    assert ws([sq])["workspace_bytes"] - ws([sq], precision=-1)["workspace_bytes"] == 7 * (r256(2 * rr) - rr)
+    assert ws([rect])["workspace_bytes"] == ws([rect], precision=-1)["workspace_bytes"]
+    assert ws([sq], split_max_r=128)["workspace_bytes"] == ws([sq], precision=-1)["workspace_bytes"]
+    x = r256(256 * 1024 * 2)
+    two = ws([rect], precision=2)["workspace_bytes"] - ws([rect], precision=-1)["workspace_bytes"]
+    assert two == 7 * (r256(2 * rr) - rr) + x
+    # the 7B layer's squares (r = 3584) and the DiT block's (r = 2048) stay plain
+    assert ws(LAYER) == ws(LAYER, precision=-1)
+    assert ws([(2048, 2048)]) == ws([(2048, 2048)], precision=-1)
