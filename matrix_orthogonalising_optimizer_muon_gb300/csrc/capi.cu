@@ -89,6 +89,20 @@ bool make_map4(CUtensorMap* map, void* base, bool bf16, uint64_t cols, uint64_t 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// W of one matrix (fp32, stored m x n row-major, 16-byte aligned, n % 4 == 0), 128 x 128
+// boxes without swizzle: the final product's L2 prefetch of a tile's W.
+bool make_w_prefetch_map(CUtensorMap* map, void* W, uint64_t m, uint64_t n) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {n, m};
+    cuuint64_t strides[1] = {n * 4};
+    cuuint32_t box[2] = {128, 128};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, W, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 // Store map over `batch` r x r row-major matrices (leading dim ld): 32 x 32 boxes
 // in the 64-byte-swizzled shared layout the pair kernel's epilogue stages.
 bool make_out_map(CUtensorMap* map, void* base, bool bf16, uint64_t r, uint64_t batch, uint64_t ld) {
@@ -192,13 +206,13 @@ struct muon_plan_s {
     unsigned char* d_transposed = nullptr;
     void** d_ptrs = nullptr;   // [G(n) | M(n) | W(n)]
 
-    ListDev rn_rows, rn_stats, rn_final, rn_apply;
+    ListDev rn_rows[kRowClasses], rn_stats, rn_final, rn_apply;   // rows by length class
     // NS steps run chunk by chunk; the chunks' X0 and r x r buffers share (alias) one
     // workspace region.  One chunk unless opts.workspace_bytes caps the workspace.
     struct Chunk {
         std::vector<int> buckets;
         ListDev mom_rows, mom_tiles, all;
-        ListDev rn_rows, rn_stats, rn_final, rn_apply;   // RowNorm of this chunk (muon_step_host)
+        ListDev rn_rows[kRowClasses], rn_stats, rn_final, rn_apply;   // RowNorm of this chunk (muon_step_host)
         int chain_clusters = 0;   // CTA pairs for the batched products beside the fused kernel
         int chain_est = 0;        // the work estimate's choice (chunks with fused and batched work)
         bool mixed = false;       // the chunk holds both fused and batched matrices
@@ -208,6 +222,10 @@ struct muon_plan_s {
     std::vector<Chunk> chunks;
 
     void** h_pinned = nullptr;
+    // per matrix: W prefetch map (kEpiApply) and its validity, host staging and device copy
+    CUtensorMap* h_wpf = nullptr;        // pinned: n maps, then n validity bytes
+    CUtensorMap* d_wpf = nullptr;
+    unsigned char* d_wpf_ok = nullptr;
     std::vector<void*> h_cache;
     cudaEvent_t upload_ev = nullptr;
     bool uploaded = false;
@@ -308,6 +326,17 @@ muon_status upload_pointers(muon_plan_s* p, float* const* params, const void* co
     }
     std::memcpy(p->h_pinned, p->h_cache.data(), 3 * n * sizeof(void*));
     MUON_TRY(cudaMemcpyAsync(p->d_ptrs, p->h_pinned, 3 * n * sizeof(void*), cudaMemcpyHostToDevice, s));
+    // W prefetch maps follow the parameter pointers (matrices on the batched products only)
+    unsigned char* ok = reinterpret_cast<unsigned char*>(p->h_wpf + n);
+    for (size_t i = 0; i < n; ++i) {
+        const MatDev& md = p->mats[i];
+        const bool batched = p->buckets[p->mat_bucket[i]].batched();
+        const bool usable = batched && md.m >= 128 && md.n >= 128 && md.n % 4 == 0 &&
+                            (reinterpret_cast<uintptr_t>(params[i]) & 15) == 0;
+        ok[i] = usable && make_w_prefetch_map(&p->h_wpf[i], params[i], (uint64_t)md.m, (uint64_t)md.n) ? 1 : 0;
+    }
+    MUON_TRY(cudaMemcpyAsync(p->d_wpf, p->h_wpf, n * sizeof(CUtensorMap), cudaMemcpyHostToDevice, s));
+    MUON_TRY(cudaMemcpyAsync(p->d_wpf_ok, ok, n, cudaMemcpyHostToDevice, s));
     MUON_TRY(cudaEventRecord(p->upload_ev, s));
     p->uploaded = true;
     return MUON_OK;
@@ -481,6 +510,7 @@ void free_plan(muon_plan_s* p) {
     if (!p) return;
     if (p->ws) cudaFree(p->ws);
     if (p->h_pinned) cudaFreeHost(p->h_pinned);
+    if (p->h_wpf) cudaFreeHost(p->h_wpf);
     if (p->upload_ev) cudaEventDestroy(p->upload_ev);
     if (p->fork_ev) cudaEventDestroy(p->fork_ev);
     if (p->join_ev) cudaEventDestroy(p->join_ev);
@@ -503,7 +533,7 @@ void free_plan(muon_plan_s* p) {
 struct Layout {
     bool restarts = false;   // opts.max_ns_steps > 0: second X buffer, every matrix batched
     size_t o_mats = 0, o_part = 0, o_cpart = 0, o_inv = 0, o_alpha = 0, o_status = 0, o_tr = 0, o_ptrs = 0,
-           o_items = 0, o_ones = 0, o_odbg = 0, o_lists = 0, o_prefix = 0, o_region = 0;
+           o_items = 0, o_ones = 0, o_wpf = 0, o_wpf_ok = 0, o_odbg = 0, o_lists = 0, o_prefix = 0, o_region = 0;
     std::vector<size_t> o_ut, o_ut1, o_rr, o_qb;   // per bucket: X0, second X, r x r, bf16 Q (in the region)
     std::vector<int> rnr_list, rnc_list;           // RowNorm: row-wise and column-wise matrices
 };
@@ -617,17 +647,20 @@ muon_status plan_layout(muon_plan_s* p, Layout& L) {
     L.o_ptrs = take(sizeof(void*) * 3 * n);
     L.o_items = take(sizeof(int) * n);   // item -> plan matrix, per bucket slice
     L.o_ones = take(sizeof(float) * n);
+    L.o_wpf = take(sizeof(CUtensorMap) * n);   // W prefetch maps (64-byte aligned: slices are 256-aligned)
+    L.o_wpf_ok = take((size_t)n);
     L.o_odbg = p->opts.keep_update ? take([&] {
         size_t t = 0;
         for (int i = 0; i < n; ++i) t += (size_t)round_up(p->mats[i].m * p->mats[i].n * 4, 256);
         return t;
     }()) : 0;
-    // launch lists: per chunk the momentum rows / tiles / all lists and its four
-    // RowNorm lists, and the four RowNorm lists of the whole plan.  Chunks partition
-    // the matrices (n chunks at most); a list of k matrices takes max(k, 1) ints and
-    // k + 1 prefixes.  Momentum lists: 2 per matrix plus 3 per chunk, at most 5n; chunk
-    // RowNorm lists (rows once, column matrices three times): at most 3n + 4n; the
-    // plan's: 3n + 4.  15n + 4 <= 17n + 16 of each.
+    // launch lists: per chunk the momentum rows / tiles / all lists and its six
+    // RowNorm lists (rows in three length classes, column statistics, finalize,
+    // apply), and the six RowNorm lists of the whole plan.  Chunks partition the
+    // matrices (n chunks at most); a list of k matrices takes max(k, 1) ints and k + 1
+    // prefixes.  Momentum lists: 2 per matrix plus 3 per chunk, at most 5n; chunk
+    // RowNorm lists (rows once, column matrices three times): at most 3n + 6n; the
+    // plan's: 3n + 6.  17n + 6 <= 17n + 16 of each.
     L.o_lists = take(sizeof(int) * (size_t)(17 * n + 16));
     L.o_prefix = take(sizeof(long long) * (size_t)(17 * n + 16));
     const size_t fixed_bytes = off;
@@ -801,6 +834,8 @@ static muon_status plan_build(muon_plan_s* p, const muon_shape* shapes, int32_t 
     p->d_transposed = reinterpret_cast<unsigned char*>(base + L.o_tr);
     p->d_ptrs = reinterpret_cast<void**>(base + L.o_ptrs);
     p->ones = reinterpret_cast<float*>(base + L.o_ones);
+    p->d_wpf = reinterpret_cast<CUtensorMap*>(base + L.o_wpf);
+    p->d_wpf_ok = reinterpret_cast<unsigned char*>(base + L.o_wpf_ok);
 
     std::vector<unsigned char> tr(n);
     for (int i = 0; i < n; ++i) tr[i] = (unsigned char)p->mats[i].transposed;
@@ -850,12 +885,22 @@ static muon_status plan_build(muon_plan_s* p, const muon_shape* shapes, int32_t 
         upload_list(rows, ch.mom_rows, 0);
         upload_list(tiles, ch.mom_tiles, 1);
         upload_list(all, ch.all, 2);
-        upload_list(rows, ch.rn_rows, 3);
+        for (int cl = 0; cl < kRowClasses; ++cl) {
+            std::vector<int> rc;
+            for (int i : rows)
+                if (rownorm_row_class(p->mats[i].n) == cl) rc.push_back(i);
+            upload_list(rc, ch.rn_rows[cl], 3);
+        }
         upload_list(tiles, ch.rn_stats, 4);
         upload_list(tiles, ch.rn_final, 5);
         upload_list(tiles, ch.rn_apply, 6);
     }
-    upload_list(L.rnr_list, p->rn_rows, 3);
+    for (int cl = 0; cl < kRowClasses; ++cl) {
+        std::vector<int> rc;
+        for (int i : L.rnr_list)
+            if (rownorm_row_class(p->mats[i].n) == cl) rc.push_back(i);
+        upload_list(rc, p->rn_rows[cl], 3);
+    }
     upload_list(L.rnc_list, p->rn_stats, 4);
     upload_list(L.rnc_list, p->rn_final, 5);
     upload_list(L.rnc_list, p->rn_apply, 6);
@@ -937,6 +982,8 @@ static muon_status plan_build(muon_plan_s* p, const muon_shape* shapes, int32_t 
         }
     }
     ok = ok && cudaMallocHost(&p->h_pinned, sizeof(void*) * 3 * n) == cudaSuccess;
+    ok = ok && cudaMallocHost(&p->h_wpf, (sizeof(CUtensorMap) + 1) * n) == cudaSuccess;
+    ok = ok && cudaMemset(p->d_wpf_ok, 0, n) == cudaSuccess;
     ok = ok && cudaEventCreateWithFlags(&p->upload_ev, cudaEventDisableTiming) == cudaSuccess;
     ok = ok && gemm_prepare(p->device) == cudaSuccess;
     ok = ok && ns_f32_prepare() == cudaSuccess;
@@ -1078,12 +1125,15 @@ void muon_plan_destroy(muon_plan p) {
 
 // The RowNorm kernels over one set of lists (m <= n rows; m > n column statistics,
 // finalize, apply).
-static muon_status rownorm_launch(muon_plan_s* p, const ListDev& rows, const ListDev& stats,
+static muon_status rownorm_launch(muon_plan_s* p, const ListDev* rows, const ListDev& stats,
                                   const ListDev& fin, const ListDev& apply, float lr, float wd, float mu, float eps,
                                   cudaStream_t s, int* launches) {
-    ElemArgs a = elem_args(p, rows, mu, lr, wd, eps);
-    MUON_TRY(launch_rownorm_rows(a, rows.blocks, s));
-    *launches += rows.blocks > 0;
+    ElemArgs a{};
+    for (int cl = 0; cl < kRowClasses; ++cl) {
+        a = elem_args(p, rows[cl], mu, lr, wd, eps);
+        MUON_TRY(launch_rownorm_rows(a, rows[cl].blocks, rownorm_class_vec(cl), s));
+        *launches += rows[cl].blocks > 0;
+    }
     a = elem_args(p, stats, mu, lr, wd, eps);
     a.partials = p->cpartials;
     MUON_TRY(launch_rownorm_colstats(a, stats.blocks, s));
@@ -1454,6 +1504,8 @@ static muon_status ns_step(muon_plan p, float* const* params, const void* const*
                     if (last) {
                         q.item_mat = b.d_item_mat;
                         q.W = W;
+                        q.wpf = p->d_wpf;
+                        q.wpf_ok = p->d_wpf_ok;
                         q.transposed = p->d_transposed;
                         q.Odbg = b.Odbg;
                         q.lr = lr;

@@ -272,9 +272,10 @@ __global__ void k_identity_bf16(__nv_bfloat16* q, int r, int ld, long long total
 }
 
 // ------------------------------------------------------------------ RowNorm, m <= n (stored rows)
-constexpr int kRowMaxVec = 8;    // float4 groups per thread kept in registers (rows <= 8192)
-
-template <bool BF16>
+// VEC float4 groups per thread kept in registers (rows <= 1024 VEC elements).  The
+// planner launches rows of up to 2048, 4096 and more elements with VEC = 2, 4 and 8,
+// so short rows do not hold the registers (and the occupancy) of the longest.
+template <bool BF16, int VEC>
 __global__ void __launch_bounds__(kElemThreads) k_rownorm_rows(const ElemArgs a) {
     pdl_trigger();
     pdl_wait();
@@ -291,20 +292,20 @@ __global__ void __launch_bounds__(kElemThreads) k_rownorm_rows(const ElemArgs a)
     float* W = a.W[mi] + base;
     const float mu = a.mu, lr = a.lr, wd = a.wd, s = md.scale;
     const int t = threadIdx.x;
-    const bool reg = (n % 4 == 0) && (n <= 4LL * kElemThreads * kRowMaxVec) && g_vec_ok<BF16>(G) &&
+    const bool reg = (n % 4 == 0) && (n <= 4LL * kElemThreads * VEC) && g_vec_ok<BF16>(G) &&
                      aligned16(M) && aligned16(W);
     float ss = 0.f;
     if (reg) {
         // W is loaded with G and M, so all three streams are in flight across the
         // row reduction
-        float4 u[kRowMaxVec], wv[kRowMaxVec];
+        float4 u[VEC], wv[VEC];
 #pragma unroll
-        for (int v = 0; v < kRowMaxVec; ++v) {
+        for (int v = 0; v < VEC; ++v) {
             const long long j = 4LL * (v * kElemThreads + t);
             if (j < n) wv[v] = *reinterpret_cast<const float4*>(W + j);
         }
 #pragma unroll
-        for (int v = 0; v < kRowMaxVec; ++v) {
+        for (int v = 0; v < VEC; ++v) {
             const long long j = 4LL * (v * kElemThreads + t);
             if (j < n) {
                 const float4 g = load_g4<BF16>(G, base + j);
@@ -320,7 +321,7 @@ __global__ void __launch_bounds__(kElemThreads) k_rownorm_rows(const ElemArgs a)
         const float inv = 1.f / fmaxf(sqrtf(tot), a.eps);
         const float k = s * inv;
 #pragma unroll
-        for (int v = 0; v < kRowMaxVec; ++v) {
+        for (int v = 0; v < VEC; ++v) {
             const long long j = 4LL * (v * kElemThreads + t);
             if (j < n) {
                 float4 w = wv[v];
@@ -506,12 +507,17 @@ cudaError_t launch_identity_bf16(__nv_bfloat16* q, int r, int ld, int batch, boo
     return launch_pdl(k_identity_bf16, dim3((unsigned)((total + 255) / 256)), dim3(256), 0, s, q, r, ld, total,
                       split ? 1 : 0);
 }
-cudaError_t launch_rownorm_rows(const ElemArgs& a, long long blocks, cudaStream_t s) {
+cudaError_t launch_rownorm_rows(const ElemArgs& a, long long blocks, int vec, cudaStream_t s) {
     if (blocks <= 0) return cudaSuccess;
-    if (a.grad_bf16)
-        return launch_pdl(k_rownorm_rows<true>, dim3((unsigned)blocks), dim3(kElemThreads), 0, s, a);
-    else
-        return launch_pdl(k_rownorm_rows<false>, dim3((unsigned)blocks), dim3(kElemThreads), 0, s, a);
+    const dim3 g((unsigned)blocks), b(kElemThreads);
+    if (vec <= 2)
+        return a.grad_bf16 ? launch_pdl(k_rownorm_rows<true, 2>, g, b, 0, s, a)
+                           : launch_pdl(k_rownorm_rows<false, 2>, g, b, 0, s, a);
+    if (vec <= 4)
+        return a.grad_bf16 ? launch_pdl(k_rownorm_rows<true, 4>, g, b, 0, s, a)
+                           : launch_pdl(k_rownorm_rows<false, 4>, g, b, 0, s, a);
+    return a.grad_bf16 ? launch_pdl(k_rownorm_rows<true, 8>, g, b, 0, s, a)
+                       : launch_pdl(k_rownorm_rows<false, 8>, g, b, 0, s, a);
 }
 cudaError_t launch_rownorm_colstats(const ElemArgs& a, long long blocks, cudaStream_t s) {
     if (blocks <= 0) return cudaSuccess;

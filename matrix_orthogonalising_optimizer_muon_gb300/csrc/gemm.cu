@@ -302,6 +302,37 @@ __device__ __forceinline__ bool upper_block(bool sym, int k0, int row0) {
     return sym && k0 >= (row0 & ~255) + 256;
 }
 
+// L2 prefetch of what the epilogue of this CTA's part of a tile (rows m0 .. m0 + 127,
+// columns n0 .. n0 + 255) reads, issued by the producer when the tile's loads start
+// (a handful of tensor prefetches, not one bulk prefetch per row): the polynomial's G'
+// (its A operand, 64-column boxes of 128 rows) and the final product's W (two 128 x 128
+// boxes of the stored layout, when the matrix has a W prefetch map).
+template <bool LOWER>
+__device__ __forceinline__ void tile_prefetch(const GemmLaunch& L, const GemmProblem& P, const TileCoord& tc) {
+    if (tc.m0 >= P.M) return;
+    if (P.epi == kEpiPoly) {
+        for (int q = 0; q < 4 && tc.n0 + 64 * q < P.N; ++q) {
+            if constexpr (LOWER) {
+                tma_prefetch_4d(&L.mapA[tc.p], 0, tc.m0, (tc.n0 >> 6) + q, tc.item);
+            } else {
+                const int za = P.a_split ? 2 * tc.item : tc.item;
+                tma_prefetch_3d(&L.mapA[tc.p], tc.n0 + 64 * q, tc.m0, za);
+                if (P.a_split) tma_prefetch_3d(&L.mapA[tc.p], tc.n0 + 64 * q, tc.m0, za + 1);
+            }
+        }
+    } else if (P.epi == kEpiApply && P.wpf) {
+        const int mat = P.item_mat[tc.item];
+        if (!P.wpf_ok[mat]) return;
+        const bool tr = P.transposed[mat] != 0;
+        for (int h = 0; h < 2 && tc.n0 + 128 * h < P.N; ++h) {
+            if (tr)
+                tma_prefetch_2d(&P.wpf[mat], tc.m0, tc.n0 + 128 * h);
+            else
+                tma_prefetch_2d(&P.wpf[mat], tc.n0 + 128 * h, tc.m0);
+        }
+    }
+}
+
 // LOWER = false: operands through 3-D maps, symmetric outputs stored whole.
 // LOWER = true: every operand through a 4-D map of 64-column chunks, one box per
 // operand per stage whichever way it is read (the map and the coordinates are
@@ -374,6 +405,7 @@ __global__ void __maxnreg__(168) gemm2_kernel(const __grid_constant__ GemmLaunch
                 const GemmProblem& P = L.prob[tc.p];
                 const int nkb = (P.K + Cfg::BK - 1) / Cfg::BK;
                 const int kblocks = LOWER ? nkb : nkb * split_passes(P);
+                tile_prefetch<LOWER>(L, P, tc);
                 // lower-triangle launches: the problem's fields and maps read once per tile
                 const bool sym_a = P.sym_a != 0, sym_b = P.sym_b != 0, bmn = P.b_mn != 0;
                 const CUtensorMap* mA = &L.mapA[tc.p];
@@ -491,7 +523,8 @@ __global__ void __maxnreg__(168) gemm2_kernel(const __grid_constant__ GemmLaunch
             const GemmProblem& P = L.prob[tc.p];
             const uint32_t acc = local & 1;
             const uint32_t aph = (local >> 1) & 1u;
-            if (P.epi == kEpiApply || P.epi == kEpiPoly)
+            // (tiles whose inputs have tensor maps are prefetched by the producer, tile_prefetch)
+            if (P.epi == kEpiApply && !(P.wpf && P.wpf_ok[P.item_mat[tc.item]]))
                 prefetch_epilogue_inputs(P, tc.item, tc.m0 + wq * 32, tc.n0 + c_begin, kBN * 4 / kEpiWarps, lane);
             if (!mbar_wait_idle(tfull + acc, aph, abort_flag, L.status, kStatusTimeoutEpilogue, true)) break;
             tc_fence_after();

@@ -129,6 +129,11 @@ struct GemmProblem {
     // out_split: the output (C, C2, Cb) is written as hi = round(v), lo = round(v - hi).
     // kEpiPoly reads its G' input split when a_split is set.  Per-thread stores only.
     int a_split, b_split, out_split;
+    // kEpiApply: per plan matrix, a tensor map of W (fp32, stored layout, 128 x 128 boxes)
+    // for the L2 prefetch of the tile's W while its MMAs run, and whether it is valid
+    // (W 16-byte aligned, stored row length a multiple of 4, both dimensions >= 128)
+    const CUtensorMap* wpf;
+    const unsigned char* wpf_ok;
 };
 constexpr int kTmaOutC = 1, kTmaOutC2 = 2, kTmaOutBf16 = 4;
 
@@ -230,8 +235,12 @@ cudaError_t launch_norm_finalize(const ElemArgs& a, cudaStream_t s);
 // Fill a batch of r x r bf16 identities (ns_steps = 0).
 // split: q holds 2 x batch items (hi, lo per matrix); the lo parts are filled with zeros.
 cudaError_t launch_identity_bf16(__nv_bfloat16* q, int r, int ld, int batch, bool split, cudaStream_t s);
-// RowNorm: rows of the stored matrix (m <= n), one block per row, fused apply.
-cudaError_t launch_rownorm_rows(const ElemArgs& a, long long blocks, cudaStream_t s);
+// RowNorm: rows of the stored matrix (m <= n), one block per row, fused apply; rows of
+// up to 1024 vec elements in registers (vec 2, 4 or 8), longer ones in two passes.
+constexpr int kRowClasses = 3;   // launch classes by row length: <= 2048, <= 4096, longer
+inline int rownorm_row_class(long long n) { return n <= 2048 ? 0 : (n <= 4096 ? 1 : 2); }
+inline int rownorm_class_vec(int cls) { return 2 << cls; }
+cudaError_t launch_rownorm_rows(const ElemArgs& a, long long blocks, int vec, cudaStream_t s);
 // RowNorm, m > n: column statistics, finalize, apply.
 cudaError_t launch_rownorm_colstats(const ElemArgs& a, long long blocks, cudaStream_t s);
 cudaError_t launch_rownorm_colfinal(const ElemArgs& a, long long blocks, cudaStream_t s);
