@@ -138,6 +138,16 @@ typedef struct {
     int32_t precision;
     /* Largest min(m, n) that precision 0 splits (0: 1024). */
     int32_t split_max_r;
+    /* NULL, or a host array of n row counts (read during muon_plan_create only) that
+       makes the plan a RowNorm plan over dim-0 shards: matrix i is a block of rows of a
+       full matrix of full_rows[i] >= rows rows and the same columns ("Scaling Muon for
+       Diffusion Transformers" sec. 1 and 2.3: RowNorm steps on dim-0-sharded momentum).
+       Orientation and the update scale follow the full shape: when full_rows[i] > cols
+       the RowNorm rows are stored columns spanning every shard, and their squared norms
+       are summed across shards between muon_rownorm_shard_stats and
+       muon_rownorm_shard_apply; otherwise each stored row is complete in the shard.
+       Such a plan runs only those two calls (the others return MUON_ERR_UNSUPPORTED). */
+    const int64_t* full_rows;
 } muon_plan_opts;
 
 typedef struct muon_plan_s* muon_plan;
@@ -279,6 +289,31 @@ muon_status muon_rownorm_step(muon_plan p, float* const* params, const void* con
                               float eps, void* stream);
 
 /*
+ * muon_rownorm_shard_stats / muon_rownorm_shard_apply - one RowNorm step of a plan
+ * created with opts.full_rows (dim-0 shards; "Scaling Muon for Diffusion Transformers"
+ * sec. 1 and 2.3: on RowNorm steps only the norm statistics of rows that span ranks are
+ * all-reduced).
+ *   stats: M <- mu M + G for every matrix; matrices whose RowNorm rows are complete in
+ *     the shard (full_rows <= cols) are also normalised and applied (W updated); for the
+ *     others, writes this shard's per-column sums of U^2 (U = mu M + G) into colsq.
+ *   colsq: device buffer of muon_plan_info's colsq_len floats, caller-owned; matrix by
+ *     matrix in plan order, each padded to a multiple of 4 floats (padding written as 0).
+ *     Between the two calls the caller sums colsq element-wise over all shards of the
+ *     same matrices (for example an all-reduce across ranks, in place).
+ *   apply: W <- W - lr (0.2 sqrt(max(full_rows, cols)) U / max(sqrt(colsq), eps) + wd W)
+ *     for the spanning matrices, with U recomputed from G and the new M.  params, grads
+ *     and momentum must be those of the stats call, unchanged in between.
+ * Arguments and errors as muon_rownorm_step; MUON_ERR_UNSUPPORTED on a plan without
+ * opts.full_rows.  With opts.check_finite, apply checks the summed squared norms.
+ */
+muon_status muon_rownorm_shard_stats(muon_plan p, float* const* params, const void* const* grads,
+                                     float* const* momentum, float lr, float wd, float mu, float eps, float* colsq,
+                                     void* stream);
+muon_status muon_rownorm_shard_apply(muon_plan p, float* const* params, const void* const* grads,
+                                     float* const* momentum, float lr, float wd, float mu, float eps,
+                                     const float* colsq, void* stream);
+
+/*
  * muon_plan_tune - a profiled planner (DMuon's per-shape autotuning, on one GPU): times
  * the plan's launch choices that change only speed on the caller's buffers and keeps
  * the fastest.  Candidates: for chunks holding both fused (min(m, n) <= 128) and
@@ -385,6 +420,7 @@ typedef struct {
     int32_t chain_clusters;       /* CTA pairs the batched products get beside the fused kernel (0: none) */
     int32_t split_buckets;        /* batched buckets in split precision (opts.precision) */
     int32_t fp32_buckets;         /* buckets on the fp32 kernel (opts.small_fp32) */
+    int64_t colsq_len;            /* floats of the colsq buffer of the shard calls (0 without opts.full_rows) */
 } muon_plan_info_t;
 
 muon_status muon_plan_info(muon_plan p, muon_plan_info_t* info);

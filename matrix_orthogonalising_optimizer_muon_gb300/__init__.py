@@ -23,7 +23,7 @@ import os
 from .build import LIB, build, up_to_date
 
 __all__ = [
-    "MuonError", "MuonPlan", "PeriodicRowNormMuon", "DistributedMuon", "partition_owners",
+    "MuonError", "MuonPlan", "PeriodicRowNormMuon", "DistributedMuon", "ShardedRowNorm", "partition_owners",
     "plan_workspace_size", "load", "build",
     "MUON_OK", "MUON_ERR_INVALID_ARG", "MUON_ERR_UNSUPPORTED", "MUON_ERR_OOM",
     "MUON_ERR_CUDA", "MUON_ERR_TIMEOUT", "MUON_ERR_NONFINITE", "MUON_F32", "MUON_BF16",
@@ -50,7 +50,8 @@ class MuonPlanOpts(ctypes.Structure):
                 ("chain_clusters", ctypes.c_int32), ("max_ns_steps", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64), ("chunks", ctypes.c_int32),
                 ("full_symmetric", ctypes.c_int32), ("small_fp32", ctypes.c_int32),
-                ("check_finite", ctypes.c_int32), ("precision", ctypes.c_int32), ("split_max_r", ctypes.c_int32)]
+                ("check_finite", ctypes.c_int32), ("precision", ctypes.c_int32), ("split_max_r", ctypes.c_int32),
+                ("full_rows", ctypes.POINTER(ctypes.c_int64))]
 
 
 class MuonPlanInfo(ctypes.Structure):
@@ -58,7 +59,7 @@ class MuonPlanInfo(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_int64), ("launches_last_step", ctypes.c_int32),
                 ("sm_count", ctypes.c_int32), ("n_chunks", ctypes.c_int32), ("lower_chunks", ctypes.c_int32),
                 ("tuned_candidates", ctypes.c_int32), ("chain_clusters", ctypes.c_int32),
-                ("split_buckets", ctypes.c_int32), ("fp32_buckets", ctypes.c_int32)]
+                ("split_buckets", ctypes.c_int32), ("fp32_buckets", ctypes.c_int32), ("colsq_len", ctypes.c_int64)]
 
 
 _P = ctypes.c_void_p
@@ -91,6 +92,10 @@ EXPORTED = {
     "muon_plan_info": (ctypes.c_int, [_P, ctypes.POINTER(MuonPlanInfo)]),
     "muon_stage_times": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_float),
                                         ctypes.POINTER(ctypes.c_double), ctypes.c_int32]),
+    "muon_rownorm_shard_stats": (ctypes.c_int, [_P, _PP, _PP, _PP, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                                ctypes.c_float, _P, _P]),
+    "muon_rownorm_shard_apply": (ctypes.c_int, [_P, _PP, _PP, _PP, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                                ctypes.c_float, _P, _P]),
     "muon_partition": (ctypes.c_int, [ctypes.POINTER(MuonShape), ctypes.c_int32, ctypes.c_int32,
                                       ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int32),
                                       ctypes.POINTER(ctypes.c_double)]),
@@ -153,14 +158,23 @@ def _ptr_array(ptrs):
 
 def _plan_args(shapes, grad_dtype, keep_update=False, timing=False, single_sm_gemm=False,
                generic_small=False, chain_clusters=0, workspace_bytes=0, max_ns_steps=0, chunks=0,
-               full_symmetric=False, small_fp32=0, check_finite=False, precision=0, split_max_r=0):
-    """(shape list, MuonShape array, dtype code, MuonPlanOpts) of a plan's arguments."""
+               full_symmetric=False, small_fp32=0, check_finite=False, precision=0, split_max_r=0,
+               full_rows=None):
+    """(shape list, MuonShape array, dtype code, MuonPlanOpts) of a plan's arguments.  The
+    options keep a reference to the full_rows array (read by the library during creation)."""
     shapes = [(int(m), int(n)) for m, n in shapes]
     arr = (MuonShape * len(shapes))(*[MuonShape(m, n) for m, n in shapes])
+    fr = None
+    if full_rows is not None:
+        if len(full_rows) != len(shapes):
+            raise ValueError("full_rows needs one entry per matrix")
+        fr = (ctypes.c_int64 * len(shapes))(*[int(x) for x in full_rows])
     opts = MuonPlanOpts(1 if keep_update else 0, 1 if timing else 0, 1 if single_sm_gemm else 0,
                         1 if generic_small else 0, int(chain_clusters), int(max_ns_steps),
                         int(workspace_bytes), int(chunks), 1 if full_symmetric else 0, int(small_fp32),
-                        1 if check_finite else 0, int(precision), int(split_max_r))
+                        1 if check_finite else 0, int(precision), int(split_max_r),
+                        ctypes.cast(fr, ctypes.POINTER(ctypes.c_int64)) if fr is not None else None)
+    opts._full_rows_ref = fr
     return shapes, arr, {"bf16": MUON_BF16, "f32": MUON_F32}[grad_dtype], opts
 
 
@@ -187,12 +201,12 @@ class MuonPlan:
                  timing: bool = False, single_sm_gemm: bool = False, generic_small: bool = False,
                  chain_clusters: int = 0, workspace_bytes: int = 0, max_ns_steps: int = 0, chunks: int = 0,
                  full_symmetric: bool = False, small_fp32: int = 0, check_finite: bool = False,
-                 precision: int = 0, split_max_r: int = 0):
+                 precision: int = 0, split_max_r: int = 0, full_rows=None):
         self.lib = load()
         self.shapes, arr, gd, opts = _plan_args(shapes, grad_dtype, keep_update, timing, single_sm_gemm,
                                                 generic_small, chain_clusters, workspace_bytes, max_ns_steps,
                                                 chunks, full_symmetric, small_fp32, check_finite, precision,
-                                                split_max_r)
+                                                split_max_r, full_rows)
         self.grad_dtype = grad_dtype
         h = ctypes.c_void_p()
         _check(self.lib.muon_plan_create(arr, len(self.shapes), gd, ctypes.byref(opts),
@@ -289,6 +303,24 @@ class MuonPlan:
         w, g, m = self._pointers(params, grads, momentum)
         _check(self.lib.muon_rownorm_step(self.handle, w, g, m, lr, wd, mu, eps,
                                           _stream_handle(stream)), "muon_rownorm_step")
+
+    def rownorm_shard_stats(self, params, grads, momentum, lr: float, wd: float, colsq, mu: float = DEFAULT_MU,
+                            eps: float = 1e-8, stream=None):
+        """``muon_rownorm_shard_stats`` on a plan created with ``full_rows``: colsq (a CUDA fp32
+        tensor of ``info()['colsq_len']`` elements) receives this shard's column sums of U^2."""
+        w, g, m = self._pointers(params, grads, momentum)
+        _check(self.lib.muon_rownorm_shard_stats(self.handle, w, g, m, lr, wd, mu, eps,
+                                                 ctypes.c_void_p(colsq.data_ptr()), _stream_handle(stream)),
+               "muon_rownorm_shard_stats")
+
+    def rownorm_shard_apply(self, params, grads, momentum, lr: float, wd: float, colsq, mu: float = DEFAULT_MU,
+                            eps: float = 1e-8, stream=None):
+        """``muon_rownorm_shard_apply``: the update of the spanning matrices from colsq summed
+        over every shard."""
+        w, g, m = self._pointers(params, grads, momentum)
+        _check(self.lib.muon_rownorm_shard_apply(self.handle, w, g, m, lr, wd, mu, eps,
+                                                 ctypes.c_void_p(colsq.data_ptr()), _stream_handle(stream)),
+               "muon_rownorm_shard_apply")
 
     def bind(self, params, grads, momentum):
         """Validate the tensors once and keep their pointer arrays for ``step_bound``.
@@ -534,5 +566,55 @@ class DistributedMuon:
 
     def close(self):
         if self.plan is not None:
+            self.plan.close()
+            self.plan = None
+
+
+class ShardedRowNorm:
+    """RowNorm steps over dim-0 shards across the ranks of a torch.distributed group
+    ("Scaling Muon for Diffusion Transformers" sec. 1 and 2.3: on RowNorm steps each rank
+    keeps its block of rows of every W, G and M; only the squared norms of the RowNorm
+    rows that span ranks are all-reduced).
+
+    ``shard_shapes[i]`` is this rank's block of rows of matrix i, whose full shape is
+    ``(full_rows[i], shard_shapes[i][1])``.  Matrices with full_rows <= cols have their
+    RowNorm rows complete in each shard; the others (the stored columns are the RowNorm
+    rows) need one sum of their per-column U^2 across ranks: one all-reduce of a single
+    fp32 buffer per step, between the library's two shard calls."""
+
+    def __init__(self, shard_shapes, full_rows, grad_dtype: str = "bf16", group=None, **plan_opts):
+        import torch
+        self.group = group
+        self.plan = self._make_plan(shard_shapes, full_rows, grad_dtype, plan_opts)
+        n = self._colsq_len()
+        self.colsq = torch.zeros(max(n, 1), dtype=torch.float32, device=self._device())
+
+    def _make_plan(self, shard_shapes, full_rows, grad_dtype, plan_opts):
+        return MuonPlan(shard_shapes, grad_dtype, full_rows=full_rows, **plan_opts)
+
+    def _colsq_len(self) -> int:
+        return self.plan.info()["colsq_len"]
+
+    def _device(self):
+        return "cuda"
+
+    def _stats(self, params, grads, momentum, lr, wd, mu, eps, stream):
+        self.plan.rownorm_shard_stats(params, grads, momentum, lr, wd, self.colsq, mu, eps, stream)
+
+    def _apply(self, params, grads, momentum, lr, wd, mu, eps, stream):
+        self.plan.rownorm_shard_apply(params, grads, momentum, lr, wd, self.colsq, mu, eps, stream)
+
+    def step(self, params, grads, momentum, lr: float, wd: float, mu: float = DEFAULT_MU, eps: float = 1e-8,
+             stream=None):
+        """One RowNorm step of this rank's shards: statistics, their sum over the ranks,
+        the update."""
+        import torch.distributed as dist
+        self._stats(params, grads, momentum, lr, wd, mu, eps, stream)
+        if dist.is_available() and dist.is_initialized() and dist.get_world_size(self.group) > 1:
+            dist.all_reduce(self.colsq, op=dist.ReduceOp.SUM, group=self.group)
+        self._apply(params, grads, momentum, lr, wd, mu, eps, stream)
+
+    def close(self):
+        if getattr(self, "plan", None) is not None and hasattr(self.plan, "close"):
             self.plan.close()
             self.plan = None

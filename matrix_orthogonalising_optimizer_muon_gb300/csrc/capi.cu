@@ -89,20 +89,6 @@ bool make_map4(CUtensorMap* map, void* base, bool bf16, uint64_t cols, uint64_t 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// W of one matrix (fp32, stored m x n row-major, 16-byte aligned, n % 4 == 0), 128 x 128
-// boxes without swizzle: the final product's L2 prefetch of a tile's W.
-bool make_w_prefetch_map(CUtensorMap* map, void* W, uint64_t m, uint64_t n) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {n, m};
-    cuuint64_t strides[1] = {n * 4};
-    cuuint32_t box[2] = {128, 128};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, W, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
-}
-
 // Store map over `batch` r x r row-major matrices (leading dim ld): 32 x 32 boxes
 // in the 64-byte-swizzled shared layout the pair kernel's epilogue stages.
 bool make_out_map(CUtensorMap* map, void* base, bool bf16, uint64_t r, uint64_t batch, uint64_t ld) {
@@ -190,6 +176,8 @@ struct muon_plan_s {
     muon_dtype gdt = MUON_F32;
     muon_plan_opts opts{};
     std::vector<muon_shape> shapes;
+    std::vector<int64_t> full_rows;   // opts.full_rows copied (dim-0 shard plans), else empty
+    long long colsq_len = 0;          // floats of the shard calls' colsq buffer
     std::vector<MatDev> mats;
     std::vector<int> mat_bucket, mat_item;
     std::vector<Bucket> buckets;
@@ -222,10 +210,6 @@ struct muon_plan_s {
     std::vector<Chunk> chunks;
 
     void** h_pinned = nullptr;
-    // per matrix: W prefetch map (kEpiApply) and its validity, host staging and device copy
-    CUtensorMap* h_wpf = nullptr;        // pinned: n maps, then n validity bytes
-    CUtensorMap* d_wpf = nullptr;
-    unsigned char* d_wpf_ok = nullptr;
     std::vector<void*> h_cache;
     cudaEvent_t upload_ev = nullptr;
     bool uploaded = false;
@@ -326,17 +310,6 @@ muon_status upload_pointers(muon_plan_s* p, float* const* params, const void* co
     }
     std::memcpy(p->h_pinned, p->h_cache.data(), 3 * n * sizeof(void*));
     MUON_TRY(cudaMemcpyAsync(p->d_ptrs, p->h_pinned, 3 * n * sizeof(void*), cudaMemcpyHostToDevice, s));
-    // W prefetch maps follow the parameter pointers (matrices on the batched products only)
-    unsigned char* ok = reinterpret_cast<unsigned char*>(p->h_wpf + n);
-    for (size_t i = 0; i < n; ++i) {
-        const MatDev& md = p->mats[i];
-        const bool batched = p->buckets[p->mat_bucket[i]].batched();
-        const bool usable = batched && md.m >= 128 && md.n >= 128 && md.n % 4 == 0 &&
-                            (reinterpret_cast<uintptr_t>(params[i]) & 15) == 0;
-        ok[i] = usable && make_w_prefetch_map(&p->h_wpf[i], params[i], (uint64_t)md.m, (uint64_t)md.n) ? 1 : 0;
-    }
-    MUON_TRY(cudaMemcpyAsync(p->d_wpf, p->h_wpf, n * sizeof(CUtensorMap), cudaMemcpyHostToDevice, s));
-    MUON_TRY(cudaMemcpyAsync(p->d_wpf_ok, ok, n, cudaMemcpyHostToDevice, s));
     MUON_TRY(cudaEventRecord(p->upload_ev, s));
     p->uploaded = true;
     return MUON_OK;
@@ -510,7 +483,6 @@ void free_plan(muon_plan_s* p) {
     if (!p) return;
     if (p->ws) cudaFree(p->ws);
     if (p->h_pinned) cudaFreeHost(p->h_pinned);
-    if (p->h_wpf) cudaFreeHost(p->h_wpf);
     if (p->upload_ev) cudaEventDestroy(p->upload_ev);
     if (p->fork_ev) cudaEventDestroy(p->fork_ev);
     if (p->join_ev) cudaEventDestroy(p->join_ev);
@@ -533,7 +505,7 @@ void free_plan(muon_plan_s* p) {
 struct Layout {
     bool restarts = false;   // opts.max_ns_steps > 0: second X buffer, every matrix batched
     size_t o_mats = 0, o_part = 0, o_cpart = 0, o_inv = 0, o_alpha = 0, o_status = 0, o_tr = 0, o_ptrs = 0,
-           o_items = 0, o_ones = 0, o_wpf = 0, o_wpf_ok = 0, o_odbg = 0, o_lists = 0, o_prefix = 0, o_region = 0;
+           o_items = 0, o_ones = 0, o_odbg = 0, o_lists = 0, o_prefix = 0, o_region = 0;
     std::vector<size_t> o_ut, o_ut1, o_rr, o_qb;   // per bucket: X0, second X, r x r, bf16 Q (in the region)
     std::vector<int> rnr_list, rnc_list;           // RowNorm: row-wise and column-wise matrices
 };
@@ -551,6 +523,9 @@ muon_status check_plan_args(const muon_shape* shapes, int32_t n, muon_dtype grad
     if (opts && (opts->max_ns_steps < 0 || opts->max_ns_steps > kMaxNsStepsRestart || opts->chunks < 0 ||
                  opts->workspace_bytes < 0))
         return MUON_ERR_INVALID_ARG;
+    if (opts && opts->full_rows)
+        for (int i = 0; i < n; ++i)
+            if (opts->full_rows[i] < shapes[i].rows || opts->full_rows[i] > kMaxDim) return MUON_ERR_INVALID_ARG;
     return MUON_OK;
 }
 
@@ -576,6 +551,11 @@ muon_status plan_layout(muon_plan_s* p, Layout& L) {
         md.c = (int)std::max(md.m, md.n);
         md.transposed = md.m > md.n;
         md.scale = 0.2f * std::sqrt((float)md.c);   // blog eq. (4)
+        if (!p->full_rows.empty()) {   // a dim-0 shard: RowNorm axis and scale of the full matrix
+            const long long fm = p->full_rows[i];
+            md.transposed = fm > md.n;
+            md.scale = 0.2f * std::sqrt((float)std::max(fm, md.n));
+        }
         size_t g = 0;
         while (g < group_rc.size() && !(group_rc[g].first == md.r && group_rc[g].second == md.c)) ++g;
         if (g == group_rc.size()) {
@@ -607,7 +587,9 @@ muon_status plan_layout(muon_plan_s* p, Layout& L) {
     // region bytes of a bucket of `batch` matrices, exactly as laid out below: its X0
     // (and second X) buffer and, batched, its seven r x r buffers, each rounded to 256
     // (split buffers hold two parts per matrix)
+    const bool sharded = !p->full_rows.empty();   // RowNorm only: no NS buffers
     auto bucket_bytes = [&](int r, int c, long long batch) -> long long {
+        if (sharded) return 0;
         const int sp = split_of(r, c);
         const long long x = round_up(batch * r * round_up(c, 8) * 2 * (sp == 2 ? 2 : 1), 256);
         const long long rr = round_up(batch * r * round_up(r, 8) * 2 * (sp ? 2 : 1), 256);
@@ -637,6 +619,7 @@ muon_status plan_layout(muon_plan_s* p, Layout& L) {
             L.rnr_list.push_back(i);
         }
     }
+    p->colsq_len = sharded ? inv_elems : 0;
     L.o_mats = take(sizeof(MatDev) * n);
     L.o_part = take(sizeof(float) * std::max<long long>(mom_part, 1));
     L.o_cpart = take(sizeof(float) * std::max<long long>(col_part, 1));
@@ -647,8 +630,6 @@ muon_status plan_layout(muon_plan_s* p, Layout& L) {
     L.o_ptrs = take(sizeof(void*) * 3 * n);
     L.o_items = take(sizeof(int) * n);   // item -> plan matrix, per bucket slice
     L.o_ones = take(sizeof(float) * n);
-    L.o_wpf = take(sizeof(CUtensorMap) * n);   // W prefetch maps (64-byte aligned: slices are 256-aligned)
-    L.o_wpf_ok = take((size_t)n);
     L.o_odbg = p->opts.keep_update ? take([&] {
         size_t t = 0;
         for (int i = 0; i < n; ++i) t += (size_t)round_up(p->mats[i].m * p->mats[i].n * 4, 256);
@@ -746,6 +727,7 @@ muon_status plan_layout(muon_plan_s* p, Layout& L) {
                 b.slot_base = slots;
                 slots += b.batch;
                 const size_t xparts = b.split == 2 ? 2 : 1, rparts = b.split ? 2 : 1;
+                if (sharded) continue;   // RowNorm only: no X0 or r x r buffers
                 o_ut[k] = rtake((size_t)b.batch * b.r * b.ldu * 2 * xparts);
                 if (restarts) o_ut1[k] = rtake((size_t)b.batch * b.r * b.ldu * 2 * xparts);
                 if (b.batched()) {
@@ -808,6 +790,8 @@ static muon_status plan_build(muon_plan_s* p, const muon_shape* shapes, int32_t 
     p->gdt = grad_dtype;
     if (opts) p->opts = *opts;
     p->shapes.assign(shapes, shapes + n);
+    if (p->opts.full_rows) p->full_rows.assign(p->opts.full_rows, p->opts.full_rows + n);
+    p->opts.full_rows = nullptr;   // read during creation only
 
     Layout L;
     {
@@ -834,14 +818,13 @@ static muon_status plan_build(muon_plan_s* p, const muon_shape* shapes, int32_t 
     p->d_transposed = reinterpret_cast<unsigned char*>(base + L.o_tr);
     p->d_ptrs = reinterpret_cast<void**>(base + L.o_ptrs);
     p->ones = reinterpret_cast<float*>(base + L.o_ones);
-    p->d_wpf = reinterpret_cast<CUtensorMap*>(base + L.o_wpf);
-    p->d_wpf_ok = reinterpret_cast<unsigned char*>(base + L.o_wpf_ok);
 
     std::vector<unsigned char> tr(n);
     for (int i = 0; i < n; ++i) tr[i] = (unsigned char)p->mats[i].transposed;
     bool ok = cudaMemcpy(p->d_mats, p->mats.data(), sizeof(MatDev) * n, cudaMemcpyHostToDevice) == cudaSuccess;
     ok = ok && cudaMemcpy(p->d_transposed, tr.data(), n, cudaMemcpyHostToDevice) == cudaSuccess;
     ok = ok && cudaMemset(p->status, 0, sizeof(int)) == cudaSuccess;
+    ok = ok && cudaMemset(p->rowinv, 0, L.o_alpha - L.o_inv) == cudaSuccess;
     ok = ok && cudaMemset(p->d_ptrs, 0, sizeof(void*) * 3 * n) == cudaSuccess;
     {
         const std::vector<float> one(n, 1.f);
@@ -912,6 +895,7 @@ static muon_status plan_build(muon_plan_s* p, const muon_shape* shapes, int32_t 
         b.d_item_mat = item_cursor;
         item_cursor += b.batch;
         ok = cudaMemcpy(b.d_item_mat, b.mats.data(), sizeof(int) * b.batch, cudaMemcpyHostToDevice) == cudaSuccess;
+        if (!p->full_rows.empty()) continue;   // dim-0 shard plans run RowNorm only: no NS buffers
         b.gscale = std::ldexp(1.f, (int)std::lround(std::log2((double)b.r)));
         b.ut_off = (long long)(L.o_ut[k] / 2);
         if (p->opts.keep_update) {
@@ -982,8 +966,6 @@ static muon_status plan_build(muon_plan_s* p, const muon_shape* shapes, int32_t 
         }
     }
     ok = ok && cudaMallocHost(&p->h_pinned, sizeof(void*) * 3 * n) == cudaSuccess;
-    ok = ok && cudaMallocHost(&p->h_wpf, (sizeof(CUtensorMap) + 1) * n) == cudaSuccess;
-    ok = ok && cudaMemset(p->d_wpf_ok, 0, n) == cudaSuccess;
     ok = ok && cudaEventCreateWithFlags(&p->upload_ev, cudaEventDisableTiming) == cudaSuccess;
     ok = ok && gemm_prepare(p->device) == cudaSuccess;
     ok = ok && ns_f32_prepare() == cudaSuccess;
@@ -1105,6 +1087,8 @@ muon_status muon_plan_workspace_size(const muon_shape* shapes, int32_t n, muon_d
         muon_plan_s plan;   // host fields only: nothing is created on the device
         if (opts) plan.opts = *opts;
         plan.shapes.assign(shapes, shapes + n);
+        if (plan.opts.full_rows) plan.full_rows.assign(plan.opts.full_rows, plan.opts.full_rows + n);
+        plan.opts.full_rows = nullptr;
         Layout L;
         const muon_status st = plan_layout(&plan, L);
         if (st != MUON_OK) return st;
@@ -1149,6 +1133,7 @@ static muon_status rownorm_launch(muon_plan_s* p, const ListDev* rows, const Lis
 muon_status muon_rownorm_step(muon_plan p, float* const* params, const void* const* grads, float* const* momentum,
                               float lr, float wd, float mu, float eps, void* stream) {
     if (!p) return MUON_ERR_INVALID_ARG;
+    if (!p->full_rows.empty()) return MUON_ERR_UNSUPPORTED;   // the shard calls sum norms across shards
     if (!finite_nonneg(lr) || !finite_nonneg(wd) || !std::isfinite(mu) || mu < 0.f || mu >= 1.f ||
         !std::isfinite(eps) || eps <= 0.f)
         return MUON_ERR_INVALID_ARG;
@@ -1169,6 +1154,59 @@ muon_status muon_rownorm_step(muon_plan p, float* const* params, const void* con
         return st;
     if (se) MUON_TRY(cudaEventRecord(se->e[5], s));
     p->last_launches = launches;
+    return MUON_OK;
+}
+
+// Checks shared by the two shard calls.
+static muon_status shard_check(muon_plan_s* p, float* const* params, const void* const* grads,
+                               float* const* momentum, float lr, float wd, float mu, float eps, const void* colsq) {
+    if (!p) return MUON_ERR_INVALID_ARG;
+    if (p->full_rows.empty()) return MUON_ERR_UNSUPPORTED;
+    if (!finite_nonneg(lr) || !finite_nonneg(wd) || !std::isfinite(mu) || mu < 0.f || mu >= 1.f ||
+        !std::isfinite(eps) || eps <= 0.f || (p->colsq_len > 0 && !colsq))
+        return MUON_ERR_INVALID_ARG;
+    muon_status st = check_pointers(p, params, grads, momentum);
+    if (st != MUON_OK) return st;
+    return check_device(p);
+}
+
+muon_status muon_rownorm_shard_stats(muon_plan p, float* const* params, const void* const* grads,
+                                     float* const* momentum, float lr, float wd, float mu, float eps, float* colsq,
+                                     void* stream) {
+    muon_status st = shard_check(p, params, grads, momentum, lr, wd, mu, eps, colsq);
+    if (st != MUON_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((st = upload_pointers(p, params, grads, momentum, s)) != MUON_OK) return st;
+    int launches = 0;
+    ElemArgs a{};
+    for (int cl = 0; cl < kRowClasses; ++cl) {   // rows complete in the shard: the whole step
+        a = elem_args(p, p->rn_rows[cl], mu, lr, wd, eps);
+        MUON_TRY(launch_rownorm_rows(a, p->rn_rows[cl].blocks, rownorm_class_vec(cl), s));
+        launches += p->rn_rows[cl].blocks > 0;
+    }
+    a = elem_args(p, p->rn_stats, mu, lr, wd, eps);   // momentum and slab sums of U^2
+    a.partials = p->cpartials;
+    MUON_TRY(launch_rownorm_colstats(a, p->rn_stats.blocks, s));
+    a = elem_args(p, p->rn_final, mu, lr, wd, eps);   // this shard's column sums into colsq
+    a.partials = p->cpartials;
+    MUON_TRY(launch_rownorm_colsum(a, p->rn_final.blocks, colsq, s));
+    launches += p->rn_stats.blocks > 0 ? 2 : 0;
+    p->last_launches = launches;
+    return MUON_OK;
+}
+
+muon_status muon_rownorm_shard_apply(muon_plan p, float* const* params, const void* const* grads,
+                                     float* const* momentum, float lr, float wd, float mu, float eps,
+                                     const float* colsq, void* stream) {
+    muon_status st = shard_check(p, params, grads, momentum, lr, wd, mu, eps, colsq);
+    if (st != MUON_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((st = upload_pointers(p, params, grads, momentum, s)) != MUON_OK) return st;
+    ElemArgs a = elem_args(p, p->rn_final, mu, lr, wd, eps);
+    MUON_TRY(launch_rownorm_colinv(a, p->rn_final.blocks, colsq, s));
+    a = elem_args(p, p->rn_apply, mu, lr, wd, eps);
+    MUON_TRY(launch_rownorm_colapply(a, p->rn_apply.blocks, s));
+    p->last_launches = p->rn_apply.blocks > 0 ? 2 : 0;
     return MUON_OK;
 }
 
@@ -1200,6 +1238,7 @@ static muon_status ns_step(muon_plan p, float* const* params, const void* const*
                            float lr, float wd, float mu, int32_t ns_steps, const float* coeffs, int32_t restart,
                            void* stream, const HostIO* io) {
     if (!p) return MUON_ERR_INVALID_ARG;
+    if (!p->full_rows.empty()) return MUON_ERR_UNSUPPORTED;   // dim-0 shard plans: RowNorm only
     const int max_steps = p->opts.max_ns_steps > 0 ? p->opts.max_ns_steps : kMaxNsSteps;
     if (!finite_nonneg(lr) || !finite_nonneg(wd) || !std::isfinite(mu) || mu < 0.f || mu >= 1.f ||
         ns_steps < 0 || ns_steps > max_steps || restart < 0 || restart > kMaxNsSteps)
@@ -1504,8 +1543,6 @@ static muon_status ns_step(muon_plan p, float* const* params, const void* const*
                     if (last) {
                         q.item_mat = b.d_item_mat;
                         q.W = W;
-                        q.wpf = p->d_wpf;
-                        q.wpf_ok = p->d_wpf_ok;
                         q.transposed = p->d_transposed;
                         q.Odbg = b.Odbg;
                         q.lr = lr;
@@ -1584,6 +1621,7 @@ muon_status muon_step_host(muon_plan p, float* const* params, const void* const*
                            const void* const* grads_host, float* const* params_host, float lr, float wd,
                            float mu, int32_t ns_steps, muon_mode mode, void* stream) {
     if (!p || !grads_host) return MUON_ERR_INVALID_ARG;
+    if (!p->full_rows.empty()) return MUON_ERR_UNSUPPORTED;
     const int n = (int)p->shapes.size();
     for (int i = 0; i < n; ++i)
         if (!grads_host[i] || (params_host && !params_host[i])) return MUON_ERR_INVALID_ARG;
@@ -1647,6 +1685,7 @@ muon_status muon_step_host(muon_plan p, float* const* params, const void* const*
 muon_status muon_plan_tune(muon_plan p, float* const* params, const void* const* grads, float* const* momentum,
                            float lr, float wd, float mu, int32_t reps, float* ms_out, void* stream) {
     if (!p || reps < 1 || reps > 100) return MUON_ERR_INVALID_ARG;
+    if (!p->full_rows.empty()) return MUON_ERR_UNSUPPORTED;
     muon_status st = check_pointers(p, params, grads, momentum);
     if (st != MUON_OK) return st;
     // candidates: CTA pairs beside the fused kernel (none, the estimate, half and one and a
@@ -1813,6 +1852,7 @@ muon_status muon_plan_info(muon_plan p, muon_plan_info_t* info) {
     }
     info->split_buckets = nsplit;
     info->fp32_buckets = nf32;
+    info->colsq_len = (int64_t)p->colsq_len;
     return MUON_OK;
 }
 

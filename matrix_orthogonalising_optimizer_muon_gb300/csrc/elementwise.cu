@@ -431,6 +431,39 @@ __global__ void __launch_bounds__(kElemThreads) k_rownorm_colfinal(const ElemArg
     a.rowinv[md.inv_off + j] = 1.f / fmaxf(sqrtf(s), a.eps);
 }
 
+// Dim-0 shards: this shard's column sums of U^2 (fixed slab order) into out[inv_off + j],
+// the padding up to a multiple of 4 written as 0, for the caller to sum across shards.
+__global__ void __launch_bounds__(kElemThreads) k_rownorm_colsum(const ElemArgs a, float* out) {
+    pdl_trigger();
+    pdl_wait();
+    const long long b = blockIdx.x;
+    const int li = find_entry(a.list_blk, a.nlist, b);
+    const MatDev md = a.mats[a.list[li]];
+    const long long j = (b - a.list_blk[li]) * kElemThreads + threadIdx.x;
+    const long long npad = (md.n + 3) / 4 * 4;
+    if (j >= npad) return;
+    float s = 0.f;
+    if (j < md.n) {
+        const long long slabs = (md.m + kColSlab - 1) / kColSlab;
+        for (long long k = 0; k < slabs; ++k) s += a.partials[md.cpart_off + k * md.n + j];
+    }
+    out[md.inv_off + j] = s;
+}
+
+// inv[j] = 1 / max(sqrt(colsq[j]), eps) from column sums already summed over the shards.
+__global__ void __launch_bounds__(kElemThreads) k_rownorm_colinv(const ElemArgs a, const float* colsq) {
+    pdl_trigger();
+    pdl_wait();
+    const long long b = blockIdx.x;
+    const int li = find_entry(a.list_blk, a.nlist, b);
+    const MatDev md = a.mats[a.list[li]];
+    const long long j = (b - a.list_blk[li]) * kElemThreads + threadIdx.x;
+    if (j >= md.n) return;
+    const float s = colsq[md.inv_off + j];
+    if (a.check_finite && !isfinite(s)) atomicOr(a.status, kStatusNonFinite);
+    a.rowinv[md.inv_off + j] = 1.f / fmaxf(sqrtf(s), a.eps);
+}
+
 // W <- W - lr (s * U * inv[col] + wd W), U recomputed from G and the stored new M.
 template <bool BF16>
 __global__ void __launch_bounds__(kElemThreads) k_rownorm_colapply(const ElemArgs a) {
@@ -529,6 +562,14 @@ cudaError_t launch_rownorm_colstats(const ElemArgs& a, long long blocks, cudaStr
 cudaError_t launch_rownorm_colfinal(const ElemArgs& a, long long blocks, cudaStream_t s) {
     if (blocks <= 0) return cudaSuccess;
     return launch_pdl(k_rownorm_colfinal, dim3((unsigned)blocks), dim3(kElemThreads), 0, s, a);
+}
+cudaError_t launch_rownorm_colsum(const ElemArgs& a, long long blocks, float* out, cudaStream_t s) {
+    if (blocks <= 0) return cudaSuccess;
+    return launch_pdl(k_rownorm_colsum, dim3((unsigned)blocks), dim3(kElemThreads), 0, s, a, out);
+}
+cudaError_t launch_rownorm_colinv(const ElemArgs& a, long long blocks, const float* colsq, cudaStream_t s) {
+    if (blocks <= 0) return cudaSuccess;
+    return launch_pdl(k_rownorm_colinv, dim3((unsigned)blocks), dim3(kElemThreads), 0, s, a, colsq);
 }
 cudaError_t launch_rownorm_colapply(const ElemArgs& a, long long blocks, cudaStream_t s) {
     if (blocks <= 0) return cudaSuccess;

@@ -302,11 +302,12 @@ __device__ __forceinline__ bool upper_block(bool sym, int k0, int row0) {
     return sym && k0 >= (row0 & ~255) + 256;
 }
 
-// L2 prefetch of what the epilogue of this CTA's part of a tile (rows m0 .. m0 + 127,
-// columns n0 .. n0 + 255) reads, issued by the producer when the tile's loads start
-// (a handful of tensor prefetches, not one bulk prefetch per row): the polynomial's G'
-// (its A operand, 64-column boxes of 128 rows) and the final product's W (two 128 x 128
-// boxes of the stored layout, when the matrix has a W prefetch map).
+// L2 prefetch of the polynomial's G' input for this CTA's part of a tile (rows m0 ..
+// m0 + 127, columns n0 .. n0 + 255), issued by the producer when the tile's loads start:
+// four tensor prefetches of the A operand's boxes (64 columns x 128 rows), in place of
+// one bulk prefetch per row from the epilogue warps.  (The final product's W keeps the
+// epilogue warps' row prefetches: the same through two 128 x 128 W boxes from the
+// producer measured 5 % slower on that stage.)
 template <bool LOWER>
 __device__ __forceinline__ void tile_prefetch(const GemmLaunch& L, const GemmProblem& P, const TileCoord& tc) {
     if (tc.m0 >= P.M) return;
@@ -319,16 +320,6 @@ __device__ __forceinline__ void tile_prefetch(const GemmLaunch& L, const GemmPro
                 tma_prefetch_3d(&L.mapA[tc.p], tc.n0 + 64 * q, tc.m0, za);
                 if (P.a_split) tma_prefetch_3d(&L.mapA[tc.p], tc.n0 + 64 * q, tc.m0, za + 1);
             }
-        }
-    } else if (P.epi == kEpiApply && P.wpf) {
-        const int mat = P.item_mat[tc.item];
-        if (!P.wpf_ok[mat]) return;
-        const bool tr = P.transposed[mat] != 0;
-        for (int h = 0; h < 2 && tc.n0 + 128 * h < P.N; ++h) {
-            if (tr)
-                tma_prefetch_2d(&P.wpf[mat], tc.m0, tc.n0 + 128 * h);
-            else
-                tma_prefetch_2d(&P.wpf[mat], tc.n0 + 128 * h, tc.m0);
         }
     }
 }
@@ -523,8 +514,7 @@ __global__ void __maxnreg__(168) gemm2_kernel(const __grid_constant__ GemmLaunch
             const GemmProblem& P = L.prob[tc.p];
             const uint32_t acc = local & 1;
             const uint32_t aph = (local >> 1) & 1u;
-            // (tiles whose inputs have tensor maps are prefetched by the producer, tile_prefetch)
-            if (P.epi == kEpiApply && !(P.wpf && P.wpf_ok[P.item_mat[tc.item]]))
+            if (P.epi == kEpiApply)   // (the polynomial's G' is prefetched by the producer)
                 prefetch_epilogue_inputs(P, tc.item, tc.m0 + wq * 32, tc.n0 + c_begin, kBN * 4 / kEpiWarps, lane);
             if (!mbar_wait_idle(tfull + acc, aph, abort_flag, L.status, kStatusTimeoutEpilogue, true)) break;
             tc_fence_after();

@@ -129,11 +129,6 @@ struct GemmProblem {
     // out_split: the output (C, C2, Cb) is written as hi = round(v), lo = round(v - hi).
     // kEpiPoly reads its G' input split when a_split is set.  Per-thread stores only.
     int a_split, b_split, out_split;
-    // kEpiApply: per plan matrix, a tensor map of W (fp32, stored layout, 128 x 128 boxes)
-    // for the L2 prefetch of the tile's W while its MMAs run, and whether it is valid
-    // (W 16-byte aligned, stored row length a multiple of 4, both dimensions >= 128)
-    const CUtensorMap* wpf;
-    const unsigned char* wpf_ok;
 };
 constexpr int kTmaOutC = 1, kTmaOutC2 = 2, kTmaOutBf16 = 4;
 
@@ -244,6 +239,11 @@ cudaError_t launch_rownorm_rows(const ElemArgs& a, long long blocks, int vec, cu
 // RowNorm, m > n: column statistics, finalize, apply.
 cudaError_t launch_rownorm_colstats(const ElemArgs& a, long long blocks, cudaStream_t s);
 cudaError_t launch_rownorm_colfinal(const ElemArgs& a, long long blocks, cudaStream_t s);
+// Dim-0 shards: column sums of U^2 of this shard into out (per matrix at inv_off, padded
+// to 4 with zeros; blocks as colfinal over ceil(round_up(n, 4) / threads)), and inverse
+// norms from the sums over all shards.
+cudaError_t launch_rownorm_colsum(const ElemArgs& a, long long blocks, float* out, cudaStream_t s);
+cudaError_t launch_rownorm_colinv(const ElemArgs& a, long long blocks, const float* colsq, cudaStream_t s);
 cudaError_t launch_rownorm_colapply(const ElemArgs& a, long long blocks, cudaStream_t s);
 
 // Block geometry the planner needs to size grids and partial-sum buffers.

@@ -25,6 +25,7 @@ int main(void) {
     FIELD(muon_plan_opts, check_finite);
     FIELD(muon_plan_opts, precision);
     FIELD(muon_plan_opts, split_max_r);
+    FIELD(muon_plan_opts, full_rows);
     printf("sizeof.muon_plan_info_t %zu\n", sizeof(muon_plan_info_t));
     FIELD(muon_plan_info_t, n_matrices);
     FIELD(muon_plan_info_t, n_buckets);
@@ -37,6 +38,7 @@ int main(void) {
     FIELD(muon_plan_info_t, chain_clusters);
     FIELD(muon_plan_info_t, split_buckets);
     FIELD(muon_plan_info_t, fp32_buckets);
+    FIELD(muon_plan_info_t, colsq_len);
     printf("sizeof.muon_shape %zu\n", sizeof(muon_shape));
 
     for (int s = MUON_OK; s <= MUON_ERR_NONFINITE; ++s) printf("status.%d %s\n", s, muon_status_string((muon_status)s));

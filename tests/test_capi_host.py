@@ -30,7 +30,10 @@ def struct_fields(name):
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     body = re.search(r"typedef struct \{([^}]*)\}\s*" + name + r"\s*;", src).group(1)
     size = {"int32_t": 4, "int64_t": 8}
-    return [(f, size[t]) for t, f in re.findall(r"\b(int32_t|int64_t)\s+(\w+)\s*;", body)]
+    out = []
+    for t, ptr, f in re.findall(r"\b(int32_t|int64_t)\s*(\*?)\s*(\w+)\s*;", body):
+        out.append((f, 8 if ptr else size[t]))   # pointers are 8 bytes on both hosts
+    return out
 
 
 def test_struct_layouts_match_the_header():

@@ -147,3 +147,92 @@ def test_two_gloo_ranks_match_one_process_bitwise(in_place):
         for i, m in res[rank]["M"].items():
             assert owners[i] == rank and np.array_equal(m, np.float32(M[i])), (rank, i)
     assert set(res[0]["M"]) | set(res[1]["M"]) == set(range(len(SHAPES)))
+
+
+# ---------------------------------------------------------------- sharded RowNorm over two gloo ranks
+FULL = [(64, 24), (24, 64), (48, 48), (130, 20), (20, 130)]   # full shapes (m, n)
+
+
+class OracleShards(mu.ShardedRowNorm):
+    """ShardedRowNorm's step (statistics, all-reduce, update) with fp64 CPU arithmetic as
+    each rank's local part, written from the RowNorm definition: R(U)_i = U_i / max(||U_i||,
+    eps) over the rows of the oriented full matrix (stored columns when m > n)."""
+
+    def _make_plan(self, shard_shapes, full_rows, grad_dtype, plan_opts):
+        self.shapes, self.full_rows = shard_shapes, full_rows
+        return None
+
+    def _colsq_len(self):
+        return sum((n + 3) // 4 * 4 for (m, n), f in zip(self.shapes, self.full_rows) if f > n)
+
+    def _device(self):
+        return "cpu"
+
+    def _stats(self, params, grads, momentum, lr, wd, mu_, eps, stream):
+        import torch
+        self.colsq = self.colsq.double()
+        off = 0
+        for (m, n), f, w, g, mo in zip(self.shapes, self.full_rows, params, grads, momentum):
+            mo.mul_(mu_).add_(g)                   # M <- mu M + G
+            u = mu_ * mo + g
+            scale = 0.2 * (max(f, n) ** 0.5)
+            if f <= n:                             # every RowNorm row is complete here
+                r = u / torch.clamp(u.norm(dim=1, keepdim=True), min=eps)
+                w.sub_(lr * (scale * r + wd * w))
+            else:
+                self.colsq[off:off + n] = (u * u).sum(dim=0)
+                off += (n + 3) // 4 * 4
+
+    def _apply(self, params, grads, momentum, lr, wd, mu_, eps, stream):
+        import torch
+        off = 0
+        for (m, n), f, w, g, mo in zip(self.shapes, self.full_rows, params, grads, momentum):
+            if f <= n:
+                continue
+            u = mu_ * mo + g
+            inv = 1.0 / torch.clamp(self.colsq[off:off + n].sqrt(), min=eps)
+            w.sub_(lr * (0.2 * (max(f, n) ** 0.5) * u * inv + wd * w))
+            off += (n + 3) // 4 * 4
+
+
+def _shard_worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    import torch
+    import torch.distributed as dist
+    from workloads import gen_tensor, seed_of
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    shard_shapes, params, grads, moms = [], [], [], []
+    for i, (m, n) in enumerate(FULL):
+        lo, hi = rank * m // world, (rank + 1) * m // world   # dim-0 shard of the full matrix
+        w = gen_tensor((m, n), 0.02, seed_of(72, 0, i, "W")).double()
+        g = gen_tensor((m, n), 1e-3, seed_of(72, 0, i, "G")).double()
+        mm = gen_tensor((m, n), 1e-3, seed_of(72, 0, i, "M")).double()
+        shard_shapes.append((hi - lo, n))
+        params.append(w[lo:hi].clone())
+        grads.append(g[lo:hi].clone())
+        moms.append(mm[lo:hi].clone())
+    opt = OracleShards(shard_shapes, [m for m, _ in FULL], "f32")
+    opt.step(params, grads, moms, LR, WD, MU, 1e-8)
+    out[rank] = [p.numpy().copy() for p in params]
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_sharded_rownorm_over_two_gloo_ranks_matches_the_full_oracle():
+    """Two ranks each hold half of the rows of every matrix; one sharded RowNorm step
+    (local statistics, one all-reduce of the column sums, local update) gives the oracle's
+    RowNorm step on the full matrices."""
+    pytest.importorskip("torch")
+    import torch.multiprocessing as mp
+    from oracle import muon_ref as R
+    from workloads import gen_tensor, seed_of
+    mgr = mp.Manager()
+    out = mgr.dict()
+    mp.start_processes(_shard_worker, args=(2, _free_port(), out), nprocs=2, join=True, start_method="spawn")
+    for i, (m, n) in enumerate(FULL):
+        w = gen_tensor((m, n), 0.02, seed_of(72, 0, i, "W")).double().numpy()
+        g = gen_tensor((m, n), 1e-3, seed_of(72, 0, i, "G")).double().numpy()
+        mm = gen_tensor((m, n), 1e-3, seed_of(72, 0, i, "M")).double().numpy()
+        w_ref, _, _ = R.muon_step(w, g, mm, LR, WD, MU, 0, "rownorm", 1e-8)
+        got = np.concatenate([out[0][i], out[1][i]], axis=0)
+        assert np.abs(got - w_ref).max() <= 1e-12 * np.abs(w_ref).max(), (i, (m, n))

@@ -1014,3 +1014,57 @@ def test_split_levels_with_restarted_segments(precision):
     res = run_step(VARIANT_SHAPES, "bf16", base_seed=62, ns_steps=10, max_ns_steps=10, precision=precision)
     for i in range(len(VARIANT_SHAPES)):
         check_ns_variant(res, i, 10, R.NS_COEFFS, TOL_O)
+
+
+def test_dim0_shard_rownorm_matches_the_full_matrix():
+    """RowNorm over dim-0 shards (opts.full_rows) on one GPU: every matrix split into two
+    row blocks that one plan holds as separate shards; the column sums of the two blocks
+    are added on the device between the two shard calls (what an all-reduce across ranks
+    does), and the blocks together must equal the oracle's RowNorm step on the full
+    matrix (M and W at 1e-5).  Covers spanning (m > n) and complete (m <= n) rows."""
+    import torch
+    import matrix_orthogonalising_optimizer_muon_gb300 as lib
+    from workloads import gen_tensor, seed_of
+    full = [(1000, 333), (333, 1000), (12288, 2048), (256, 1024), (2048, 2048), (130, 7)]
+    shards, full_rows, parts = [], [], []
+    for i, (m, n) in enumerate(full):
+        k = (m // 3) // 8 * 8 + 5                     # ragged split point
+        for lo, hi in ((0, k), (k, m)):
+            shards.append((hi - lo, n))
+            full_rows.append(m)
+            parts.append((i, lo, hi))
+    W = [gen_tensor(s, 0.02, seed_of(73, 0, i, "W"), "cuda") for i, s in enumerate(full)]
+    G = [gen_tensor(s, 1e-3, seed_of(73, 0, i, "G"), "cuda", "bf16") for i, s in enumerate(full)]
+    M = [gen_tensor(s, 1e-3, seed_of(73, 0, i, "M"), "cuda") for i, s in enumerate(full)]
+    ref = [R.muon_step(W[i].double().cpu().numpy(), G[i].double().cpu().numpy(), M[i].double().cpu().numpy(),
+                       LR, WD, MU, 0, "rownorm", 1e-8) for i in range(len(full))]
+    Ws = [W[i][lo:hi].clone() for i, lo, hi in parts]
+    Gs = [G[i][lo:hi].clone() for i, lo, hi in parts]
+    Ms = [M[i][lo:hi].clone() for i, lo, hi in parts]
+    plan = lib.MuonPlan(shards, "bf16", full_rows=full_rows)
+    n_col = plan.info()["colsq_len"]
+    offs, off = [], 0
+    for (rows, n), f in zip(shards, full_rows):
+        offs.append(off if f > n else None)
+        off += (n + 3) // 4 * 4 if f > n else 0
+    assert n_col == off
+    colsq = torch.full((n_col,), float("nan"), device="cuda")
+    plan.rownorm_shard_stats(Ws, Gs, Ms, LR, WD, colsq)
+    for j in range(0, len(shards), 2):                 # the two blocks of one matrix
+        if offs[j] is None:
+            continue
+        n = shards[j][1]
+        a, b = colsq[offs[j]:offs[j] + n].clone(), colsq[offs[j + 1]:offs[j + 1] + n].clone()
+        colsq[offs[j]:offs[j] + n] = a + b
+        colsq[offs[j + 1]:offs[j + 1] + n] = a + b
+    plan.rownorm_shard_apply(Ws, Gs, Ms, LR, WD, colsq)
+    plan.sync()
+    with pytest.raises(lib.MuonError) as ei:
+        plan.step(Ws, Gs, Ms, LR, WD, MU)               # a shard plan runs RowNorm only
+    assert ei.value.code == lib.MUON_ERR_UNSUPPORTED
+    for i in range(len(full)):
+        w = torch.cat([Ws[j] for j, (ii, _, _) in enumerate(parts) if ii == i]).double().cpu().numpy()
+        m = torch.cat([Ms[j] for j, (ii, _, _) in enumerate(parts) if ii == i]).double().cpu().numpy()
+        assert rel(m, ref[i][1]) <= TOL_FP32, (full[i], rel(m, ref[i][1]))
+        assert rel(w, ref[i][0]) <= TOL_FP32, (full[i], rel(w, ref[i][0]))
+    plan.close()

@@ -195,3 +195,14 @@ def test_split_precision_doubles_the_split_buffers():
     # the 7B layer's squares (r = 3584) and the DiT block's (r = 2048) stay plain
     assert ws(LAYER) == ws(LAYER, precision=-1)
     assert ws([(2048, 2048)]) == ws([(2048, 2048)], precision=-1)
+
+
+def test_dim0_shard_plans_hold_no_newton_schulz_buffers():
+    """opts.full_rows makes a RowNorm-only plan over dim-0 shards: no X0 or r x r buffers,
+    and row counts above the full matrix's are refused."""
+    shards = [(512, 2048), (1024, 2048), (2048, 512)]
+    plain = ws(shards)["workspace_bytes"]
+    sharded = ws(shards, full_rows=[6144, 2048, 4096])["workspace_bytes"]
+    assert sharded < plain and sharded < 4 << 20
+    with pytest.raises(mu.MuonError):
+        ws(shards, full_rows=[256, 2048, 4096])   # a shard of 512 rows of a 256-row matrix
