@@ -148,6 +148,13 @@ typedef struct {
        muon_rownorm_shard_apply; otherwise each stored row is complete in the shard.
        Such a plan runs only those two calls (the others return MUON_ERR_UNSUPPORTED). */
     const int64_t* full_rows;
+    /* NULL, or a host array of n entries (read during muon_plan_create only) choosing the
+       precision of each matrix on the batched products: < 0 plain, 1 or 2 that split level,
+       0 the plan-wide rule of opts.precision.  Matrices of one oriented shape with different
+       entries form separate buckets.  Matrices on the one-CTA kernels ignore it.  A caller
+       (or MuonPlan.select_precision in the Python binding) can thus keep the plain recipe
+       where it meets a tolerance on its own data and split only where it does not. */
+    const int32_t* precision_of;
 } muon_plan_opts;
 
 typedef struct muon_plan_s* muon_plan;
@@ -355,6 +362,15 @@ muon_status muon_debug_wait_timeout(muon_plan p, int32_t limit_us, void* stream)
  * floats).  Needs opts.keep_update; synchronises stream.
  */
 muon_status muon_debug_copy_update(muon_plan p, int32_t i, float* dst, void* stream);
+
+/*
+ * muon_debug_update_error - relative Frobenius difference ||O_i - ref|| / ||ref|| (the
+ * plain norm of O_i when ref is zero) between the orthogonalised update O of matrix i from
+ * the last NS step and ref (device memory, fp32, stored layout m x n), computed on the
+ * device in fp64.  Needs opts.keep_update; synchronises stream.  Used to check one
+ * precision of the Newton-Schulz recursion against another on the caller's own data.
+ */
+muon_status muon_debug_update_error(muon_plan p, int32_t i, const float* ref, double* rel, void* stream);
 
 /*
  * muon_debug_copy_workspace - copy one workspace buffer of matrix i, as it is

@@ -24,6 +24,7 @@ from .build import LIB, build, up_to_date
 
 __all__ = [
     "MuonError", "MuonPlan", "PeriodicRowNormMuon", "DistributedMuon", "ShardedRowNorm", "partition_owners",
+    "select_precision",
     "plan_workspace_size", "load", "build",
     "MUON_OK", "MUON_ERR_INVALID_ARG", "MUON_ERR_UNSUPPORTED", "MUON_ERR_OOM",
     "MUON_ERR_CUDA", "MUON_ERR_TIMEOUT", "MUON_ERR_NONFINITE", "MUON_F32", "MUON_BF16",
@@ -51,7 +52,7 @@ class MuonPlanOpts(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_int64), ("chunks", ctypes.c_int32),
                 ("full_symmetric", ctypes.c_int32), ("small_fp32", ctypes.c_int32),
                 ("check_finite", ctypes.c_int32), ("precision", ctypes.c_int32), ("split_max_r", ctypes.c_int32),
-                ("full_rows", ctypes.POINTER(ctypes.c_int64))]
+                ("full_rows", ctypes.POINTER(ctypes.c_int64)), ("precision_of", ctypes.POINTER(ctypes.c_int32))]
 
 
 class MuonPlanInfo(ctypes.Structure):
@@ -85,6 +86,7 @@ EXPORTED = {
     "muon_plan_tune": (ctypes.c_int, [_P, _PP, _PP, _PP, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                       ctypes.c_int32, ctypes.POINTER(ctypes.c_float), _P]),
     "muon_debug_copy_update": (ctypes.c_int, [_P, ctypes.c_int32, _P, _P]),
+    "muon_debug_update_error": (ctypes.c_int, [_P, ctypes.c_int32, _P, ctypes.POINTER(ctypes.c_double), _P]),
     "muon_debug_copy_workspace": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int32, _P,
                                                  ctypes.POINTER(ctypes.c_int32), _P]),
     "muon_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -159,7 +161,7 @@ def _ptr_array(ptrs):
 def _plan_args(shapes, grad_dtype, keep_update=False, timing=False, single_sm_gemm=False,
                generic_small=False, chain_clusters=0, workspace_bytes=0, max_ns_steps=0, chunks=0,
                full_symmetric=False, small_fp32=0, check_finite=False, precision=0, split_max_r=0,
-               full_rows=None):
+               full_rows=None, precision_of=None):
     """(shape list, MuonShape array, dtype code, MuonPlanOpts) of a plan's arguments.  The
     options keep a reference to the full_rows array (read by the library during creation)."""
     shapes = [(int(m), int(n)) for m, n in shapes]
@@ -169,12 +171,18 @@ def _plan_args(shapes, grad_dtype, keep_update=False, timing=False, single_sm_ge
         if len(full_rows) != len(shapes):
             raise ValueError("full_rows needs one entry per matrix")
         fr = (ctypes.c_int64 * len(shapes))(*[int(x) for x in full_rows])
+    po = None
+    if precision_of is not None:
+        if len(precision_of) != len(shapes):
+            raise ValueError("precision_of needs one entry per matrix")
+        po = (ctypes.c_int32 * len(shapes))(*[int(x) for x in precision_of])
     opts = MuonPlanOpts(1 if keep_update else 0, 1 if timing else 0, 1 if single_sm_gemm else 0,
                         1 if generic_small else 0, int(chain_clusters), int(max_ns_steps),
                         int(workspace_bytes), int(chunks), 1 if full_symmetric else 0, int(small_fp32),
                         1 if check_finite else 0, int(precision), int(split_max_r),
-                        ctypes.cast(fr, ctypes.POINTER(ctypes.c_int64)) if fr is not None else None)
-    opts._full_rows_ref = fr
+                        ctypes.cast(fr, ctypes.POINTER(ctypes.c_int64)) if fr is not None else None,
+                        ctypes.cast(po, ctypes.POINTER(ctypes.c_int32)) if po is not None else None)
+    opts._arrays = (fr, po)
     return shapes, arr, {"bf16": MUON_BF16, "f32": MUON_F32}[grad_dtype], opts
 
 
@@ -201,12 +209,12 @@ class MuonPlan:
                  timing: bool = False, single_sm_gemm: bool = False, generic_small: bool = False,
                  chain_clusters: int = 0, workspace_bytes: int = 0, max_ns_steps: int = 0, chunks: int = 0,
                  full_symmetric: bool = False, small_fp32: int = 0, check_finite: bool = False,
-                 precision: int = 0, split_max_r: int = 0, full_rows=None):
+                 precision: int = 0, split_max_r: int = 0, full_rows=None, precision_of=None):
         self.lib = load()
         self.shapes, arr, gd, opts = _plan_args(shapes, grad_dtype, keep_update, timing, single_sm_gemm,
                                                 generic_small, chain_clusters, workspace_bytes, max_ns_steps,
                                                 chunks, full_symmetric, small_fp32, check_finite, precision,
-                                                split_max_r, full_rows)
+                                                split_max_r, full_rows, precision_of)
         self.grad_dtype = grad_dtype
         h = ctypes.c_void_p()
         _check(self.lib.muon_plan_create(arr, len(self.shapes), gd, ctypes.byref(opts),
@@ -361,6 +369,13 @@ class MuonPlan:
         _check(self.lib.muon_debug_copy_update(self.handle, i, ctypes.c_void_p(out.data_ptr()),
                                                _stream_handle(stream)), "muon_debug_copy_update")
         return out
+
+    def debug_update_error(self, i: int, ref, stream=None) -> float:
+        """||O_i - ref|| / ||ref|| on the device (``muon_debug_update_error``; needs keep_update)."""
+        out = ctypes.c_double()
+        _check(self.lib.muon_debug_update_error(self.handle, i, ctypes.c_void_p(ref.data_ptr()), ctypes.byref(out),
+                                                _stream_handle(stream)), "muon_debug_update_error")
+        return out.value
 
     def debug_workspace(self, i: int, which: int, stream=None):
         """A workspace buffer of matrix i (``muon_debug_copy_workspace``) as a CPU fp32
@@ -618,3 +633,68 @@ class ShardedRowNorm:
         if getattr(self, "plan", None) is not None and hasattr(self.plan, "close"):
             self.plan.close()
             self.plan = None
+
+
+def select_precision(shapes, grad_dtype, params, grads, momentum, mu: float = DEFAULT_MU, tol: float = 1e-2,
+                     sample: int = 4, candidates=(-1, 1), reference: int = 2, ns_steps: int = DEFAULT_NS_STEPS,
+                     stream=None, **plan_opts):
+    """Per-matrix precision levels for ``precision_of``, chosen on the caller's own data:
+    DMuon's plan-time profiling per shape (technical summary sec. 2.3 and 2.4), with an
+    accuracy check added because the candidates differ in their results.
+
+    For every oriented shape, up to ``sample`` of its matrices run one NS step at the
+    reference level (split level 2) and at each candidate level (< 0: the plain recipe,
+    1: split recursion); a candidate passes when the O of every sampled matrix is within
+    ``tol`` (relative Frobenius, ``muon_debug_update_error``) of the reference's O, and each
+    shape takes the fastest passing candidate (step time of the sample, measured with CUDA
+    events), else the reference.  The caller's tensors are not modified: the steps run on
+    copies with lr = wd = 0.  Returns (levels, report): one level per matrix and, per shape,
+    each candidate's error and milliseconds."""
+    import torch
+    shapes = [(int(m), int(n)) for m, n in shapes]
+    groups = {}
+    for i, (m, n) in enumerate(shapes):
+        groups.setdefault((min(m, n), max(m, n)), []).append(i)
+    picked = [i for key in groups for i in groups[key][:sample]]
+    sub = [shapes[i] for i in picked]
+    grads_s = [grads[i] for i in picked]
+    levels_all = [reference] + [c for c in candidates if c != reference]
+
+    def run(level, ref):
+        plan = MuonPlan(sub, grad_dtype, keep_update=True, precision_of=[level] * len(sub), **plan_opts)
+        try:
+            W = [params[i].clone() for i in picked]
+            M = [momentum[i].clone() for i in picked]
+            plan.step(W, grads_s, M, 0.0, 0.0, mu, ns_steps, stream=stream)
+            plan.sync(stream)
+            if ref is None:
+                out = [plan.debug_update(j) for j in range(len(sub))]
+            else:
+                out = [plan.debug_update_error(j, ref[j], stream) for j in range(len(sub))]
+            s = torch.cuda.current_stream() if stream is None else stream
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for _ in range(2):
+                plan.step(W, grads_s, M, 0.0, 0.0, mu, ns_steps, stream=stream)
+            e1.record(s)
+            e1.synchronize()
+            return out, e0.elapsed_time(e1) / 2
+        finally:
+            plan.close()
+
+    ref_o, ref_ms = run(reference, None)
+    errs, times = {reference: [0.0] * len(sub)}, {reference: ref_ms}
+    for lv in levels_all[1:]:
+        errs[lv], times[lv] = run(lv, ref_o)
+    del ref_o
+    levels = [reference] * len(shapes)
+    report = {}
+    for key, idx in groups.items():
+        js = [picked.index(i) for i in idx[:sample]]
+        rep = {lv: {"err": max(errs[lv][j] for j in js), "ms_sample": times[lv]} for lv in levels_all}
+        ok = [lv for lv in levels_all if rep[lv]["err"] <= tol]
+        chosen = min(ok, key=lambda lv: (times[lv], lv)) if ok else reference
+        for i in idx:
+            levels[i] = chosen
+        report[key] = {"chosen": chosen, "candidates": rep}
+    return levels, report

@@ -173,10 +173,12 @@ struct muon_plan_s {
     cudaStream_t s2 = nullptr;
     cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
     float* ones = nullptr;   // per matrix 1.0 (alpha of the iterates after a restart)
+    double* diff = nullptr;  // muon_debug_update_error's partial sums (2 + 2 kDiffParts doubles)
     muon_dtype gdt = MUON_F32;
     muon_plan_opts opts{};
     std::vector<muon_shape> shapes;
     std::vector<int64_t> full_rows;   // opts.full_rows copied (dim-0 shard plans), else empty
+    std::vector<int32_t> prec_of;     // opts.precision_of copied (per-matrix precision), else empty
     long long colsq_len = 0;          // floats of the shard calls' colsq buffer
     std::vector<MatDev> mats;
     std::vector<int> mat_bucket, mat_item;
@@ -505,7 +507,7 @@ void free_plan(muon_plan_s* p) {
 struct Layout {
     bool restarts = false;   // opts.max_ns_steps > 0: second X buffer, every matrix batched
     size_t o_mats = 0, o_part = 0, o_cpart = 0, o_inv = 0, o_alpha = 0, o_status = 0, o_tr = 0, o_ptrs = 0,
-           o_items = 0, o_ones = 0, o_odbg = 0, o_lists = 0, o_prefix = 0, o_region = 0;
+           o_items = 0, o_ones = 0, o_diff = 0, o_odbg = 0, o_lists = 0, o_prefix = 0, o_region = 0;
     std::vector<size_t> o_ut, o_ut1, o_rr, o_qb;   // per bucket: X0, second X, r x r, bf16 Q (in the region)
     std::vector<int> rnr_list, rnc_list;           // RowNorm: row-wise and column-wise matrices
 };
@@ -541,6 +543,7 @@ muon_status plan_layout(muon_plan_s* p, Layout& L) {
     p->mat_bucket.resize(n);
     p->mat_item.resize(n);
     std::vector<std::pair<int, int>> group_rc;
+    std::vector<int> group_lv;   // per group: the matrices' opts.precision_of entry (0: the plan's rule)
     std::vector<std::vector<int>> group_mats;
     for (int i = 0; i < n; ++i) {
         MatDev& md = p->mats[i];
@@ -557,9 +560,13 @@ muon_status plan_layout(muon_plan_s* p, Layout& L) {
             md.scale = 0.2f * std::sqrt((float)std::max(fm, md.n));
         }
         size_t g = 0;
-        while (g < group_rc.size() && !(group_rc[g].first == md.r && group_rc[g].second == md.c)) ++g;
+        const int lv = p->prec_of.empty() ? 0 : p->prec_of[i];
+        while (g < group_rc.size() &&
+               !(group_rc[g].first == md.r && group_rc[g].second == md.c && group_lv[g] == lv))
+            ++g;
         if (g == group_rc.size()) {
             group_rc.push_back({md.r, md.c});
+            group_lv.push_back(lv);
             group_mats.emplace_back();
         }
         group_mats[g].push_back(i);
@@ -578,8 +585,11 @@ muon_status plan_layout(muon_plan_s* p, Layout& L) {
     const bool fused_ok = !p->opts.generic_small && !restarts;
     auto is_fused = [&](int r, int c) { return fused_ok && r <= kSmallMaxR && !is_f32(r, c); };
     // split precision of a batched bucket (opts.precision, opts.split_max_r)
-    auto split_of = [&](int r, int c) -> int {
-        if (is_fused(r, c) || is_f32(r, c) || p->opts.precision < 0) return 0;
+    // lv: the matrices' opts.precision_of entry (< 0 plain, 1 or 2 that level, 0 the plan's rule)
+    auto split_of = [&](int r, int c, int lv) -> int {
+        if (is_fused(r, c) || is_f32(r, c)) return 0;
+        if (lv != 0) return lv < 0 ? 0 : (lv >= 2 ? 2 : 1);
+        if (p->opts.precision < 0) return 0;
         if (p->opts.precision > 0) return p->opts.precision >= 2 ? 2 : 1;
         const int rmax = p->opts.split_max_r > 0 ? p->opts.split_max_r : 1024;
         return (4LL * c < 5LL * r && r <= rmax) ? 1 : 0;
@@ -588,9 +598,9 @@ muon_status plan_layout(muon_plan_s* p, Layout& L) {
     // (and second X) buffer and, batched, its seven r x r buffers, each rounded to 256
     // (split buffers hold two parts per matrix)
     const bool sharded = !p->full_rows.empty();   // RowNorm only: no NS buffers
-    auto bucket_bytes = [&](int r, int c, long long batch) -> long long {
+    auto bucket_bytes = [&](int r, int c, int lv, long long batch) -> long long {
         if (sharded) return 0;
-        const int sp = split_of(r, c);
+        const int sp = split_of(r, c, lv);
         const long long x = round_up(batch * r * round_up(c, 8) * 2 * (sp == 2 ? 2 : 1), 256);
         const long long rr = round_up(batch * r * round_up(r, 8) * 2 * (sp ? 2 : 1), 256);
         return (restarts ? 2 : 1) * x + (is_fused(r, c) || is_f32(r, c) ? 0 : 7 * rr);
@@ -630,6 +640,7 @@ muon_status plan_layout(muon_plan_s* p, Layout& L) {
     L.o_ptrs = take(sizeof(void*) * 3 * n);
     L.o_items = take(sizeof(int) * n);   // item -> plan matrix, per bucket slice
     L.o_ones = take(sizeof(float) * n);
+    L.o_diff = take(sizeof(double) * (2 + 2 * kDiffParts));
     L.o_odbg = p->opts.keep_update ? take([&] {
         size_t t = 0;
         for (int i = 0; i < n; ++i) t += (size_t)round_up(p->mats[i].m * p->mats[i].n * 4, 256);
@@ -653,13 +664,16 @@ muon_status plan_layout(muon_plan_s* p, Layout& L) {
     if (cap > 0) {
         region_cap = (double)cap - (double)fixed_bytes;
         double need = 0;
-        for (int i = 0; i < n; ++i) need = std::max(need, (double)bucket_bytes(p->mats[i].r, p->mats[i].c, 1));
+        for (int i = 0; i < n; ++i)
+            need = std::max(need, (double)bucket_bytes(p->mats[i].r, p->mats[i].c,
+                                                       p->prec_of.empty() ? 0 : p->prec_of[i], 1));
         if (region_cap < need) return MUON_ERR_OOM;   // the cap cannot hold even the largest single matrix
     }
     if (p->opts.chunks > 1) {   // about opts.chunks chunks, each at least one matrix
         double total = 0, largest = 0;
         for (int i = 0; i < n; ++i) {
-            const double b = (double)bucket_bytes(p->mats[i].r, p->mats[i].c, 1);
+            const double b =
+                (double)bucket_bytes(p->mats[i].r, p->mats[i].c, p->prec_of.empty() ? 0 : p->prec_of[i], 1);
             total += b;
             largest = std::max(largest, b);
         }
@@ -670,16 +684,16 @@ muon_status plan_layout(muon_plan_s* p, Layout& L) {
         long long used = 0;   // region bytes of the current chunk, exactly
         p->chunks.emplace_back();
         for (size_t g = 0; g < group_rc.size(); ++g) {
-            const int r = group_rc[g].first, c = group_rc[g].second;
+            const int r = group_rc[g].first, c = group_rc[g].second, lv = group_lv[g];
             int cur = -1;   // bucket of this group in the current chunk
             for (int i : group_mats[g]) {
                 const long long k = cur < 0 ? 0 : (long long)p->buckets[cur].mats.size();
-                long long grow = bucket_bytes(r, c, k + 1) - (k > 0 ? bucket_bytes(r, c, k) : 0);
+                long long grow = bucket_bytes(r, c, lv, k + 1) - (k > 0 ? bucket_bytes(r, c, lv, k) : 0);
                 if ((double)(used + grow) > region_cap && used > 0) {
                     p->chunks.emplace_back();
                     used = 0;
                     cur = -1;
-                    grow = bucket_bytes(r, c, 1);
+                    grow = bucket_bytes(r, c, lv, 1);
                 }
                 if (cur < 0) {
                     Bucket nb{};   // value-initialised: the tensor maps are filled in later
@@ -689,7 +703,7 @@ muon_status plan_layout(muon_plan_s* p, Layout& L) {
                     nb.ldu = (int)round_up(c, 8);
                     nb.fused = is_fused(r, c);
                     nb.f32 = is_f32(r, c);
-                    nb.split = split_of(r, c);
+                    nb.split = split_of(r, c, lv);
                     nb.chunk = (int)p->chunks.size() - 1;
                     p->buckets.push_back(nb);
                     cur = (int)p->buckets.size() - 1;
@@ -791,7 +805,9 @@ static muon_status plan_build(muon_plan_s* p, const muon_shape* shapes, int32_t 
     if (opts) p->opts = *opts;
     p->shapes.assign(shapes, shapes + n);
     if (p->opts.full_rows) p->full_rows.assign(p->opts.full_rows, p->opts.full_rows + n);
+    if (p->opts.precision_of) p->prec_of.assign(p->opts.precision_of, p->opts.precision_of + n);
     p->opts.full_rows = nullptr;   // read during creation only
+    p->opts.precision_of = nullptr;
 
     Layout L;
     {
@@ -818,6 +834,7 @@ static muon_status plan_build(muon_plan_s* p, const muon_shape* shapes, int32_t 
     p->d_transposed = reinterpret_cast<unsigned char*>(base + L.o_tr);
     p->d_ptrs = reinterpret_cast<void**>(base + L.o_ptrs);
     p->ones = reinterpret_cast<float*>(base + L.o_ones);
+    p->diff = reinterpret_cast<double*>(base + L.o_diff);
 
     std::vector<unsigned char> tr(n);
     for (int i = 0; i < n; ++i) tr[i] = (unsigned char)p->mats[i].transposed;
@@ -1088,7 +1105,9 @@ muon_status muon_plan_workspace_size(const muon_shape* shapes, int32_t n, muon_d
         if (opts) plan.opts = *opts;
         plan.shapes.assign(shapes, shapes + n);
         if (plan.opts.full_rows) plan.full_rows.assign(plan.opts.full_rows, plan.opts.full_rows + n);
+        if (plan.opts.precision_of) plan.prec_of.assign(plan.opts.precision_of, plan.opts.precision_of + n);
         plan.opts.full_rows = nullptr;
+        plan.opts.precision_of = nullptr;
         Layout L;
         const muon_status st = plan_layout(&plan, L);
         if (st != MUON_OK) return st;
@@ -1779,6 +1798,20 @@ muon_status muon_debug_copy_update(muon_plan p, int32_t i, float* dst, void* str
         cudaSuccess)
         return MUON_ERR_CUDA;
     return cudaStreamSynchronize(s) == cudaSuccess ? MUON_OK : MUON_ERR_CUDA;
+}
+
+muon_status muon_debug_update_error(muon_plan p, int32_t i, const float* ref, double* rel, void* stream) {
+    if (!p || !ref || !rel || i < 0 || i >= (int)p->shapes.size()) return MUON_ERR_INVALID_ARG;
+    if (!p->opts.keep_update || !p->full_rows.empty()) return MUON_ERR_INVALID_ARG;
+    const Bucket& b = p->buckets[p->mat_bucket[i]];
+    const long long numel = (long long)b.r * b.c;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    MUON_TRY(launch_sq_diff(b.Odbg + (size_t)p->mat_item[i] * numel, ref, numel, p->diff, s));
+    double sums[2] = {0.0, 0.0};
+    MUON_TRY(cudaMemcpyAsync(sums, p->diff, sizeof(sums), cudaMemcpyDeviceToHost, s));
+    MUON_TRY(cudaStreamSynchronize(s));
+    *rel = sums[1] > 0.0 ? std::sqrt(sums[0] / sums[1]) : std::sqrt(sums[0]);
+    return MUON_OK;
 }
 
 muon_status muon_debug_copy_workspace(muon_plan p, int32_t i, int32_t which, void* dst, int32_t* ld,

@@ -579,6 +579,52 @@ cudaError_t launch_rownorm_colapply(const ElemArgs& a, long long blocks, cudaStr
         return launch_pdl(k_rownorm_colapply<false>, dim3((unsigned)blocks), dim3(kElemThreads), 0, s, a);
 }
 
+// ------------------------------------------------------------------ relative difference (debug / tuning)
+// Sums of (a - b)^2 and b^2 over n floats in fp64: kDiffParts blocks write their partial
+// sums (fixed order inside a block), one block adds them in order into out[0], out[1].
+__global__ void __launch_bounds__(kElemThreads) k_diff_partial(const float* a, const float* b, long long n,
+                                                               double* part) {
+    __shared__ double sd[kElemThreads], sb[kElemThreads];
+    double d = 0.0, bb = 0.0;
+    for (long long e = (long long)blockIdx.x * kElemThreads + threadIdx.x; e < n;
+         e += (long long)gridDim.x * kElemThreads) {
+        const double x = a[e], y = b[e];
+        d += (x - y) * (x - y);
+        bb += y * y;
+    }
+    sd[threadIdx.x] = d;
+    sb[threadIdx.x] = bb;
+    __syncthreads();
+    for (int w = kElemThreads / 2; w > 0; w >>= 1) {
+        if ((int)threadIdx.x < w) {
+            sd[threadIdx.x] += sd[threadIdx.x + w];
+            sb[threadIdx.x] += sb[threadIdx.x + w];
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        part[2 * blockIdx.x] = sd[0];
+        part[2 * blockIdx.x + 1] = sb[0];
+    }
+}
+
+__global__ void k_diff_final(const double* part, int nparts, double* out) {
+    if (threadIdx.x != 0) return;
+    double d = 0.0, bb = 0.0;
+    for (int k = 0; k < nparts; ++k) {
+        d += part[2 * k];
+        bb += part[2 * k + 1];
+    }
+    out[0] = d;
+    out[1] = bb;
+}
+
+cudaError_t launch_sq_diff(const float* a, const float* b, long long n, double* scratch, cudaStream_t s) {
+    k_diff_partial<<<kDiffParts, kElemThreads, 0, s>>>(a, b, n, scratch + 2);
+    k_diff_final<<<1, 32, 0, s>>>(scratch + 2, kDiffParts, scratch);
+    return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ bounded-wait self test
 // One wait on an mbarrier whose phase nothing completes: the bounded wait gives
 // up after limit_ns, raises the abort flag and records kStatusTimeoutSelftest in

@@ -286,6 +286,11 @@ struct F32Launch {
 cudaError_t ns_f32_prepare();   // sets the kernel's dynamic shared-memory limit
 cudaError_t ns_f32_launch(const F32Launch& L, int grid, cudaStream_t s);
 
+// Sums of (a - b)^2 and b^2 over n floats (fp64, fixed order) into scratch[0], scratch[1];
+// scratch holds 2 + 2 kDiffParts doubles of device memory.
+constexpr int kDiffParts = 256;
+cudaError_t launch_sq_diff(const float* a, const float* b, long long n, double* scratch, cudaStream_t s);
+
 // Remembers a CUDA error for muon_last_error_detail (this host thread's last one).
 void record_cuda_error(cudaError_t e);
 

@@ -26,6 +26,7 @@ int main(void) {
     FIELD(muon_plan_opts, precision);
     FIELD(muon_plan_opts, split_max_r);
     FIELD(muon_plan_opts, full_rows);
+    FIELD(muon_plan_opts, precision_of);
     printf("sizeof.muon_plan_info_t %zu\n", sizeof(muon_plan_info_t));
     FIELD(muon_plan_info_t, n_matrices);
     FIELD(muon_plan_info_t, n_buckets);

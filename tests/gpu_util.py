@@ -33,7 +33,7 @@ def host_inputs(shapes, grad_dtype, base_seed, step=0):
 def run_step(shapes, grad_dtype="bf16", base_seed=100, ns_steps=5, mode="ns", lr=LR, wd=WD, mu=MU,
              eps=1e-8, keep_update=True, inputs=None, plan=None, single_sm_gemm=False, generic_small=False,
              chain_clusters=0, workspace_bytes=0, coeffs=None, restart=0, max_ns_steps=0, small_fp32=0,
-             precision=0, full_symmetric=False):
+             precision=0, full_symmetric=False, precision_of=None):
     """One library step on copies of the seeded inputs; returns a dict of CPU results."""
     import torch
     import matrix_orthogonalising_optimizer_muon_gb300 as lib
@@ -45,7 +45,7 @@ def run_step(shapes, grad_dtype="bf16", base_seed=100, ns_steps=5, mode="ns", lr
         plan = lib.MuonPlan(shapes, grad_dtype, keep_update=keep_update, single_sm_gemm=single_sm_gemm,
                             generic_small=generic_small, chain_clusters=chain_clusters,
                             workspace_bytes=workspace_bytes, max_ns_steps=max_ns_steps, small_fp32=small_fp32,
-                            precision=precision, full_symmetric=full_symmetric)
+                            precision=precision, full_symmetric=full_symmetric, precision_of=precision_of)
     W = [w.cuda() for w, _, _ in inputs]
     G = [g.cuda() for _, g, _ in inputs]
     M = [m.cuda() for _, _, m in inputs]

@@ -1068,3 +1068,32 @@ def test_dim0_shard_rownorm_matches_the_full_matrix():
         assert rel(m, ref[i][1]) <= TOL_FP32, (full[i], rel(m, ref[i][1]))
         assert rel(w, ref[i][0]) <= TOL_FP32, (full[i], rel(w, ref[i][0]))
     plan.close()
+
+
+def test_select_precision_splits_only_where_the_plain_recipe_misses_the_tolerance():
+    """select_precision on the caller's data: per oriented shape, the plain recipe, split
+    level 1 and the reference (level 2) run on a sample; 256 x 256 (plain measured at
+    2.1e-2) must take level 1, the rectangular 300 x 700 (3.5e-3) stays plain.  The chosen
+    per-matrix levels then build the plan (precision_of), which meets the oracle's bar on
+    every matrix, and the caller's tensors are left untouched by the selection."""
+    import torch
+    import matrix_orthogonalising_optimizer_muon_gb300 as lib
+    shapes = [(256, 256)] * 3 + [(300, 700)] * 2 + [(1024, 1024)] + [(96, 96)]
+    inputs = host_inputs(shapes, "bf16", base_seed=74)
+    W = [w.cuda() for w, _, _ in inputs]
+    G = [g.cuda() for _, g, _ in inputs]
+    M = [m.cuda() for _, _, m in inputs]
+    W0, M0 = [w.clone() for w in W], [m.clone() for m in M]
+    levels, report = lib.select_precision(shapes, "bf16", W, G, M, tol=1e-2, sample=2)
+    for a, b in zip(W + M, W0 + M0):
+        assert torch.equal(a, b)
+    assert report[(256, 256)]["chosen"] == 1, report[(256, 256)]
+    assert report[(300, 700)]["chosen"] == -1, report[(300, 700)]
+    assert report[(256, 256)]["candidates"][-1]["err"] > 1e-2
+    assert report[(256, 256)]["candidates"][1]["err"] <= 1e-2
+    assert levels[:3] == [1] * 3 and levels[3:5] == [-1] * 2
+    res = run_step(shapes, "bf16", inputs=inputs, precision_of=levels)
+    split_shapes = {min(s) for s, lv in zip(shapes, levels) if lv > 0 and min(s) > 128}
+    assert res["plan"].info()["split_buckets"] == len(split_shapes)
+    for i in range(len(shapes)):
+        assert_ns(res, i)

@@ -206,3 +206,16 @@ def test_dim0_shard_plans_hold_no_newton_schulz_buffers():
     assert sharded < plain and sharded < 4 << 20
     with pytest.raises(mu.MuonError):
         ws(shards, full_rows=[256, 2048, 4096])   # a shard of 512 rows of a 256-row matrix
+
+
+def test_precision_of_splits_buckets_per_matrix():
+    """opts.precision_of: matrices of one oriented shape with different levels form separate
+    buckets, each sized for its own level."""
+    sq = [(256, 256)] * 2
+    assert ws(sq, precision_of=[-1, 1])["n_buckets"] == 2
+    assert ws(sq, precision_of=[1, 1])["n_buckets"] == 1
+    rr = r256(256 * 256 * 2)   # one plain r x r buffer of one matrix
+    plain2 = ws(sq, precision_of=[-1, -1])["workspace_bytes"]
+    mixed = ws(sq, precision_of=[-1, 1])["workspace_bytes"]
+    assert mixed - plain2 == 7 * rr                  # the split matrix's seven buffers hold two parts
+    assert ws(sq, precision_of=[0, 0]) == ws(sq)     # 0: the plan-wide rule
