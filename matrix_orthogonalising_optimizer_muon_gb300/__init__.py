@@ -24,7 +24,7 @@ from .build import LIB, build, up_to_date
 
 __all__ = [
     "MuonError", "MuonPlan", "PeriodicRowNormMuon", "DistributedMuon", "ShardedRowNorm", "partition_owners",
-    "select_precision",
+    "select_precision", "measure_costs",
     "plan_workspace_size", "load", "build",
     "MUON_OK", "MUON_ERR_INVALID_ARG", "MUON_ERR_UNSUPPORTED", "MUON_ERR_OOM",
     "MUON_ERR_CUDA", "MUON_ERR_TIMEOUT", "MUON_ERR_NONFINITE", "MUON_F32", "MUON_BF16",
@@ -698,3 +698,41 @@ def select_precision(shapes, grad_dtype, params, grads, momentum, mu: float = DE
             levels[i] = chosen
         report[key] = {"chosen": chosen, "candidates": rep}
     return levels, report
+
+
+def measure_costs(shapes, grad_dtype: str = "bf16", sample: int = 4, reps: int = 2, ns_steps: int = DEFAULT_NS_STEPS,
+                  **plan_opts):
+    """Measured cost (milliseconds per matrix) of every matrix's NS step on this GPU, for
+    ``partition_owners`` / ``DistributedMuon(costs=...)`` (DMuon technical summary sec. 2.3:
+    the owner assignment balances measured per-shape times).  For every oriented shape, a
+    plan over up to ``sample`` matrices of that shape (scratch tensors, seeded Gaussian
+    values) is timed with CUDA events over ``reps`` steps after one warm-up; each matrix of
+    the shape costs that time divided by the matrices timed."""
+    import torch
+    shapes = [(int(m), int(n)) for m, n in shapes]
+    groups = {}
+    for i, (m, n) in enumerate(shapes):
+        groups.setdefault((min(m, n), max(m, n)), []).append(i)
+    gdt = torch.bfloat16 if grad_dtype == "bf16" else torch.float32
+    per_shape = {}
+    for key, idx in groups.items():
+        sub = [shapes[i] for i in idx[:sample]]
+        gen = torch.Generator(device="cuda").manual_seed(len(per_shape) + 1)
+        W = [torch.randn(s, device="cuda", generator=gen) * 0.02 for s in sub]
+        G = [(torch.randn(s, device="cuda", generator=gen) * 1e-3).to(gdt) for s in sub]
+        M = [torch.randn(s, device="cuda", generator=gen) * 1e-3 for s in sub]
+        plan = MuonPlan(sub, grad_dtype, **plan_opts)
+        try:
+            plan.step(W, G, M, 0.02, 0.1, DEFAULT_MU, ns_steps)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                plan.step(W, G, M, 0.02, 0.1, DEFAULT_MU, ns_steps)
+            e1.record()
+            e1.synchronize()
+            plan.sync()
+            per_shape[key] = e0.elapsed_time(e1) / reps / len(sub)
+        finally:
+            plan.close()
+        del W, G, M
+    return [per_shape[(min(m, n), max(m, n))] for m, n in shapes]

@@ -175,11 +175,11 @@ __global__ void __launch_bounds__(kElemThreads) k_momentum_tiles(const ElemArgs 
     float ss = 0.f;
     const bool full = (i0 + kTileRows <= md.m) && (j0 + kTile <= md.n) && (md.n % 4 == 0) && g_vec_ok<BF16>(G) &&
                       aligned16(M);
-    const int cq = t & 15, rr = t >> 4;
+    const int cq = t % kTileTpr, rr = t / kTileTpr;
     if (full) {
 #pragma unroll
-        for (int p = 0; p < kTileRows / 16; ++p) {
-            const long long i = i0 + rr + 16 * p;
+        for (int p = 0; p < kTileRows / kTileRpp; ++p) {
+            const long long i = i0 + rr + kTileRpp * p;
             const long long e = i * md.n + j0 + 4 * cq;
             const float4 g = load_g4<BF16>(G, e);
             float4 m = *reinterpret_cast<float4*>(M + e);
@@ -187,15 +187,15 @@ __global__ void __launch_bounds__(kElemThreads) k_momentum_tiles(const ElemArgs 
             *reinterpret_cast<float4*>(M + e) = m;
             const float u0 = mu * m.x + g.x, u1 = mu * m.y + g.y, u2 = mu * m.z + g.z, u3 = mu * m.w + g.w;
             ss += u0 * u0 + u1 * u1 + u2 * u2 + u3 * u3;
-            tile[4 * cq + 0][rr + 16 * p] = u0;
-            tile[4 * cq + 1][rr + 16 * p] = u1;
-            tile[4 * cq + 2][rr + 16 * p] = u2;
-            tile[4 * cq + 3][rr + 16 * p] = u3;
+            tile[4 * cq + 0][rr + kTileRpp * p] = u0;
+            tile[4 * cq + 1][rr + kTileRpp * p] = u1;
+            tile[4 * cq + 2][rr + kTileRpp * p] = u2;
+            tile[4 * cq + 3][rr + kTileRpp * p] = u3;
         }
     } else {
 #pragma unroll
-        for (int p = 0; p < kTileRows / 16; ++p) {
-            const long long i = i0 + rr + 16 * p;
+        for (int p = 0; p < kTileRows / kTileRpp; ++p) {
+            const long long i = i0 + rr + kTileRpp * p;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const long long j = j0 + 4 * cq + q;
@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(kElemThreads) k_momentum_tiles(const ElemArgs 
                     u = mu * m + g;
                     ss += u * u;
                 }
-                tile[4 * cq + q][rr + 16 * p] = u;
+                tile[4 * cq + q][rr + kTileRpp * p] = u;
             }
         }
     }

@@ -250,12 +250,19 @@ cudaError_t launch_rownorm_colapply(const ElemArgs& a, long long blocks, cudaStr
 constexpr int kElemThreads = 256;
 constexpr int kMomVecPerThread = 4;                                  // 8-element vectors per thread
 constexpr long long kMomElemsPerBlock = 8LL * kElemThreads * kMomVecPerThread;   // rows kernel
-constexpr int kTile = 64;                                            // transpose tile: 64 stored columns
+#ifndef MUON_TILE_COLS
+#define MUON_TILE_COLS 64
+#endif
+constexpr int kTile = MUON_TILE_COLS;                                // transpose tile: stored columns ...
+constexpr int kTileTpr = kTile / 4;                                  // threads per stored row (float4 each)
+constexpr int kTileRpp = kElemThreads / kTileTpr;                    // stored rows per pass of the block
 #ifndef MUON_TILE_ROWS
 #define MUON_TILE_ROWS 128
 #endif
 constexpr int kTileRows = MUON_TILE_ROWS;                            // ... x kTileRows stored rows
 static_assert(kTileRows % 32 == 0 && kTileRows <= 128, "transpose tile rows");
+static_assert(kTile % 32 == 0 && kTile <= 128 && kTileRows % kTileRpp == 0 && kTile * (kTileRows + 1) * 4 <= 40000,
+              "transpose tile columns");
 constexpr int kColSlab = 64;                                         // RowNorm column-stat rows per block
 constexpr int kColWidth = 4 * kElemThreads;                          // columns per column-stat block
 constexpr long long kApplyElemsPerBlock = 4LL * kElemThreads * 4;    // RowNorm col apply

@@ -1097,3 +1097,17 @@ def test_select_precision_splits_only_where_the_plain_recipe_misses_the_toleranc
     assert res["plan"].info()["split_buckets"] == len(split_shapes)
     for i in range(len(shapes)):
         assert_ns(res, i)
+
+
+def test_measured_costs_drive_the_owner_partition():
+    """measure_costs times every oriented shape on this GPU; the owner partition over those
+    costs covers every matrix once and keeps the ranks' loads within the largest cost."""
+    import matrix_orthogonalising_optimizer_muon_gb300 as lib
+    shapes = [(512, 2048)] * 6 + [(2048, 512)] * 2 + [(1024, 1024)] * 3 + [(128, 1024)] * 8
+    costs = lib.measure_costs(shapes, "bf16", sample=2, reps=2)
+    assert len(costs) == len(shapes) and all(c > 0 for c in costs)
+    assert costs[0] == costs[6]                          # one oriented shape, one cost
+    owners, loads = lib.partition_owners(shapes, 3, costs)
+    assert sorted(set(owners)) == [0, 1, 2]
+    assert abs(sum(loads) - sum(costs)) < 1e-6 * sum(costs)
+    assert max(loads) - min(loads) <= max(costs) + 1e-9
