@@ -296,13 +296,19 @@ __global__ void __launch_bounds__(kElemThreads) k_rownorm_rows(const ElemArgs a)
                      aligned16(M) && aligned16(W);
     float ss = 0.f;
     if (reg) {
-        // W is loaded with G and M, so all three streams are in flight across the
-        // row reduction
+        // Rows of up to 4096 elements load W with G and M, so all three streams are in
+        // flight across the row reduction.  Longer rows (VEC = 8) load W after it: holding
+        // W too took 80-94 registers (3 blocks per SM) against 64 (4 blocks), and the
+        // extra resident rows keep more loads in flight (RowNorm step of the DiT set 7.10
+        // -> 6.85 ms in a same-box comparison).
+        constexpr bool kEarlyW = VEC < 8;
         float4 u[VEC], wv[VEC];
+        if (kEarlyW) {
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) {
-            const long long j = 4LL * (v * kElemThreads + t);
-            if (j < n) wv[v] = *reinterpret_cast<const float4*>(W + j);
+            for (int v = 0; v < VEC; ++v) {
+                const long long j = 4LL * (v * kElemThreads + t);
+                if (j < n) wv[v] = *reinterpret_cast<const float4*>(W + j);
+            }
         }
 #pragma unroll
         for (int v = 0; v < VEC; ++v) {
@@ -324,7 +330,7 @@ __global__ void __launch_bounds__(kElemThreads) k_rownorm_rows(const ElemArgs a)
         for (int v = 0; v < VEC; ++v) {
             const long long j = 4LL * (v * kElemThreads + t);
             if (j < n) {
-                float4 w = wv[v];
+                float4 w = kEarlyW ? wv[v] : *reinterpret_cast<const float4*>(W + j);
                 w.x = w.x - lr * (k * u[v].x + wd * w.x);
                 w.y = w.y - lr * (k * u[v].y + wd * w.y);
                 w.z = w.z - lr * (k * u[v].z + wd * w.z);
