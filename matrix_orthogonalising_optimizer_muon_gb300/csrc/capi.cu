@@ -405,9 +405,12 @@ struct Grouper {
     // caller); the pair kernel then writes them with TMA stores.
     // a4 / b4: the operands' 4-D maps, used by lower-triangle launches (B of an
     // MN-major problem through b4.t).
+    // og: for a polynomial product, the store map of its G' input (32 x 32 boxes), through
+    // which the pair kernel's epilogue loads G' by TMA.
     void add(const CUtensorMap& a128, const CUtensorMap& b256, const CUtensorMap& b128, GemmProblem q,
-             const CUtensorMap* oc, const CUtensorMap* oc2, Maps4 a4, Maps4 b4) {
+             const CUtensorMap* oc, const CUtensorMap* oc2, Maps4 a4, Maps4 b4, const CUtensorMap* og = nullptr) {
         if (q.a_split || q.b_split || q.out_split) q.tma_out = 0;   // split parts: per-thread stores
+        q.gin_tma = 0;
         if (q.M > kBM && p->pair_clusters > 0) {
             if (L2.nprob == kMaxProblems) flush2();
             q.tiles_m = (int)ceil_div(q.M, 256);
@@ -417,6 +420,10 @@ struct Grouper {
             if (q.tma_out) {
                 L2.mapC[L2.nprob] = *oc;
                 if (oc2) L2.mapC2[L2.nprob] = *oc2;
+                if (og && q.epi == kEpiPoly) {
+                    L2.mapG[L2.nprob] = *og;
+                    q.gin_tma = 1;
+                }
             }
             if (lower) {
                 q.lower_out = q.sym;
@@ -1481,7 +1488,7 @@ static muon_status ns_step(muon_plan p, float* const* params, const void* const*
                         // fp16 P (and the fp16 copy Q_1): TMA stores; P with a bf16 Q_1 (J = 1): per thread
                         q.tma_out = q.Cb ? 0 : (kTmaOutC | (q.C2 ? kTmaOutC2 : 0));
                         const Maps4 g4{&b.gk[gc], &b.gt[gc], true};
-                        g.add(b.ga[gc], b.gb[gc], b.ga[gc], q, &b.op, q.C2 ? &b.oq[0] : nullptr, g4, g4);
+                        g.add(b.ga[gc], b.gb[gc], b.ga[gc], q, &b.op, q.C2 ? &b.oq[0] : nullptr, g4, g4, &b.og[gc]);
                     }
                     g.flush();
                     if (g.st != MUON_OK) return g.st;

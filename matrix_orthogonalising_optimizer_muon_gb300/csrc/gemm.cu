@@ -227,6 +227,7 @@ __global__ void __maxnreg__(168) gemm_kernel(const __grid_constant__ GemmLaunch 
                     tmem_ld_wait();
                     apply_store(P, ac, tc.item, row, col0, raw, w);
                 } else {
+                    tmem_ld32(tbase + cc, raw);
                     tmem_ld_wait();
                     epilogue_chunk(P, tc.item, row, col0, raw);
                 }
@@ -260,10 +261,12 @@ struct Gemm2Cfg {
     static constexpr int B_BYTES = 128 * BK * ESZ;       // this CTA's half of B
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int MN_CHUNK_BYTES = 64 * BK * ESZ;
-    static constexpr int OUT_OFFSET = kStages2 * STAGE_BYTES;    // per epilogue warp: 2 x 2 KB store staging
-    static constexpr int OUT_BYTES = kEpiWarps * 4096;
+    // per epilogue warp: 2 x 2 KB store staging, then 2 x 2 KB of the polynomial's G' blocks
+    static constexpr int OUT_OFFSET = kStages2 * STAGE_BYTES;
+    static constexpr int OUT_WARP = 8192;
+    static constexpr int OUT_BYTES = kEpiWarps * OUT_WARP;
     static constexpr int BAR_OFFSET = OUT_OFFSET + OUT_BYTES;
-    static constexpr int SMEM_BYTES = BAR_OFFSET + 256 + 1024;
+    static constexpr int SMEM_BYTES = BAR_OFFSET + 512 + 1024;
 };
 static_assert(Gemm2Cfg::SMEM_BYTES <= 232448, "CTA-pair kernel exceeds the shared memory of one CTA");
 
@@ -343,6 +346,7 @@ __global__ void __maxnreg__(168) gemm2_kernel(const __grid_constant__ GemmLaunch
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    uint64_t* gbar = reinterpret_cast<uint64_t*>(tmem_slot + 2);   // per epilogue warp: its two G' blocks
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -364,6 +368,7 @@ __global__ void __maxnreg__(168) gemm2_kernel(const __grid_constant__ GemmLaunch
             mbar_init(tempty + a, 2 * kEpiWarps);   // leader: every epilogue warp of both CTAs
         }
         mbar_init(drain, 1);
+        for (int w = 0; w < 2 * kEpiWarps; ++w) mbar_init(gbar + w, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -507,27 +512,51 @@ __global__ void __maxnreg__(168) gemm2_kernel(const __grid_constant__ GemmLaunch
         const int wq = warp & 3;
         const int c_begin = ((warp - 2) >> 2) * (kBN * 4 / kEpiWarps);
         const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), lead);
-        uint8_t* stage_l = smem + Cfg::OUT_OFFSET + (warp - 2) * 4096;
+        uint8_t* stage_l = smem + Cfg::OUT_OFFSET + (warp - 2) * Cfg::OUT_WARP;
+        uint8_t* gin_buf = stage_l + 4096;            // two 2 KB blocks of G'
+        uint64_t* gb = gbar + 2 * (warp - 2);
+        uint32_t gph = 0;                             // phase bit per G' buffer (bits 0, 1)
+        uint32_t gpend = 0;                           // G' loads in flight (bits 0, 1)
         int local = 0;
         for (int t = cluster_id; t < L.total_tiles; t += nclusters, ++local) {
             const TileCoord tc = decode(t);
             const GemmProblem& P = L.prob[tc.p];
             const uint32_t acc = local & 1;
             const uint32_t aph = (local >> 1) & 1u;
-            if (P.epi == kEpiApply)   // (the polynomial's G' is prefetched by the producer)
+            if (BF16 && P.epi == kEpiApply)   // (the polynomial's G' is prefetched by the producer)
                 prefetch_epilogue_inputs(P, tc.item, tc.m0 + wq * 32, tc.n0 + c_begin, kBN * 4 / kEpiWarps, lane);
+            // The polynomial's G' blocks (rows R0 .. R0 + 31, this warp's 32-column chunks) come
+            // by TMA into the warp's two G' buffers, the first two while the MMAs run, each next
+            // one as soon as its buffer has been read.  gn: the chunks this warp processes.
+            int gn = 0;
+            const bool gt = !BF16 && P.epi == kEpiPoly && P.gin_tma;
+            if (gt) {
+                const int wrmax = tc.m0 + wq * 32 + 31;
+                while (gn < 4 && tc.n0 + c_begin + 32 * gn < P.N && tc.n0 + c_begin + 32 * gn <= wrmax) ++gn;
+                for (int k = 0; k < 2 && k < gn; ++k) {
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(gb + k, 2048);
+                        tma_load_3d(gin_buf + 2048 * k, &L.mapG[tc.p], gb + k, tc.n0 + c_begin + 32 * k,
+                                    tc.m0 + wq * 32, tc.item);
+                    }
+                    gpend |= 1u << k;
+                }
+            }
             if (!mbar_wait_idle(tfull + acc, aph, abort_flag, L.status, kStatusTimeoutEpilogue, true)) break;
             tc_fence_after();
             const int row = tc.m0 + wq * 32 + lane;
             const int warp_row_max = tc.m0 + wq * 32 + 31;
             const uint32_t tbase = tmem_base + acc * kBN + (static_cast<uint32_t>(wq * 32) << 16);
-            const WPiece wc = w_piece_ctx(P, P.epi == kEpiApply ? tc.item : -1);
-            for (int cc = c_begin; cc < c_begin + kBN * 4 / kEpiWarps; cc += 32) {
+            // fp16 launches carry only r x r products (kEpiPoly, kEpiPlain); the final product's
+            // W pieces exist in the bf16 instantiations alone
+            const WPiece wc = w_piece_ctx(P, BF16 && P.epi == kEpiApply ? tc.item : -1);
+            bool gabort = false;
+            for (int cc = c_begin, kc = 0; cc < c_begin + kBN * 4 / kEpiWarps; cc += 32, ++kc) {
                 const int col0 = tc.n0 + cc;
                 if (col0 >= P.N) break;
                 if (P.sym && col0 > warp_row_max) break;
                 uint32_t raw[32];
-                if (P.epi == kEpiApply) {
+                if (BF16 && P.epi == kEpiApply) {
                     // W piece (rows R0.., columns col0..) in with coalesced cp.async, updated
                     // in shared memory, out with coalesced 16-byte stores
                     const int R0 = tc.m0 + wq * 32;
@@ -542,16 +571,40 @@ __global__ void __maxnreg__(168) gemm2_kernel(const __grid_constant__ GemmLaunch
                     __syncwarp();
                     continue;
                 }
-                tmem_ld32(tbase + cc, raw);
                 if (P.tma_out) {
+                    const uint8_t* gin_s = nullptr;
+                    if (!BF16 && gt) {   // this chunk's G' block (chunk kc, buffer kc % 2)
+                        const uint32_t bsel = kc & 1;
+                        if (!mbar_wait_idle(gb + bsel, (gph >> bsel) & 1u, abort_flag, L.status, kStatusTimeoutEpilogue,
+                                            false)) {
+                            gabort = true;
+                            break;
+                        }
+                        gph ^= 1u << bsel;
+                        gpend &= ~(1u << bsel);
+                        gin_s = gin_buf + 2048 * bsel;
+                    }
+                    tmem_ld32(tbase + cc, raw);
                     tmem_ld_wait();
                     epilogue_chunk_tma(P, &L.mapC[tc.p], &L.mapC2[tc.p], tc.item, tc.m0 + wq * 32, col0, lane, raw,
-                                       stage_l, stage_l + 2048);
+                                       stage_l, stage_l + 2048, gin_s);
+                    if (!BF16 && gt && kc + 2 < gn) {   // every lane has read the block: load chunk kc + 2 into it
+                        const uint32_t bsel = kc & 1;
+                        __syncwarp();
+                        if (lane == 0) {
+                            mbar_arrive_expect_tx(gb + bsel, 2048);
+                            tma_load_3d(gin_buf + 2048 * bsel, &L.mapG[tc.p], gb + bsel, col0 + 64, tc.m0 + wq * 32,
+                                        tc.item);
+                        }
+                        gpend |= 1u << bsel;
+                    }
                 } else {
+                    tmem_ld32(tbase + cc, raw);
                     tmem_ld_wait();
                     epilogue_chunk(P, tc.item, row, col0, raw);
                 }
             }
+            if (gabort) break;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -561,6 +614,8 @@ __global__ void __maxnreg__(168) gemm2_kernel(const __grid_constant__ GemmLaunch
                     mbar_arrive_remote(tempty_leader + acc * 8);
             }
         }
+        for (int k = 0; k < 2; ++k)   // G' loads still in flight after an abort
+            if (gpend & (1u << k)) mbar_drain(gb + k, (gph >> k) & 1u);
         if (lane == 0) bulk_wait<0>();   // TMA stores of the staging complete before the CTA exits
     }
 

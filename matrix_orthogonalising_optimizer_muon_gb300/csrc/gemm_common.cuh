@@ -243,10 +243,15 @@ __device__ __forceinline__ void prefetch_epilogue_inputs(const GemmProblem& P, i
     }
 }
 
+__device__ __forceinline__ uint32_t stage64_off(int y, int x);
+
 // Values of one 32-column chunk of a symmetric result for this thread's row:
 // kEpiSyrk scales, kEpiPoly adds a I + b' G', kEpiPlain passes the accumulator.
+// gin_s (kEpiPoly, may be null): the warp's 32 x 32 block of G' already in shared
+// memory (64-byte-swizzled rows, row = lane), instead of per-thread global loads.
 __device__ __forceinline__ void epilogue_values(const GemmProblem& P, int item, int row, int col0,
-                                                const uint32_t (&raw)[32], float (&v)[32]) {
+                                                const uint32_t (&raw)[32], float (&v)[32],
+                                                const uint8_t* gin_s = nullptr) {
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(raw[j]);
     if (P.epi == kEpiSyrk) {
@@ -254,6 +259,20 @@ __device__ __forceinline__ void epilogue_values(const GemmProblem& P, int item, 
         const float k = P.out_scale * al * al;
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] *= k;
+    } else if (P.epi == kEpiPoly && gin_s != nullptr) {
+        const int lane = threadIdx.x & 31;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 t = *reinterpret_cast<const uint4*>(gin_s + stage64_off(lane, 8 * q));
+            const uint32_t w4[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
+                const int j = 8 * q + 2 * e;
+                v[j] = P.coef_c * v[j] + P.coef_b * f.x + ((col0 + j == row) ? P.coef_a : 0.f);
+                v[j + 1] = P.coef_c * v[j + 1] + P.coef_b * f.y + ((col0 + j + 1 == row) ? P.coef_a : 0.f);
+            }
+        }
     } else if (P.epi == kEpiPoly) {
         // P = a I + b' G' + c' G'^2, with G' read (8 values at a time) from the fp16
         // input the MMA used
@@ -353,9 +372,10 @@ __device__ __forceinline__ uint32_t stage64_off(int y, int x) {   // 2-byte elem
 
 __device__ __forceinline__ void epilogue_chunk_tma(const GemmProblem& P, const CUtensorMap* mc,
                                                    const CUtensorMap* mc2, int item, int R0, int col0, int lane,
-                                                   const uint32_t (&raw)[32], uint8_t* stl, uint8_t* stm) {
+                                                   const uint32_t (&raw)[32], uint8_t* stl, uint8_t* stm,
+                                                   const uint8_t* gin_s = nullptr) {
     float v[32];
-    epilogue_values(P, item, R0 + lane, col0, raw, v);
+    epilogue_values(P, item, R0 + lane, col0, raw, v, gin_s);
     const bool diag = col0 == R0;
     // the transposed block goes to the mirror position unless the output is stored as
     // its lower triangle and the block lies below the diagonal 256 x 256 tile

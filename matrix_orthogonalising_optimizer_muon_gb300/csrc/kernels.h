@@ -26,7 +26,7 @@ constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kStages = 4;      // 1-SM kernel: 48 KB per stage
 #ifndef MUON_PAIR_STAGES
-#define MUON_PAIR_STAGES 6
+#define MUON_PAIR_STAGES 5
 #endif
 constexpr int kStages2 = MUON_PAIR_STAGES;   // 2-SM kernel: 32 KB per stage per CTA
 constexpr int kMaxProblems = 8;
@@ -129,6 +129,9 @@ struct GemmProblem {
     // out_split: the output (C, C2, Cb) is written as hi = round(v), lo = round(v - hi).
     // kEpiPoly reads its G' input split when a_split is set.  Per-thread stores only.
     int a_split, b_split, out_split;
+    // kEpiPoly on the CTA-pair kernel with TMA-stored output: the G' input is read by TMA
+    // (mapG, 32 x 32 boxes) into the epilogue warp's shared memory, one chunk ahead
+    int gin_tma;
 };
 constexpr int kTmaOutC = 1, kTmaOutC2 = 2, kTmaOutBf16 = 4;
 
@@ -160,6 +163,7 @@ struct GemmLaunch {
     // shared memory (mapBt also serves an MN-major B such as X0 in the final product).
     CUtensorMap mapAt[kMaxProblems];
     CUtensorMap mapBt[kMaxProblems];
+    CUtensorMap mapG[kMaxProblems];    // kEpiPoly with gin_tma: its G' input, 32 x 32 boxes (64-byte swizzle)
     GemmProblem prob[kMaxProblems];
     int nprob;
     int total_tiles;
