@@ -89,6 +89,20 @@ bool make_map4(CUtensorMap* map, void* base, bool bf16, uint64_t cols, uint64_t 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// W of one matrix (fp32, stored m x n row-major, 16-byte aligned, n % 4 == 0) in 32 x 32
+// boxes with 128-byte swizzle: exactly the staged layout of a W piece of the final product.
+bool make_w_piece_map(CUtensorMap* map, void* W, uint64_t m, uint64_t n) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {n, m};
+    cuuint64_t strides[1] = {n * 4};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, W, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 // Store map over `batch` r x r row-major matrices (leading dim ld): 32 x 32 boxes
 // in the 64-byte-swizzled shared layout the pair kernel's epilogue stages.
 bool make_out_map(CUtensorMap* map, void* base, bool bf16, uint64_t r, uint64_t batch, uint64_t ld) {
@@ -212,6 +226,11 @@ struct muon_plan_s {
     std::vector<Chunk> chunks;
 
     void** h_pinned = nullptr;
+    // per matrix: W piece map of the final product (re-encoded when the parameter pointers
+    // change) and its validity; pinned host staging (n maps, then n bytes) and device copy
+    CUtensorMap* h_wmap = nullptr;
+    CUtensorMap* d_wmap = nullptr;
+    unsigned char* d_wmap_ok = nullptr;
     std::vector<void*> h_cache;
     cudaEvent_t upload_ev = nullptr;
     bool uploaded = false;
@@ -312,6 +331,17 @@ muon_status upload_pointers(muon_plan_s* p, float* const* params, const void* co
     }
     std::memcpy(p->h_pinned, p->h_cache.data(), 3 * n * sizeof(void*));
     MUON_TRY(cudaMemcpyAsync(p->d_ptrs, p->h_pinned, 3 * n * sizeof(void*), cudaMemcpyHostToDevice, s));
+    if (p->h_wmap) {   // W piece maps follow the parameter pointers (batched matrices only)
+        unsigned char* ok = reinterpret_cast<unsigned char*>(p->h_wmap + n);
+        for (size_t i = 0; i < n; ++i) {
+            const MatDev& md = p->mats[i];
+            const bool usable = p->buckets[p->mat_bucket[i]].batched() && md.n % 4 == 0 &&
+                                (reinterpret_cast<uintptr_t>(params[i]) & 15) == 0;
+            ok[i] = usable && make_w_piece_map(&p->h_wmap[i], params[i], (uint64_t)md.m, (uint64_t)md.n) ? 1 : 0;
+        }
+        MUON_TRY(cudaMemcpyAsync(p->d_wmap, p->h_wmap, n * sizeof(CUtensorMap), cudaMemcpyHostToDevice, s));
+        MUON_TRY(cudaMemcpyAsync(p->d_wmap_ok, ok, n, cudaMemcpyHostToDevice, s));
+    }
     MUON_TRY(cudaEventRecord(p->upload_ev, s));
     p->uploaded = true;
     return MUON_OK;
@@ -375,6 +405,7 @@ struct Grouper {
     cudaStream_t s;
     bool bf16;
     bool lower;         // lower-triangle launches (the chunk's Chunk::lower)
+    bool wtma = false;  // final products whose every matrix has a W map: W pieces by TMA
     int clusters = 0;   // CTA pairs for the pair kernel, CTAs for the one-SM kernel
     int grid1 = 0;
     GemmLaunch L1;   // 1-SM kernel, 128 x 256 tiles
@@ -452,7 +483,7 @@ struct Grouper {
     void flush2() {
         if (L2.nprob == 0) return;
         if (st == MUON_OK) {
-            st = cuda_status(gemm2_launch(L2, bf16, clusters, s, lower));
+            st = cuda_status(gemm2_launch(L2, bf16, clusters, s, lower, wtma));
             ++launches;
         }
         reset(L2);
@@ -492,6 +523,7 @@ void free_plan(muon_plan_s* p) {
     if (!p) return;
     if (p->ws) cudaFree(p->ws);
     if (p->h_pinned) cudaFreeHost(p->h_pinned);
+    if (p->h_wmap) cudaFreeHost(p->h_wmap);
     if (p->upload_ev) cudaEventDestroy(p->upload_ev);
     if (p->fork_ev) cudaEventDestroy(p->fork_ev);
     if (p->join_ev) cudaEventDestroy(p->join_ev);
@@ -514,7 +546,7 @@ void free_plan(muon_plan_s* p) {
 struct Layout {
     bool restarts = false;   // opts.max_ns_steps > 0: second X buffer, every matrix batched
     size_t o_mats = 0, o_part = 0, o_cpart = 0, o_inv = 0, o_alpha = 0, o_status = 0, o_tr = 0, o_ptrs = 0,
-           o_items = 0, o_ones = 0, o_diff = 0, o_odbg = 0, o_lists = 0, o_prefix = 0, o_region = 0;
+           o_items = 0, o_ones = 0, o_diff = 0, o_wmap = 0, o_wmap_ok = 0, o_odbg = 0, o_lists = 0, o_prefix = 0, o_region = 0;
     std::vector<size_t> o_ut, o_ut1, o_rr, o_qb;   // per bucket: X0, second X, r x r, bf16 Q (in the region)
     std::vector<int> rnr_list, rnc_list;           // RowNorm: row-wise and column-wise matrices
 };
@@ -648,6 +680,8 @@ muon_status plan_layout(muon_plan_s* p, Layout& L) {
     L.o_items = take(sizeof(int) * n);   // item -> plan matrix, per bucket slice
     L.o_ones = take(sizeof(float) * n);
     L.o_diff = take(sizeof(double) * (2 + 2 * kDiffParts));
+    L.o_wmap = take(sizeof(CUtensorMap) * n);   // W piece maps (slices are 256-byte aligned)
+    L.o_wmap_ok = take((size_t)n);
     L.o_odbg = p->opts.keep_update ? take([&] {
         size_t t = 0;
         for (int i = 0; i < n; ++i) t += (size_t)round_up(p->mats[i].m * p->mats[i].n * 4, 256);
@@ -842,6 +876,8 @@ static muon_status plan_build(muon_plan_s* p, const muon_shape* shapes, int32_t 
     p->d_ptrs = reinterpret_cast<void**>(base + L.o_ptrs);
     p->ones = reinterpret_cast<float*>(base + L.o_ones);
     p->diff = reinterpret_cast<double*>(base + L.o_diff);
+    p->d_wmap = reinterpret_cast<CUtensorMap*>(base + L.o_wmap);
+    p->d_wmap_ok = reinterpret_cast<unsigned char*>(base + L.o_wmap_ok);
 
     std::vector<unsigned char> tr(n);
     for (int i = 0; i < n; ++i) tr[i] = (unsigned char)p->mats[i].transposed;
@@ -990,6 +1026,8 @@ static muon_status plan_build(muon_plan_s* p, const muon_shape* shapes, int32_t 
         }
     }
     ok = ok && cudaMallocHost(&p->h_pinned, sizeof(void*) * 3 * n) == cudaSuccess;
+    ok = ok && cudaMallocHost(&p->h_wmap, (sizeof(CUtensorMap) + 1) * n) == cudaSuccess;
+    ok = ok && cudaMemset(p->d_wmap_ok, 0, n) == cudaSuccess;
     ok = ok && cudaEventCreateWithFlags(&p->upload_ev, cudaEventDisableTiming) == cudaSuccess;
     ok = ok && gemm_prepare(p->device) == cudaSuccess;
     ok = ok && ns_f32_prepare() == cudaSuccess;
@@ -1556,6 +1594,14 @@ static muon_status ns_step(muon_plan p, float* const* params, const void* const*
             // layout; earlier segments: X' = alpha Q X (bf16) into the other X buffer
             {
                 Grouper g(p, sc, true, ch.lower, gc_clusters, g_grid1);
+                if (last) {   // W pieces by TMA when every batched matrix of the chunk has a W map
+                    const unsigned char* wok = reinterpret_cast<const unsigned char*>(p->h_wmap + n);
+                    bool all = true;
+                    for (int bk : ch.buckets)
+                        if (p->buckets[bk].batched())
+                            for (int i : p->buckets[bk].mats) all = all && wok[i];
+                    g.wtma = all;
+                }
                 float* const* W = reinterpret_cast<float* const*>(p->d_ptrs + 2 * n);
                 for (int bk : ch.buckets) {
                     Bucket& b = p->buckets[bk];
@@ -1569,6 +1615,8 @@ static muon_status ns_step(muon_plan p, float* const* params, const void* const*
                     if (last) {
                         q.item_mat = b.d_item_mat;
                         q.W = W;
+                        q.wmap = p->d_wmap;
+                        q.wmap_ok = p->d_wmap_ok;
                         q.transposed = p->d_transposed;
                         q.Odbg = b.Odbg;
                         q.lr = lr;

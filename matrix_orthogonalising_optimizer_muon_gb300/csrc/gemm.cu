@@ -334,7 +334,10 @@ __device__ __forceinline__ void tile_prefetch(const GemmLaunch& L, const GemmPro
 // as their lower triangle (lower_out) and read back through the mirror (sym_a /
 // sym_b).  The same MMAs on the same operand values in the same order: both give
 // bitwise the same results.
-template <bool BF16, bool LOWER>
+// WTMA (bf16 only): final products whose every matrix has a W map move their W pieces by TMA;
+// the cp.async path is compiled out of that instantiation and the TMA one out of the others,
+// which keeps each within the 168 registers a 10-warp CTA gets.
+template <bool BF16, bool LOWER, bool WTMA>
 __global__ void __maxnreg__(168) gemm2_kernel(const __grid_constant__ GemmLaunch L) {
     using Cfg = Gemm2Cfg;
     extern __shared__ uint8_t smem_raw[];
@@ -525,6 +528,32 @@ __global__ void __maxnreg__(168) gemm2_kernel(const __grid_constant__ GemmLaunch
             const uint32_t aph = (local >> 1) & 1u;
             if (BF16 && P.epi == kEpiApply)   // (the polynomial's G' is prefetched by the producer)
                 prefetch_epilogue_inputs(P, tc.item, tc.m0 + wq * 32, tc.n0 + c_begin, kBN * 4 / kEpiWarps, lane);
+            // Final product with a W map: this warp's W pieces (rows R0w .. R0w + 31, its 32-column
+            // chunks) come by TMA into two 4 KB buffers (the shared memory the symmetric stores and
+            // the G' blocks use in other launches), the first two while the MMAs run, each next one
+            // once the previous store from its buffer has read it; box coordinates are those of
+            // the stored layout.  wn: the pieces this warp processes.
+            const CUtensorMap* wm = nullptr;
+            bool wtr = false;
+            int wn = 0;
+            const int R0w = tc.m0 + wq * 32;
+            if (WTMA && P.epi == kEpiApply) {   // (the host launches WTMA only when every map is valid)
+                const int mat = P.item_mat[tc.item];
+                if (R0w < P.M) {
+                    wm = &P.wmap[mat];
+                    wtr = P.transposed[mat] != 0;
+                    while (wn < 4 && tc.n0 + c_begin + 32 * wn < P.N) ++wn;
+                    if (lane == 0 && wn > 0) bulk_wait_read<0>();   // earlier stores have read the buffers
+                    for (int k = 0; k < 2 && k < wn; ++k) {
+                        if (lane == 0) {
+                            const int c0 = tc.n0 + c_begin + 32 * k;
+                            mbar_arrive_expect_tx(gb + k, kWPiece);
+                            tma_load_2d(stage_l + 4096 * k, wm, gb + k, wtr ? R0w : c0, wtr ? c0 : R0w);
+                        }
+                        gpend |= 1u << k;
+                    }
+                }
+            }
             // The polynomial's G' blocks (rows R0 .. R0 + 31, this warp's 32-column chunks) come
             // by TMA into the warp's two G' buffers, the first two while the MMAs run, each next
             // one as soon as its buffer has been read.  gn: the chunks this warp processes.
@@ -556,7 +585,38 @@ __global__ void __maxnreg__(168) gemm2_kernel(const __grid_constant__ GemmLaunch
                 if (col0 >= P.N) break;
                 if (P.sym && col0 > warp_row_max) break;
                 uint32_t raw[32];
-                if (BF16 && P.epi == kEpiApply) {
+                if (WTMA && P.epi == kEpiApply) {   // this chunk's W piece (chunk kc, buffer kc % 2)
+                    if (wm == nullptr) break;       // rows beyond the matrix: no pieces
+                    const uint32_t bsel = kc & 1;
+                    if (!mbar_wait_idle(gb + bsel, (gph >> bsel) & 1u, abort_flag, L.status, kStatusTimeoutEpilogue,
+                                        false)) {
+                        gabort = true;
+                        break;
+                    }
+                    gph ^= 1u << bsel;
+                    gpend &= ~(1u << bsel);
+                    uint8_t* wbuf = stage_l + 4096 * bsel;
+                    tmem_ld32(tbase + cc, raw);
+                    tmem_ld_wait();
+                    w_piece_update(P, wc, tc.item, R0w, col0, wbuf, lane, raw);
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // updates visible to TMA
+                    __syncwarp();
+                    const bool more = kc + 2 < wn;
+                    if (lane == 0) {
+                        tma_store_2d(wm, wbuf, wtr ? R0w : col0, wtr ? col0 : R0w);
+                        bulk_commit();
+                        if (more) {
+                            const int c2 = col0 + 64;
+                            bulk_wait_read<0>();   // the store has read the piece: its buffer is free
+                            mbar_arrive_expect_tx(gb + bsel, kWPiece);
+                            tma_load_2d(wbuf, wm, gb + bsel, wtr ? R0w : c2, wtr ? c2 : R0w);
+                        }
+                    }
+                    if (more) gpend |= 1u << bsel;
+                    __syncwarp();
+                    continue;
+                }
+                if (BF16 && !WTMA && P.epi == kEpiApply) {
                     // W piece (rows R0.., columns col0..) in with coalesced cp.async, updated
                     // in shared memory, out with coalesced 16-byte stores
                     const int R0 = tc.m0 + wq * 32;
@@ -636,10 +696,12 @@ cudaError_t gemm_prepare(int device) {
                                  GemmCfg::SMEM_BYTES);
     const int n = Gemm2Cfg::SMEM_BYTES;
     const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm2_kernel<true, false>, a, n);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm2_kernel<false, false>, a, n);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm2_kernel<true, true>, a, n);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm2_kernel<false, true>, a, n);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm2_kernel<true, false, false>, a, n);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm2_kernel<false, false, false>, a, n);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm2_kernel<true, true, false>, a, n);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm2_kernel<false, true, false>, a, n);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm2_kernel<true, false, true>, a, n);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm2_kernel<true, true, true>, a, n);
     if (e == cudaSuccess) e = ns_small_prepare();
     return e;
 }
@@ -656,20 +718,23 @@ cudaError_t gemm2_max_clusters(int* out) {
     cfg.dynamicSmemBytes = Gemm2Cfg::SMEM_BYTES;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaOccupancyMaxActiveClusters(out, gemm2_kernel<true, false>, &cfg);
+    return cudaOccupancyMaxActiveClusters(out, gemm2_kernel<true, false, false>, &cfg);
 }
 
-cudaError_t gemm2_launch(const GemmLaunch& L, bool bf16, int clusters, cudaStream_t s, bool lower) {
+cudaError_t gemm2_launch(const GemmLaunch& L, bool bf16, int clusters, cudaStream_t s, bool lower, bool wtma) {
     if (L.total_tiles <= 0) return cudaSuccess;
     if (clusters > L.total_tiles) clusters = L.total_tiles;
     if (clusters < 1) clusters = 1;
     const dim3 grid(2 * clusters), blk(kGemmThreads);
     const size_t sm = Gemm2Cfg::SMEM_BYTES;
+    if (bf16 && wtma)
+        return lower ? launch_pdl_cluster(gemm2_kernel<true, true, true>, grid, blk, sm, s, 2u, L)
+                     : launch_pdl_cluster(gemm2_kernel<true, false, true>, grid, blk, sm, s, 2u, L);
     if (lower)
-        return bf16 ? launch_pdl_cluster(gemm2_kernel<true, true>, grid, blk, sm, s, 2u, L)
-                    : launch_pdl_cluster(gemm2_kernel<false, true>, grid, blk, sm, s, 2u, L);
-    return bf16 ? launch_pdl_cluster(gemm2_kernel<true, false>, grid, blk, sm, s, 2u, L)
-                : launch_pdl_cluster(gemm2_kernel<false, false>, grid, blk, sm, s, 2u, L);
+        return bf16 ? launch_pdl_cluster(gemm2_kernel<true, true, false>, grid, blk, sm, s, 2u, L)
+                    : launch_pdl_cluster(gemm2_kernel<false, true, false>, grid, blk, sm, s, 2u, L);
+    return bf16 ? launch_pdl_cluster(gemm2_kernel<true, false, false>, grid, blk, sm, s, 2u, L)
+                : launch_pdl_cluster(gemm2_kernel<false, false, false>, grid, blk, sm, s, 2u, L);
 }
 
 cudaError_t gemm_launch(const GemmLaunch& L, bool bf16, int grid, cudaStream_t s) {

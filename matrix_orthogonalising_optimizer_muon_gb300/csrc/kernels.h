@@ -132,6 +132,13 @@ struct GemmProblem {
     // kEpiPoly on the CTA-pair kernel with TMA-stored output: the G' input is read by TMA
     // (mapG, 32 x 32 boxes) into the epilogue warp's shared memory, one chunk ahead
     int gin_tma;
+    int pad4;
+    // kEpiApply on the CTA-pair kernel: per plan matrix, a tensor map of W (fp32, stored
+    // layout, 32 x 32 boxes with 128-byte swizzle: the layout of a staged W piece).  The host
+    // launches the TMA W path only when every matrix of the launch has a valid map (W 16-byte
+    // aligned, stored row length a multiple of 4); wmap_ok holds the validity per matrix.
+    const CUtensorMap* wmap;
+    const unsigned char* wmap_ok;
 };
 constexpr int kTmaOutC = 1, kTmaOutC2 = 2, kTmaOutBf16 = 4;
 
@@ -180,7 +187,8 @@ cudaError_t gemm_launch(const GemmLaunch& L, bool bf16, int grid, cudaStream_t s
 // use pair tiling: tiles_m = ceil(M / 256), tiles_n = ceil(N / 256).
 // lower: the lower-triangle variant (4-D operand maps, lower_out / sym_a / sym_b honoured).
 cudaError_t gemm2_max_clusters(int* out);
-cudaError_t gemm2_launch(const GemmLaunch& L, bool bf16, int clusters, cudaStream_t s, bool lower);
+// wtma: a launch of final products whose every matrix has a valid W map (GemmProblem::wmap).
+cudaError_t gemm2_launch(const GemmLaunch& L, bool bf16, int clusters, cudaStream_t s, bool lower, bool wtma);
 // Whole NS step (SYRK, r x r recursion, final product + fused update) of matrices
 // with r <= 128, one matrix per CTA at a time.  One problem per bucket: M = r,
 // N = c, batch = matrices, tile_begin = prefix over matrices; mapA = X with
