@@ -447,7 +447,11 @@ def report_ours(args, res, rank, world):
         gbs = small_bytes / (per_ns[5] * 1e-3) / 1e9
         ns5["fused_small_ms"] = round(per_ns[5], 3)
         ns5["fused_small_gbs"] = round(gbs, 1)
-        if per_ns[5] > gemm_ms:
+        # the fused kernel dominates when it takes longer than the products, or when the
+        # products run beside it on the few CTA pairs left to them (a tensor roofline against
+        # the whole GPU's peak would not describe them)
+        beside = res["plan"] is not None and res["plan"].info().get("chain_clusters", 0) > 0
+        if per_ns[5] > gemm_ms or beside:
             roofline = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                         "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": small_traffic(wl.name),
                         "kernel": "ns_small_kernel: the whole NS5 step of the %d matrices with r <= 128 "
@@ -472,6 +476,11 @@ def report_ours(args, res, rank, world):
         "stages_ms_per_ns_step": {"momentum_norm": round(per_ns[0], 3), "syrk": round(per_ns[1], 3),
                                   "ns_rxr": round(per_ns[2], 3), "final_apply": round(per_ns[3], 3),
                                   "fused_small": round(per_ns[5], 3)},
+        # stage time x median SM clock = SM clock cycles (millions): comparable across runs whose
+        # power-capped clocks differ, for the tensor-bound stages
+        "stages_sm_mcycles_per_ns_step": ({k: round(v * res["clocks"]["sm_mhz"] / 1e3, 1) for k, v in
+                                           (("syrk", per_ns[1]), ("ns_rxr", per_ns[2]), ("final_apply", per_ns[3]))}
+                                          if (res["clocks"] or {}).get("sm_mhz") else None),
         "ms_per_step_median": round(statistics.median(res["per_step"]), 3),
         "ms_per_step_min": round(min(res["per_step"]), 3),
         "ns_steps_timed": n_ns,

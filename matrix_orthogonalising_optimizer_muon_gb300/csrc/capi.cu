@@ -331,11 +331,12 @@ muon_status upload_pointers(muon_plan_s* p, float* const* params, const void* co
     }
     std::memcpy(p->h_pinned, p->h_cache.data(), 3 * n * sizeof(void*));
     MUON_TRY(cudaMemcpyAsync(p->d_ptrs, p->h_pinned, 3 * n * sizeof(void*), cudaMemcpyHostToDevice, s));
-    if (p->h_wmap) {   // W piece maps follow the parameter pointers (batched matrices only)
+    if (p->h_wmap) {   // W piece maps follow the parameter pointers (tensor-core final products)
         unsigned char* ok = reinterpret_cast<unsigned char*>(p->h_wmap + n);
         for (size_t i = 0; i < n; ++i) {
             const MatDev& md = p->mats[i];
-            const bool usable = p->buckets[p->mat_bucket[i]].batched() && md.n % 4 == 0 &&
+            const Bucket& bk = p->buckets[p->mat_bucket[i]];
+            const bool usable = (bk.batched() || bk.fused) && md.n % 4 == 0 &&
                                 (reinterpret_cast<uintptr_t>(params[i]) & 15) == 0;
             ok[i] = usable && make_w_piece_map(&p->h_wmap[i], params[i], (uint64_t)md.m, (uint64_t)md.n) ? 1 : 0;
         }
@@ -1401,6 +1402,8 @@ static muon_status ns_step(muon_plan p, float* const* params, const void* const*
                 q.alpha = p->alpha + b.slot_base;
                 q.item_mat = b.d_item_mat;
                 q.W = W;
+                q.wmap = p->d_wmap;        // W pieces by TMA for the matrices with a valid map
+                q.wmap_ok = p->d_wmap_ok;
                 q.transposed = p->d_transposed;
                 q.Odbg = b.Odbg;
                 q.lr = lr;

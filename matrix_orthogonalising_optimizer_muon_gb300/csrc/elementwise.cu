@@ -177,20 +177,36 @@ __global__ void __launch_bounds__(kElemThreads) k_momentum_tiles(const ElemArgs 
                       aligned16(M);
     const int cq = t % kTileTpr, rr = t / kTileTpr;
     if (full) {
+        // G and M of kTileAhead passes are loaded before the first of their M stores (which
+        // the compiler may not move loads across): 96 B in flight per thread instead of 24
+        // (momentum of the 56 transposed 18944 x 3584 matrices 14.8 -> 13.9 ms per step)
+        constexpr int kPasses = kTileRows / kTileRpp;
+        constexpr int kTileAhead = kPasses < 4 ? kPasses : 4;
+        static_assert(kPasses % kTileAhead == 0, "passes per load batch");
 #pragma unroll
-        for (int p = 0; p < kTileRows / kTileRpp; ++p) {
-            const long long i = i0 + rr + kTileRpp * p;
-            const long long e = i * md.n + j0 + 4 * cq;
-            const float4 g = load_g4<BF16>(G, e);
-            float4 m = *reinterpret_cast<float4*>(M + e);
-            m.x = mu * m.x + g.x; m.y = mu * m.y + g.y; m.z = mu * m.z + g.z; m.w = mu * m.w + g.w;
-            *reinterpret_cast<float4*>(M + e) = m;
-            const float u0 = mu * m.x + g.x, u1 = mu * m.y + g.y, u2 = mu * m.z + g.z, u3 = mu * m.w + g.w;
-            ss += u0 * u0 + u1 * u1 + u2 * u2 + u3 * u3;
-            tile[4 * cq + 0][rr + kTileRpp * p] = u0;
-            tile[4 * cq + 1][rr + kTileRpp * p] = u1;
-            tile[4 * cq + 2][rr + kTileRpp * p] = u2;
-            tile[4 * cq + 3][rr + kTileRpp * p] = u3;
+        for (int p0 = 0; p0 < kPasses; p0 += kTileAhead) {
+            float4 gv[kTileAhead], mv[kTileAhead];
+#pragma unroll
+            for (int q = 0; q < kTileAhead; ++q) {
+                const long long e = (i0 + rr + kTileRpp * (p0 + q)) * md.n + j0 + 4 * cq;
+                gv[q] = load_g4<BF16>(G, e);
+                mv[q] = *reinterpret_cast<const float4*>(M + e);
+            }
+#pragma unroll
+            for (int q = 0; q < kTileAhead; ++q) {
+                const int p = p0 + q;
+                const long long e = (i0 + rr + kTileRpp * p) * md.n + j0 + 4 * cq;
+                const float4 g = gv[q];
+                float4 m = mv[q];
+                m.x = mu * m.x + g.x; m.y = mu * m.y + g.y; m.z = mu * m.z + g.z; m.w = mu * m.w + g.w;
+                *reinterpret_cast<float4*>(M + e) = m;
+                const float u0 = mu * m.x + g.x, u1 = mu * m.y + g.y, u2 = mu * m.z + g.z, u3 = mu * m.w + g.w;
+                ss += u0 * u0 + u1 * u1 + u2 * u2 + u3 * u3;
+                tile[4 * cq + 0][rr + kTileRpp * p] = u0;
+                tile[4 * cq + 1][rr + kTileRpp * p] = u1;
+                tile[4 * cq + 2][rr + kTileRpp * p] = u2;
+                tile[4 * cq + 3][rr + kTileRpp * p] = u3;
+            }
         }
     } else {
 #pragma unroll

@@ -25,11 +25,16 @@ namespace muon {
 // leaves rows < r unchanged.
 //
 // The W update of the final product goes through shared memory: each epilogue
-// warp streams its 32 x 32 fp32 pieces of W in with cp.async (three pieces in
-// flight), updates them from the accumulator, and writes them back with
+// warp streams its 32 x 32 fp32 pieces of W in (two pieces ahead of the one it
+// updates), updates them from the accumulator and writes them back.  With a W
+// tensor map for the matrix (32 x 32 fp32 boxes, 128-byte swizzle: the staged
+// piece layout) the pieces move by TMA tile loads and stores, one instruction
+// per piece each way, the stores asynchronous; otherwise by cp.async and
 // coalesced 16-byte stores.  The staging uses the r x r operand buffers, which
 // the final product does not read; with one NS step the last on-chip epilogue
-// still reads and writes them, so the epilogue warps meet before staging W.
+// still reads and writes them, so the epilogue warps meet before staging W, and
+// every warp's stores have read its staging before the next matrix's epilogues
+// write operands there.
 constexpr int kSmallRing = 3;                       // X stream ring (SYRK k-blocks, final chunks)
 constexpr int kSmallThreads = 320;                  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-9 epilogue
 constexpr int kSmallEpiWarps = 8;
@@ -43,8 +48,11 @@ struct SmallCfg {
     static constexpr int TS = QS + MAT;             // T (fp16); then Q_J (bf16) for the final product
     static constexpr int STAGE = GS;                // W staging of the final phase: GS, PS, QS
     static constexpr int BAR = TS + MAT;
-    static constexpr int SMEM_BYTES = BAR + 256 + 1024;
+    static constexpr int WBAR = BAR + 256;          // per epilogue warp, one mbarrier per W buffer
+    static constexpr int SMEM_BYTES = BAR + 512 + 1024;
 };
+static_assert(kSmallEpiWarps * kWBufs * 8 <= 256, "W buffer barriers");
+static_assert(SmallCfg::SMEM_BYTES <= 232448, "fused kernel exceeds the shared memory of one CTA");
 static_assert(kSmallEpiWarps * kWBufs * kWPiece <= 3 * SmallCfg::MAT, "W staging must fit in GS, PS, QS");
 
 // byte offset of element (row, col) of a 128 x 128 2-byte operand in the
@@ -169,10 +177,12 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
     uint64_t* rr_free = stage_free + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rr_free + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    uint64_t* wbar = reinterpret_cast<uint64_t*>(smem + Cfg::WBAR);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
+        for (int w = 0; w < kSmallEpiWarps * kWBufs; ++w) mbar_init(wbar + w, 1);
         for (int s = 0; s < kSmallRing; ++s) {
             mbar_init(full + s, 1);
             mbar_init(empty + s, 1);
@@ -349,6 +359,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
         const uint32_t tmem_row = tmem_base + (static_cast<uint32_t>(wq * 32) << 16);
         uint8_t* stage = smem + Cfg::STAGE + (warp - 2) * kWBufs * kWPiece;
         const uint32_t stage_u32 = smem_u32(stage);
+        uint64_t* wb = wbar + kWBufs * (warp - 2);
+        uint32_t wph = 0;    // phase bit per W buffer (TMA path)
+        uint32_t wpend = 0;  // W loads in flight per buffer (TMA path)
         uint32_t sc = 0, fc = 0, mc = 0, jc = 0;
         bool ok = true;
         auto step = [&](int kind, int k, int J, const GemmProblem& P, int item) -> bool {
@@ -393,6 +406,83 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
             const int rw = wq * 32;
             const int npieces = 2 * nch;
             auto piece_col = [&](int i) { return (i >> 1) * 128 + c_begin + 32 * (i & 1); };
+            const int mat = P.item_mat[item];
+            const CUtensorMap* wm = (P.wmap != nullptr && rw < P.M && P.wmap_ok[mat]) ? P.wmap + mat : nullptr;
+            if (wm != nullptr) {
+                // TMA pieces: box coordinates in the stored layout; piece i in buffer i % kWBufs,
+                // loaded kWBufs - 1 pieces ahead once the store of the piece before it has read
+                // the buffer
+                const bool wtr = P.transposed[mat] != 0;
+                auto issue = [&](int i) {
+                    const int c0 = piece_col(i), bs = i % kWBufs;
+                    mbar_arrive_expect_tx(wb + bs, kWPiece);
+                    tma_load_2d(stage + bs * kWPiece, wm, wb + bs, wtr ? rw : c0, wtr ? c0 : rw);
+                };
+#pragma unroll 1
+                for (int i = 0; i < kWBufs - 1 && i < npieces; ++i) {
+                    if (piece_col(i) >= P.N) continue;
+                    if (lane == 0) issue(i);
+                    wpend |= 1u << (i % kWBufs);
+                }
+#pragma unroll 1
+                for (int i = 0; i < npieces; ++i) {
+                    const int h = i & 1;
+                    const uint32_t b = fc & 1u;
+                    const int col0 = piece_col(i);
+                    const int ahead = i + kWBufs - 1;
+                    if (ahead < npieces && piece_col(ahead) < P.N) {
+                        if (lane == 0) {
+                            bulk_wait_read<0>();
+                            issue(ahead);
+                        }
+                        wpend |= 1u << (ahead % kWBufs);
+                    }
+                    if (h == 0) {
+                        if (!mbar_wait_idle(accf_full + b, (fc >> 1) & 1u, abort_flag, L.status,
+                                            kStatusTimeoutEpilogue, false)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
+                    uint32_t acc[32];
+                    tmem_ld32(tmem_row + 256 + 128 * b + c_begin + 32 * h, acc);
+                    tmem_ld_wait();
+                    if (h == 1) {   // both halves read: the accumulator may be reused
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(accf_empty + b);
+                        ++fc;
+                    }
+                    if (col0 < P.N) {
+                        const int bs = i % kWBufs;
+                        if (!mbar_wait_idle(wb + bs, (wph >> bs) & 1u, abort_flag, L.status, kStatusTimeoutEpilogue,
+                                            false)) {
+                            ok = false;
+                            break;
+                        }
+                        wph ^= 1u << bs;
+                        wpend &= ~(1u << bs);
+                        uint8_t* buf = stage + bs * kWPiece;
+                        w_piece_update(P, wc, item, rw, col0, buf, lane, acc);
+                        fence_proxy_async_smem();   // the updated piece visible to the TMA store
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(wm, buf, wtr ? rw : col0, wtr ? col0 : rw);
+                            bulk_commit();
+                        }
+                    }
+                    __syncwarp();
+                }
+                if (lane == 0) bulk_wait_read<0>();   // the stores have read the staging
+                __syncwarp();
+                if (!ok) break;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(stage_free);
+                ok = mbar_wait_idle(stage_free, mc & 1u, abort_flag, L.status, kStatusTimeoutEpilogue, false);
+                ++mc;
+                continue;
+            }
 #pragma unroll 1
             for (int i = 0; i < kWBufs - 1; ++i) {
                 if (i < npieces) w_piece_load(wc, rw, piece_col(i), stage_u32 + i * kWPiece, lane);
@@ -441,6 +531,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1) ns_small_kernel(const __grid
             ++mc;
         }
         cp_async_wait<0>();
+        for (int k = 0; k < kWBufs; ++k)   // TMA W loads still in flight after an abort
+            if (wpend & (1u << k)) mbar_drain(wb + k, (wph >> k) & 1u);
+        if (lane == 0) bulk_wait<0>();     // TMA W stores complete before the CTA exits
     }
 
     tc_fence_before();
