@@ -321,6 +321,54 @@ def test_rownorm_step(grad_dtype):
         assert e["m"] <= TOL_FP32 and e["w"] <= TOL_FP32, (ROWNORM_SHAPES[i], e)
 
 
+# m > n matrices of the column path (statistics, finalize, apply): column counts past a
+# multiple of the blocks' 1024 columns, fewer rows than a statistics slab (8, 20), next
+# to m <= n matrices.
+COLPATH_SHAPES = [(1000, 332), (2049, 256), (130, 20), (5000, 516), (300, 8), (64, 64), (256, 1024),
+                 (20000, 132)]
+
+
+@pytest.mark.parametrize("grad_dtype", ["bf16", "f32"])
+def test_rownorm_column_path_aligned_and_not(grad_dtype):
+    """The m > n matrices take the three column kernels beside the row kernels, with W
+    16-byte aligned (vector loads) or one float past the boundary (element by element).
+    Within 1e-5 of the oracle over two steps in a row."""
+    import torch
+    import matrix_orthogonalising_optimizer_muon_gb300 as lib
+    inputs = host_inputs(COLPATH_SHAPES, grad_dtype, base_seed=34)
+    plan = lib.MuonPlan(COLPATH_SHAPES, grad_dtype)
+    row_launches = len({lib_row_class(n) for m, n in COLPATH_SHAPES if m <= n})
+    for aligned in (True, False):
+        W = []
+        for w, _, _ in inputs:
+            if aligned:
+                W.append(w.cuda())
+            else:   # every W one float past a 16-byte boundary
+                buf = torch.empty(w.numel() + 1, device="cuda")
+                v = buf[1:].view(w.shape)
+                v.copy_(w.cuda())
+                W.append(v)
+        G = [x[1].cuda() for x in inputs]
+        M = [x[2].cuda() for x in inputs]
+        w_ref = [x[0].double().numpy() for x in inputs]
+        m_ref = [x[2].double().numpy() for x in inputs]
+        for t in range(2):
+            plan.rownorm_step(W, G, M, LR, WD, MU, 1e-8)
+            plan.sync()
+            assert plan.info()["launches_last_step"] == row_launches + 3
+            for i in range(len(COLPATH_SHAPES)):
+                w_ref[i], m_ref[i], _ = R.muon_step(w_ref[i], inputs[i][1].double().numpy(), m_ref[i], LR, WD, MU,
+                                                    0, "rownorm", 1e-8)
+                assert rel(M[i].cpu().numpy(), m_ref[i]) <= TOL_FP32, (COLPATH_SHAPES[i], aligned, t)
+                assert rel(W[i].cpu().numpy(), w_ref[i]) <= TOL_FP32, (COLPATH_SHAPES[i], aligned, t)
+    plan.close()
+
+
+def lib_row_class(n):
+    """Launch class of a RowNorm row of n elements (rows up to 2048, 4096, longer)."""
+    return 0 if n <= 2048 else (1 if n <= 4096 else 2)
+
+
 def test_rownorm_eps_floor():
     """Rows whose norm is below eps are divided by eps, not normalised."""
     import torch
