@@ -145,3 +145,50 @@ def test_dit_periodic_rownorm_8_steps():
         # two NS refreshes with O within 2e-2 each; RowNorm steps match to fp32
         bound = (2 * LR * R.update_scale(mm, nn) * TOL_O * math.sqrt(min(mm, nn))) / np.linalg.norm(w_ref[i])
         assert rel(W[i].cpu().numpy(), w_ref[i]) <= bound + TOL_FP32, i
+
+
+def test_qwen7b_28l_one_matrix_per_shape_per_layer():
+    """The 196-matrix set: in every layer one randomly chosen matrix of each oriented
+    shape (q / o 3584 x 3584, k / v 512 x 3584, gate / up / down 3584 x 18944): momentum
+    and W given O at 1e-5 (the 3584 x 18944 ones in seven random layers, the others in
+    all 28), O against the oracle for the 512 x 3584 ones of every layer and the
+    3584 x 3584 ones of three random layers.  Inputs are regenerated from their seeds
+    after the step, so no host copy of the whole set is kept."""
+    import torch
+    import workloads
+    import matrix_orthogonalising_optimizer_muon_gb300 as lib
+    wl = workloads.WORKLOADS["qwen7b_28l"]
+    rng = np.random.default_rng(2028)
+    within = {"sq": (0, 3), "kv": (1, 2), "ffn": (4, 5, 6)}   # q, k, v, o, gate, up, down
+    ffn_layers = set(rng.choice(28, 7, replace=False).tolist())
+    o_sq_layers = set(rng.choice(28, 3, replace=False).tolist())
+    picks = [(layer, kind, 7 * layer + int(rng.choice(idx))) for layer in range(28) for kind, idx in within.items()]
+    W, G, M = device_inputs(wl)
+    plan = lib.MuonPlan(list(wl.shapes), wl.grad_dtype, keep_update=True)
+    plan.step(W, G, M, LR, WD, MU, 5, "ns")
+    plan.sync()
+    worst = {"m": 0.0, "w": 0.0, "o": 0.0}
+    for layer, kind, i in picks:
+        if kind == "ffn" and layer not in ffn_layers:
+            continue
+        shape = wl.shapes[i]
+
+        def seeded(kind_, std, dtype="f32"):
+            t = workloads.gen_tensor(shape, std, workloads.seed_of(wl.index, 0, i, kind_), "cuda", dtype)
+            return t.double().cpu().numpy()
+
+        w0, g, m0 = seeded("W", workloads.W_STD), seeded("G", workloads.G_STD, wl.grad_dtype), seeded("M", workloads.M_STD)
+        m_ref = R.momentum(m0, g, MU)
+        e_m = rel(M[i].cpu().numpy(), m_ref)
+        o = plan.debug_update(i).cpu().double().numpy()
+        e_w = rel(W[i].cpu().numpy(), R.apply_update(w0, o, LR, WD, R.update_scale(*shape)))
+        assert e_m <= TOL_FP32 and e_w <= TOL_FP32, (layer, kind, i, e_m, e_w)
+        worst["m"], worst["w"] = max(worst["m"], e_m), max(worst["w"], e_w)
+        if kind == "kv" or (kind == "sq" and layer in o_sq_layers):
+            e_o = rel(o, R.orthogonalised_update(R.nesterov(m_ref, g, MU), 5, form="gram"))
+            assert e_o <= TOL_O, (layer, kind, i, e_o)
+            worst["o"] = max(worst["o"], e_o)
+    del W, G, M
+    plan.close()
+    torch.cuda.empty_cache()
+    print("qwen7b_28l sampled per layer:", {k: "%.2e" % v for k, v in worst.items()})
