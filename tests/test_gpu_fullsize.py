@@ -105,7 +105,7 @@ def test_qwen7b_28l_layers_0_and_27():
 
 
 def test_dit_periodic_rownorm_8_steps():
-    """28 DiT blocks, K = 4 over 8 steps with fresh grads; blocks 0 and 27 followed by the
+    """28 DiT blocks, K = 4 over 8 steps with fresh grads; blocks 0, 13 and 27 followed by the
     oracle, and at the RowNorm step t = 1 every matrix's update direction, recovered from W
     before and after, has unit oriented rows (a property of R_eps at any size)."""
     import torch
@@ -113,7 +113,7 @@ def test_dit_periodic_rownorm_8_steps():
     import matrix_orthogonalising_optimizer_muon_gb300 as lib
     wl = workloads.WORKLOADS["dit1p3b"]
     W, G, M = device_inputs(wl)
-    sample = list(range(5)) + list(range(135, 140))
+    sample = list(range(5)) + list(range(65, 70)) + list(range(135, 140))
     w_ref = {i: W[i].double().cpu().numpy() for i in sample}
     m_ref = {i: M[i].double().cpu().numpy() for i in sample}
     plan = lib.MuonPlan(list(wl.shapes), wl.grad_dtype)
