@@ -371,11 +371,14 @@ def run_ours(args, rank, world, local):
                 setup_s=setup_s, one_step=one_step)
 
 
-def run_e2e(res, args):
+def run_e2e(res, args, copy_back=True):
     """Same step through the public API with host buffers (``muon_step_host``): every
     step copies the gradients host->device from pinned memory and the updated weights
     back device->host.  The plan runs in ``args.e2e_chunks`` chunks so that one chunk's
-    copies overlap another chunk's compute; the stream waits for the last copy back."""
+    copies overlap another chunk's compute; the stream waits for the last copy back.
+    copy_back=False: the parameters stay on the device (as in training, where they live
+    there) and each step's result read on the host is the plan's status word
+    (``muon_sync``, 4 bytes)."""
     import torch
     import matrix_orthogonalising_optimizer_muon_gb300 as lib
     import workloads
@@ -384,7 +387,7 @@ def run_e2e(res, args):
     if not shapes:
         return 0.0, 0, 0, 0, 0
     host_g = [torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in G]
-    host_w = [torch.empty(w.shape, dtype=w.dtype, pin_memory=True) for w in W]
+    host_w = [torch.empty(w.shape, dtype=w.dtype, pin_memory=True) for w in W] if copy_back else None
     for hg, g in zip(host_g, G):
         hg.copy_(g)
     plan = lib.MuonPlan(shapes, wl.grad_dtype, chunks=args.e2e_chunks)
@@ -395,6 +398,8 @@ def run_e2e(res, args):
     def one(t):
         mode = "rownorm" if wl.rownorm_k and t % wl.rownorm_k != 0 else "ns"
         plan.step_host(W, G, M, host_g, host_w, lr, wd, mu, 5, mode, stream=stream)
+        if not copy_back:
+            plan.sync(stream)   # the step's status, read on the host
 
     one(0)   # warm-up: the plan's copy streams and events are created on first use
     torch.cuda.synchronize()
@@ -408,7 +413,7 @@ def run_e2e(res, args):
     plan.sync()
     plan.close()
     h2d = sum(g.numel() * g.element_size() for g in G)
-    d2h = sum(w.numel() * w.element_size() for w in W)
+    d2h = sum(w.numel() * w.element_size() for w in W) if copy_back else 4
     return ev0.elapsed_time(ev1) / steps, h2d, d2h, steps, chunks
 
 
@@ -567,6 +572,12 @@ def main():
                        "what": "muon_step_host: grads host->device (pinned) and updated weights "
                                "device->host, overlapped chunk by chunk with the step" +
                                ("; each rank its own matrices, bytes summed over ranks" if world > 1 else "")}
+        if world == 1:
+            r_ms, r_h2d, r_d2h, r_steps, _ = run_e2e(res, args, copy_back=False)
+            line["e2e_params_resident"] = {
+                "value": round(r_ms, 3), "unit": "ms", "h2d_bytes_per_step": r_h2d, "d2h_bytes_per_step": r_d2h,
+                "steps": r_steps, "what": "muon_step_host without the copy back: grads host->device (pinned), "
+                                          "overlapped chunk by chunk; muon_sync reads the status every step"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         t, detail = oracle_sample(res["shapes"], res["wl"].grad_dtype, seed=res["wl"].index)
         line["cpu_baseline"] = {"value": round(t * 1e3, 1), "unit": "ms", "cores": os.cpu_count(),
