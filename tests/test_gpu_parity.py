@@ -1159,3 +1159,34 @@ def test_measured_costs_drive_the_owner_partition():
     assert sorted(set(owners)) == [0, 1, 2]
     assert abs(sum(loads) - sum(costs)) < 1e-6 * sum(costs)
     assert max(loads) - min(loads) <= max(costs) + 1e-9
+
+
+def test_plan_follows_new_tensors_between_steps():
+    """One plan, three NS steps on two different sets of device tensors (A, B, A): the plan
+    uploads the new pointers and re-encodes the W maps of its final products (fused r <= 128
+    and batched, both orientations) whenever they change.  Every step against the oracle:
+    M and W given O at 1e-5, O within the bar."""
+    import torch
+    import matrix_orthogonalising_optimizer_muon_gb300 as lib
+    shapes = [(128, 3584), (3584, 128), (300, 700), (700, 300), (96, 96), (256, 1024)]
+    plan = lib.MuonPlan(shapes, "bf16", keep_update=True)
+    sets = []
+    for seed in (61, 62):
+        inp = host_inputs(shapes, "bf16", seed)
+        sets.append(([x[0].cuda() for x in inp], [x[1].cuda() for x in inp], [x[2].cuda() for x in inp]))
+    assert all(a.data_ptr() != b.data_ptr() for a, b in zip(sets[0][0], sets[1][0]))
+    for k in (0, 1, 0):
+        W, G, M = sets[k]
+        w0 = [w.double().cpu().numpy() for w in W]
+        m0 = [m.double().cpu().numpy() for m in M]
+        plan.step(W, G, M, LR, WD, MU, 5, "ns")
+        plan.sync()
+        for i, (m, n) in enumerate(shapes):
+            g = G[i].double().cpu().numpy()
+            m_ref = R.momentum(m0[i], g, MU)
+            assert rel(M[i].cpu().numpy(), m_ref) <= TOL_FP32, (k, i)
+            o = plan.debug_update(i).double().cpu().numpy()
+            assert rel(W[i].cpu().numpy(), R.apply_update(w0[i], o, LR, WD, R.update_scale(m, n))) <= TOL_FP32, (k, i)
+            e = rel(o, R.orthogonalised_update(R.nesterov(m_ref, g, MU), 5, form="gram"))
+            assert e <= TOL_O, (k, i, shapes[i], e)
+    plan.close()
