@@ -18,8 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmuon_gb300.so")
-SOURCES = ["capi.cu", "gemm.cu", "ns_small.cu", "ns_f32.cu", "elementwise.cu", "noalloc.cu"]
-HEADERS = ["kernels.h", "ptx.cuh", "gemm_common.cuh"]
+SOURCES = ["plan.cu", "step.cu", "capi.cu", "gemm.cu", "ns_small.cu", "ns_f32.cu", "elementwise.cu", "noalloc.cu"]
+HEADERS = ["kernels.h", "plan.h", "ptx.cuh", "gemm_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE] + ARCH
 

@@ -1,5 +1,6 @@
 // Kernel parameter blocks and launch entry points shared by the host planner
-// (capi.cu) and the kernel translation units (gemm.cu, elementwise.cu).
+// (plan.cu, step.cu, capi.cu) and the kernel translation units (gemm.cu, ns_small.cu,
+// ns_f32.cu, elementwise.cu, noalloc.cu).
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
